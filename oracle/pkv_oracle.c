@@ -1,0 +1,462 @@
+/*
+ * pkv_oracle.c -- CPU float64 oracle for one batched paged-KV decode step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, plain, obviously-correct
+ * statement of what the decode step computes.  Only the tests, the smoke check
+ * and the benchmark's CPU-baseline leg may load it.  It shares no code, header,
+ * table or helper with the CUDA library (paged_kv_decode_table_gb300/csrc), and
+ * the CUDA library never calls it.
+ *
+ * Sources (web pages; cited by title and section):
+ *  [LAB]  "Bai Lab tong hop -- Inference Engineering" (openarchlab.com,
+ *         inference-lab), block [6] KV state manager (KVPool: block pool of
+ *         shape [num_blocks, n_heads, block_size, d_head], write/gather through
+ *         a per-sequence block table), block [5] forward (scores q.K/sqrt(d),
+ *         max-subtracted softmax over positions, weights times V), block [8]
+ *         sample (temperature softmax, top-k, renormalise, top-p, draw over
+ *         vocabulary order).
+ *  [CH5]  "Suy luan & Toi uu hoa (Inference)" (foundations-of-llms-vi, chapter
+ *         5), section 1.2 (temperature p_i(T), top-k, the nucleus set V^(p) =
+ *         smallest sorted prefix whose cumulative probability reaches p, and the
+ *         renormalised distribution), section 3.1 (GQA: n_q query heads in equal
+ *         groups sharing one K/V head), section 3.2 (PagedAttention block table),
+ *         section 4.1 (online softmax running max / sum / output).
+ *  [SERVE] "LLM inference serving tutorial" (wanshuiyin.github.io, ARIS-in-AI-
+ *         Offer), section 3.1 (sampler table: T=0 is a separate greedy branch
+ *         with lowest-index tie-break; top-k ties broken by (-z, token_id);
+ *         top-p keeps the boundary token), section 1.6 (one RNG stream per
+ *         request), appendix A invariants [D01]/[D02].
+ *  [PHILOX] J. Salmon, M. Moraes, R. Dror, D. Shaw, "Parallel Random Numbers:
+ *         As Easy as 1, 2, 3", SC'11: the Philox4x64-10 counter-based generator.
+ *
+ * Readings where the pages leave a step open (each also listed in the design
+ * notes): seq_lens counts the new token (the decode row attends to its own
+ * position); query head qh reads KV head qh / (Hq/Hkv); scale defaults to
+ * 1/sqrt(D); top-p acts on the renormalised top-k distribution; the draw walks
+ * the kept set in token-id order; the uniform is the first Philox4x64-10 output
+ * word of counter (offset,0,0,0) under key (seed,0), top 53 bits times 2^-53.
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fopenmp -shared -fPIC (no fast-math).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Status codes returned by the oracle (same meanings as the library's, but
+ * defined here independently). */
+#define OR_OK 0
+#define OR_INVALID_ARG 1
+#define OR_DEVICE_BOUNDS 4
+#define OR_NONFINITE 6
+
+/* Element types of KV / q inputs. */
+#define OR_F32 0
+#define OR_BF16 1
+
+/* ------------------------------------------------------------------------ */
+/* Philox4x64-10 [PHILOX]: 10 rounds of the Philox S-box on a 4x64-bit counter,
+ * with a Weyl-sequence key schedule.  Multipliers and Weyl constants are the
+ * published ones. */
+static const uint64_t PHILOX_M0 = 0xD2E7470EE14C6C93ULL;
+static const uint64_t PHILOX_M1 = 0xCA5A826395121157ULL;
+static const uint64_t PHILOX_W0 = 0x9E3779B97F4A7C15ULL; /* golden ratio */
+static const uint64_t PHILOX_W1 = 0xBB67AE8584CAA73BULL; /* sqrt(3) - 1 */
+
+void oracle_philox4x64_10(const uint64_t counter[4], const uint64_t key[2], uint64_t out[4]) {
+    uint64_t x0 = counter[0], x1 = counter[1], x2 = counter[2], x3 = counter[3];
+    uint64_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        unsigned __int128 prod0 = (unsigned __int128)PHILOX_M0 * x0;
+        unsigned __int128 prod1 = (unsigned __int128)PHILOX_M1 * x2;
+        uint64_t hi0 = (uint64_t)(prod0 >> 64), lo0 = (uint64_t)prod0;
+        uint64_t hi1 = (uint64_t)(prod1 >> 64), lo1 = (uint64_t)prod1;
+        uint64_t y0 = hi1 ^ x1 ^ k0;
+        uint64_t y1 = lo1;
+        uint64_t y2 = hi0 ^ x3 ^ k1;
+        uint64_t y3 = lo0;
+        x0 = y0; x1 = y1; x2 = y2; x3 = y3;
+        k0 += PHILOX_W0;
+        k1 += PHILOX_W1;
+    }
+    out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
+}
+
+/* Per-request uniform in [0,1): the request's own stream ([SERVE] 1.6) is the
+ * Philox key (seed, 0); the decode step picks the counter (offset, 0, 0, 0). */
+double oracle_uniform(uint64_t seed, uint64_t offset) {
+    uint64_t ctr[4] = {offset, 0, 0, 0};
+    uint64_t key[2] = {seed, 0};
+    uint64_t out[4];
+    oracle_philox4x64_10(ctr, key, out);
+    return (double)(out[0] >> 11) * (1.0 / 9007199254740992.0); /* 2^-53 */
+}
+
+/* ------------------------------------------------------------------------ */
+/* Element access: bf16 is the top half of an IEEE float32. */
+static double load_elem(const void* base, size_t idx, int dtype) {
+    if (dtype == OR_F32) return (double)((const float*)base)[idx];
+    uint32_t bits = (uint32_t)((const uint16_t*)base)[idx] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+static size_t elem_size(int dtype) { return dtype == OR_F32 ? 4 : 2; }
+
+/* Offset (in elements) of token `pos` of sequence b, KV head h, in a pool laid
+ * out [num_blocks, Hkv, BS, D] ([LAB] block [6]: the token at position pos lives
+ * in physical block blocks[pos // BS], slot pos % BS).  Returns -1 when the
+ * block-table entry is out of range. */
+static long long pool_offset(const int32_t* block_tables, int max_blocks, int b, int pos,
+                             int h, int Hkv, int BS, int D, int NB) {
+    int logical = pos / BS;
+    int slot = pos % BS;
+    int32_t blk = block_tables[(size_t)b * max_blocks + logical];
+    if (blk < 0 || blk >= NB) return -1;
+    return (((long long)blk * Hkv + h) * BS + slot) * (long long)D;
+}
+
+/* ------------------------------------------------------------------------ */
+/* KV append ([LAB] block [6] KVPool.write, one new token per sequence):
+ * seq_lens[b] is the length AFTER the append, so the new token sits at
+ * position L-1.  Copies element bits (no arithmetic).  Sequences whose length
+ * is outside [1, max_blocks*BS] or whose block id is out of range are skipped
+ * and reported. */
+int oracle_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                     const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
+                     int B, int Hkv, int D, int BS, int NB, int dtype) {
+    size_t es = elem_size(dtype);
+    int status = OR_OK;
+    for (int b = 0; b < B; ++b) {
+        int L = seq_lens[b];
+        if (L < 1 || (long long)L > (long long)max_blocks * BS) { status = OR_DEVICE_BOUNDS; continue; }
+        int pos = L - 1;
+        for (int h = 0; h < Hkv; ++h) {
+            long long off = pool_offset(block_tables, max_blocks, b, pos, h, Hkv, BS, D, NB);
+            if (off < 0) { status = OR_DEVICE_BOUNDS; continue; }
+            size_t src = ((size_t)b * Hkv + h) * D;
+            memcpy((char*)k_cache + (size_t)off * es, (const char*)k_new + src * es, D * es);
+            memcpy((char*)v_cache + (size_t)off * es, (const char*)v_new + src * es, D * es);
+        }
+    }
+    return status;
+}
+
+/* Gather ([LAB] block [6] KVPool.gather): the first L cached tokens of sequence
+ * b, head h, in position order, as float64 [L, D].  Returns non-zero on a bad
+ * block id. */
+int oracle_gather(const void* cache, const int32_t* block_tables, int max_blocks, int b, int L,
+                  int h, int Hkv, int D, int BS, int NB, int dtype, double* out) {
+    for (int pos = 0; pos < L; ++pos) {
+        long long off = pool_offset(block_tables, max_blocks, b, pos, h, Hkv, BS, D, NB);
+        if (off < 0) return OR_DEVICE_BOUNDS;
+        for (int d = 0; d < D; ++d) out[(size_t)pos * D + d] = load_elem(cache, (size_t)off + d, dtype);
+    }
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Decode attention for one (sequence, query head), two-pass definition ([LAB]
+ * block [5] forward: scores = q.K / sqrt(d), causal row covering every cached
+ * position including the new one, softmax with the max subtracted, weights times
+ * V; [CH5] 3.1: query head qh uses KV head qh / G).  out[D] in float64.
+ * Writes sum(weights) - 1 to *wsum_err.  L = 0 gives zeros. */
+static int attention_row(const void* q, const void* k_cache, const void* v_cache, int dtype,
+                         const int32_t* block_tables, int max_blocks, int b, int qh, int L,
+                         int Hq, int Hkv, int D, int BS, int NB, double scale, double* out,
+                         double* wsum_err) {
+    int G = Hq / Hkv;
+    int h = qh / G;
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    *wsum_err = 0.0;
+    if (L == 0) return OR_OK;
+    double* K = (double*)malloc(sizeof(double) * (size_t)L * D);
+    double* V = (double*)malloc(sizeof(double) * (size_t)L * D);
+    double* s = (double*)malloc(sizeof(double) * (size_t)L);
+    double* qv = (double*)malloc(sizeof(double) * (size_t)D);
+    int st = oracle_gather(k_cache, block_tables, max_blocks, b, L, h, Hkv, D, BS, NB, dtype, K);
+    if (st == OR_OK) st = oracle_gather(v_cache, block_tables, max_blocks, b, L, h, Hkv, D, BS, NB, dtype, V);
+    if (st == OR_OK) {
+        for (int d = 0; d < D; ++d) qv[d] = load_elem(q, ((size_t)b * Hq + qh) * D + d, dtype);
+        double mx = -INFINITY;
+        for (int j = 0; j < L; ++j) {
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d) acc += qv[d] * K[(size_t)j * D + d];
+            s[j] = acc * scale;
+            if (s[j] > mx) mx = s[j];
+        }
+        double z = 0.0;
+        for (int j = 0; j < L; ++j) { s[j] = exp(s[j] - mx); z += s[j]; }
+        double wsum = 0.0;
+        for (int j = 0; j < L; ++j) {
+            double w = s[j] / z;
+            wsum += w;
+            for (int d = 0; d < D; ++d) out[d] += w * V[(size_t)j * D + d];
+        }
+        *wsum_err = wsum - 1.0;
+    } else {
+        for (int d = 0; d < D; ++d) out[d] = 0.0;
+    }
+    free(K); free(V); free(s); free(qv);
+    return st;
+}
+
+/* Batched decode attention.  rows == NULL: every (b, qh) pair, out is
+ * [B, Hq, D].  Otherwise rows holds nrows flat indices b*Hq+qh and out is
+ * [nrows, D].  scale <= 0 selects 1/sqrt(D).  Sequences with L outside
+ * [0, max_blocks*BS] or a bad block id give zeros and a status.  max_wsum_err
+ * receives max |sum(weights) - 1|. */
+int oracle_paged_attention(double* out, const void* q, const void* k_cache, const void* v_cache,
+                           int dtype, const int32_t* block_tables, int max_blocks,
+                           const int32_t* seq_lens, int B, int Hq, int Hkv, int D, int BS, int NB,
+                           double scale, const int64_t* rows, long long nrows,
+                           double* max_wsum_err) {
+    if (Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || BS <= 0) return OR_INVALID_ARG;
+    if (scale <= 0.0) scale = 1.0 / sqrt((double)D);
+    long long n = rows ? nrows : (long long)B * Hq;
+    int status = OR_OK;
+    double werr = 0.0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(max : werr)
+    for (long long i = 0; i < n; ++i) {
+        long long flat = rows ? rows[i] : i;
+        int b = (int)(flat / Hq), qh = (int)(flat % Hq);
+        int L = seq_lens[b];
+        double e = 0.0;
+        int st;
+        if (L < 0 || (long long)L > (long long)max_blocks * BS) {
+            for (int d = 0; d < D; ++d) out[i * D + d] = 0.0;
+            st = OR_DEVICE_BOUNDS;
+        } else {
+            st = attention_row(q, k_cache, v_cache, dtype, block_tables, max_blocks, b, qh, L, Hq,
+                               Hkv, D, BS, NB, scale, out + i * D, &e);
+        }
+        if (st != OR_OK) {
+#pragma omp atomic write
+            status = st;
+        }
+        if (fabs(e) > werr) werr = fabs(e);
+    }
+    if (max_wsum_err) *max_wsum_err = werr;
+    return status;
+}
+
+/* Split-KV statement of the same row ([CH5] 4.1 online softmax): the L
+ * positions are cut at multiples of chunk_tokens; chunk c yields its own max m_c,
+ * sum l_c = sum exp(s - m_c) and unnormalised o_c = sum exp(s - m_c) V; the
+ * chunks merge as M = max m_c, Lsum = sum l_c e^(m_c - M),
+ * out = sum o_c e^(m_c - M) / Lsum.  Used to pin the split algebra against the
+ * two-pass definition. */
+int oracle_attention_split_row(double* out, const void* q, const void* k_cache,
+                               const void* v_cache, int dtype, const int32_t* block_tables,
+                               int max_blocks, int b, int qh, int L, int Hq, int Hkv, int D,
+                               int BS, int NB, double scale, int chunk_tokens) {
+    int G = Hq / Hkv, h = qh / G;
+    if (scale <= 0.0) scale = 1.0 / sqrt((double)D);
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    if (L == 0) return OR_OK;
+    if (chunk_tokens <= 0) return OR_INVALID_ARG;
+    double* K = (double*)malloc(sizeof(double) * (size_t)L * D);
+    double* V = (double*)malloc(sizeof(double) * (size_t)L * D);
+    double* qv = (double*)malloc(sizeof(double) * (size_t)D);
+    double* oc = (double*)malloc(sizeof(double) * (size_t)D);
+    int nchunks = (L + chunk_tokens - 1) / chunk_tokens;
+    double* mc = (double*)malloc(sizeof(double) * nchunks);
+    double* lc = (double*)malloc(sizeof(double) * nchunks);
+    double* occ = (double*)malloc(sizeof(double) * (size_t)nchunks * D);
+    int st = oracle_gather(k_cache, block_tables, max_blocks, b, L, h, Hkv, D, BS, NB, dtype, K);
+    if (st == OR_OK) st = oracle_gather(v_cache, block_tables, max_blocks, b, L, h, Hkv, D, BS, NB, dtype, V);
+    if (st == OR_OK) {
+        for (int d = 0; d < D; ++d) qv[d] = load_elem(q, ((size_t)b * Hq + qh) * D + d, dtype);
+        for (int c = 0; c < nchunks; ++c) {
+            int j0 = c * chunk_tokens, j1 = j0 + chunk_tokens < L ? j0 + chunk_tokens : L;
+            double m = -INFINITY;
+            for (int j = j0; j < j1; ++j) {
+                double acc = 0.0;
+                for (int d = 0; d < D; ++d) acc += qv[d] * K[(size_t)j * D + d];
+                acc *= scale;
+                if (acc > m) m = acc;
+            }
+            double l = 0.0;
+            for (int d = 0; d < D; ++d) oc[d] = 0.0;
+            for (int j = j0; j < j1; ++j) {
+                double acc = 0.0;
+                for (int d = 0; d < D; ++d) acc += qv[d] * K[(size_t)j * D + d];
+                double e = exp(acc * scale - m);
+                l += e;
+                for (int d = 0; d < D; ++d) oc[d] += e * V[(size_t)j * D + d];
+            }
+            mc[c] = m; lc[c] = l;
+            for (int d = 0; d < D; ++d) occ[(size_t)c * D + d] = oc[d];
+        }
+        double M = -INFINITY;
+        for (int c = 0; c < nchunks; ++c) if (mc[c] > M) M = mc[c];
+        double Ls = 0.0;
+        for (int c = 0; c < nchunks; ++c) Ls += lc[c] * exp(mc[c] - M);
+        for (int d = 0; d < D; ++d) {
+            double acc = 0.0;
+            for (int c = 0; c < nchunks; ++c) acc += occ[(size_t)c * D + d] * exp(mc[c] - M);
+            out[d] = acc / Ls;
+        }
+    }
+    free(K); free(V); free(qv); free(oc); free(mc); free(lc); free(occ);
+    return st;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Sampler. */
+
+typedef struct {
+    float z;
+    int32_t id;
+} zid_t;
+
+/* Sort key ([SERVE] 3.1 top-k row): descending logit, then ascending token id.
+ * Compared as doubles, so -0.0 and +0.0 are equal and fall back to the id. */
+static int cmp_zid(const void* a, const void* b) {
+    const zid_t* x = (const zid_t*)a;
+    const zid_t* y = (const zid_t*)b;
+    double zx = (double)x->z, zy = (double)y->z;
+    if (zx > zy) return -1;
+    if (zx < zy) return 1;
+    return (x->id < y->id) ? -1 : (x->id > y->id ? 1 : 0);
+}
+
+/* One row of the logits -> token step.
+ *   T == 0      greedy branch: argmax, lowest index among ties ([SERVE] 3.1).
+ *   T > 0       p_i = exp((z_i - z_max)/T) over finite logits ([CH5] 1.2 eq.
+ *               for p_i(T), max subtracted as in [LAB] block [8] softmax);
+ *               top-k keeps the first k of the (-z, id) order when 0 < k < |E|
+ *               (E = finite logits; -inf entries are banned tokens, [SERVE] 3.3);
+ *               renormalise over the top-k set ([LAB] block [8]);
+ *               top-p (p < 1) keeps the smallest sorted prefix whose cumulative
+ *               renormalised probability is >= p, boundary token included
+ *               ([CH5] 1.2 set V^(p); [SERVE] 3.1 top-p row);
+ *               renormalise over the nucleus ([CH5] 1.2 p~);
+ *               draw: walk the kept tokens in token-id order and return the
+ *               first whose running CDF exceeds u ([LAB] block [8] draws over
+ *               VOCAB order; u from the request's own Philox stream).
+ * Errors: a NaN or +inf logit, or no finite logit -> OR_NONFINITE;
+ * T < 0 / NaN or p <= 0 / NaN -> OR_INVALID_ARG; token = -1 then.
+ * Diagnostics: draw_margin = distance from u to the nearer CDF edge of the
+ * chosen token; cut_margin = distance from p to the nearer of the two
+ * cumulative sums that bracket the top-p cut (1.0 when top-p is off);
+ * n_kept = size of the final support; probs (optional, length V) = final
+ * renormalised distribution in token-id order. */
+int oracle_sample_row(const float* z, int V, float temperature, int top_k, float top_p,
+                      uint64_t seed, uint64_t offset, int32_t* token, double* draw_margin,
+                      double* cut_margin, int32_t* n_kept, double* probs) {
+    *token = -1;
+    *draw_margin = 0.0;
+    *cut_margin = 1.0;
+    *n_kept = 0;
+    if (probs) for (int i = 0; i < V; ++i) probs[i] = 0.0;
+    int n_fin = 0;
+    for (int i = 0; i < V; ++i) {
+        if (isnan(z[i]) || (isinf(z[i]) && z[i] > 0)) return OR_NONFINITE;
+        if (isfinite(z[i])) ++n_fin;
+    }
+    if (n_fin == 0) return OR_NONFINITE;
+    if (!(temperature >= 0.0f)) return OR_INVALID_ARG; /* negative or NaN */
+    if (temperature == 0.0f) {
+        int best = -1;
+        for (int i = 0; i < V; ++i)
+            if (isfinite(z[i]) && (best < 0 || z[i] > z[best])) best = i;
+        *token = best;
+        *n_kept = 1;
+        *draw_margin = 1.0;
+        if (probs) probs[best] = 1.0;
+        return OR_OK;
+    }
+    if (!(top_p > 0.0f)) return OR_INVALID_ARG; /* p <= 0 or NaN */
+
+    zid_t* ord = (zid_t*)malloc(sizeof(zid_t) * (size_t)n_fin);
+    int n = 0;
+    for (int i = 0; i < V; ++i)
+        if (isfinite(z[i])) { ord[n].z = z[i]; ord[n].id = i; ++n; }
+    qsort(ord, (size_t)n, sizeof(zid_t), cmp_zid);
+
+    /* top-k */
+    if (top_k > 0 && top_k < n) n = top_k;
+
+    /* temperature softmax over the top-k set, renormalised */
+    double T = (double)temperature;
+    double zmax = (double)ord[0].z;
+    double* q = (double*)malloc(sizeof(double) * (size_t)n);
+    double S = 0.0;
+    for (int j = 0; j < n; ++j) { q[j] = exp(((double)ord[j].z - zmax) / T); S += q[j]; }
+    for (int j = 0; j < n; ++j) q[j] /= S;
+
+    /* top-p: smallest prefix with cumulative >= p */
+    int m = n;
+    if (top_p < 1.0f) {
+        double p = (double)top_p;
+        double cum = 0.0, prev = 0.0;
+        for (int j = 0; j < n; ++j) {
+            prev = cum;
+            cum += q[j];
+            if (cum >= p) { m = j + 1; break; }
+        }
+        double d1 = fabs(cum - p), d0 = fabs(prev - p);
+        *cut_margin = d1 < d0 ? d1 : d0;
+    }
+
+    /* renormalise over the nucleus; draw in token-id order */
+    double Sp = 0.0;
+    for (int j = 0; j < m; ++j) Sp += q[j];
+    double* pi = (double*)calloc((size_t)V, sizeof(double));
+    unsigned char* kept = (unsigned char*)calloc((size_t)V, 1);
+    for (int j = 0; j < m; ++j) { pi[ord[j].id] = q[j] / Sp; kept[ord[j].id] = 1; }
+    double u = oracle_uniform(seed, offset);
+    double c = 0.0, cprev = 0.0;
+    int tok = -1, last = -1;
+    for (int i = 0; i < V; ++i) {
+        if (!kept[i]) continue;
+        last = i;
+        cprev = c;
+        c += pi[i];
+        if (c > u) { tok = i; break; }
+    }
+    if (tok < 0) { tok = last; *draw_margin = 0.0; }
+    else {
+        double a = u - cprev, bnd = c - u;
+        *draw_margin = a < bnd ? a : bnd;
+    }
+    *token = tok;
+    *n_kept = m;
+    if (probs) for (int i = 0; i < V; ++i) probs[i] = pi[i];
+    free(ord); free(q); free(pi); free(kept);
+    return OR_OK;
+}
+
+/* Batched sampler over B rows of logits [B, V] (rows independent).  Per-row
+ * status goes to status_out (may be NULL); returns the first non-zero status. */
+int oracle_sample_batch(const float* logits, int B, int V, const float* temperature,
+                        const int32_t* top_k, const float* top_p, const uint64_t* seeds,
+                        const uint64_t* offsets, int32_t* tokens, double* draw_margin,
+                        double* cut_margin, int32_t* n_kept, int32_t* status_out) {
+    int status = OR_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        int st = oracle_sample_row(logits + (size_t)b * V, V, temperature[b], top_k[b], top_p[b],
+                                   seeds[b], offsets[b], tokens + b, draw_margin + b,
+                                   cut_margin + b, n_kept + b, NULL);
+        if (status_out) status_out[b] = st;
+        if (st != OR_OK) {
+#pragma omp atomic write
+            status = st;
+        }
+    }
+    return status;
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
