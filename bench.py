@@ -1,0 +1,417 @@
+"""Benchmark of one batched paged-KV decode step on GB300.
+
+A step = kv_append (new K/V token per sequence) -> paged_decode_attention
+(plan, split-KV main kernel, combine) -> sample_tokens, over one batch of the
+Llama-style GQA workload: batch 64, 32 query / 8 KV heads, head_dim 128,
+block_size 16, lengths uniform in [512, 4096], shuffled block tables, bf16 KV,
+logits over a 128256-token vocabulary (T = 0.7, top_k = 50, top_p = 0.9).
+
+Printed (one JSON line, rank 0):
+  value          algorithmic HBM bytes of the whole step / device step time (GB/s)
+  sampled_tokens_per_s   batch / device step time
+  roofline       paged_decode_attention's achieved GB/s (CUDA events around each
+                 launch inside the timed region) against the measured copy peak
+  e2e            the same metric with host buffers: pinned H2D of the step's inputs,
+                 the three calls, D2H of the sampled tokens
+  cpu_baseline   the float64 oracle on this host's cores on a bounded sample
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from paged_kv_decode_table_gb300 import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention KV GB/s (% of HBM peak); sampled tokens/sec"
+WORKLOAD = 2
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def _source_hash():
+    h = hashlib.sha256()
+    for rel in ("paged_kv_decode_table_gb300/csrc/decode_attention.cu",
+                "paged_kv_decode_table_gb300/csrc/pkv_common.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_per_launch():
+    """DRAM bytes per attention call from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "decode_attention_gqa_b64_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    kv = {}
+    with open(p) as f:
+        for line in f:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+    if kv.get("source_sha256_16") != _source_hash():
+        return None
+    try:
+        return int(float(kv["traffic_bytes_per_call"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="pkv_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 8:
+                    rows.append(parts)
+        os.unlink(self.path)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        sm, smax = [], None
+        for r in rows:
+            try:
+                sm.append(float(r[0]))
+                smax = float(r[1])
+            except ValueError:
+                continue
+            for i, n in enumerate(names):
+                if r[4 + i].lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    n = int(os.environ.get("WORLD_SIZE", "1"))
+    if n > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return n, rank, local
+
+
+def _max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _sum_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t)
+    return float(t.item())
+
+
+def _barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def _config(w, inp, extra=None):
+    sl = inp["seq_lens"]
+    cfg = {
+        "workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
+        "head_dim": w.head_dim, "block_size": w.block_size, "seq_len_range": [w.len_lo, w.len_hi],
+        "total_tokens": int(sl.to(torch.int64).sum()), "num_blocks": inp["num_blocks"], "vocab": w.vocab,
+        "sampler": {"temperature": w.temperature, "top_k": w.top_k, "top_p": w.top_p},
+        "kv_dtype": "bf16", "logits_dtype": "f32",
+        "step": "kv_append -> paged_decode_attention (plan, main, combine) -> sample_tokens",
+    }
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ---------------------------------------------------------------- oracle baseline
+def _oracle_sample_step(w, host_inp, n_seq: int, n_rows: int):
+    """One bounded oracle step: append for every sequence, attention for the
+    first n_seq sequences (all heads), sampler for the first n_rows rows.
+    Returns (seconds, algorithmic bytes processed)."""
+    import numpy as np
+    import oracle
+    h = host_inp
+    t0 = time.perf_counter()
+    K, V = h["k_cache"], h["v_cache"]
+    oracle.kv_append(h["k_new"], h["v_new"], K, V, h["block_tables"], h["seq_lens"], w.block_size)
+    rows = np.arange(n_seq * w.n_q_heads, dtype=np.int64)
+    oracle.paged_attention(h["q"], K, V, h["block_tables"], h["seq_lens"], rows=rows)
+    oracle.sample_batch(h["logits"][:n_rows], h["temperature"][:n_rows], h["top_k"][:n_rows],
+                        h["top_p"][:n_rows], h["seeds"][:n_rows], h["offsets"][:n_rows])
+    dt = time.perf_counter() - t0
+    sl = h["seq_lens"][:n_seq].astype(np.int64)
+    e = w.elem_bytes
+    attn = int(sl.sum()) * w.n_kv_heads * w.head_dim * 2 * e + 2 * n_seq * w.n_q_heads * w.head_dim * e \
+        + 4 * int(((sl + w.block_size - 1) // w.block_size).sum()) + 4 * n_seq
+    append = 2 * (2 * w.batch * w.n_kv_heads * w.head_dim * e) + 8 * w.batch
+    samp = 4 * n_rows * w.vocab + n_rows * 32 + 4 * n_rows
+    return dt, attn + append + samp
+
+
+def _host_copy(inp):
+    import numpy as np
+    out = {}
+    for k, v in inp.items():
+        if not isinstance(v, torch.Tensor):
+            out[k] = v
+            continue
+        t = v.detach().contiguous().cpu()
+        if t.dtype == torch.bfloat16:
+            out[k] = t.view(torch.int16).numpy().view(np.uint16).copy()
+        elif k in ("seeds", "offsets"):
+            out[k] = t.numpy().view(np.uint64).copy()
+        else:
+            out[k] = t.numpy().copy()
+    return out
+
+
+def cpu_baseline(w, inp, budget_s: float = 12.0):
+    import oracle
+    oracle.build()
+    h = _host_copy(inp)
+    n_seq, n_rows = 2, 2
+    dt, by = _oracle_sample_step(w, h, n_seq, n_rows)       # also warms the library
+    # grow the sample to roughly fill the time budget
+    scale = max(1.0, min(w.batch / n_seq, budget_s / max(dt, 1e-3)))
+    n_seq = int(min(w.batch, max(1, n_seq * scale)))
+    n_rows = int(min(w.batch, max(1, n_rows * scale)))
+    dt, by = _oracle_sample_step(w, h, n_seq, n_rows)
+    return {"value": by / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"append of all {w.batch} sequences + attention of {n_seq} sequences x {w.n_q_heads} "
+                      f"heads + sampler on {n_rows} rows, float64 C oracle, {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    w = W.workload(WORKLOAD)
+    inp = W.make_decode_inputs(w, "cpu")
+    h = _host_copy(inp)
+    # each step: a bounded sample sized so that warmup + steps stay within ~2 minutes
+    dt1, _ = _oracle_sample_step(w, h, 1, 1)
+    per_step_budget = max(0.02, 120.0 / max(1, args.steps + args.warmup))
+    n = max(1, min(w.batch, int(per_step_budget / max(dt1, 1e-4))))
+    for _ in range(args.warmup):
+        _oracle_sample_step(w, h, n, n)
+    tot_t, tot_b = 0.0, 0
+    for _ in range(args.steps):
+        dt, by = _oracle_sample_step(w, h, n, n)
+        tot_t += dt
+        tot_b += by
+    val = tot_b / tot_t / 1e9
+    cb = {"value": val, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+          "sample": f"per step: append of all {w.batch} sequences + attention of {n} sequences x "
+                    f"{w.n_q_heads} heads + sampler on {n} rows (float64 C oracle)"}
+    line = {"metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": tot_t / max(1, args.steps) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": _config(w, inp, {"impl_note": "float64 CPU oracle on a bounded sample per step"}),
+            "impl": "reference", "cpu_baseline": cb,
+            "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_gpu(args):
+    import paged_kv_decode_table_gb300 as pkv
+    from paged_kv_decode_table_gb300 import build as pkv_build
+    world, rank, local = _dist()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pkv_build.build()
+    pkv.load_library()
+    w = W.workload(WORKLOAD)
+    inp = W.make_decode_inputs(w, dev)
+    B = w.batch
+    bytes_step = W.step_bytes(w, inp["seq_lens"])
+    out = torch.empty_like(inp["q"])
+    tokens = torch.empty(B, dtype=torch.int32, device=dev)
+    ws = torch.empty(pkv.decode_workspace_bytes(B, w.n_q_heads, w.head_dim), dtype=torch.uint8, device=dev)
+    status = pkv.new_status(dev)
+    k_cache, v_cache = inp["k_cache"], inp["v_cache"]
+
+    def step(q, k_new, v_new, bt, sl, logits, temp, tk, tp, seeds, offs):
+        pkv.kv_append(k_new, v_new, k_cache, v_cache, bt, sl, status=status)
+        pkv.paged_decode_attention(q, k_cache, v_cache, bt, sl, out=out, workspace=ws, status=status)
+        pkv.sample_tokens(logits, temp, tk, tp, seeds, offs, tokens=tokens, status=status)
+
+    dev_args = (inp["q"], inp["k_new"], inp["v_new"], inp["block_tables"], inp["seq_lens"], inp["logits"],
+                inp["temperature"], inp["top_k"], inp["top_p"], inp["seeds"], inp["offsets"])
+    for _ in range(max(3, args.warmup)):
+        step(*dev_args)
+    torch.cuda.synchronize()
+    if pkv.check_status(status) != 0:
+        raise SystemExit(f"device status {pkv.status_string(pkv.check_status(status))} during warm-up")
+
+    stream = torch.cuda.current_stream(dev)
+    a0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    a1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    _barrier(world)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(args.steps):
+        pkv.kv_append(inp["k_new"], inp["v_new"], k_cache, v_cache, inp["block_tables"], inp["seq_lens"],
+                      status=status)
+        a0[i].record(stream)
+        pkv.paged_decode_attention(inp["q"], k_cache, v_cache, inp["block_tables"], inp["seq_lens"], out=out,
+                                   workspace=ws, status=status)
+        a1[i].record(stream)
+        pkv.sample_tokens(inp["logits"], inp["temperature"], inp["top_k"], inp["top_p"], inp["seeds"],
+                          inp["offsets"], tokens=tokens, status=status)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    _barrier(world)
+    clk = clocks.stop()
+    ms_local = t0.elapsed_time(t1) / args.steps
+    ms = _max_over_ranks(ms_local, world, dev)
+    attn_ms = sum(a0[i].elapsed_time(a1[i]) for i in range(args.steps)) / args.steps
+    if pkv.check_status(status) != 0:
+        raise SystemExit(f"device status {pkv.status_string(pkv.check_status(status))} in the timed region")
+
+    # end to end through the public API with host buffers (pinned), per step:
+    # H2D of the step inputs, the three calls, D2H of the tokens
+    host_in = {k: v.cpu().pin_memory() for k, v in inp.items()
+               if isinstance(v, torch.Tensor) and k not in ("k_cache", "v_cache")}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    tok_host = torch.empty(B, dtype=torch.int32).pin_memory()
+    dbuf = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+    e2e_steps = max(10, min(args.steps, 200))
+
+    def e2e_step():
+        for k, t in host_in.items():
+            dbuf[k].copy_(t, non_blocking=True)
+        step(dbuf["q"], dbuf["k_new"], dbuf["v_new"], dbuf["block_tables"], dbuf["seq_lens"], dbuf["logits"],
+             dbuf["temperature"], dbuf["top_k"], dbuf["top_p"], dbuf["seeds"], dbuf["offsets"])
+        tok_host.copy_(tokens, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    _barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = _max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+
+    total_bytes = _sum_over_ranks(float(bytes_step["total"]), world, dev)
+    value = total_bytes / (ms * 1e-3) / 1e9
+    peak, peak_kind = _peaks()
+    attn_gbs = bytes_step["attention"] / (attn_ms * 1e-3) / 1e9
+    traffic = _traffic_per_launch()
+    fast = True  # bf16, D=128, BS=16, Hkv=8: TMA/mma path -> plan + main + combine
+    launches = args.steps * (1 + (3 if fast else 1) + 1)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": _config(w, inp, {
+            "l2": f"no flush: every step reads {bytes_step['total'] / 1e6:.0f} MB (> 126 MB L2)",
+            "parallelism": f"dp{world} (independent sequence shards, no collective)",
+            "bytes_per_step": bytes_step}),
+        "sampled_tokens_per_s": B * world / (ms * 1e-3),
+        "pct_of_8TBps": value / 8000.0 * 100.0,
+        "pct_of_measured_peak": value / peak * 100.0,
+        "roofline": {"kernel": "paged_decode_attention (plan + split-KV main + combine), per call",
+                     "bound": "hbm", "achieved": attn_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": attn_gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "traffic": traffic, "algorithmic_bytes_per_call": bytes_step["attention"],
+                     "ms_per_call": attn_ms},
+        "e2e": {"value": total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": B * 4},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, inp)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

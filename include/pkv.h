@@ -1,0 +1,160 @@
+/*
+ * pkv.h -- C ABI of the paged-KV decode step for GB300 (sm_103a).
+ *
+ * One batched decode iteration over a paged KV cache, in three calls:
+ *   pkv_kv_append               write each sequence's new K/V token into its
+ *                               physical block through the block table;
+ *   pkv_paged_decode_attention  GQA decode attention for one query token per
+ *                               sequence over all cached K/V (split-KV inside);
+ *   pkv_sample_tokens           temperature -> top-k -> renormalise -> top-p ->
+ *                               renormalise -> seeded per-request draw.
+ *
+ * Conventions shared by every call
+ *  - Every pointer argument is a DEVICE pointer unless stated otherwise.  The
+ *    caller allocates and owns every buffer; the library allocates nothing,
+ *    keeps no per-call state and never synchronises the stream.  All work is
+ *    enqueued on `stream` (a cudaStream_t passed as void*; NULL = legacy
+ *    default stream) in call order.
+ *  - Host-detectable errors (null pointers, unsupported shapes, undersized
+ *    workspace, misaligned pointers) return before anything is launched.
+ *    B == 0 is a no-op returning PKV_OK.
+ *  - Data-dependent problems found on the device (a block id outside
+ *    [0, num_blocks), a sequence length outside the table, a NaN/+inf logit, an
+ *    all -inf row, T < 0, top_p <= 0) never trap: the kernel records the first
+ *    such code into *dev_status with an atomic compare-and-swap from 0, writes
+ *    a defined value for the affected unit (zeros for attention rows, token -1
+ *    for sampler rows) and carries on.  dev_status may be NULL to skip the
+ *    report.  Read it after the stream has synchronised.
+ *  - Layouts are row-major and dense:
+ *      KV pools   k_cache, v_cache : [num_blocks, Hkv, block_size, D]
+ *      new K/V    k_new, v_new     : [B, Hkv, D]
+ *      queries    q                : [B, Hq, D]      output out: [B, Hq, D]
+ *      tables     block_tables     : int32 [B, max_blocks_per_seq]
+ *      lengths    seq_lens         : int32 [B], length AFTER this step's append
+ *      logits                      : float32 [B, V]
+ *
+ * Sources (web pages, cited by title and section):
+ *  [LAB]   "Bai Lab tong hop -- Inference Engineering", block [6] KV state
+ *          manager (KVPool.write / gather), block [5] forward, block [8] sample.
+ *  [CH5]   "Suy luan & Toi uu hoa (Inference)", chapter 5: 1.2 temperature /
+ *          top-k / nucleus set and renormalisation; 3.1 GQA; 3.2 PagedAttention
+ *          block table; 4.1 online softmax.
+ *  [SERVE] "LLM inference serving tutorial": 3.1 sampler definitions and tie
+ *          rules; 1.6 per-request RNG streams; appendix A [D01]/[D02].
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,   /* host: bad pointer/shape/size; device: T < 0 or top_p <= 0 */
+    PKV_ERR_UNSUPPORTED = 2,   /* host: a shape this build has no kernel for */
+    PKV_ERR_CUDA = 3,          /* host: a CUDA runtime call or launch failed */
+    PKV_ERR_DEVICE_BOUNDS = 4, /* device: block id or sequence length out of range */
+    PKV_ERR_TIMEOUT = 5,       /* device: a bounded wait ran out (kernel returned early) */
+    PKV_ERR_NONFINITE = 6      /* device: NaN / +inf logit, or no finite logit in a row */
+} pkv_status;
+
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* Human-readable name of a status code (static string; never NULL). */
+const char* pkv_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int pkv_version(void);
+
+/*
+ * KV append ([LAB] block [6] KVPool.write; [CH5] 3.2).
+ * For every sequence b and KV head h: pos = seq_lens[b] - 1,
+ * blk = block_tables[b][pos / block_size], slot = pos % block_size, and
+ *   k_cache[blk][h][slot][:] = k_new[b][h][:],  v_cache[...] = v_new[b][h][:].
+ * Bit copy (no arithmetic).  A sequence needs 1 <= seq_lens[b] <=
+ * max_blocks_per_seq * block_size and a block id in [0, num_blocks); otherwise
+ * it is skipped and PKV_ERR_DEVICE_BOUNDS is recorded.  Two sequences that map
+ * the same slot race (the caller's tables must not alias a written slot).
+ * dtype: element type of k_new/v_new/k_cache/v_cache.
+ */
+pkv_status pkv_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                         const int32_t* block_tables, int max_blocks_per_seq,
+                         const int32_t* seq_lens, int B, int Hkv, int D, int block_size,
+                         int num_blocks, pkv_dtype dtype, int32_t* dev_status, void* stream);
+
+/*
+ * Workspace bytes pkv_paged_decode_attention needs for batch B, Hq query heads
+ * and head dim D on a device with num_sms SMs (num_sms <= 0: the current
+ * device).  The workspace holds the split-KV schedule and the per-split partial
+ * results (max, sum, output) merged by the combine kernel.  Returns 0 on error.
+ * Pure host arithmetic when num_sms > 0.
+ */
+size_t pkv_decode_workspace_bytes(int B, int Hq, int D, int num_sms);
+
+/*
+ * GQA paged decode attention, one query token per sequence ([LAB] block [5];
+ * [CH5] 3.1, 3.2, 4.1).  For query head qh of sequence b, with KV head
+ * h = qh / (Hq / Hkv) and L = seq_lens[b]:
+ *   s_j = scale * <q[b][qh], K_j>  for j < L, K_j/V_j read through the table;
+ *   out[b][qh] = sum_j softmax(s)_j V_j        (L == 0 gives zeros).
+ * scale <= 0 selects 1/sqrt(D).  Accumulation is float32; the result is written
+ * in `dtype`.  Long sequences are cut into balanced chunks across all SMs and
+ * merged with the online-softmax rule; `workspace` (device, >=
+ * pkv_decode_workspace_bytes(B, Hq, D, 0) bytes, 16-byte aligned, contents
+ * ignored on entry) holds the partials.  Requires Hq % Hkv == 0 and
+ * 1 <= D <= 256; the fast path (bf16, D = 128, block_size % 16 == 0,
+ * Hkv in {1, 2, 4, 8}, Hq/Hkv <= 16, Hkv * block_size <= 128, 16-byte aligned
+ * pools) uses TMA and tensor-core MMA; other shapes use a generic CUDA-core
+ * kernel.  Sequences with a length outside [0, max_blocks_per_seq*block_size]
+ * or a block id outside [0, num_blocks) get zero output and
+ * PKV_ERR_DEVICE_BOUNDS.  The KV slots past L in a sequence's last block are
+ * never used (their contents may be anything, NaN included).
+ */
+pkv_status pkv_paged_decode_attention(void* out, const void* q, const void* k_cache,
+                                      const void* v_cache, const int32_t* block_tables,
+                                      int max_blocks_per_seq, const int32_t* seq_lens, int B,
+                                      int Hq, int Hkv, int D, int block_size, int num_blocks,
+                                      float scale, pkv_dtype dtype, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * Workspace bytes pkv_sample_tokens needs (B rows of V logits).  The current
+ * sampler keeps each row on chip and needs none: returns 0.
+ */
+size_t pkv_sample_workspace_bytes(int B, int V);
+
+/*
+ * Logits -> token, one row per request ([CH5] 1.2; [LAB] block [8];
+ * [SERVE] 3.1, 1.6).  Per row b with z = logits[b]:
+ *   temperature[b] == 0 : greedy, argmax of z, lowest id among ties.
+ *   temperature[b] >  0 : p_i = exp((z_i - max z) / T) over finite z_i (a -inf
+ *     logit is a banned token); if 0 < top_k[b] < #finite keep the top_k
+ *     largest under the order (z descending, token id ascending); renormalise;
+ *     if top_p[b] < 1 keep the smallest prefix of that order whose cumulative
+ *     probability is >= top_p[b] (boundary token kept); renormalise; draw
+ *     u = Philox4x64-10(key = (seeds[b], 0), counter = (offsets[b], 0, 0, 0))
+ *     word 0, top 53 bits * 2^-53, and return the first kept token, walking
+ *     token ids in ascending order, whose running probability exceeds u.
+ * temperature, top_p: float32 [B]; top_k: int32 [B] (<= 0 or >= V: off);
+ * seeds, offsets: uint64 [B]; tokens: int32 [B] output.  Errors per row (token
+ * -1): NaN or +inf logit / no finite logit -> PKV_ERR_NONFINITE; T < 0 (or NaN)
+ * or top_p <= 0 (or NaN) -> PKV_ERR_INVALID_ARG.  Exponentials are float32 and
+ * the probability masses are accumulated exactly in 64-bit fixed point, so a
+ * draw can differ from a float64 evaluation only when u falls within ~1e-6 of a
+ * CDF edge (or the top-p cut is within ~1e-6 of p).  Deterministic: the same
+ * inputs give the same tokens on every run.  Requires 1 <= V <= 2^23.
+ */
+pkv_status pkv_sample_tokens(int32_t* tokens, const float* logits, int B, int V,
+                             const float* temperature, const int32_t* top_k, const float* top_p,
+                             const uint64_t* seeds, const uint64_t* offsets, void* workspace,
+                             size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

@@ -1,2 +1,225 @@
-"""Paged-KV decode step for GB300 (sm_103a): KV append, GQA paged decode attention
-with split-KV, and the temperature / top-k / top-p / Philox sampler."""
+"""Paged-KV decode step for GB300 (sm_103a).
+
+Thin ctypes binding over the C ABI in ``include/pkv.h`` (``libpkv.so``, built
+in-tree by ``paged_kv_decode_table_gb300.build``).  Every function here only
+checks and marshals torch tensors (device, dtype, contiguity, shapes) and passes
+raw device pointers plus the current CUDA stream; all arithmetic runs in the
+library's CUDA kernels.  There is no CPU fallback: if the library cannot be
+loaded, every call raises.
+
+Calls (names follow the C ABI):
+  kv_append(k_new, v_new, k_cache, v_cache, block_tables, seq_lens)
+  paged_decode_attention(q, k_cache, v_cache, block_tables, seq_lens, out=None, scale=0.0)
+  sample_tokens(logits, temperature, top_k, top_p, seeds, offsets, tokens=None)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = ["PkvError", "load_library", "library_path", "kv_append", "paged_decode_attention",
+           "decode_workspace_bytes", "sample_tokens", "sample_workspace_bytes", "status_string",
+           "new_status", "check_status", "STATUS"]
+
+STATUS = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED", 3: "PKV_ERR_CUDA",
+          4: "PKV_ERR_DEVICE_BOUNDS", 5: "PKV_ERR_TIMEOUT", 6: "PKV_ERR_NONFINITE"}
+PKV_F32, PKV_BF16 = 0, 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libpkv.so")
+_lib = None
+_lock = threading.Lock()
+_ws_cache: dict = {}
+
+
+class PkvError(RuntimeError):
+    def __init__(self, call: str, code: int):
+        super().__init__(f"{call} failed: {STATUS.get(code, code)} ({code})")
+        self.code = code
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libpkv.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is missing: run paged_kv_decode_table_gb300.build.build() first")
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.pkv_status_string.argtypes = [i32]
+        lib.pkv_status_string.restype = ctypes.c_char_p
+        lib.pkv_version.argtypes = []
+        lib.pkv_version.restype = i32
+        lib.pkv_kv_append.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, P, P]
+        lib.pkv_kv_append.restype = i32
+        lib.pkv_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
+        lib.pkv_decode_workspace_bytes.restype = sz
+        lib.pkv_paged_decode_attention.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, f32,
+                                                   i32, P, sz, P, P]
+        lib.pkv_paged_decode_attention.restype = i32
+        lib.pkv_sample_workspace_bytes.argtypes = [i32, i32]
+        lib.pkv_sample_workspace_bytes.restype = sz
+        lib.pkv_sample_tokens.argtypes = [P, P, i32, i32, P, P, P, P, P, P, sz, P, P]
+        lib.pkv_sample_tokens.restype = i32
+        _lib = lib
+        return lib
+
+
+def status_string(code: int) -> str:
+    return load_library().pkv_status_string(int(code)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check_cuda(name: str, t: torch.Tensor, dtype=None, shape=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return PKV_F32
+    if t.dtype == torch.bfloat16:
+        return PKV_BF16
+    raise TypeError(f"unsupported element type {t.dtype} (float32 or bfloat16)")
+
+
+def _raise(name, code):
+    if code != 0:
+        raise PkvError(name, code)
+
+
+def new_status(device="cuda") -> torch.Tensor:
+    """A zeroed device status word to pass as `status=`."""
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def check_status(status: torch.Tensor) -> int:
+    """Read a device status word (synchronises); returns the code."""
+    return int(status.item())
+
+
+def kv_append(k_new, v_new, k_cache, v_cache, block_tables, seq_lens, status=None):
+    """Write k_new/v_new [B, Hkv, D] at position seq_lens[b]-1 of each sequence."""
+    NB, Hkv, BS, D = k_cache.shape
+    B = seq_lens.shape[0]
+    dev = k_cache.device
+    _check_cuda("k_cache", k_cache)
+    _check_cuda("v_cache", v_cache, k_cache.dtype, k_cache.shape, dev)
+    _check_cuda("k_new", k_new, k_cache.dtype, (B, Hkv, D), dev)
+    _check_cuda("v_new", v_new, k_cache.dtype, (B, Hkv, D), dev)
+    _check_cuda("block_tables", block_tables, torch.int32, device=dev)
+    _check_cuda("seq_lens", seq_lens, torch.int32, (B,), dev)
+    if block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise ValueError("block_tables must be [B, max_blocks_per_seq]")
+    if status is not None:
+        _check_cuda("status", status, torch.int32, (1,), dev)
+    code = load_library().pkv_kv_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                        _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B,
+                                        Hkv, D, BS, NB, _dtype_code(k_cache), _ptr(status),
+                                        _stream(dev))
+    _raise("pkv_kv_append", code)
+
+
+def decode_workspace_bytes(B: int, Hq: int, D: int, num_sms: int = 0) -> int:
+    return int(load_library().pkv_decode_workspace_bytes(B, Hq, D, num_sms))
+
+
+def _workspace(dev, nbytes: int) -> torch.Tensor:
+    key = (dev, nbytes)
+    ws = _ws_cache.get(key)
+    if ws is None:
+        ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+        _ws_cache.clear()
+        _ws_cache[key] = ws
+    return ws
+
+
+def paged_decode_attention(q, k_cache, v_cache, block_tables, seq_lens, out=None, scale: float = 0.0,
+                           workspace=None, status=None):
+    """GQA decode attention over the paged cache; returns out [B, Hq, D]."""
+    B, Hq, D = q.shape
+    NB, Hkv, BS, D2 = k_cache.shape
+    dev = q.device
+    if D2 != D:
+        raise ValueError("head_dim of q and the cache differ")
+    _check_cuda("q", q)
+    _check_cuda("k_cache", k_cache, q.dtype, device=dev)
+    _check_cuda("v_cache", v_cache, q.dtype, k_cache.shape, dev)
+    _check_cuda("block_tables", block_tables, torch.int32, device=dev)
+    _check_cuda("seq_lens", seq_lens, torch.int32, (B,), dev)
+    if block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise ValueError("block_tables must be [B, max_blocks_per_seq]")
+    if out is None:
+        out = torch.empty_like(q)
+    _check_cuda("out", out, q.dtype, q.shape, dev)
+    lib = load_library()
+    need = int(lib.pkv_decode_workspace_bytes(B, Hq, D, 0))
+    if workspace is None:
+        with torch.cuda.device(dev):
+            workspace = _workspace(dev, need)
+    _check_cuda("workspace", workspace, device=dev)
+    if status is not None:
+        _check_cuda("status", status, torch.int32, (1,), dev)
+    code = lib.pkv_paged_decode_attention(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                          _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
+                                          B, Hq, Hkv, D, BS, NB, float(scale), _dtype_code(q),
+                                          _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                          _ptr(status), _stream(dev))
+    _raise("pkv_paged_decode_attention", code)
+    return out
+
+
+def sample_workspace_bytes(B: int, V: int) -> int:
+    return int(load_library().pkv_sample_workspace_bytes(B, V))
+
+
+def sample_tokens(logits, temperature, top_k, top_p, seeds, offsets, tokens=None, status=None):
+    """One token per row of logits [B, V] (float32); returns tokens [B] int32.
+
+    seeds / offsets are int64 tensors holding uint64 bit patterns."""
+    B, V = logits.shape
+    dev = logits.device
+    _check_cuda("logits", logits, torch.float32)
+    _check_cuda("temperature", temperature, torch.float32, (B,), dev)
+    _check_cuda("top_k", top_k, torch.int32, (B,), dev)
+    _check_cuda("top_p", top_p, torch.float32, (B,), dev)
+    if seeds.dtype not in (torch.int64, torch.uint64) or offsets.dtype not in (torch.int64, torch.uint64):
+        raise TypeError("seeds and offsets must be 64-bit integer tensors")
+    _check_cuda("seeds", seeds, shape=(B,), device=dev)
+    _check_cuda("offsets", offsets, shape=(B,), device=dev)
+    if tokens is None:
+        tokens = torch.empty(B, dtype=torch.int32, device=dev)
+    _check_cuda("tokens", tokens, torch.int32, (B,), dev)
+    if status is not None:
+        _check_cuda("status", status, torch.int32, (1,), dev)
+    code = load_library().pkv_sample_tokens(_ptr(tokens), _ptr(logits), B, V, _ptr(temperature),
+                                            _ptr(top_k), _ptr(top_p), _ptr(seeds), _ptr(offsets),
+                                            None, 0, _ptr(status), _stream(dev))
+    _raise("pkv_sample_tokens", code)
+    return tokens

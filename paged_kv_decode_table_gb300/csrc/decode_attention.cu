@@ -1,0 +1,765 @@
+// decode_attention.cu -- GQA paged decode attention (one query token per sequence).
+//
+// What it computes ("Bai Lab tong hop -- Inference Engineering", block [5]
+// forward; "Suy luan & Toi uu hoa (Inference)" 3.1 GQA, 3.2 PagedAttention, 4.1
+// online softmax): for query head qh of sequence b, KV head h = qh / G,
+//   out[b][qh] = softmax_j(scale * <q, K_j>) . V_j   over the L = seq_lens[b]
+// cached positions, K_j / V_j read from physical block block_tables[b][j / BS],
+// slot j % BS of the pools [NB, Hkv, BS, D].
+//
+// Fast path (bf16, D = 128, BS % 16 == 0): a persistent, balanced split-KV kernel.
+//  * Work unit = one logical block of one sequence, ALL KV heads: in the
+//    [NB, Hkv, BS, D] layout the K (and V) rows of a block for every head are one
+//    contiguous Hkv*BS*256-byte run, fetched by two 128B-swizzled 2-D TMA boxes.
+//  * The sum over sequences of ceil(L/BS) blocks is cut into P = #SM equal
+//    contiguous ranges (plan kernel); CTA c streams range c through an
+//    nst-deep mbarrier ring fed by one producer lane, so each SM keeps
+//    ~128 KB of KV in flight regardless of how lengths are distributed.
+//  * One consumer warp per KV head computes S = Q K^T and O += P V with
+//    mma.sync m16n8k16 (query heads of the group on the M axis, 16 tokens on N/K),
+//    online softmax in the log2 domain, fp32 accumulation.
+//  * A sequence cut by a range boundary leaves per-piece (max, sum, unnormalised
+//    output) partials in the workspace; the combine kernel merges them with the
+//    online-softmax rule.  Sequences wholly inside one range are written directly.
+// Generic path (fp32, other shapes): one CTA per (sequence, query head),
+// CUDA-core fp32, chunked online softmax.
+#include <cuda.h>
+#include <math.h>
+
+#include "pkv_common.cuh"
+
+namespace pkv {
+
+// ------------------------------------------------------------------ workspace
+struct SeqInfo {       // 32 bytes per sequence
+    int s;             // first global block index of the sequence in the split order
+    int n;             // number of blocks (0 for an empty or invalid sequence)
+    int first;         // index of the CTA whose range holds block s
+    int pieces;        // number of CTA ranges the sequence spans
+    int base;          // first partial slot of the sequence
+    int L;             // length
+    int valid;         // 0 if the length is out of range
+    int pad;
+};
+struct PlanHdr {
+    int total;         // total blocks
+    int W;             // blocks per CTA range
+    int P;             // number of CTA ranges
+    int pad;
+};
+
+struct WsLayout {
+    size_t hdr, info, ml, o, total;
+};
+
+static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+static WsLayout ws_layout(int B, int Hq, int D, int P) {
+    WsLayout w;
+    const size_t slots = static_cast<size_t>(B) + static_cast<size_t>(P);
+    w.hdr = 0;
+    w.info = 256;
+    w.ml = align_up(w.info + sizeof(SeqInfo) * static_cast<size_t>(B), 256);
+    w.o = align_up(w.ml + slots * Hq * 2 * sizeof(float), 256);
+    w.total = align_up(w.o + slots * Hq * static_cast<size_t>(D) * sizeof(float), 256);
+    return w;
+}
+
+size_t decode_workspace_bytes(int B, int Hq, int D, int P) { return ws_layout(B, Hq, D, P).total; }
+
+// ------------------------------------------------------------------ block scan (1024 threads)
+__device__ __forceinline__ int block_excl_scan_1024(int v, int* warp_tot, int& total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int t = warp_tot[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        warp_tot[lane] = t;  // inclusive
+    }
+    __syncthreads();
+    const int before = warp ? warp_tot[warp - 1] : 0;
+    total = warp_tot[31];
+    __syncthreads();
+    return before + x - v;
+}
+
+// ------------------------------------------------------------------ plan kernel
+// Splits the sequence of all (b, logical block) pairs into P equal ranges and
+// records, per sequence, which ranges it spans and where its partials go.
+__global__ void __launch_bounds__(1024)
+    plan_kernel(const int32_t* __restrict__ seq_lens, int B, int max_blocks, int BS, int P,
+                SeqInfo* __restrict__ info, PlanHdr* __restrict__ hdr, int32_t* status) {
+    __shared__ int warp_tot[32];
+    __shared__ int s_carry;
+    if (threadIdx.x == 0) s_carry = 0;
+    __syncthreads();
+    const long long cap = static_cast<long long>(max_blocks) * BS;
+    for (int base = 0; base < B; base += 1024) {
+        const int b = base + threadIdx.x;
+        int n = 0, L = 0, valid = 0;
+        if (b < B) {
+            L = seq_lens[b];
+            valid = (L >= 0 && static_cast<long long>(L) <= cap);
+            if (!valid) report(status, PKV_ERR_DEVICE_BOUNDS);
+            n = valid ? (L + BS - 1) / BS : 0;
+        }
+        int tot;
+        const int ex = block_excl_scan_1024(n, warp_tot, tot);
+        const int carry = s_carry;
+        if (b < B) {
+            info[b].s = carry + ex;
+            info[b].n = n;
+            info[b].L = valid ? L : 0;
+            info[b].valid = valid;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) s_carry = carry + tot;
+        __syncthreads();
+    }
+    const int total = s_carry;
+    const int W = total > 0 ? (total + P - 1) / P : 1;
+    __syncthreads();
+    if (threadIdx.x == 0) s_carry = 0;
+    __syncthreads();
+    for (int base = 0; base < B; base += 1024) {
+        const int b = base + threadIdx.x;
+        int pieces = 0, first = 0;
+        if (b < B) {
+            const int s = info[b].s, n = info[b].n;
+            first = s / W;
+            pieces = n > 0 ? (s + n - 1) / W - first + 1 : 0;
+        }
+        int tot;
+        const int ex = block_excl_scan_1024(pieces, warp_tot, tot);
+        const int carry = s_carry;
+        if (b < B) {
+            info[b].first = first;
+            info[b].pieces = pieces;
+            info[b].base = carry + ex;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) s_carry = carry + tot;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        hdr->total = total;
+        hdr->W = W;
+        hdr->P = P;
+    }
+}
+
+// ------------------------------------------------------------------ fast kernel
+constexpr int kMaxStages = 8;
+constexpr int kDim = 128;
+
+struct StageMeta {
+    int b, j, ntok, flags;
+};
+enum : int { kValid = 1, kFirst = 2, kLast = 4, kWhole = 8 };
+
+// Layout of the dynamic shared memory (base rounded up to 1024 bytes for the
+// 128-byte TMA swizzle): nst stages of [K lo | K hi | V lo | V hi] boxes, each
+// box Hkv*BS rows x 128 bytes; a 2-slot ring of query rows [Hq][128] bf16; the
+// mbarriers; the per-stage metadata.
+static inline size_t fast_smem_bytes(int nst, int stage_bytes, int q_bytes) {
+    return 1024 + static_cast<size_t>(nst) * stage_bytes + 2 * static_cast<size_t>(q_bytes) +
+           (2 * kMaxStages + 4) * sizeof(uint64_t) + kMaxStages * sizeof(StageMeta) + 16;
+}
+
+constexpr int kFastMaxKvHeads = 8;
+
+template <bool kRows16>  // true when G > 8: query rows 8..15 of the MMA tile are live
+__global__ void __launch_bounds__((kFastMaxKvHeads + 1) * 32, 1)
+    decode_attn_fast_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                            const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ out,
+                            const int32_t* __restrict__ block_tables, int max_blocks, int B, int Hq, int Hkv,
+                            int BS, int NB, float scale_log2, int nst, const SeqInfo* __restrict__ info,
+                            const PlanHdr* __restrict__ hdr, float* __restrict__ part_ml,
+                            float* __restrict__ part_o, int32_t* status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int R = Hkv * BS;
+    const uint32_t box_bytes = static_cast<uint32_t>(R) * 128u;
+    const uint32_t stage_bytes = 4u * box_bytes;
+    const uint32_t q_bytes = static_cast<uint32_t>(Hq) * (kDim * 2);
+    uint8_t* stages = smem;
+    uint8_t* qring = smem + static_cast<size_t>(nst) * stage_bytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(qring + 2 * static_cast<size_t>(q_bytes));
+    uint64_t* empty = full + kMaxStages;
+    uint64_t* qfull = empty + kMaxStages;
+    uint64_t* qempty = qfull + 2;
+    StageMeta* meta = reinterpret_cast<StageMeta*>(qempty + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int CW = Hkv;  // consumer warps: one per KV head
+    const int G = Hq / Hkv;
+    const int total = hdr->total, W = hdr->W;
+    const int start = blockIdx.x * W;
+    const int end = min(total, start + W);
+    if (start >= end) return;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < nst; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], CW);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&qfull[s], 1);
+            mbar_init(&qempty[s], CW);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == CW) {
+        // ------------------------------------------------ producer (one lane)
+        if (lane != 0) return;
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+        // first sequence whose block range reaches past `start`: s + n is
+        // non-decreasing in b, and some b < B satisfies it because start < total.
+        int lo = 0, hi = B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            const SeqInfo si = info[mid];
+            if (si.s + si.n > start) hi = mid; else lo = mid + 1;
+        }
+        int b = lo;
+        SeqInfo cur = info[b];
+        int piece = 0;
+        for (int i = start, it = 0; i < end; ++i, ++it) {
+            while (cur.s + cur.n <= i) cur = info[++b];
+            const int j = i - cur.s;
+            const bool first = (j == 0) || (i == start);
+            const bool last = (j == cur.n - 1) || (i == end - 1);
+            const bool whole = (cur.s >= start) && (cur.s + cur.n <= end);
+            const int stage = it % nst;
+            const uint32_t round = static_cast<uint32_t>(it / nst);
+            if (!mbar_wait(&empty[stage], (round & 1u) ^ 1u)) {
+                report(status, PKV_ERR_TIMEOUT);
+                return;
+            }
+            if (first) {
+                const int qs = piece & 1;
+                const uint32_t qr = static_cast<uint32_t>(piece >> 1);
+                if (!mbar_wait(&qempty[qs], (qr & 1u) ^ 1u)) {
+                    report(status, PKV_ERR_TIMEOUT);
+                    return;
+                }
+                mbar_arrive_expect_tx(&qfull[qs], q_bytes);
+                tma_load_1d(qring + static_cast<size_t>(qs) * q_bytes, q + static_cast<size_t>(b) * Hq * kDim,
+                            q_bytes, &qfull[qs]);
+                ++piece;
+            }
+            const int blk = block_tables[static_cast<size_t>(b) * max_blocks + j];
+            const bool valid = blk >= 0 && blk < NB;
+            StageMeta mt;
+            mt.b = b;
+            mt.j = j;
+            mt.ntok = min(BS, cur.L - j * BS);
+            mt.flags = (valid ? kValid : 0) | (first ? kFirst : 0) | (last ? kLast : 0) | (whole ? kWhole : 0);
+            meta[stage] = mt;
+            uint64_t* fb = &full[stage];
+            if (valid) {
+                mbar_arrive_expect_tx(fb, stage_bytes);
+                uint8_t* st = stages + static_cast<size_t>(stage) * stage_bytes;
+                const int y = blk * R;
+                tma_load_2d(st, &tmK, 0, y, fb);
+                tma_load_2d(st + box_bytes, &tmK, 64, y, fb);
+                tma_load_2d(st + 2 * box_bytes, &tmV, 0, y, fb);
+                tma_load_2d(st + 3 * box_bytes, &tmV, 64, y, fb);
+            } else {
+                report(status, PKV_ERR_DEVICE_BOUNDS);
+                mbar_arrive(fb);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------- consumers: warp h
+    const int h = warp;
+    const int g = lane >> 2, r = lane & 3;
+    const int mi = lane >> 3, rr = lane & 7;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float O[16][4];
+    uint32_t qa[8][4];
+    bool poisoned = false;
+    int piece = 0;
+    const uint32_t stages_u32 = smem_u32(stages);
+
+    for (int i = start, it = 0; i < end; ++i, ++it) {
+        const int stage = it % nst;
+        const uint32_t round = static_cast<uint32_t>(it / nst);
+        if (!mbar_wait(&full[stage], round & 1u)) {
+            if (lane == 0) report(status, PKV_ERR_TIMEOUT);
+            return;
+        }
+        const StageMeta mt = meta[stage];
+        if (mt.flags & kFirst) {
+            const int qs = piece & 1;
+            const uint32_t qr = static_cast<uint32_t>(piece >> 1);
+            if (!mbar_wait(&qfull[qs], qr & 1u)) {
+                if (lane == 0) report(status, PKV_ERR_TIMEOUT);
+                return;
+            }
+            const __nv_bfloat16* qsm = reinterpret_cast<const __nv_bfloat16*>(qring + static_cast<size_t>(qs) * q_bytes);
+            const int row0 = h * G + g, row1 = h * G + g + 8;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const int c0 = kk * 16 + 2 * r;
+                qa[kk][0] = g < G ? *reinterpret_cast<const uint32_t*>(qsm + row0 * kDim + c0) : 0u;
+                qa[kk][2] = g < G ? *reinterpret_cast<const uint32_t*>(qsm + row0 * kDim + c0 + 8) : 0u;
+                if (kRows16) {
+                    qa[kk][1] = (g + 8) < G ? *reinterpret_cast<const uint32_t*>(qsm + row1 * kDim + c0) : 0u;
+                    qa[kk][3] = (g + 8) < G ? *reinterpret_cast<const uint32_t*>(qsm + row1 * kDim + c0 + 8) : 0u;
+                } else {
+                    qa[kk][1] = 0u;
+                    qa[kk][3] = 0u;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&qempty[qs]);
+            ++piece;
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < 16; ++nt) O[nt][0] = O[nt][1] = O[nt][2] = O[nt][3] = 0.f;
+            poisoned = false;
+        }
+        if (mt.flags & kValid) {
+            const uint32_t kb = stages_u32 + static_cast<uint32_t>(stage) * stage_bytes;
+            const uint32_t vb = kb + 2 * box_bytes;
+            if (mt.ntok < BS) {
+                // Slots past the sequence end may hold anything (NaN included):
+                // clear this head's V rows there so that 0 * V stays 0.
+                uint8_t* vsm = stages + static_cast<size_t>(stage) * stage_bytes + 2 * box_bytes;
+                const int nrows = BS - mt.ntok;
+                for (int e = lane; e < nrows * 16; e += 32) {  // 2 boxes x 128 B = 16 x 16 B per row
+                    const int row = h * BS + mt.ntok + (e >> 4);
+                    const int part = e & 15;
+                    uint4* dst = reinterpret_cast<uint4*>(vsm + (part >> 3) * box_bytes + row * 128 + (part & 7) * 16);
+                    *dst = make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            const int nchunk = (min(mt.ntok, BS) + 15) >> 4;
+            for (int c = 0; c < nchunk; ++c) {
+                const int rbase = h * BS + c * 16;
+                // ---- S = Q K^T for 16 tokens (two n-tiles of 8)
+                float s[2][4];
+#pragma unroll
+                for (int t = 0; t < 2; ++t) s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const int tok = (mi >> 1) * 8 + rr;
+                    const int dc = kk * 2 + (mi & 1);
+                    const int row = rbase + tok;
+                    const uint32_t addr = kb + static_cast<uint32_t>(dc >> 3) * box_bytes +
+                                          static_cast<uint32_t>(row) * 128u +
+                                          (static_cast<uint32_t>((dc & 7) ^ (row & 7)) << 4);
+                    uint32_t b0, b1, b2, b3;
+                    ldmatrix_x4(b0, b1, b2, b3, addr);
+                    mma_bf16_16816(s[0], qa[kk], b0, b1);
+                    mma_bf16_16816(s[1], qa[kk], b2, b3);
+                }
+                // ---- online softmax (log2 domain), masking tokens past the end
+                const int tb = c * 16;
+#pragma unroll
+                for (int t = 0; t < 2; ++t)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int tk = tb + t * 8 + 2 * r + (e & 1);
+                        const float v = s[t][e] * scale_log2;
+                        s[t][e] = tk < mt.ntok ? v : -INFINITY;
+                    }
+                float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+                const float mn0 = fmaxf(m0, mx0);
+                const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+                const float a0 = exp2f(m0 - mu0);
+                m0 = mn0;
+                float a1 = 1.f, mu1 = 0.f;
+                if (kRows16) {
+                    float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                    const float mn1 = fmaxf(m1, mx1);
+                    mu1 = mn1 == -INFINITY ? 0.f : mn1;
+                    a1 = exp2f(m1 - mu1);
+                    m1 = mn1;
+                }
+                uint32_t pa[4];
+                pa[0] = pack_bf16x2(exp2f(s[0][0] - mu0), exp2f(s[0][1] - mu0));
+                pa[2] = pack_bf16x2(exp2f(s[1][0] - mu0), exp2f(s[1][1] - mu0));
+                l0 = l0 * a0 + ((bf16_lo(pa[0]) + bf16_hi(pa[0])) + (bf16_lo(pa[2]) + bf16_hi(pa[2])));
+                if (kRows16) {
+                    pa[1] = pack_bf16x2(exp2f(s[0][2] - mu1), exp2f(s[0][3] - mu1));
+                    pa[3] = pack_bf16x2(exp2f(s[1][2] - mu1), exp2f(s[1][3] - mu1));
+                    l1 = l1 * a1 + ((bf16_lo(pa[1]) + bf16_hi(pa[1])) + (bf16_lo(pa[3]) + bf16_hi(pa[3])));
+                } else {
+                    pa[1] = 0u;
+                    pa[3] = 0u;
+                }
+#pragma unroll
+                for (int nt = 0; nt < 16; ++nt) {
+                    O[nt][0] *= a0;
+                    O[nt][1] *= a0;
+                    if (kRows16) {
+                        O[nt][2] *= a1;
+                        O[nt][3] *= a1;
+                    }
+                }
+                // ---- O += P V
+#pragma unroll
+                for (int dp = 0; dp < 8; ++dp) {
+                    const int tok = (mi & 1) * 8 + rr;
+                    const int dc = dp * 2 + (mi >> 1);
+                    const int row = rbase + tok;
+                    const uint32_t addr = vb + static_cast<uint32_t>(dc >> 3) * box_bytes +
+                                          static_cast<uint32_t>(row) * 128u +
+                                          (static_cast<uint32_t>((dc & 7) ^ (row & 7)) << 4);
+                    uint32_t v0, v1, v2, v3;
+                    ldmatrix_x4_trans(v0, v1, v2, v3, addr);
+                    mma_bf16_16816(O[2 * dp], pa, v0, v1);
+                    mma_bf16_16816(O[2 * dp + 1], pa, v2, v3);
+                }
+            }
+        } else {
+            poisoned = true;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);
+
+        if (mt.flags & kLast) {
+            float lt0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
+            lt0 += __shfl_xor_sync(0xffffffffu, lt0, 2);
+            float lt1 = 0.f;
+            if (kRows16) {
+                lt1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
+                lt1 += __shfl_xor_sync(0xffffffffu, lt1, 2);
+            }
+            const int b = mt.b;
+            const int qh0 = h * G + g, qh1 = h * G + g + 8;
+            const bool live0 = g < G, live1 = kRows16 && (g + 8) < G;
+            if (mt.flags & kWhole) {
+                const float inv0 = (!poisoned && lt0 > 0.f) ? 1.f / lt0 : 0.f;
+                const float inv1 = (!poisoned && lt1 > 0.f) ? 1.f / lt1 : 0.f;
+#pragma unroll
+                for (int nt = 0; nt < 16; ++nt) {
+                    const int d = nt * 8 + 2 * r;
+                    if (live0)
+                        *reinterpret_cast<uint32_t*>(out + (static_cast<size_t>(b) * Hq + qh0) * kDim + d) =
+                            pack_bf16x2(O[nt][0] * inv0, O[nt][1] * inv0);
+                    if (live1)
+                        *reinterpret_cast<uint32_t*>(out + (static_cast<size_t>(b) * Hq + qh1) * kDim + d) =
+                            pack_bf16x2(O[nt][2] * inv1, O[nt][3] * inv1);
+                }
+            } else {
+                const SeqInfo si = info[b];
+                const size_t slot = static_cast<size_t>(si.base + (static_cast<int>(blockIdx.x) - si.first));
+                if (r == 0) {
+                    if (live0) {
+                        part_ml[(slot * Hq + qh0) * 2 + 0] = m0;
+                        part_ml[(slot * Hq + qh0) * 2 + 1] = poisoned ? -1.f : lt0;
+                    }
+                    if (live1) {
+                        part_ml[(slot * Hq + qh1) * 2 + 0] = m1;
+                        part_ml[(slot * Hq + qh1) * 2 + 1] = poisoned ? -1.f : lt1;
+                    }
+                }
+#pragma unroll
+                for (int nt = 0; nt < 16; ++nt) {
+                    const int d = nt * 8 + 2 * r;
+                    if (live0)
+                        *reinterpret_cast<float2*>(part_o + (slot * Hq + qh0) * kDim + d) =
+                            make_float2(O[nt][0], O[nt][1]);
+                    if (live1)
+                        *reinterpret_cast<float2*>(part_o + (slot * Hq + qh1) * kDim + d) =
+                            make_float2(O[nt][2], O[nt][3]);
+                }
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ combine kernel
+// Merges the per-range partials of sequences that span several CTA ranges:
+// M = max m_c, out = sum o_c 2^(m_c - M) / sum l_c 2^(m_c - M) (log2 domain).
+// Writes zeros for empty or invalid sequences; skips single-range sequences,
+// which the fast kernel wrote directly.
+template <typename T>
+__global__ void __launch_bounds__(256)
+    combine_kernel(const SeqInfo* __restrict__ info, const float* __restrict__ part_ml,
+                   const float* __restrict__ part_o, T* __restrict__ out, int Hq, int D) {
+    const int b = blockIdx.x;
+    const SeqInfo si = info[b];
+    if (si.pieces == 1) return;
+    T* ob = out + static_cast<size_t>(b) * Hq * D;
+    if (si.pieces == 0) {
+        for (int idx = threadIdx.x; idx < Hq * D; idx += blockDim.x) ob[idx] = from_f32<T>(0.f);
+        return;
+    }
+    for (int idx = threadIdx.x; idx < Hq * D; idx += blockDim.x) {
+        const int qh = idx / D, d = idx - qh * D;
+        float M = -INFINITY;
+        bool bad = false;
+        for (int c = 0; c < si.pieces; ++c) {
+            const size_t slot = static_cast<size_t>(si.base + c);
+            M = fmaxf(M, part_ml[(slot * Hq + qh) * 2]);
+            bad |= part_ml[(slot * Hq + qh) * 2 + 1] < 0.f;
+        }
+        float num = 0.f, den = 0.f;
+        if (!bad && M != -INFINITY) {
+            for (int c = 0; c < si.pieces; ++c) {
+                const size_t slot = static_cast<size_t>(si.base + c);
+                const float w = exp2f(part_ml[(slot * Hq + qh) * 2] - M);
+                den += part_ml[(slot * Hq + qh) * 2 + 1] * w;
+                num += part_o[(slot * Hq + qh) * D + d] * w;
+            }
+        }
+        ob[idx] = from_f32<T>(den > 0.f ? num / den : 0.f);
+    }
+}
+
+// ------------------------------------------------------------------ generic kernel
+// One CTA per (sequence, query head); 128 threads; chunks of 128 tokens; fp32
+// online softmax across chunks.  Handles any D <= 256, any block size, fp32 or
+// bf16 storage.
+constexpr int kGenThreads = 128;
+
+template <typename T>
+__global__ void __launch_bounds__(kGenThreads)
+    decode_attn_generic_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __restrict__ k_cache,
+                               const T* __restrict__ v_cache, const int32_t* __restrict__ block_tables,
+                               int max_blocks, const int32_t* __restrict__ seq_lens, int Hq, int Hkv, int D,
+                               int BS, int NB, float scale, int32_t* status) {
+    __shared__ float qs[256];
+    __shared__ float ps[kGenThreads];
+    __shared__ int blks[kGenThreads];
+    __shared__ float red[kGenThreads / 32];
+    __shared__ int bad;
+    const int b = blockIdx.x / Hq, qh = blockIdx.x % Hq;
+    const int G = Hq / Hkv, h = qh / G;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    T* o = out + (static_cast<size_t>(b) * Hq + qh) * D;
+    const int L = seq_lens[b];
+    if (L < 0 || static_cast<long long>(L) > static_cast<long long>(max_blocks) * BS) {
+        if (tid == 0) report(status, PKV_ERR_DEVICE_BOUNDS);
+        for (int d = tid; d < D; d += kGenThreads) o[d] = from_f32<T>(0.f);
+        return;
+    }
+    for (int d = tid; d < D; d += kGenThreads) qs[d] = to_f32(q[(static_cast<size_t>(b) * Hq + qh) * D + d]);
+    if (tid == 0) bad = 0;
+    __syncthreads();
+    float m = -INFINITY, l = 0.f;
+    float acc[2] = {0.f, 0.f};
+    for (int t0 = 0; t0 < L; t0 += kGenThreads) {
+        const int n = min(kGenThreads, L - t0);
+        float s = -INFINITY;
+        if (tid < n) {
+            const int pos = t0 + tid;
+            const int blk = block_tables[static_cast<size_t>(b) * max_blocks + pos / BS];
+            blks[tid] = blk;
+            if (blk < 0 || blk >= NB) {
+                bad = 1;
+            } else {
+                const T* kr = k_cache + ((static_cast<size_t>(blk) * Hkv + h) * BS + pos % BS) * D;
+                float dot = 0.f;
+                for (int d = 0; d < D; ++d) dot = fmaf(qs[d], to_f32(kr[d]), dot);
+                s = dot * scale;
+            }
+        }
+        // block max
+        float mx = s;
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        if (lane == 0) red[warp] = mx;
+        __syncthreads();
+        mx = red[0];
+        for (int w = 1; w < kGenThreads / 32; ++w) mx = fmaxf(mx, red[w]);
+        __syncthreads();
+        const float mn = fmaxf(m, mx);
+        const float mu = mn == -INFINITY ? 0.f : mn;
+        const float alpha = expf(m - mu);
+        const float p = (tid < n && s != -INFINITY) ? expf(s - mu) : 0.f;
+        ps[tid] = p;
+        float sm = p;
+        for (int off = 16; off > 0; off >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, off);
+        if (lane == 0) red[warp] = sm;
+        __syncthreads();
+        float psum = 0.f;
+        for (int w = 0; w < kGenThreads / 32; ++w) psum += red[w];
+        l = l * alpha + psum;
+        m = mn;
+        for (int k = 0; k < 2; ++k) {
+            const int d = tid + k * kGenThreads;
+            if (d < D) {
+                float a = acc[k] * alpha;
+                for (int t = 0; t < n; ++t) {
+                    const float pt = ps[t];
+                    const int blk = blks[t];
+                    if (pt != 0.f && blk >= 0 && blk < NB) {
+                        const int pos = t0 + t;
+                        a = fmaf(pt, to_f32(v_cache[((static_cast<size_t>(blk) * Hkv + h) * BS + pos % BS) * D + d]), a);
+                    }
+                }
+                acc[k] = a;
+            }
+        }
+        __syncthreads();
+    }
+    const bool poisoned = bad != 0;
+    if (poisoned && tid == 0) report(status, PKV_ERR_DEVICE_BOUNDS);
+    const float inv = (!poisoned && l > 0.f) ? 1.f / l : 0.f;
+    for (int k = 0; k < 2; ++k) {
+        const int d = tid + k * kGenThreads;
+        if (d < D) o[d] = from_f32<T>(acc[k] * inv);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult qres;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qres) ==
+                cudaSuccess &&
+            qres == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        tried = true;
+    }
+    return fn;
+}
+
+static bool encode_pool_map(CUtensorMap* map, const void* pool, int NB, int Hkv, int BS) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return false;
+    const cuuint64_t rows = static_cast<cuuint64_t>(NB) * Hkv * BS;
+    cuuint64_t gdim[2] = {static_cast<cuuint64_t>(kDim), rows};
+    cuuint64_t gstride[1] = {static_cast<cuuint64_t>(kDim) * 2};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(Hkv * BS)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult res = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), gdim, gstride, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return res == CUDA_SUCCESS;
+}
+
+int device_sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+static int max_optin_smem() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    return n;
+}
+
+struct FastPlan {
+    bool ok;
+    int nst, stage_bytes, q_bytes;
+    size_t smem;
+};
+
+static FastPlan plan_fast(int Hq, int Hkv, int D, int BS, pkv_dtype dt, const void* k, const void* v,
+                          const void* q) {
+    FastPlan fp{false, 0, 0, 0, 0};
+    auto aligned16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (dt != PKV_BF16 || D != kDim || BS % 16 != 0 || Hkv < 1 || Hkv > kFastMaxKvHeads) return fp;
+    const int G = Hq / Hkv;
+    if (G < 1 || G > 16) return fp;
+    const int R = Hkv * BS;
+    if (R > 256) return fp;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(q)) return fp;
+    fp.stage_bytes = 4 * R * 128;
+    fp.q_bytes = Hq * kDim * 2;
+    const long long budget = max_optin_smem();
+    long long nst = (budget - static_cast<long long>(fast_smem_bytes(0, fp.stage_bytes, fp.q_bytes))) / fp.stage_bytes;
+    if (nst > kMaxStages) nst = kMaxStages;
+    if (nst < 2) return fp;
+    fp.nst = static_cast<int>(nst);
+    fp.smem = fast_smem_bytes(fp.nst, fp.stage_bytes, fp.q_bytes);
+    fp.ok = true;
+    return fp;
+}
+
+cudaError_t launch_decode_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* block_tables, int max_blocks, const int32_t* seq_lens, int B,
+                                    int Hq, int Hkv, int D, int BS, int NB, float scale, pkv_dtype dtype,
+                                    void* workspace, int P, int32_t* status, cudaStream_t stream,
+                                    bool* used_fast) {
+    if (scale <= 0.f) scale = 1.0f / sqrtf(static_cast<float>(D));
+    const FastPlan fp = plan_fast(Hq, Hkv, D, BS, dtype, k_cache, v_cache, q);
+    CUtensorMap tmK, tmV;
+    bool fast = fp.ok && encode_pool_map(&tmK, k_cache, NB, Hkv, BS) && encode_pool_map(&tmV, v_cache, NB, Hkv, BS);
+    if (used_fast) *used_fast = fast;
+    if (!fast) {
+        const unsigned grid = static_cast<unsigned>(B) * Hq;
+        if (dtype == PKV_F32)
+            decode_attn_generic_kernel<float><<<grid, kGenThreads, 0, stream>>>(
+                static_cast<float*>(out), static_cast<const float*>(q), static_cast<const float*>(k_cache),
+                static_cast<const float*>(v_cache), block_tables, max_blocks, seq_lens, Hq, Hkv, D, BS, NB, scale,
+                status);
+        else
+            decode_attn_generic_kernel<__nv_bfloat16><<<grid, kGenThreads, 0, stream>>>(
+                static_cast<__nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(q),
+                static_cast<const __nv_bfloat16*>(k_cache), static_cast<const __nv_bfloat16*>(v_cache), block_tables,
+                max_blocks, seq_lens, Hq, Hkv, D, BS, NB, scale, status);
+        return cudaGetLastError();
+    }
+    const WsLayout wl = ws_layout(B, Hq, D, P);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    PlanHdr* hdr = reinterpret_cast<PlanHdr*>(ws + wl.hdr);
+    SeqInfo* info = reinterpret_cast<SeqInfo*>(ws + wl.info);
+    float* part_ml = reinterpret_cast<float*>(ws + wl.ml);
+    float* part_o = reinterpret_cast<float*>(ws + wl.o);
+    plan_kernel<<<1, 1024, 0, stream>>>(seq_lens, B, max_blocks, BS, P, info, hdr, status);
+    const float scale_log2 = scale * 1.4426950408889634f;
+    const int G = Hq / Hkv;
+    const unsigned threads = static_cast<unsigned>((Hkv + 1) * 32);
+    cudaError_t err;
+    if (G > 8) {
+        err = cudaFuncSetAttribute(decode_attn_fast_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(fp.smem));
+        if (err != cudaSuccess) return err;
+        decode_attn_fast_kernel<true><<<P, threads, fp.smem, stream>>>(
+            tmK, tmV, static_cast<const __nv_bfloat16*>(q), static_cast<__nv_bfloat16*>(out), block_tables, max_blocks,
+            B, Hq, Hkv, BS, NB, scale_log2, fp.nst, info, hdr, part_ml, part_o, status);
+    } else {
+        err = cudaFuncSetAttribute(decode_attn_fast_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(fp.smem));
+        if (err != cudaSuccess) return err;
+        decode_attn_fast_kernel<false><<<P, threads, fp.smem, stream>>>(
+            tmK, tmV, static_cast<const __nv_bfloat16*>(q), static_cast<__nv_bfloat16*>(out), block_tables, max_blocks,
+            B, Hq, Hkv, BS, NB, scale_log2, fp.nst, info, hdr, part_ml, part_o, status);
+    }
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    combine_kernel<__nv_bfloat16><<<B, 256, 0, stream>>>(info, part_ml, part_o, static_cast<__nv_bfloat16*>(out), Hq,
+                                                         D);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

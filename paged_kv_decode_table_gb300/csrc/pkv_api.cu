@@ -1,0 +1,103 @@
+// pkv_api.cu -- the extern "C" entry points declared in include/pkv.h.
+//
+// Host-side argument validation, then one or more kernel launches on the
+// caller's stream.  Nothing here allocates device memory or synchronises.
+#include <cuda_runtime.h>
+
+#include "pkv_common.cuh"
+
+namespace pkv {
+cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                             const int32_t* block_tables, int max_blocks, const int32_t* seq_lens, int B, int Hkv,
+                             int D, int BS, int NB, pkv_dtype dtype, int32_t* status, cudaStream_t stream);
+cudaError_t launch_decode_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* block_tables, int max_blocks, const int32_t* seq_lens, int B,
+                                    int Hq, int Hkv, int D, int BS, int NB, float scale, pkv_dtype dtype,
+                                    void* workspace, int P, int32_t* status, cudaStream_t stream, bool* used_fast);
+size_t decode_workspace_bytes(int B, int Hq, int D, int P);
+int device_sm_count();
+cudaError_t launch_sampler(int32_t* tokens, const float* logits, int B, int V, const float* temperature,
+                           const int32_t* top_k, const float* top_p, const uint64_t* seeds, const uint64_t* offsets,
+                           int32_t* status, cudaStream_t stream);
+}  // namespace pkv
+
+namespace {
+bool dtype_ok(pkv_dtype d) { return d == PKV_F32 || d == PKV_BF16; }
+pkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
+}  // namespace
+
+extern "C" {
+
+const char* pkv_status_string(int status) {
+    switch (status) {
+        case PKV_OK: return "PKV_OK";
+        case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG";
+        case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+        case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+        case PKV_ERR_DEVICE_BOUNDS: return "PKV_ERR_DEVICE_BOUNDS";
+        case PKV_ERR_TIMEOUT: return "PKV_ERR_TIMEOUT";
+        case PKV_ERR_NONFINITE: return "PKV_ERR_NONFINITE";
+        default: return "PKV_ERR_UNKNOWN";
+    }
+}
+
+int pkv_version(void) { return 100; }
+
+pkv_status pkv_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                         const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens, int B, int Hkv,
+                         int D, int block_size, int num_blocks, pkv_dtype dtype, int32_t* dev_status, void* stream) {
+    if (B < 0 || Hkv < 1 || D < 1 || block_size < 1 || num_blocks < 1 || max_blocks_per_seq < 1 || !dtype_ok(dtype))
+        return PKV_ERR_INVALID_ARG;
+    if (B == 0) return PKV_OK;
+    if (!k_new || !v_new || !k_cache || !v_cache || !block_tables || !seq_lens) return PKV_ERR_INVALID_ARG;
+    return cuda_status(pkv::launch_kv_append(k_new, v_new, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                             seq_lens, B, Hkv, D, block_size, num_blocks, dtype, dev_status,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+size_t pkv_decode_workspace_bytes(int B, int Hq, int D, int num_sms) {
+    if (B < 0 || Hq < 1 || D < 1) return 0;
+    const int P = num_sms > 0 ? num_sms : pkv::device_sm_count();
+    if (P <= 0) return 0;
+    return pkv::decode_workspace_bytes(B, Hq, D, P);
+}
+
+pkv_status pkv_paged_decode_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                                      int B, int Hq, int Hkv, int D, int block_size, int num_blocks, float scale,
+                                      pkv_dtype dtype, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                      void* stream) {
+    if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || D < 1 || D > 256 || block_size < 1 || num_blocks < 1 ||
+        max_blocks_per_seq < 1 || !dtype_ok(dtype))
+        return PKV_ERR_INVALID_ARG;
+    if (B == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !workspace) return PKV_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return PKV_ERR_INVALID_ARG;
+    const int P = pkv::device_sm_count();
+    if (P <= 0) return PKV_ERR_CUDA;
+    if (workspace_bytes < pkv::decode_workspace_bytes(B, Hq, D, P)) return PKV_ERR_INVALID_ARG;
+    return cuda_status(pkv::launch_decode_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                                    seq_lens, B, Hq, Hkv, D, block_size, num_blocks, scale, dtype,
+                                                    workspace, P, dev_status, static_cast<cudaStream_t>(stream),
+                                                    nullptr));
+}
+
+size_t pkv_sample_workspace_bytes(int B, int V) {
+    (void)B;
+    (void)V;
+    return 0;
+}
+
+pkv_status pkv_sample_tokens(int32_t* tokens, const float* logits, int B, int V, const float* temperature,
+                             const int32_t* top_k, const float* top_p, const uint64_t* seeds, const uint64_t* offsets,
+                             void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    if (B < 0 || V < 1 || V > (1 << 23)) return PKV_ERR_INVALID_ARG;
+    if (B == 0) return PKV_OK;
+    if (!tokens || !logits || !temperature || !top_k || !top_p || !seeds || !offsets) return PKV_ERR_INVALID_ARG;
+    return cuda_status(pkv::launch_sampler(tokens, logits, B, V, temperature, top_k, top_p, seeds, offsets, dev_status,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -106,7 +106,10 @@ WORKLOADS = {
 def workload(number: int, **overrides) -> DecodeWorkload:
     """A named workload, optionally shrunk (e.g. batch=4, len_hi=300) for fast tests."""
     w = WORKLOADS[number]
-    return replace(w, **overrides) if overrides else w
+    w = replace(w, **overrides) if overrides else w
+    if not w.fixed_lens and w.len_hi and w.len_lo > w.len_hi:
+        raise ValueError(f"len_lo {w.len_lo} > len_hi {w.len_hi}: override both")
+    return w
 
 
 def _cpu_gen(seed: int) -> torch.Generator:
