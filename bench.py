@@ -137,7 +137,8 @@ class ClockSampler:
 def _dist():
     n = int(os.environ.get("WORLD_SIZE", "1"))
     if n > 1 and not torch.distributed.is_initialized():
-        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        backend = os.environ.get("PKV_DIST_BACKEND") or ("nccl" if torch.cuda.is_available() else "gloo")
+        torch.distributed.init_process_group(backend)
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return n, rank, local

@@ -498,39 +498,64 @@ __global__ void __launch_bounds__((kFastMaxKvHeads + 1) * 32, 1)
 // ------------------------------------------------------------------ combine kernel
 // Merges the per-range partials of sequences that span several CTA ranges:
 // M = max m_c, out = sum o_c 2^(m_c - M) / sum l_c 2^(m_c - M) (log2 domain).
+// One CTA per (sequence, query head); the piece weights are computed once into
+// shared memory, then each thread reduces its output dimensions over the pieces.
 // Writes zeros for empty or invalid sequences; skips single-range sequences,
 // which the fast kernel wrote directly.
+constexpr int kCombineThreads = 128;
+constexpr int kCombineMaxPieces = 1024;
+
 template <typename T>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const SeqInfo* __restrict__ info, const float* __restrict__ part_ml,
                    const float* __restrict__ part_o, T* __restrict__ out, int Hq, int D) {
-    const int b = blockIdx.x;
+    __shared__ float wsh[kCombineMaxPieces];
+    __shared__ float red[kCombineThreads / 32];
+    __shared__ int bad_sh;
+    const int b = blockIdx.x / Hq, qh = blockIdx.x - (blockIdx.x / Hq) * Hq;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const SeqInfo si = info[b];
     if (si.pieces == 1) return;
-    T* ob = out + static_cast<size_t>(b) * Hq * D;
-    if (si.pieces == 0) {
-        for (int idx = threadIdx.x; idx < Hq * D; idx += blockDim.x) ob[idx] = from_f32<T>(0.f);
-        return;
+    T* o = out + (static_cast<size_t>(b) * Hq + qh) * D;
+    const int np = min(si.pieces, kCombineMaxPieces);
+    if (tid == 0) bad_sh = (si.pieces == 0 || si.pieces > kCombineMaxPieces) ? 1 : 0;
+    __syncthreads();
+    // max over pieces (and poisoned-piece detection)
+    float M = -INFINITY;
+    for (int c = tid; c < np; c += kCombineThreads) {
+        const float2 ml = *reinterpret_cast<const float2*>(part_ml + ((static_cast<size_t>(si.base) + c) * Hq + qh) * 2);
+        M = fmaxf(M, ml.x);
+        if (ml.y < 0.f) bad_sh = 1;
     }
-    for (int idx = threadIdx.x; idx < Hq * D; idx += blockDim.x) {
-        const int qh = idx / D, d = idx - qh * D;
-        float M = -INFINITY;
-        bool bad = false;
-        for (int c = 0; c < si.pieces; ++c) {
-            const size_t slot = static_cast<size_t>(si.base + c);
-            M = fmaxf(M, part_ml[(slot * Hq + qh) * 2]);
-            bad |= part_ml[(slot * Hq + qh) * 2 + 1] < 0.f;
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if (lane == 0) red[warp] = M;
+    __syncthreads();
+    M = red[0];
+    for (int w = 1; w < kCombineThreads / 32; ++w) M = fmaxf(M, red[w]);
+    const bool bad = bad_sh != 0 || M == -INFINITY;
+    __syncthreads();
+    // weights 2^(m_c - M) and the merged denominator
+    float L = 0.f;
+    for (int c = tid; c < np; c += kCombineThreads) {
+        const float2 ml = *reinterpret_cast<const float2*>(part_ml + ((static_cast<size_t>(si.base) + c) * Hq + qh) * 2);
+        const float wgt = bad ? 0.f : exp2f(ml.x - M);
+        wsh[c] = wgt;
+        L += ml.y * wgt;
+    }
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    if (lane == 0) red[warp] = L;
+    __syncthreads();
+    L = 0.f;
+    for (int w = 0; w < kCombineThreads / 32; ++w) L += red[w];
+    const float inv = (!bad && L > 0.f) ? 1.f / L : 0.f;
+    for (int d = tid; d < D; d += kCombineThreads) {
+        float acc = 0.f;
+        if (!bad) {
+            const float* po = part_o + (static_cast<size_t>(si.base) * Hq + qh) * D + d;
+            const size_t stride = static_cast<size_t>(Hq) * D;
+            for (int c = 0; c < np; ++c) acc = fmaf(wsh[c], po[c * stride], acc);
         }
-        float num = 0.f, den = 0.f;
-        if (!bad && M != -INFINITY) {
-            for (int c = 0; c < si.pieces; ++c) {
-                const size_t slot = static_cast<size_t>(si.base + c);
-                const float w = exp2f(part_ml[(slot * Hq + qh) * 2] - M);
-                den += part_ml[(slot * Hq + qh) * 2 + 1] * w;
-                num += part_o[(slot * Hq + qh) * D + d] * w;
-            }
-        }
-        ob[idx] = from_f32<T>(den > 0.f ? num / den : 0.f);
+        o[d] = from_f32<T>(acc * inv);
     }
 }
 
@@ -757,8 +782,8 @@ cudaError_t launch_decode_attention(void* out, const void* q, const void* k_cach
     }
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    combine_kernel<__nv_bfloat16><<<B, 256, 0, stream>>>(info, part_ml, part_o, static_cast<__nv_bfloat16*>(out), Hq,
-                                                         D);
+    combine_kernel<__nv_bfloat16><<<static_cast<unsigned>(B) * Hq, kCombineThreads, 0, stream>>>(
+        info, part_ml, part_o, static_cast<__nv_bfloat16*>(out), Hq, D);
     return cudaGetLastError();
 }
 

@@ -11,13 +11,21 @@
 //
 // GB300 design: one thread-block cluster (up to 8 CTAs) per row; each CTA pulls
 // its slice of the row from HBM once (1-D TMA bulk copy) into shared memory, and
-// every later pass runs on chip.  Selections are radix searches over 32-bit
-// order-preserving keys (digits of 11/11/10 bits) whose per-CTA histograms are
-// summed through distributed shared memory.  Masses are exp() in fp32 turned
-// into 64-bit fixed point (floor(w * 2^40)), so every sum, cut and CDF
-// comparison afterwards is exact integer arithmetic and run-to-run deterministic.
-// When top-k leaves few candidates, the cluster gathers them into rank 0, which
-// finishes alone without further cluster barriers.
+// every later pass runs on chip; CTAs exchange small summaries through
+// distributed shared memory.  A token's mass is exp2((z - zmax) * log2(e)/T) in
+// fp32 turned into 64-bit fixed point (floor(w * 2^40)), so every sum, cut and
+// CDF comparison is exact integer arithmetic and run-to-run deterministic.
+//  * top-k rows: a histogram of 2048 bins linear in (zmax - z) finds the bin of
+//    the k-th largest logit; the candidates above it (a superset of the top-k set,
+//    typically k plus a few) are gathered into rank 0, which sorts them by
+//    (z desc, id asc) and finishes top-k, top-p and the draw alone;
+//  * top-p-only rows: the same bins carry fp32 masses that locate the cut
+//    approximately; the bins around it are gathered into rank 0 and the exact
+//    cut is found there, verified against exact fixed-point masses; every CTA
+//    then walks its slice for the draw;
+//  * rows that fail either fast path (too many candidates, or a cut outside the
+//    window) take an exact radix search over 11/11/10-bit key digits with
+//    64-bit shared-memory histograms.
 #include <cooperative_groups.h>
 #include <limits.h>
 #include <math.h>
@@ -30,22 +38,27 @@ namespace pkv {
 
 constexpr int kST = 512;           // threads per CTA
 constexpr int kSW = kST / 32;      // warps per CTA
-constexpr int kHistBins = 2048;    // widest radix digit (11 bits)
+constexpr int kHistBins = 2048;    // widest radix digit (11 bits) and linear bins
 constexpr int kListCap = 2048;     // candidate list capacity (rank 0, gathered)
+constexpr int kTopkBins = 512;     // bins of the bounded top-k histogram
 constexpr int kMaxCluster = 8;
 constexpr int kSliceSmemMax = 24576;  // floats of a row slice kept in shared memory
 
-struct SampSmem {
-    unsigned long long hist[kHistBins];
-    unsigned long long xch[2][4];
-    unsigned long long gath[kMaxCluster][4];
+struct __align__(16) SampSmem {
+    unsigned long long hist[kHistBins];  // u64 radix histogram, or u32 counts + f32 masses
+    unsigned long long list[kListCap];   // rank 0: gathered candidates (sort keys)
+    unsigned long long xch[2][8];
+    unsigned long long gath[kMaxCluster][8];
     unsigned long long wsum[kSW];
-    unsigned long long bc[4];
-    float list_z[kListCap];
-    int list_id[kListCap];
-    uint64_t bar;
+    unsigned long long bc[8];
+    unsigned long long aslot[kMaxCluster];
+    uint64_t bar[4];        // one per chunk of the slice load
+    unsigned int gcount;    // rank 0: candidates gathered so far
     int imin;
 };
+// The row slice follows the struct in shared memory; TMA bulk copies and the
+// 16-byte vector loads need it 16-byte aligned.
+static_assert(sizeof(SampSmem) % 16 == 0, "slice after SampSmem must stay 16-byte aligned");
 
 // ------------------------------------------------------------------ numeric helpers
 // Order-preserving key of a float (larger float -> larger key); -0.0 is folded
@@ -59,23 +72,29 @@ __device__ __forceinline__ float key_float(uint32_t k) {
     const uint32_t u = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
     return __uint_as_float(u);
 }
-// floor(w * 2^40) for w in [0, 1], exactly, from the float's bits.
-__device__ __forceinline__ uint64_t fx40(float w) {
-    const uint32_t u = __float_as_uint(w);
-    const int e = static_cast<int>((u >> 23) & 0xffu);
-    if (e == 0 || e > 127) return 0ull;  // zero / denormal (or outside [0, 1], which cannot occur)
-    const uint64_t m = static_cast<uint64_t>((u & 0x7fffffu) | 0x800000u);
-    const int sh = e - 110;  // w * 2^40 = m * 2^(e - 110)
-    if (sh >= 0) return m << sh;
-    if (sh <= -24) return 0ull;
-    return m >> (-sh);
+// floor(w * 2^40) for w in [0, 1]: scaling by 2^40 is exact, and the float ->
+// u64 conversion truncates (a float carries 24 significant bits, so the
+// integer part is exact).
+__device__ __forceinline__ uint64_t fx40(float w) { return __float2ull_rz(w * 1099511627776.0f); }
+// 2^x by the hardware's approximate base-2 exponential (subnormal results flush
+// to zero; they are below 2^-40 and weigh nothing anyway).
+__device__ __forceinline__ float hw_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
-// Fixed-point mass of a finite logit; the maximum itself weighs exactly 2^40
-// (also when 1/T overflows and 0 * inf would be NaN).
-__device__ __forceinline__ uint64_t mass(float z, float zmax, float invT) {
-    const float d = z - zmax;
-    if (d == 0.f) return 1ull << 40;
-    return fx40(expf(d * invT));
+// Weight of a logit relative to the row maximum, w = 2^((z - zmax) * c2) with
+// c2 = log2(e) / T clamped to a finite value, so that the maximum weighs 2^0 = 1
+// and a banned (-inf) logit weighs 2^-inf = 0.
+__device__ __forceinline__ float weight(float z, float zmax, float c2) { return hw_exp2((z - zmax) * c2); }
+// Its 64-bit fixed-point mass floor(w * 2^40).
+__device__ __forceinline__ uint64_t mass(float z, float zmax, float c2) { return fx40(weight(z, zmax, c2)); }
+// Sort key with (z desc, id asc) as descending u64 order.
+__device__ __forceinline__ uint64_t sort_key(float z, int id) {
+    return (static_cast<uint64_t>(okey(z)) << 32) | static_cast<uint32_t>(0xffffffffu - static_cast<uint32_t>(id));
+}
+__device__ __forceinline__ int sort_key_id(uint64_t k) {
+    return static_cast<int>(0xffffffffu - static_cast<uint32_t>(k & 0xffffffffull));
 }
 // ceil(p * S) for p a float in (0, 1) and S < 2^63, exactly.
 __device__ __forceinline__ uint64_t ceil_mul_p(float p, uint64_t S) {
@@ -156,6 +175,13 @@ struct Keep {
     bool k_on, p_on;
     uint32_t tauk, taup;
     int idk, idp;
+    float zk, zp;  // key_float(tauk), key_float(taup)
+    // Same predicates on floats (-0.0 == +0.0 as with the keys); -inf never passes.
+    __device__ __forceinline__ bool keep_f(float z, int id) const {
+        const bool ok_k = !k_on || z > zk || (z == zk && id <= idk);
+        const bool ok_p = !p_on || z > zp || (z == zp && id <= idp);
+        return ok_k && ok_p && z > -INFINITY;
+    }
     __device__ __forceinline__ bool topk(uint32_t key, int id) const {
         return !k_on || key > tauk || (key == tauk && id <= idk);
     }
@@ -167,18 +193,49 @@ struct Keep {
 struct Ctx {
     SampSmem* sm;
     int nc, rank, xb;
-    bool solo;  // true once rank 0 owns every candidate and runs alone
-    __device__ __forceinline__ int nce() const { return solo ? 1 : nc; }
-    __device__ __forceinline__ int rke() const { return solo ? 0 : rank; }
-    __device__ __forceinline__ void csync() const {
-        if (solo) __syncthreads();
-        else cg::this_cluster().sync();
-    }
+    __device__ __forceinline__ int nce() const { return nc; }
+    __device__ __forceinline__ int rke() const { return rank; }
+    __device__ __forceinline__ void csync() const { cg::this_cluster().sync(); }
     template <typename T>
     __device__ __forceinline__ T* remote(T* p, int r) const {
-        return solo ? p : cg::this_cluster().map_shared_rank(p, r);
+        return cg::this_cluster().map_shared_rank(p, r);
     }
 };
+
+// Split cluster barrier: arrive (release) as soon as this CTA's remote reads are
+// done, wait (acquire) only before leaving.
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Bitonic sort of a[0..n) (n a power of two) in shared memory by one CTA.
+__device__ void bitonic_sort(unsigned long long* a, int n, bool descending) {
+    for (int k = 2; k <= n; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < n; i += kST) {
+                const int l = i ^ j;
+                if (l > i) {
+                    const bool up = ((i & k) == 0) != descending;
+                    const unsigned long long x = a[i], y = a[l];
+                    if ((x > y) == up) {
+                        a[i] = y;
+                        a[l] = x;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+__device__ __forceinline__ int pow2_ceil(int n) {
+    int p = 1;
+    while (p < n) p <<= 1;
+    return p;
+}
 
 // Publish xch[xb][0..k) (written by thread 0 before the call) to every CTA of
 // the cluster; afterwards gath[j][s] holds rank j's value s.
@@ -202,7 +259,7 @@ __device__ void exch(Ctx& c, int k) {
 template <bool kMass>
 __device__ void radix_pass(Ctx& c, const View& v, const Keep& kp, bool use_topk, uint32_t prefix, int pbits,
                            int shift, int nbits, uint64_t& target, uint64_t& above, uint32_t& digit, uint64_t& binw,
-                           float zmax, float invT, bool p_first, float top_p, uint64_t* S_out) {
+                           float zmax, float c2, bool p_first, float top_p, uint64_t* S_out) {
     SampSmem* sm = c.sm;
     const int tid = threadIdx.x;
     const int nb = 1 << nbits;
@@ -220,7 +277,7 @@ __device__ void radix_pass(Ctx& c, const View& v, const Keep& kp, bool use_topk,
         if (pbits && (key >> (32 - pbits)) != prefix) continue;
         if (use_topk && !kp.topk(key, v.idat(i))) continue;
         const uint32_t d = (key >> shift) & static_cast<uint32_t>(nb - 1);
-        const uint64_t w = kMass ? mass(z, zmax, invT) : 1ull;
+        const uint64_t w = kMass ? mass(z, zmax, c2) : 1ull;
         if (w) atomicAdd(&sm->hist[d], static_cast<unsigned long long>(w));
     }
     c.csync();
@@ -302,7 +359,329 @@ __device__ int tie_select(Ctx& c, const View& v, const Keep& kp, bool use_topk, 
     return best;
 }
 
+// ------------------------------------------------------------------ linear bins
+// Bin of a finite logit on 2048 bins linear in (zmax - z): bin 0 holds the
+// largest logits.  Monotone non-increasing in z, so "bin < b" implies a larger
+// logit than any element of bin b.
+struct Bins {
+    float zmax, scale;
+    int nb;  // number of bins (<= kHistBins)
+    __device__ __forceinline__ int operator()(float z) const {
+        if (scale == 0.f) return 0;
+        const float t = (zmax - z) * scale;
+        return t >= static_cast<float>(nb - 1) ? nb - 1 : static_cast<int>(t);
+    }
+};
+
+// Four consecutive logits of the slice starting at e (a multiple of 4); entries
+// at or past n read as -inf.  The vector path is used only for the shared-memory
+// copy of the slice, whose buffer is padded to a multiple of 4.
+__device__ __forceinline__ float4 load4(const View& v, int e, bool vec) {
+    float4 q;
+    if (vec) {
+        q = *reinterpret_cast<const float4*>(v.z + e);
+    } else {
+        q.x = e < v.n ? v.z[e] : 0.f;
+        q.y = e + 1 < v.n ? v.z[e + 1] : 0.f;
+        q.z = e + 2 < v.n ? v.z[e + 2] : 0.f;
+        q.w = e + 3 < v.n ? v.z[e + 3] : 0.f;
+    }
+    if (e >= v.n) q.x = -INFINITY;
+    if (e + 1 >= v.n) q.y = -INFINITY;
+    if (e + 2 >= v.n) q.z = -INFINITY;
+    if (e + 3 >= v.n) q.w = -INFINITY;
+    return q;
+}
+__device__ __forceinline__ float f4at(const float4& q, int j) {
+    return j == 0 ? q.x : (j == 1 ? q.y : (j == 2 ? q.z : q.w));
+}
+
+// Per-thread run length for thread-contiguous passes: a multiple of 4 with an
+// odd quotient, so that 16-byte loads of a quarter-warp hit distinct banks.
+__device__ __forceinline__ int run_len4(int n) {
+    int q = (n + 4 * kST - 1) / (4 * kST);
+    if (q < 1) q = 1;
+    if (!(q & 1)) ++q;
+    return 4 * q;
+}
+
+// Append the lane's candidate (when pred) to rank 0's gathered list; one remote
+// atomic per warp and element slot.  Every lane of the warp must call this.
+__device__ __forceinline__ void gather_push(bool pred, unsigned long long key, unsigned int* gcount0,
+                                            unsigned long long* list0) {
+    const unsigned int mask = __ballot_sync(0xffffffffu, pred);
+    if (mask == 0u) return;
+    const int lane = threadIdx.x & 31;
+    unsigned int base = 0;
+    if (lane == __ffs(mask) - 1) base = atomicAdd(gcount0, static_cast<unsigned int>(__popc(mask)));
+    base = __shfl_sync(0xffffffffu, base, __ffs(mask) - 1);
+    if (pred) {
+        const unsigned int pos = base + static_cast<unsigned int>(__popc(mask & ((1u << lane) - 1u)));
+        if (pos < static_cast<unsigned int>(kListCap)) list0[pos] = key;
+    }
+}
+
+// Sum over the cluster of this thread's 4 consecutive histogram bins (16-byte
+// remote loads, issued four ranks at a time).
+__device__ __forceinline__ void sum_remote_u4(cg::cluster_group& cl, unsigned int* h, int nc, uint32_t (&g)[4]) {
+#pragma unroll
+    for (int r0 = 0; r0 < kMaxCluster; r0 += 4) {
+        uint4 t[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (r0 + j < nc) t[j] = reinterpret_cast<const uint4*>(cl.map_shared_rank(h, r0 + j))[threadIdx.x];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (r0 + j < nc) {
+                g[0] += t[j].x;
+                g[1] += t[j].y;
+                g[2] += t[j].z;
+                g[3] += t[j].w;
+            }
+    }
+}
+__device__ __forceinline__ void sum_remote_f4(cg::cluster_group& cl, float* h, int nc, float (&g)[4]) {
+#pragma unroll
+    for (int r0 = 0; r0 < kMaxCluster; r0 += 4) {
+        float4 t[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (r0 + j < nc) t[j] = reinterpret_cast<const float4*>(cl.map_shared_rank(h, r0 + j))[threadIdx.x];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (r0 + j < nc) {
+                g[0] += t[j].x;
+                g[1] += t[j].y;
+                g[2] += t[j].z;
+                g[3] += t[j].w;
+            }
+    }
+}
+
+// ------------------------------------------------------------------ draw (whole cluster)
+// First kept id (ascending) whose running fixed-point mass exceeds
+// floor(u * S_p), S_p = total kept mass.  The CTA that holds it writes the token.
+// Ends with this CTA's arrival on the cluster barrier; the caller waits on it.
+__device__ void draw_pass(Ctx& c, const View& v, const Keep& kp, bool vec, float zmax, float c2, uint64_t seed,
+                          uint64_t offset, int32_t* tok_out) {
+    SampSmem* sm = c.sm;
+    const int tid = threadIdx.x;
+    const int E = run_len4(v.n);
+    const int b0 = min(v.n, tid * E), b1 = min(v.n, b0 + E);
+    const bool filt = kp.k_on || kp.p_on;
+    // -inf logits weigh 0, so without a filter every slot is simply summed
+    auto kept = [&](float z, int id) { return !filt || kp.keep_f(z, id); };
+    uint64_t w = 0;
+    if (!filt) {
+        for (int e = b0; e < b1; e += 4) {
+            const float4 q = load4(v, e, vec);
+            w += mass(q.x, zmax, c2) + mass(q.y, zmax, c2) + mass(q.z, zmax, c2) + mass(q.w, zmax, c2);
+        }
+    } else {
+        for (int e = b0; e < b1; e += 4) {
+            const float4 q = load4(v, e, vec);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float z = f4at(q, j);
+                if (kp.keep_f(z, v.idbase + e + j)) w += mass(z, zmax, c2);
+            }
+        }
+    }
+    uint64_t tot;
+    const uint64_t ex = block_excl_scan_u64(w, sm->wsum, tot);
+    if (tid == 0) sm->xch[c.xb][0] = tot;
+    exch(c, 1);
+    uint64_t Sp = 0, pre = 0;
+    for (int j = 0; j < c.nc; ++j) {
+        Sp += sm->gath[j][0];
+        if (j < c.rank) pre += sm->gath[j][0];
+    }
+    cluster_arrive();  // all remote reads of this CTA are done
+    const uint64_t u53 = philox_word0(seed, offset) >> 11;
+    const uint64_t X = static_cast<uint64_t>((static_cast<unsigned __int128>(u53) * Sp) >> 53);  // floor(u*Sp) < Sp
+    if (pre + ex <= X && X < pre + ex + w) {
+        uint64_t cum = pre + ex;
+        for (int e = b0; e < b1; ++e) {
+            const float z = v.z[e];
+            const int id = v.idbase + e;
+            if (!kept(z, id)) continue;
+            cum += mass(z, zmax, c2);
+            if (cum > X) {
+                *tok_out = id;
+                break;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ rank-0 finish on a gathered list
+// The list holds n distinct candidate sort keys, a superset of the top-kk set.
+// Small lists (n <= 128): the first four warps alone; candidate i computes its
+// rank, its cumulative mass in rank order and its cumulative mass in id order
+// directly (no sort), with a 128-thread named barrier instead of CTA barriers.
+constexpr int kSmallList = 128;
+
+__device__ __forceinline__ void sync128() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ uint64_t reduce128(uint64_t v, unsigned long long* scratch) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
+    sync128();
+    const uint64_t t = scratch[0] + scratch[1] + scratch[2] + scratch[3];
+    sync128();
+    return t;
+}
+
+__device__ void solo_finish_small(SampSmem* sm, int n, int kk, float pp, float zmax, float c2, uint64_t seed,
+                                  uint64_t offset, int32_t* tok_out) {
+    const int i = threadIdx.x;
+    if (i >= 128) return;
+    const unsigned long long* a = sm->list;
+    unsigned long long* wv = sm->hist;                                    // masses [n]
+    unsigned int* rk = reinterpret_cast<unsigned int*>(sm->hist + kListCap / 4);  // ranks [n]
+    unsigned int* kf = rk + kListCap / 4;                                  // kept flags [n]
+    unsigned long long ki = 0;
+    unsigned int rank = 0;
+    uint64_t W = 0;
+    if (i < n) {
+        ki = a[i];
+        for (int j = 0; j < n; ++j) rank += (a[j] > ki) ? 1u : 0u;
+        W = mass(key_float(static_cast<uint32_t>(ki >> 32)), zmax, c2);
+        wv[i] = W;
+        rk[i] = rank;
+    }
+    const bool in_k = i < n && rank < static_cast<unsigned int>(kk);
+    const uint64_t sk = reduce128(in_k ? W : 0ull, sm->wsum);  // its barriers also publish wv / rk
+    bool kept = in_k;
+    if (pp < 1.f && in_k) {
+        const uint64_t target = ceil_mul_p(pp, sk);
+        uint64_t before = 0;
+        for (int j = 0; j < n; ++j)
+            if (rk[j] < rank) before += wv[j];
+        kept = before < target;  // inside the smallest prefix whose mass reaches target
+    }
+    if (i < n) kf[i] = kept ? 1u : 0u;
+    const uint64_t Sp = reduce128(kept ? W : 0ull, sm->wsum);
+    if (kept && W > 0) {
+        const uint64_t u53 = philox_word0(seed, offset) >> 11;
+        const uint64_t X = static_cast<uint64_t>((static_cast<unsigned __int128>(u53) * Sp) >> 53);
+        const int id = sort_key_id(ki);
+        uint64_t before = 0;
+        for (int j = 0; j < n; ++j)
+            if (kf[j] && sort_key_id(a[j]) < id) before += wv[j];
+        if (before <= X && X < before + W) *tok_out = id;
+    }
+}
+
+// Larger lists: bitonic sort by (z desc, id asc), keep the first kk, apply
+// top-p exactly, re-sort the kept tokens by id and draw.
+__device__ void solo_finish(SampSmem* sm, int n, int kk, float pp, float zmax, float c2, uint64_t seed,
+                            uint64_t offset, int32_t* tok_out) {
+    if (n <= kSmallList) {
+        solo_finish_small(sm, n, kk, pp, zmax, c2, seed, offset, tok_out);
+        return;
+    }
+    const int tid = threadIdx.x;
+    unsigned long long* a = sm->list;
+    const int np2 = pow2_ceil(n);
+    for (int i = n + tid; i < np2; i += kST) a[i] = 0ull;
+    if (tid == 0) sm->bc[1] = static_cast<unsigned long long>(min(kk, n));
+    __syncthreads();
+    bitonic_sort(a, np2, true);
+    const int m0 = min(kk, n);
+    int m = m0;
+    {
+        const int E = run_len(m0);
+        const int b0 = min(m0, tid * E), b1 = min(m0, b0 + E);
+        uint64_t w = 0;
+        for (int j = b0; j < b1; ++j) w += mass(key_float(static_cast<uint32_t>(a[j] >> 32)), zmax, c2);
+        uint64_t tot;
+        const uint64_t ex = block_excl_scan_u64(w, sm->wsum, tot);
+        if (pp < 1.f) {
+            const uint64_t target = ceil_mul_p(pp, tot);
+            if (ex < target && ex + w >= target) {
+                uint64_t cum = ex;
+                for (int j = b0; j < b1; ++j) {
+                    cum += mass(key_float(static_cast<uint32_t>(a[j] >> 32)), zmax, c2);
+                    if (cum >= target) {
+                        sm->bc[1] = static_cast<unsigned long long>(j + 1);
+                        break;
+                    }
+                }
+            }
+            __syncthreads();
+            m = static_cast<int>(sm->bc[1]);
+        }
+    }
+    __syncthreads();
+    // kept tokens re-keyed as (id << 41 | mass) and sorted by id
+    for (int j = tid; j < m; j += kST) {
+        const unsigned long long k = a[j];
+        const uint64_t W = mass(key_float(static_cast<uint32_t>(k >> 32)), zmax, c2);
+        a[j] = (static_cast<unsigned long long>(sort_key_id(k)) << 41) | W;
+    }
+    const int mp2 = pow2_ceil(m);
+    for (int i = m + tid; i < mp2; i += kST) a[i] = ~0ull;
+    __syncthreads();
+    bitonic_sort(a, mp2, false);
+    const unsigned long long wmask = (1ull << 41) - 1;
+    const int E = run_len(m);
+    const int b0 = min(m, tid * E), b1 = min(m, b0 + E);
+    uint64_t w = 0;
+    for (int j = b0; j < b1; ++j) w += a[j] & wmask;
+    uint64_t Sp;
+    const uint64_t ex = block_excl_scan_u64(w, sm->wsum, Sp);
+    const uint64_t u53 = philox_word0(seed, offset) >> 11;
+    const uint64_t X = static_cast<uint64_t>((static_cast<unsigned __int128>(u53) * Sp) >> 53);
+    if (ex <= X && X < ex + w) {
+        uint64_t cum = ex;
+        for (int j = b0; j < b1; ++j) {
+            cum += a[j] & wmask;
+            if (cum > X) {
+                *tok_out = static_cast<int>(a[j] >> 41);
+                break;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ exact fallback (whole cluster)
+__device__ void fallback_select_and_draw(Ctx& c, const View& v, Keep& kp, bool vec, int kk, float pp, float zmax,
+                                         float c2, uint64_t seed, uint64_t offset, int32_t* tok_out) {
+    if (kk > 0) {
+        kp.k_on = true;
+        uint64_t target = static_cast<uint64_t>(kk), above = 0, binw = 0;
+        uint32_t d0, d1, d2;
+        radix_pass<false>(c, v, kp, false, 0u, 0, 21, 11, target, above, d0, binw, zmax, c2, false, 0.f, nullptr);
+        radix_pass<false>(c, v, kp, false, d0, 11, 10, 11, target, above, d1, binw, zmax, c2, false, 0.f, nullptr);
+        radix_pass<false>(c, v, kp, false, (d0 << 11) | d1, 22, 0, 10, target, above, d2, binw, zmax, c2, false, 0.f,
+                          nullptr);
+        kp.tauk = (d0 << 21) | (d1 << 10) | d2;
+        kp.zk = key_float(kp.tauk);
+        kp.idk = tie_select(c, v, kp, false, kp.tauk, target - above);
+    }
+    if (pp < 1.f) {
+        kp.p_on = true;
+        uint64_t target = 0, above = 0, binw = 0, Sk = 0;
+        uint32_t d0, d1, d2;
+        radix_pass<true>(c, v, kp, true, 0u, 0, 21, 11, target, above, d0, binw, zmax, c2, true, pp, &Sk);
+        radix_pass<true>(c, v, kp, true, d0, 11, 10, 11, target, above, d1, binw, zmax, c2, false, 0.f, nullptr);
+        radix_pass<true>(c, v, kp, true, (d0 << 11) | d1, 22, 0, 10, target, above, d2, binw, zmax, c2, false, 0.f,
+                         nullptr);
+        kp.taup = (d0 << 21) | (d1 << 10) | d2;
+        const uint64_t wt = mass(key_float(kp.taup), zmax, c2);
+        uint64_t need = 1;
+        if (wt > 0 && target > above) need = (target - above + wt - 1) / wt;
+        kp.zp = key_float(kp.taup);
+        kp.idp = tie_select(c, v, kp, true, kp.taup, need);
+    }
+    draw_pass(c, v, kp, vec, zmax, c2, seed, offset, tok_out);
+}
+
 // ------------------------------------------------------------------ kernel
+constexpr int kLoadChunks = 4;
+
 __global__ void __launch_bounds__(kST, 2)
     sampler_kernel(int32_t* __restrict__ tokens, const float* __restrict__ logits, int V, int S, int smem_slice,
                    const float* __restrict__ temperature, const int32_t* __restrict__ top_k,
@@ -317,230 +696,438 @@ __global__ void __launch_bounds__(kST, 2)
     c.nc = static_cast<int>(cluster.num_blocks());
     c.rank = static_cast<int>(cluster.block_rank());
     c.xb = 0;
-    c.solo = false;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int row = blockIdx.x / c.nc;
     const int lo = c.rank * S;
     const int n = max(0, min(S, V - lo));
     const float* grow = logits + static_cast<size_t>(row) * V + lo;
+    int32_t* tok_out = tokens + row;
 
-    // ---- load this CTA's slice (bulk copy when 16-byte aligned)
     View v;
     v.id = nullptr;
     v.n = n;
     v.idbase = lo;
+    v.z = smem_slice ? zslice : grow;
+    const bool vec = smem_slice != 0;
+
+    // row parameters first: they decide what the passes must track
+    const float T = temperature[row];
+    const float pp = top_p[row];
+    const int kk_in = top_k[row];
+    const uint64_t seed = seeds[row], offset = offsets[row];
+    const int nvec = (n + 3) & ~3;  // element slots visited by the 4-wide loops
+
+    // ---- load (chunked bulk copies) overlapped with the first pass: max and min
+    // over finite logits, NaN/+inf flag
+    float zmx = -INFINITY, zmn = INFINITY;
+    unsigned int bad = 0;
+    auto stat1 = [&](float z) {
+        zmx = fmaxf(zmx, z);
+        zmn = fminf(zmn, z > -INFINITY ? z : INFINITY);
+        bad |= (z < INFINITY) ? 0u : 1u;  // NaN or +inf
+    };
+    if (tid == 0) sm->gcount = 0u;
     if (smem_slice) {
         const bool aligned = ((reinterpret_cast<uintptr_t>(grow) & 15u) == 0);
         const int nbulk = aligned ? (n & ~3) : 0;
+        const int cs = ((nbulk + 4 * kLoadChunks - 1) / (4 * kLoadChunks)) * 4;  // chunk length, multiple of 4
         if (tid == 0) {
-            mbar_init(&sm->bar, 1);
+            for (int k = 0; k < kLoadChunks; ++k) mbar_init(&sm->bar[k], 1);
             fence_mbar_init();
         }
         __syncthreads();
         if (tid == 0) {
-            if (nbulk > 0) {
-                mbar_arrive_expect_tx(&sm->bar, static_cast<uint32_t>(nbulk) * 4u);
-                tma_load_1d(zslice, grow, static_cast<uint32_t>(nbulk) * 4u, &sm->bar);
-            } else {
-                mbar_arrive(&sm->bar);
+            for (int k = 0; k < kLoadChunks; ++k) {
+                const int c0 = min(nbulk, k * cs), c1 = min(nbulk, c0 + cs);
+                if (c1 > c0) {
+                    mbar_arrive_expect_tx(&sm->bar[k], static_cast<uint32_t>(c1 - c0) * 4u);
+                    tma_load_1d(zslice + c0, grow + c0, static_cast<uint32_t>(c1 - c0) * 4u, &sm->bar[k]);
+                } else {
+                    mbar_arrive(&sm->bar[k]);
+                }
             }
         }
-        for (int i = nbulk + tid; i < n; i += kST) zslice[i] = grow[i];
-        if (!mbar_wait(&sm->bar, 0)) report(status, PKV_ERR_TIMEOUT);
-        __syncthreads();
-        v.z = zslice;
-    } else {
-        v.z = grow;
-    }
-
-    // ---- pass 1: max / argmax / finite count / non-finite flag
-    uint64_t best = 0ull, nfin = 0ull, bad = 0ull;
-    for (int i = tid; i < n; i += kST) {
-        const float z = v.z[i];
-        if (isfinite(z)) {
-            ++nfin;
-            const uint64_t pk = (static_cast<uint64_t>(okey(z)) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(lo + i));
-            best = pk > best ? pk : best;
-        } else if (!(z < 0.f)) {
-            bad = 1ull;  // NaN or +inf
+        for (int i = nbulk + tid; i < S; i += kST) zslice[i] = i < n ? grow[i] : -INFINITY;  // tail and padding
+        for (int k = 0; k < kLoadChunks; ++k) {
+            const int c0 = min(nbulk, k * cs), c1 = min(nbulk, c0 + cs);
+            if (!mbar_wait(&sm->bar[k], 0)) report(status, PKV_ERR_TIMEOUT);
+            for (int e = c0 + 4 * tid; e < c1; e += 4 * kST) {
+                const float4 q = *reinterpret_cast<const float4*>(zslice + e);
+                stat1(q.x);
+                stat1(q.y);
+                stat1(q.z);
+                stat1(q.w);
+            }
         }
+        __syncthreads();  // tail written by every thread is visible
+        for (int i = nbulk + tid; i < n; i += kST) stat1(zslice[i]);
+    } else {
+        for (int i = tid; i < n; i += kST) stat1(grow[i]);
     }
+    const float tmax = zmx;  // this thread's own maximum
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-        const uint64_t b2 = __shfl_xor_sync(0xffffffffu, best, o);
-        best = b2 > best ? b2 : best;
-        nfin += __shfl_xor_sync(0xffffffffu, nfin, o);
+        zmx = fmaxf(zmx, __shfl_xor_sync(0xffffffffu, zmx, o));
+        zmn = fminf(zmn, __shfl_xor_sync(0xffffffffu, zmn, o));
         bad |= __shfl_xor_sync(0xffffffffu, bad, o);
     }
     {
-        __shared__ unsigned long long wb[kSW][3];
-        if ((tid & 31) == 0) {
-            wb[tid >> 5][0] = best;
-            wb[tid >> 5][1] = nfin;
-            wb[tid >> 5][2] = bad;
+        __shared__ float wz[kSW], wn[kSW];
+        __shared__ unsigned int wb[kSW];
+        __shared__ float lmax_sh, lmin_sh, xr_sh;
+        __shared__ unsigned int h64[64];
+        if (lane == 0) {
+            wz[warp] = zmx;
+            wn[warp] = zmn;
+            wb[warp] = bad;
         }
+        if (tid < 64) h64[tid] = 0u;
         __syncthreads();
         if (tid == 0) {
-            uint64_t b = 0, f = 0, x = 0;
+            float z = -INFINITY, zn = INFINITY;
+            unsigned int b = 0;
             for (int w = 0; w < kSW; ++w) {
-                b = wb[w][0] > b ? wb[w][0] : b;
-                f += wb[w][1];
-                x |= wb[w][2];
+                z = fmaxf(z, wz[w]);
+                zn = fminf(zn, wn[w]);
+                b |= wb[w];
             }
-            sm->xch[c.xb][0] = b;
-            sm->xch[c.xb][1] = f;
-            sm->xch[c.xb][2] = x;
+            lmax_sh = z;
+            lmin_sh = zn;
+            xr_sh = -INFINITY;
+            sm->xch[c.xb][0] = __float_as_uint(z);
+            sm->xch[c.xb][1] = __float_as_uint(zn);
+            sm->xch[c.xb][2] = b;
+        }
+        __syncthreads();
+        // Local top-k bound: x_r such that at least top_k of this CTA's thread
+        // maxima (hence top_k distinct logits) are >= x_r; then no member of the
+        // row's top-k set lies below x_r.  Found on 64 bins over [min, max].
+        if (kk_in > 0 && kk_in <= kST && T > 0.f) {
+            const float lmax = lmax_sh, range = lmax_sh - lmin_sh;
+            if (range > 0.f && range < INFINITY && tmax > -INFINITY) {
+                const float t = (lmax - tmax) * (64.0f / range);
+                atomicAdd(&h64[t >= 63.f ? 63 : static_cast<int>(t)], 1u);
+            }
+            __syncthreads();
+            if (warp == 0 && range > 0.f && range < INFINITY) {
+                const unsigned int two = h64[2 * lane] + h64[2 * lane + 1];
+                unsigned int inc = two;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned int y = __shfl_up_sync(0xffffffffu, inc, o);
+                    if (lane >= o) inc += y;
+                }
+                const unsigned int exl = inc - two;
+                const unsigned int kq = static_cast<unsigned int>(kk_in);
+                if (exl < kq && inc >= kq) {
+                    const int b = exl + h64[2 * lane] >= kq ? 2 * lane : 2 * lane + 1;
+                    xr_sh = lmax - (static_cast<float>(b) + 2.0f) * (range / 64.0f);  // one bin of margin
+                }
+            }
+            __syncthreads();
+            if (tid == 0) sm->xch[c.xb][3] = __float_as_uint(xr_sh);
+        } else if (tid == 0) {
+            sm->xch[c.xb][3] = __float_as_uint(-INFINITY);
         }
     }
-    exch(c, 3);
-    uint64_t gbest = 0, gfin = 0, gbad = 0;
+    exch(c, 4);
+    float zmax = -INFINITY, zmin = INFINITY, kbound = -INFINITY;
+    unsigned int gbad = 0;
     for (int j = 0; j < c.nc; ++j) {
-        gbest = sm->gath[j][0] > gbest ? sm->gath[j][0] : gbest;
-        gfin += sm->gath[j][1];
-        gbad |= sm->gath[j][2];
+        zmax = fmaxf(zmax, __uint_as_float(static_cast<uint32_t>(sm->gath[j][0])));
+        zmin = fminf(zmin, __uint_as_float(static_cast<uint32_t>(sm->gath[j][1])));
+        gbad |= static_cast<unsigned int>(sm->gath[j][2]);
+        kbound = fmaxf(kbound, __uint_as_float(static_cast<uint32_t>(sm->gath[j][3])));
     }
-    const float T = temperature[row];
-    const float pp = top_p[row];
-    const int kk_in = top_k[row];
-    int token = -1;
     int err = 0;
-    if (gbad || gfin == 0) err = PKV_ERR_NONFINITE;
+    if (gbad || !(zmax > -INFINITY)) err = PKV_ERR_NONFINITE;  // NaN / +inf, or no finite logit
     else if (!(T >= 0.f)) err = PKV_ERR_INVALID_ARG;
-    else if (T == 0.f) token = static_cast<int>(~static_cast<uint32_t>(gbest & 0xffffffffull));
-    else if (!(pp > 0.f)) err = PKV_ERR_INVALID_ARG;
-    if (err || token >= 0) {
+    else if (T != 0.f && !(pp > 0.f)) err = PKV_ERR_INVALID_ARG;
+    if (err) {
         if (c.rank == 0 && tid == 0) {
-            tokens[row] = err ? -1 : token;
-            if (err) report(status, err);
+            *tok_out = -1;
+            report(status, err);
         }
         cluster.sync();  // no CTA leaves while a peer may still read its shared memory
         return;
     }
+    if (T == 0.f) {
+        // greedy: the lowest id holding the maximum
+        int amin = INT_MAX;
+        for (int e = 4 * tid; e < nvec; e += 4 * kST) {
+            const float4 q = load4(v, e, vec);
+            if (q.w == zmax) amin = lo + e + 3;
+            if (q.z == zmax) amin = lo + e + 2;
+            if (q.y == zmax) amin = lo + e + 1;
+            if (q.x == zmax) amin = lo + e;
+            if (amin != INT_MAX) break;  // later slots of this thread hold larger ids
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amin = min(amin, __shfl_xor_sync(0xffffffffu, amin, o));
+        if (tid == 0) sm->imin = INT_MAX;
+        __syncthreads();
+        if (lane == 0 && amin != INT_MAX) atomicMin(&sm->imin, amin);
+        __syncthreads();
+        if (tid == 0) sm->xch[c.xb][0] = static_cast<uint32_t>(sm->imin);
+        exch(c, 1);
+        if (c.rank == 0 && tid == 0) {
+            int a = INT_MAX;
+            for (int j = 0; j < c.nc; ++j) a = min(a, static_cast<int>(static_cast<uint32_t>(sm->gath[j][0])));
+            *tok_out = a;
+        }
+        cluster.sync();
+        return;
+    }
 
-    const float zmax = key_float(static_cast<uint32_t>(gbest >> 32));
-    const float invT = 1.0f / T;
-    const int kk = (kk_in > 0 && static_cast<uint64_t>(kk_in) < gfin) ? kk_in : 0;
+    const float c2 = fminf(1.4426950408889634f / T, 1.0e30f);  // log2(e) / T, kept finite
     Keep kp;
-    kp.k_on = kk > 0;
-    kp.p_on = pp < 1.0f;
+    kp.k_on = false;
+    kp.p_on = false;
     kp.tauk = kp.taup = 0u;
     kp.idk = kp.idp = INT_MAX;
+    kp.zk = kp.zp = 0.f;
+    Bins bins;
+    bins.zmax = zmax;
+    bins.nb = kHistBins;
+    {
+        const float range = zmax - zmin;
+        const float sc = static_cast<float>(kHistBins) / range;
+        bins.scale = (range > 0.f && sc < INFINITY) ? sc : 0.f;
+    }
+    unsigned int* cnt = reinterpret_cast<unsigned int*>(sm->hist);
+    float* fmass = reinterpret_cast<float*>(sm->hist) + kHistBins;
+    unsigned int* gcount0 = cluster.map_shared_rank(&sm->gcount, 0);
+    unsigned long long* list0 = cluster.map_shared_rank(&sm->list[0], 0);
+    int kk = 0;  // effective top-k (0: off); set once the finite count is known
 
-    // ---- top-k: three count passes (11/11/10 bits), candidate gather after the first
-    if (kp.k_on) {
-        uint64_t target = static_cast<uint64_t>(kk), above = 0, binw = 0;
-        uint32_t d0, d1, d2;
-        radix_pass<false>(c, v, kp, false, 0u, 0, 21, 11, target, above, d0, binw, zmax, invT, false, 0.f, nullptr);
-        // Candidates: finite keys whose top digit is >= d0 (a superset of the top-k set).
-        {
-            const int E = run_len(v.n);
-            const int b0 = min(v.n, tid * E), b1 = min(v.n, b0 + E);
-            uint64_t cnt = 0;
-            for (int i = b0; i < b1; ++i) {
-                const float z = v.z[i];
-                cnt += (isfinite(z) && (okey(z) >> 21) >= d0) ? 1u : 0u;
-            }
-            uint64_t tot;
-            const uint64_t ex = block_excl_scan_u64(cnt, sm->wsum, tot);
-            if (tid == 0) sm->xch[c.xb][0] = tot;
-            exch(c, 1);
-            uint64_t all = 0, pre = 0;
-            for (int j = 0; j < c.nc; ++j) {
-                all += sm->gath[j][0];
-                if (j < c.rank) pre += sm->gath[j][0];
-            }
-            if (all <= static_cast<uint64_t>(kListCap)) {
-                // gather every rank's candidates, in id order, into rank 0
-                float* lz = cluster.map_shared_rank(&sm->list_z[0], 0);
-                int* li = cluster.map_shared_rank(&sm->list_id[0], 0);
-                uint64_t pos = pre + ex;
-                for (int i = b0; i < b1; ++i) {
-                    const float z = v.z[i];
-                    if (isfinite(z) && (okey(z) >> 21) >= d0) {
-                        lz[pos] = z;
-                        li[pos] = lo + i;
-                        ++pos;
+    if (kk_in > 0) {
+        // ---------------- top-k: count histogram over [kbound, zmax] (every top-k
+        // member is >= kbound), candidate bin, gather, finish on rank 0
+        const bool bounded = kbound > -INFINITY;
+        Bins kb = bins;
+        if (bounded) {
+            kb.nb = kTopkBins;
+            const float range = zmax - kbound;
+            const float sc = static_cast<float>(kTopkBins) / range;
+            kb.scale = (range > 0.f && sc < INFINITY) ? sc : 0.f;
+        }
+        const float zfloor = bounded ? kbound : -INFINITY;
+        for (int i = tid; i < kb.nb; i += kST) cnt[i] = 0u;
+        if (tid == 0) {
+            sm->bc[0] = kb.nb - 1;
+            sm->bc[1] = 0;
+        }
+        __syncthreads();
+        for (int e = 4 * tid; e < nvec; e += 4 * kST) {
+            const float4 q = load4(v, e, vec);
+            if (q.x > -INFINITY && q.x >= zfloor) atomicAdd(&cnt[kb(q.x)], 1u);
+            if (q.y > -INFINITY && q.y >= zfloor) atomicAdd(&cnt[kb(q.y)], 1u);
+            if (q.z > -INFINITY && q.z >= zfloor) atomicAdd(&cnt[kb(q.z)], 1u);
+            if (q.w > -INFINITY && q.w >= zfloor) atomicAdd(&cnt[kb(q.w)], 1u);
+        }
+        cluster.sync();
+        uint32_t g[4] = {0u, 0u, 0u, 0u};
+        if (tid * 4 < kb.nb) sum_remote_u4(cluster, cnt, c.nc, g);
+        const uint64_t tsum = static_cast<uint64_t>(g[0]) + g[1] + g[2] + g[3];
+        uint64_t counted;  // unbounded: every finite logit; bounded: those >= kbound (>= top_k of them)
+        const uint64_t ex = block_excl_scan_u64(tsum, sm->wsum, counted);
+        if (bounded || static_cast<uint64_t>(kk_in) < counted) {
+            kk = kk_in;
+            if (ex < static_cast<uint64_t>(kk) && ex + tsum >= static_cast<uint64_t>(kk)) {
+                uint64_t cc = ex;
+                for (int q = 0; q < 4; ++q) {
+                    cc += g[q];
+                    if (cc >= static_cast<uint64_t>(kk)) {
+                        sm->bc[0] = static_cast<unsigned long long>(tid * 4 + q);
+                        sm->bc[1] = cc;  // candidates: every counted logit in bins 0..bk
+                        break;
                     }
                 }
-                cluster.sync();
-                if (c.rank != 0) return;  // rank 0 finishes the row alone
-                c.solo = true;
-                v.z = sm->list_z;
-                v.id = sm->list_id;
-                v.n = static_cast<int>(all);
-                v.idbase = 0;
+            }
+            __syncthreads();
+            const int bk = static_cast<int>(sm->bc[0]);
+            const uint64_t total = sm->bc[1];
+            if (total >= static_cast<uint64_t>(kk) && total <= static_cast<uint64_t>(kListCap)) {
+                // every candidate has z >= zlow (two bins of margin for rounding)
+                const float zlow =
+                    kb.scale > 0.f ? fmaxf(zfloor, zmax - (static_cast<float>(bk) + 3.0f) / kb.scale) : zfloor;
+                for (int e = 4 * tid - 4 * lane; e < nvec; e += 4 * kST) {  // warp-uniform trip count
+                    const int el = e + 4 * lane;
+                    const float4 q =
+                        el < nvec ? load4(v, el, vec) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                    const bool any = q.x >= zlow || q.y >= zlow || q.z >= zlow || q.w >= zlow;
+                    if (!__any_sync(0xffffffffu, any)) continue;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float z = f4at(q, j);
+                        const bool pred = z > -INFINITY && z >= zfloor && kb(z) <= bk;
+                        gather_push(pred, pred ? sort_key(z, lo + el + j) : 0ull, gcount0, list0);
+                    }
+                }
+                cluster.sync();  // candidates complete in rank 0; no remote access follows
+                if (c.rank != 0) return;
+                solo_finish(sm, static_cast<int>(total), kk, pp, zmax, c2, seed, offset, tok_out);
+                return;
+            }
+            cluster.sync();  // remote histogram reads are done before the fallback reuses it
+            fallback_select_and_draw(c, v, kp, vec, kk, pp, zmax, c2, seed, offset, tok_out);
+            cluster_wait();
+            return;
+        }
+        cluster.sync();  // top_k >= finite count: top-k is off; the histogram is reused below
+    }
+
+    if (pp < 1.f) {
+        // ---------------- top-p only: approximate fp32 bin masses locate the cut,
+        // rank 0 resolves it exactly on the gathered bins around it
+        for (int i = tid; i < kHistBins; i += kST) {
+            cnt[i] = 0u;
+            fmass[i] = 0.f;
+        }
+        if (tid == 0) {
+            sm->bc[2] = kHistBins - 1;
+            sm->bc[3] = kHistBins - 1;
+        }
+        __syncthreads();
+        uint64_t st = 0;
+        for (int e = 4 * tid; e < nvec; e += 4 * kST) {
+            const float4 q = load4(v, e, vec);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float z = f4at(q, j);
+                if (!(z > -INFINITY)) continue;
+                const int b = bins(z);
+                const float wf = weight(z, zmax, c2);
+                st += fx40(wf);
+                atomicAdd(&cnt[b], 1u);
+                atomicAdd(&fmass[b], wf);
             }
         }
-        const uint32_t p1 = d0;
-        radix_pass<false>(c, v, kp, false, p1, 11, 10, 11, target, above, d1, binw, zmax, invT, false, 0.f, nullptr);
-        const uint32_t p2 = (d0 << 11) | d1;
-        radix_pass<false>(c, v, kp, false, p2, 22, 0, 10, target, above, d2, binw, zmax, invT, false, 0.f, nullptr);
-        kp.tauk = (d0 << 21) | (d1 << 10) | d2;
-        kp.idk = tie_select(c, v, kp, false, kp.tauk, target - above);
-    }
-
-    // ---- top-p: three mass passes over the top-k set; the first also yields S_k
-    if (kp.p_on) {
-        uint64_t target = 0, above = 0, binw = 0, Sk = 0;
-        uint32_t d0, d1, d2;
-        radix_pass<true>(c, v, kp, true, 0u, 0, 21, 11, target, above, d0, binw, zmax, invT, true, pp, &Sk);
-        radix_pass<true>(c, v, kp, true, d0, 11, 10, 11, target, above, d1, binw, zmax, invT, false, 0.f, nullptr);
-        radix_pass<true>(c, v, kp, true, (d0 << 11) | d1, 22, 0, 10, target, above, d2, binw, zmax, invT, false, 0.f,
-                         nullptr);
-        kp.taup = (d0 << 21) | (d1 << 10) | d2;
-        const uint64_t wt = mass(key_float(kp.taup), zmax, invT);
-        uint64_t need = 1;
-        if (wt > 0 && target > above) need = (target - above + wt - 1) / wt;
-        kp.idp = tie_select(c, v, kp, true, kp.taup, need);
-    }
-
-    // ---- draw: first kept id (ascending) whose running mass exceeds u * S_p
-    {
-        const int E = run_len(v.n);
-        const int b0 = min(v.n, tid * E), b1 = min(v.n, b0 + E);
-        uint64_t w = 0;
-        for (int i = b0; i < b1; ++i) {
-            const float z = v.z[i];
-            if (!isfinite(z)) continue;
-            const uint32_t key = okey(z);
-            const int id = v.idat(i);
-            if (kp.topk(key, id) && kp.topp(key, id)) w += mass(z, zmax, invT);
+        uint64_t scta;
+        block_excl_scan_u64(st, sm->wsum, scta);
+        if (tid == 0) sm->xch[c.xb][0] = scta;
+        exch(c, 1);  // also publishes every CTA's histograms
+        uint64_t S = 0;
+        for (int j = 0; j < c.nc; ++j) S += sm->gath[j][0];
+        const uint64_t target = ceil_mul_p(pp, S);
+        const uint64_t eps = S / 10000 + 1;
+        const uint64_t lo_t = target > eps ? target - eps : 0;
+        const uint64_t hi_t = target + eps;
+        float fs[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t gcn[4] = {0u, 0u, 0u, 0u};
+        sum_remote_f4(cluster, fmass, c.nc, fs);
+        sum_remote_u4(cluster, cnt, c.nc, gcn);
+        uint64_t gm[4];
+        uint64_t tsum = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            gm[q] = static_cast<uint64_t>(static_cast<double>(fs[q]) * 1099511627776.0);
+            tsum += gm[q];
         }
-        if (tid == 0) sm->imin = INT_MAX;
         uint64_t tot;
-        const uint64_t ex = block_excl_scan_u64(w, sm->wsum, tot);
-        if (tid == 0) sm->xch[c.xb][0] = tot;
-        exch(c, 1);
-        uint64_t Sp = 0, pre = 0;
-        for (int j = 0; j < c.nce(); ++j) {
-            Sp += sm->gath[j][0];
-            if (j < c.rke()) pre += sm->gath[j][0];
-        }
-        const uint64_t u53 = philox_word0(seeds[row], offsets[row]) >> 11;
-        const uint64_t X = static_cast<uint64_t>((static_cast<unsigned __int128>(u53) * Sp) >> 53);  // floor(u*Sp) < Sp
-        if (pre <= X && X < pre + tot && pre + ex <= X && X < pre + ex + w) {
-            uint64_t cum = pre + ex;
-            for (int i = b0; i < b1; ++i) {
-                const float z = v.z[i];
-                if (!isfinite(z)) continue;
-                const uint32_t key = okey(z);
-                const int id = v.idat(i);
-                if (!(kp.topk(key, id) && kp.topp(key, id))) continue;
-                cum += mass(z, zmax, invT);
-                if (cum > X) {
-                    atomicMin(&sm->imin, id);
-                    break;
-                }
+        const uint64_t ex = block_excl_scan_u64(tsum, sm->wsum, tot);
+        {
+            uint64_t cc = ex;
+            for (int q = 0; q < 4; ++q) {
+                // first bin whose inclusive approximate cumulative reaches lo_t / hi_t
+                const int b = tid * 4 + q;
+                const uint64_t nx = cc + gm[q];
+                if (nx >= lo_t && (b == 0 || cc < lo_t)) sm->bc[2] = static_cast<unsigned long long>(b);
+                if (nx >= hi_t && (b == 0 || cc < hi_t)) sm->bc[3] = static_cast<unsigned long long>(b);
+                cc = nx;
             }
         }
         __syncthreads();
-        if (tid == 0) sm->xch[c.xb][0] = static_cast<unsigned long long>(static_cast<uint32_t>(sm->imin));
-        exch(c, 1);
-        int tok = INT_MAX;
-        for (int j = 0; j < c.nce(); ++j) tok = min(tok, static_cast<int>(static_cast<uint32_t>(sm->gath[j][0])));
-        if (c.rke() == 0 && tid == 0) tokens[row] = tok == INT_MAX ? -1 : tok;
+        const int blo = static_cast<int>(sm->bc[2]);
+        const int bhi = max(blo, static_cast<int>(sm->bc[3]));
+        // exact count of the window from the summed histograms
+        uint64_t wc = 0;
+        for (int q = 0; q < 4; ++q) {
+            const int b = tid * 4 + q;
+            if (b >= blo && b <= bhi) wc += gcn[q];
+        }
+        uint64_t total;
+        block_excl_scan_u64(wc, sm->wsum, total);
+        if (total >= 1 && total <= static_cast<uint64_t>(kListCap)) {
+            uint64_t at = 0;
+            for (int e = 4 * tid - 4 * lane; e < nvec; e += 4 * kST) {  // warp-uniform trip count
+                const int el = e + 4 * lane;
+                const float4 q = el < nvec ? load4(v, el, vec) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float z = f4at(q, j);
+                    const bool fin = z > -INFINITY;
+                    const int b = fin ? bins(z) : kHistBins;
+                    if (fin && b < blo) at += mass(z, zmax, c2);
+                    const bool pred = fin && b >= blo && b <= bhi;
+                    gather_push(pred, pred ? sort_key(z, lo + el + j) : 0ull, gcount0, list0);
+                }
+            }
+            uint64_t acta;
+            block_excl_scan_u64(at, sm->wsum, acta);
+            if (tid == 0) *cluster.map_shared_rank(&sm->aslot[c.rank], 0) = acta;
+            cluster.sync();  // window gathered and exact masses above it posted in rank 0
+            if (c.rank == 0) {
+                uint64_t A = 0;
+                for (int r = 0; r < c.nc; ++r) A += sm->aslot[r];
+                unsigned long long* a = sm->list;
+                const int nw = static_cast<int>(total);
+                const int np2 = pow2_ceil(nw);
+                for (int i = nw + tid; i < np2; i += kST) a[i] = 0ull;
+                if (tid == 0) {
+                    sm->bc[4] = 0ull;  // ok flag
+                    sm->bc[5] = 0ull;
+                    sm->bc[6] = 0ull;
+                }
+                __syncthreads();
+                bitonic_sort(a, np2, true);
+                const int E = run_len(nw);
+                const int b0 = min(nw, tid * E), b1 = min(nw, b0 + E);
+                uint64_t w = 0;
+                for (int j = b0; j < b1; ++j) w += mass(key_float(static_cast<uint32_t>(a[j] >> 32)), zmax, c2);
+                uint64_t wtot;
+                const uint64_t wex = block_excl_scan_u64(w, sm->wsum, wtot);
+                if (A < target && A + wtot >= target && A + wex < target && A + wex + w >= target) {
+                    uint64_t cum = A + wex;
+                    for (int j = b0; j < b1; ++j) {
+                        cum += mass(key_float(static_cast<uint32_t>(a[j] >> 32)), zmax, c2);
+                        if (cum >= target) {
+                            sm->bc[4] = 1ull;
+                            sm->bc[5] = a[j] >> 32;
+                            sm->bc[6] = static_cast<unsigned long long>(static_cast<uint32_t>(sort_key_id(a[j])));
+                            break;
+                        }
+                    }
+                }
+                __syncthreads();
+                if (tid < c.nc) {
+                    unsigned long long* rb = cluster.map_shared_rank(&sm->bc[0], tid);
+                    rb[4] = sm->bc[4];
+                    rb[5] = sm->bc[5];
+                    rb[6] = sm->bc[6];
+                }
+            }
+            cluster.sync();  // cut broadcast to every rank
+            if (sm->bc[4]) {
+                kp.p_on = true;
+                kp.taup = static_cast<uint32_t>(sm->bc[5]);
+                kp.zp = key_float(kp.taup);
+                kp.idp = static_cast<int>(static_cast<uint32_t>(sm->bc[6]));
+                draw_pass(c, v, kp, vec, zmax, c2, seed, offset, tok_out);
+                cluster_wait();
+                return;
+            }
+        } else {
+            cluster.sync();  // remote histogram reads are done before the fallback reuses it
+        }
+        fallback_select_and_draw(c, v, kp, vec, 0, pp, zmax, c2, seed, offset, tok_out);
+        cluster_wait();
+        return;
     }
-    if (!c.solo) cluster.sync();
+
+    // ---------------- no filter: draw over every finite logit
+    draw_pass(c, v, kp, vec, zmax, c2, seed, offset, tok_out);
+    cluster_wait();
 }
 
 // ------------------------------------------------------------------ host side
@@ -559,7 +1146,7 @@ static SamplerPlan plan_sampler(int V) {
     p.nc = nc;
     p.S = S;
     p.smem_slice = S <= kSliceSmemMax ? 1 : 0;
-    p.smem = sizeof(SampSmem) + (p.smem_slice ? static_cast<size_t>(S) * 4 : 0);
+    p.smem = sizeof(SampSmem) + (p.smem_slice ? static_cast<size_t>(S) * 4 : 0);  // S is a multiple of 4
     return p;
 }
 

@@ -224,6 +224,11 @@ def test_sampler_special_rows():
     add(zz, T=1.0, k=7, p=0.5)                                # +-0 ties -> id order
     add((base * 40).clone(), T=0.5, k=1000, p=0.99)           # very peaked
     add(torch.full((V,), 3.0), T=1.0, k=10)                   # all equal, top-k by id
+    add(torch.full((V,), 1.0), T=1.0, p=0.5, seed=11)         # all equal, top-p only (exact fallback)
+    add(base.clone(), T=0.9, k=3000, p=0.9)                   # top-k beyond the gather list (fallback)
+    add(base.clone(), T=0.6, p=0.3)                           # top-p only, narrow nucleus
+    zs = base.clone(); zs[100] += 30.0
+    add(zs, T=1.0, p=0.999999)                                # one dominant token, p near 1
     logits = torch.stack(rows).float().cuda()
     B = logits.shape[0]
     s = dict(logits=logits,
@@ -240,5 +245,6 @@ def test_sampler_special_rows():
     assert tok[0] == am and tok[1] == 5 and tok[2] == am and tok[3] == am and tok[4] == am
     assert tok[7] == -1 and tok[8] == -1 and tok[9] == -1 and tok[10] == -1 and tok[11] == -1
     assert tok[14] < 10
+    assert tok[15] < V // 2 + 1                               # equal masses: the nucleus is the lowest ids
     c = compare_tokens(torch.from_numpy(tok), s)
     assert list(c["status"][7:12]) == [6, 6, 1, 1, 6]
