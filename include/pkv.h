@@ -122,6 +122,32 @@ pkv_status pkv_paged_decode_attention(void* out, const void* q, const void* k_ca
                                       size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /*
+ * pkv_paged_decode_attention without a caller-supplied workspace.  The pages
+ * have no counterpart to this call: it exists for callers that cannot allocate
+ * device memory at attention time (a serving loop that handed all free HBM to
+ * its KV pool at start-up, code that must not risk the implicit device
+ * synchronisation of an allocation, or a C host program with no allocator).
+ * Same arguments, semantics and results as pkv_paged_decode_attention; the
+ * split-KV workspace is instead a fixed 16 MiB device array inside the library,
+ * present on every GPU that loads it until the process exits.  The first call
+ * on a device looks up that array's device address (cudaGetSymbolAddress), so
+ * make the first call on each device before any stream capture.  Requests that
+ * would need more than 16 MiB of workspace (pkv_decode_workspace_bytes(B, Hq, D,
+ * 0) > 16 MiB; e.g. B = 512, Hq = 32, D = 128 needs about 11 MiB) return
+ * PKV_ERR_UNSUPPORTED and launch nothing.  Nothing is allocated or freed.  All
+ * calls share the one array: calls that can overlap on the GPU (different
+ * streams without ordering, or different host threads) race and corrupt each
+ * other's partial results; serialise them on one stream.  The array keeps the
+ * last call's contents; every call rewrites what it reads before reading it.
+ */
+pkv_status pkv_paged_decode_attention_noalloc(void* out, const void* q, const void* k_cache,
+                                              const void* v_cache, const int32_t* block_tables,
+                                              int max_blocks_per_seq, const int32_t* seq_lens, int B,
+                                              int Hq, int Hkv, int D, int block_size, int num_blocks,
+                                              float scale, pkv_dtype dtype, int32_t* dev_status,
+                                              void* stream);
+
+/*
  * Workspace bytes pkv_sample_tokens needs (B rows of V logits).  The current
  * sampler keeps each row on chip and needs none: returns 0.
  */

@@ -26,6 +26,8 @@
 #include <cuda.h>
 #include <math.h>
 
+#include <mutex>
+
 #include "pkv_common.cuh"
 
 namespace pkv {
@@ -788,3 +790,66 @@ cudaError_t launch_decode_attention(void* out, const void* q, const void* k_cach
 }
 
 }  // namespace pkv
+
+// ------------------------------------------------------------------ allocation-free variant
+// Some callers cannot allocate device memory when they run attention: a serving
+// loop that reserved all free HBM for its KV pool up front, code that must not
+// risk the implicit synchronisation an allocation can cause, or a plain C host
+// program with no device allocator of its own.  For them the split-KV
+// workspace lives in this fixed, file-scope device array instead.  It is
+// allocated when the library is loaded onto a GPU and stays until the process
+// exits, on every GPU that loads the library.
+namespace pkv {
+
+constexpr size_t kStaticScratchBytes = static_cast<size_t>(16) << 20;  // 16 MiB
+static __device__ __align__(256) uint8_t g_decode_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+
+// Device address of g_decode_scratch on the current device, looked up once per
+// device (the host-side symbol is only a stand-in, never a device address).
+static void* decode_scratch_address(cudaError_t* err) {
+    static std::mutex mu;
+    static void* addr[kMaxDevices] = {};
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess) return nullptr;
+    if (dev < 0 || dev >= kMaxDevices) {
+        *err = cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void* p = nullptr;
+        *err = cudaGetSymbolAddress(&p, g_decode_scratch);
+        if (*err != cudaSuccess) return nullptr;
+        addr[dev] = p;
+    }
+    *err = cudaSuccess;
+    return addr[dev];
+}
+
+}  // namespace pkv
+
+extern "C" pkv_status pkv_paged_decode_attention_noalloc(void* out, const void* q, const void* k_cache,
+                                                         const void* v_cache, const int32_t* block_tables,
+                                                         int max_blocks_per_seq, const int32_t* seq_lens, int B,
+                                                         int Hq, int Hkv, int D, int block_size, int num_blocks,
+                                                         float scale, pkv_dtype dtype, int32_t* dev_status,
+                                                         void* stream) {
+    if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || D < 1 || D > 256 || block_size < 1 || num_blocks < 1 ||
+        max_blocks_per_seq < 1 || (dtype != PKV_F32 && dtype != PKV_BF16))
+        return PKV_ERR_INVALID_ARG;
+    if (B == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens) return PKV_ERR_INVALID_ARG;
+    const int P = pkv::device_sm_count();
+    if (P <= 0) return PKV_ERR_CUDA;
+    if (pkv::decode_workspace_bytes(B, Hq, D, P) > pkv::kStaticScratchBytes) return PKV_ERR_UNSUPPORTED;
+    cudaError_t err;
+    void* ws = pkv::decode_scratch_address(&err);
+    if (ws == nullptr) return PKV_ERR_CUDA;
+    err = pkv::launch_decode_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, B, Hq,
+                                       Hkv, D, block_size, num_blocks, scale, dtype, ws, P, dev_status,
+                                       static_cast<cudaStream_t>(stream), nullptr);
+    return err == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
