@@ -108,6 +108,9 @@ __global__ void __launch_bounds__(1024)
                 __nv_bfloat16* __restrict__ out, int Hq, int32_t* status) {
     __shared__ int warp_tot[32];
     __shared__ int s_carry;
+    // The main kernel may launch now and run its prologue; it waits for this
+    // grid's completion (griddepcontrol.wait) before reading the schedule.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) s_carry = 0;
     __syncthreads();
     const long long cap = static_cast<long long>(max_blocks) * BS;
@@ -322,11 +325,8 @@ __global__ void __launch_bounds__((kFastMaxKvHeads + 1) * 32, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int CW = Hkv;  // consumer warps: one per KV head
     const int G = Hq / Hkv;
-    const int total = hdr->total, W = hdr->W;
-    const int start = blockIdx.x * W;
-    const int end = min(total, start + W);
-    if (start >= end) return;
 
+    // prologue independent of the schedule (overlaps the plan kernel)
     if (threadIdx.x == 0) {
         for (int s = 0; s < nst; ++s) {
             mbar_init(&full[s], 1);
@@ -337,14 +337,19 @@ __global__ void __launch_bounds__((kFastMaxKvHeads + 1) * 32, 1)
             mbar_init(&qempty[s], CW);
         }
         fence_mbar_init();
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
     }
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the plan kernel's results are visible
+    const int total = hdr->total, W = hdr->W;
+    const int start = blockIdx.x * W;
+    const int end = min(total, start + W);
     __syncthreads();
+    if (start >= end) return;
 
     if (warp == CW) {
         // ------------------------------------------------ producer (one lane)
         if (lane != 0) return;
-        prefetch_tmap(&tmK);
-        prefetch_tmap(&tmV);
         // first sequence whose block range reaches past `start`: s + n is
         // non-decreasing in b, and some b < B satisfies it because start < total.
         int lo = 0, hi = B - 1;
@@ -837,22 +842,24 @@ cudaError_t launch_decode_attention(void* out, const void* q, const void* k_cach
     const float scale_log2 = scale * 1.4426950408889634f;
     const int G = Hq / Hkv;
     const unsigned threads = static_cast<unsigned>((Hkv + 1) * 32);
-    cudaError_t err;
-    if (G > 8) {
-        err = cudaFuncSetAttribute(decode_attn_fast_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   static_cast<int>(fp.smem));
-        if (err != cudaSuccess) return err;
-        decode_attn_fast_kernel<true><<<P, threads, fp.smem, stream>>>(
-            tmK, tmV, static_cast<const __nv_bfloat16*>(q), static_cast<__nv_bfloat16*>(out), block_tables, max_blocks,
-            B, Hq, Hkv, BS, NB, scale_log2, fp.nst, info, hdr, part_ml, part_o, counters, status);
-    } else {
-        err = cudaFuncSetAttribute(decode_attn_fast_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   static_cast<int>(fp.smem));
-        if (err != cudaSuccess) return err;
-        decode_attn_fast_kernel<false><<<P, threads, fp.smem, stream>>>(
-            tmK, tmV, static_cast<const __nv_bfloat16*>(q), static_cast<__nv_bfloat16*>(out), block_tables, max_blocks,
-            B, Hq, Hkv, BS, NB, scale_log2, fp.nst, info, hdr, part_ml, part_o, counters, status);
-    }
+    auto kern = G > 8 ? decode_attn_fast_kernel<true> : decode_attn_fast_kernel<false>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(fp.smem));
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(P), 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = fp.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, kern, tmK, tmV, static_cast<const __nv_bfloat16*>(q),
+                             static_cast<__nv_bfloat16*>(out), block_tables, max_blocks, B, Hq, Hkv, BS, NB,
+                             scale_log2, fp.nst, static_cast<const SeqInfo*>(info), static_cast<const PlanHdr*>(hdr),
+                             part_ml, part_o, counters, status);
+    if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 
