@@ -173,7 +173,7 @@ def _config(w, inp, extra=None):
         "total_tokens": int(sl.to(torch.int64).sum()), "num_blocks": inp["num_blocks"], "vocab": w.vocab,
         "sampler": {"temperature": w.temperature, "top_k": w.top_k, "top_p": w.top_p},
         "kv_dtype": "bf16", "logits_dtype": "f32",
-        "step": "kv_append -> paged_decode_attention (plan, split-KV main with in-kernel merge) -> sample_tokens",
+        "step": "kv_append -> paged_decode_attention (plan, split-KV main, combine) -> sample_tokens",
     }
     if extra:
         cfg.update(extra)
@@ -368,8 +368,8 @@ def run_gpu(args):
     peak, peak_kind = _peaks()
     attn_gbs = bytes_step["attention"] / (attn_ms * 1e-3) / 1e9
     traffic = _traffic_per_launch()
-    fast = True  # bf16, D=128, BS=16, Hkv=8: TMA/mma path -> plan kernel + main kernel
-    launches = args.steps * (1 + (2 if fast else 1) + 1)  # append + attention + sampler
+    fast = True  # bf16, D=128, BS=16, Hkv=8: TMA/mma path -> plan, main and combine kernels
+    launches = args.steps * (1 + (3 if fast else 1) + 1)  # append + attention + sampler
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -381,7 +381,7 @@ def run_gpu(args):
         "sampled_tokens_per_s": B * world / (ms * 1e-3),
         "pct_of_8TBps": value / 8000.0 * 100.0,
         "pct_of_measured_peak": value / peak * 100.0,
-        "roofline": {"kernel": "paged_decode_attention (plan + split-KV main kernel), per call",
+        "roofline": {"kernel": "paged_decode_attention (plan + split-KV main + combine kernels), per call",
                      "bound": "hbm", "achieved": attn_gbs, "peak": peak, "unit": "GB/s",
                      "frac": attn_gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",

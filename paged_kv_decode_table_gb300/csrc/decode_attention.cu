@@ -19,10 +19,11 @@
 //    mma.sync m16n8k16 (query heads of the group on the M axis, 16 tokens on N/K),
 //    online softmax in the log2 domain, fp32 accumulation.
 //  * A sequence cut by a range boundary leaves per-piece (max, sum, unnormalised
-//    output) partials in the workspace and bumps a per-(sequence, KV head)
-//    counter; the warp that arrives last merges the pieces with the
-//    online-softmax rule at the end of its range (no separate combine launch).
-//    Sequences wholly inside one range are written directly.
+//    output) partials in the workspace; the combine kernel merges them with the
+//    online-softmax rule.  Sequences wholly inside one range are written directly.
+//  * plan -> main -> combine are chained with programmatic dependent launch: each
+//    kernel launches while its predecessor runs and waits (griddepcontrol.wait)
+//    only before reading the predecessor's results.
 // Generic path (fp32, other shapes): one CTA per (sequence, query head),
 // CUDA-core fp32, chunked online softmax.
 #include <cuda.h>
@@ -53,7 +54,7 @@ struct PlanHdr {
 };
 
 struct WsLayout {
-    size_t hdr, info, cnt, ml, o, total;
+    size_t hdr, info, ml, o, total;
 };
 
 static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -63,8 +64,7 @@ static WsLayout ws_layout(int B, int Hq, int D, int P) {
     const size_t slots = static_cast<size_t>(B) + static_cast<size_t>(P);
     w.hdr = 0;
     w.info = 256;
-    w.cnt = align_up(w.info + sizeof(SeqInfo) * static_cast<size_t>(B), 256);
-    w.ml = align_up(w.cnt + sizeof(unsigned int) * 8 * static_cast<size_t>(B), 256);  // 8 = max KV heads, fast path
+    w.ml = align_up(w.info + sizeof(SeqInfo) * static_cast<size_t>(B), 256);
     w.o = align_up(w.ml + slots * Hq * 2 * sizeof(float), 256);
     w.total = align_up(w.o + slots * Hq * static_cast<size_t>(D) * sizeof(float), 256);
     return w;
@@ -104,8 +104,7 @@ __device__ __forceinline__ int block_excl_scan_1024(int v, int* warp_tot, int& t
 // records, per sequence, which ranges it spans and where its partials go.
 __global__ void __launch_bounds__(1024)
     plan_kernel(const int32_t* __restrict__ seq_lens, int B, int max_blocks, int BS, int P,
-                SeqInfo* __restrict__ info, PlanHdr* __restrict__ hdr, unsigned int* __restrict__ counters,
-                __nv_bfloat16* __restrict__ out, int Hq, int32_t* status) {
+                SeqInfo* __restrict__ info, PlanHdr* __restrict__ hdr, int32_t* status) {
     __shared__ int warp_tot[32];
     __shared__ int s_carry;
     // The main kernel may launch now and run its prologue; it waits for this
@@ -166,13 +165,6 @@ __global__ void __launch_bounds__(1024)
         hdr->W = W;
         hdr->P = P;
     }
-    // merge counters start at zero; empty or invalid sequences get zero output
-    for (int i = threadIdx.x; i < 8 * B; i += 1024) counters[i] = 0u;
-    for (int b = threadIdx.x; b < B; b += 1024) {
-        if (info[b].n != 0) continue;
-        uint4* ob = reinterpret_cast<uint4*>(out + static_cast<size_t>(b) * Hq * 128);
-        for (int i = 0; i < Hq * 128 / 8; ++i) ob[i] = make_uint4(0, 0, 0, 0);
-    }
 }
 
 // ------------------------------------------------------------------ fast kernel
@@ -193,111 +185,6 @@ static inline size_t fast_smem_bytes(int nst, int stage_bytes, int q_bytes) {
            (2 * kMaxStages + 4) * sizeof(uint64_t) + kMaxStages * sizeof(StageMeta) + 16;
 }
 
-// Merge of every piece of sequence b for the G query heads of KV head h by one
-// warp (the last writer): M = max m_c, out = sum o_c 2^(m_c - M) / sum l_c 2^(m_c - M).
-// Partials are read through L2 (ld.cg): other SMs wrote them.  When the G x pieces
-// statistics fit the warp, lane g*np+c loads (m, l) of head g, piece c once and
-// the rest travels by shuffle; the output loads of all heads of a piece are in
-// flight together, so the merge costs a few L2 round trips.
-__device__ __forceinline__ void merge_pieces_warp(int b, int h, int G, int Hq, SeqInfo si, const float* part_ml,
-                                                  const float* part_o, __nv_bfloat16* out) {
-    __threadfence();
-    const int lane = threadIdx.x & 31;
-    const int d = lane * 4;
-    const int np = si.pieces;
-    const size_t base = static_cast<size_t>(si.base);
-    if (np * G <= 32 && G <= 8) {
-        float2 ml = make_float2(-INFINITY, 0.f);
-        if (lane < np * G) {
-            const int g = lane / np, c = lane - (lane / np) * np;
-            ml = __ldcg(reinterpret_cast<const float2*>(part_ml + ((base + c) * Hq + h * G + g) * 2));
-        }
-        float M[8], L[8];
-        bool bad[8];
-        float4 acc[8];
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-            M[g] = -INFINITY;
-            L[g] = 0.f;
-            bad[g] = false;
-            acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        for (int c = 0; c < np; ++c) {
-#pragma unroll
-            for (int g = 0; g < 8; ++g) {
-                const float m = __shfl_sync(0xffffffffu, ml.x, (g * np + c) & 31);
-                const float l = __shfl_sync(0xffffffffu, ml.y, (g * np + c) & 31);
-                if (g < G) {
-                    M[g] = fmaxf(M[g], m);
-                    bad[g] |= l < 0.f;
-                }
-            }
-        }
-        for (int c = 0; c < np; ++c) {
-            float4 o4[8];
-#pragma unroll
-            for (int g = 0; g < 8; ++g)
-                if (g < G)
-                    o4[g] = __ldcg(reinterpret_cast<const float4*>(part_o + ((base + c) * Hq + h * G + g) * kDim + d));
-#pragma unroll
-            for (int g = 0; g < 8; ++g) {
-                const float m = __shfl_sync(0xffffffffu, ml.x, (g * np + c) & 31);
-                const float l = __shfl_sync(0xffffffffu, ml.y, (g * np + c) & 31);
-                if (g < G && !bad[g] && M[g] > -INFINITY) {
-                    const float w = exp2f(m - M[g]);
-                    L[g] = fmaf(l, w, L[g]);
-                    acc[g].x = fmaf(w, o4[g].x, acc[g].x);
-                    acc[g].y = fmaf(w, o4[g].y, acc[g].y);
-                    acc[g].z = fmaf(w, o4[g].z, acc[g].z);
-                    acc[g].w = fmaf(w, o4[g].w, acc[g].w);
-                }
-            }
-        }
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-            if (g < G) {
-                const float inv = (!bad[g] && L[g] > 0.f) ? 1.f / L[g] : 0.f;
-                uint2 pk;
-                pk.x = pack_bf16x2(acc[g].x * inv, acc[g].y * inv);
-                pk.y = pack_bf16x2(acc[g].z * inv, acc[g].w * inv);
-                *reinterpret_cast<uint2*>(out + (static_cast<size_t>(b) * Hq + h * G + g) * kDim + d) = pk;
-            }
-        }
-        return;
-    }
-    // many pieces: one head at a time
-    for (int g = 0; g < G; ++g) {
-        const int qh = h * G + g;
-        float M = -INFINITY;
-        bool bad = false;
-        for (int c = 0; c < np; ++c) {
-            const float2 ml = __ldcg(reinterpret_cast<const float2*>(part_ml + ((base + c) * Hq + qh) * 2));
-            M = fmaxf(M, ml.x);
-            bad |= ml.y < 0.f;
-        }
-        float L = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (!bad && M > -INFINITY) {
-            for (int c = 0; c < np; ++c) {
-                const size_t slot = base + c;
-                const float2 ml = __ldcg(reinterpret_cast<const float2*>(part_ml + (slot * Hq + qh) * 2));
-                const float w = exp2f(ml.x - M);
-                L += ml.y * w;
-                const float4 o4 = __ldcg(reinterpret_cast<const float4*>(part_o + (slot * Hq + qh) * kDim + d));
-                acc.x = fmaf(w, o4.x, acc.x);
-                acc.y = fmaf(w, o4.y, acc.y);
-                acc.z = fmaf(w, o4.z, acc.z);
-                acc.w = fmaf(w, o4.w, acc.w);
-            }
-        }
-        const float inv = (!bad && L > 0.f) ? 1.f / L : 0.f;
-        uint2 pk;
-        pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-        pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-        *reinterpret_cast<uint2*>(out + (static_cast<size_t>(b) * Hq + qh) * kDim + d) = pk;
-    }
-}
-
 constexpr int kFastMaxKvHeads = 8;
 
 template <bool kRows16>  // true when G > 8: query rows 8..15 of the MMA tile are live
@@ -307,7 +194,7 @@ __global__ void __launch_bounds__((kFastMaxKvHeads + 1) * 32, 1)
                             const int32_t* __restrict__ block_tables, int max_blocks, int B, int Hq, int Hkv,
                             int BS, int NB, float scale_log2, int nst, const SeqInfo* __restrict__ info,
                             const PlanHdr* __restrict__ hdr, float* __restrict__ part_ml,
-                            float* __restrict__ part_o, unsigned int* __restrict__ counters, int32_t* status) {
+                            float* __restrict__ part_o, int32_t* status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int R = Hkv * BS;
@@ -341,6 +228,7 @@ __global__ void __launch_bounds__((kFastMaxKvHeads + 1) * 32, 1)
         prefetch_tmap(&tmV);
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the plan kernel's results are visible
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the combine kernel may launch
     const int total = hdr->total, W = hdr->W;
     const int start = blockIdx.x * W;
     const int end = min(total, start + W);
@@ -419,10 +307,6 @@ __global__ void __launch_bounds__((kFastMaxKvHeads + 1) * 32, 1)
     uint32_t qa[8][4];
     bool poisoned = false;
     int piece = 0;
-    // A sequence split over several CTA ranges contains a range boundary, so at
-    // most two of them (the one entering and the one leaving this range) have a
-    // piece here: a warp is the last writer of at most two merges.
-    int pend0 = -1, pend1 = -1;
     const uint32_t stages_u32 = smem_u32(stages);
 
     for (int i = start, it = 0; i < end; ++i, ++it) {
@@ -617,22 +501,75 @@ __global__ void __launch_bounds__((kFastMaxKvHeads + 1) * 32, 1)
                         *reinterpret_cast<float2*>(part_o + (slot * Hq + qh1) * kDim + d) =
                             make_float2(O[nt][2], O[nt][3]);
                 }
-                // publish the partial, then count it; the last of the pieces merges
-                __threadfence();
-                __syncwarp();
-                unsigned int prev = 0;
-                if (lane == 0) prev = atomicAdd(&counters[b * 8 + h], 1u);
-                prev = __shfl_sync(0xffffffffu, prev, 0);
-                if (prev + 1 == static_cast<unsigned int>(si.pieces)) {
-                    if (pend0 < 0) pend0 = b;
-                    else pend1 = b;
-                }
             }
         }
     }
-    // merges this warp completed last, deferred so the stream of stages never waits on them
-    if (pend0 >= 0) merge_pieces_warp(pend0, h, G, Hq, info[pend0], part_ml, part_o, out);
-    if (pend1 >= 0) merge_pieces_warp(pend1, h, G, Hq, info[pend1], part_ml, part_o, out);
+}
+
+// ------------------------------------------------------------------ combine kernel
+// Merges the per-range partials of sequences that span several CTA ranges:
+// M = max m_c, out = sum o_c 2^(m_c - M) / sum l_c 2^(m_c - M) (log2 domain).
+// One CTA per (sequence, query head); the piece weights are computed once into
+// shared memory, then each thread reduces its output dimensions over the pieces.
+// Writes zeros for empty or invalid sequences; skips single-range sequences,
+// which the fast kernel wrote directly.
+constexpr int kCombineThreads = 128;
+constexpr int kCombineMaxPieces = 1024;
+
+template <typename T>
+__global__ void __launch_bounds__(kCombineThreads)
+    combine_kernel(const SeqInfo* __restrict__ info, const float* __restrict__ part_ml,
+                   const float* __restrict__ part_o, T* __restrict__ out, int Hq, int D) {
+    __shared__ float wsh[kCombineMaxPieces];
+    __shared__ float red[kCombineThreads / 32];
+    __shared__ int bad_sh;
+    const int b = blockIdx.x / Hq, qh = blockIdx.x - (blockIdx.x / Hq) * Hq;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the main kernel's partials are visible
+    const SeqInfo si = info[b];
+    if (si.pieces == 1) return;
+    T* o = out + (static_cast<size_t>(b) * Hq + qh) * D;
+    const int np = min(si.pieces, kCombineMaxPieces);
+    if (tid == 0) bad_sh = (si.pieces == 0 || si.pieces > kCombineMaxPieces) ? 1 : 0;
+    __syncthreads();
+    // max over pieces (and poisoned-piece detection)
+    float M = -INFINITY;
+    for (int c = tid; c < np; c += kCombineThreads) {
+        const float2 ml = *reinterpret_cast<const float2*>(part_ml + ((static_cast<size_t>(si.base) + c) * Hq + qh) * 2);
+        M = fmaxf(M, ml.x);
+        if (ml.y < 0.f) bad_sh = 1;
+    }
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if (lane == 0) red[warp] = M;
+    __syncthreads();
+    M = red[0];
+    for (int w = 1; w < kCombineThreads / 32; ++w) M = fmaxf(M, red[w]);
+    const bool bad = bad_sh != 0 || M == -INFINITY;
+    __syncthreads();
+    // weights 2^(m_c - M) and the merged denominator
+    float L = 0.f;
+    for (int c = tid; c < np; c += kCombineThreads) {
+        const float2 ml = *reinterpret_cast<const float2*>(part_ml + ((static_cast<size_t>(si.base) + c) * Hq + qh) * 2);
+        const float wgt = bad ? 0.f : exp2f(ml.x - M);
+        wsh[c] = wgt;
+        L += ml.y * wgt;
+    }
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    if (lane == 0) red[warp] = L;
+    __syncthreads();
+    L = 0.f;
+    for (int w = 0; w < kCombineThreads / 32; ++w) L += red[w];
+    const float inv = (!bad && L > 0.f) ? 1.f / L : 0.f;
+    for (int d = tid; d < D; d += kCombineThreads) {
+        float acc = 0.f;
+        if (!bad) {
+            const float* po = part_o + (static_cast<size_t>(si.base) * Hq + qh) * D + d;
+            const size_t stride = static_cast<size_t>(Hq) * D;
+#pragma unroll 8
+            for (int c = 0; c < np; ++c) acc = fmaf(wsh[c], po[c * stride], acc);
+        }
+        o[d] = from_f32<T>(acc * inv);
+    }
 }
 
 // ------------------------------------------------------------------ generic kernel
@@ -836,9 +773,7 @@ cudaError_t launch_decode_attention(void* out, const void* q, const void* k_cach
     SeqInfo* info = reinterpret_cast<SeqInfo*>(ws + wl.info);
     float* part_ml = reinterpret_cast<float*>(ws + wl.ml);
     float* part_o = reinterpret_cast<float*>(ws + wl.o);
-    unsigned int* counters = reinterpret_cast<unsigned int*>(ws + wl.cnt);
-    plan_kernel<<<1, 1024, 0, stream>>>(seq_lens, B, max_blocks, BS, P, info, hdr, counters,
-                                        static_cast<__nv_bfloat16*>(out), Hq, status);
+    plan_kernel<<<1, 1024, 0, stream>>>(seq_lens, B, max_blocks, BS, P, info, hdr, status);
     const float scale_log2 = scale * 1.4426950408889634f;
     const int G = Hq / Hkv;
     const unsigned threads = static_cast<unsigned>((Hkv + 1) * 32);
@@ -858,7 +793,18 @@ cudaError_t launch_decode_attention(void* out, const void* q, const void* k_cach
     err = cudaLaunchKernelEx(&cfg, kern, tmK, tmV, static_cast<const __nv_bfloat16*>(q),
                              static_cast<__nv_bfloat16*>(out), block_tables, max_blocks, B, Hq, Hkv, BS, NB,
                              scale_log2, fp.nst, static_cast<const SeqInfo*>(info), static_cast<const PlanHdr*>(hdr),
-                             part_ml, part_o, counters, status);
+                             part_ml, part_o, status);
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t ccfg = {};
+    ccfg.gridDim = dim3(static_cast<unsigned>(B) * Hq, 1, 1);
+    ccfg.blockDim = dim3(kCombineThreads, 1, 1);
+    ccfg.dynamicSmemBytes = 0;
+    ccfg.stream = stream;
+    ccfg.attrs = attr;
+    ccfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&ccfg, combine_kernel<__nv_bfloat16>, static_cast<const SeqInfo*>(info),
+                             static_cast<const float*>(part_ml), static_cast<const float*>(part_o),
+                             static_cast<__nv_bfloat16*>(out), Hq, D);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
