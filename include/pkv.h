@@ -106,10 +106,11 @@ size_t pkv_decode_workspace_bytes(int B, int Hq, int D, int num_sms);
  * merged with the online-softmax rule; `workspace` (device, >=
  * pkv_decode_workspace_bytes(B, Hq, D, 0) bytes, 16-byte aligned, contents
  * ignored on entry) holds the partials.  Requires Hq % Hkv == 0 and
- * 1 <= D <= 256; the fast path (bf16, D = 128, block_size % 16 == 0,
- * Hkv in {1, 2, 4, 8}, Hq/Hkv <= 16, Hkv * block_size <= 128, 16-byte aligned
- * pools) uses TMA and tensor-core MMA; other shapes use a generic CUDA-core
- * kernel.  Sequences with a length outside [0, max_blocks_per_seq*block_size]
+ * 1 <= D <= 256; the fast path (bf16, D = 128, block_size a multiple of 16,
+ * 1 <= Hkv <= 8, Hq/Hkv <= 16, Hkv * block_size <= 256 with at least two
+ * 512*Hkv*block_size-byte stages fitting in shared memory, 16-byte aligned q
+ * and pools) uses TMA and tensor-core MMA in three kernels chained by
+ * programmatic dependent launch; other shapes use a generic CUDA-core kernel.  Sequences with a length outside [0, max_blocks_per_seq*block_size]
  * or a block id outside [0, num_blocks) get zero output and
  * PKV_ERR_DEVICE_BOUNDS.  The KV slots past L in a sequence's last block are
  * never used (their contents may be anything, NaN included).
