@@ -377,10 +377,10 @@ struct Bins {
 // at or past n read as -inf.  The vector path is used only for the shared-memory
 // copy of the slice, whose buffer is padded to a multiple of 4.
 __device__ __forceinline__ float4 load4(const View& v, int e, bool vec) {
+    // the shared-memory slice is padded with -inf up to a multiple of 4 slots
+    if (vec) return *reinterpret_cast<const float4*>(v.z + e);
     float4 q;
-    if (vec) {
-        q = *reinterpret_cast<const float4*>(v.z + e);
-    } else {
+    {
         q.x = e < v.n ? v.z[e] : 0.f;
         q.y = e + 1 < v.n ? v.z[e + 1] : 0.f;
         q.z = e + 2 < v.n ? v.z[e + 2] : 0.f;
@@ -516,61 +516,112 @@ __device__ void draw_pass(Ctx& c, const View& v, const Keep& kp, bool vec, float
 
 // ------------------------------------------------------------------ rank-0 finish on a gathered list
 // The list holds n distinct candidate sort keys, a superset of the top-kk set.
-// Small lists (n <= 128): the first four warps alone; candidate i computes its
-// rank, its cumulative mass in rank order and its cumulative mass in id order
-// directly (no sort), with a 128-thread named barrier instead of CTA barriers.
+// Small lists (n <= 128): one warp, four candidates per lane in registers.
+// Ranks by comparison with every candidate; masses are scattered to their rank
+// (top-p prefix) and then to their id order among the kept tokens (draw), each
+// followed by a warp scan; only __syncwarp, no block barriers.
 constexpr int kSmallList = 128;
 
-__device__ __forceinline__ void sync128() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
-__device__ __forceinline__ uint64_t reduce128(uint64_t v, unsigned long long* scratch) {
+// Exclusive scan of buf[0..128) (4 consecutive entries per lane) in place; returns the total.
+__device__ __forceinline__ uint64_t warp_scan128(unsigned long long* buf) {
+    const int lane = threadIdx.x & 31;
+    uint64_t v[4], t = 0;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
-    sync128();
-    const uint64_t t = scratch[0] + scratch[1] + scratch[2] + scratch[3];
-    sync128();
-    return t;
+    for (int q = 0; q < 4; ++q) {
+        v[q] = buf[4 * lane + q];
+        t += v[q];
+    }
+    uint64_t inc = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+    }
+    const uint64_t total = __shfl_sync(0xffffffffu, inc, 31);
+    uint64_t run = inc - t;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        buf[4 * lane + q] = run;
+        run += v[q];
+    }
+    __syncwarp();
+    return total;
 }
 
 __device__ void solo_finish_small(SampSmem* sm, int n, int kk, float pp, float zmax, float c2, uint64_t seed,
                                   uint64_t offset, int32_t* tok_out) {
-    const int i = threadIdx.x;
-    if (i >= 128) return;
+    if (threadIdx.x >= 32) return;
+    const int lane = threadIdx.x;
     const unsigned long long* a = sm->list;
-    unsigned long long* wv = sm->hist;                                    // masses [n]
-    unsigned int* rk = reinterpret_cast<unsigned int*>(sm->hist + kListCap / 4);  // ranks [n]
-    unsigned int* kf = rk + kListCap / 4;                                  // kept flags [n]
-    unsigned long long ki = 0;
-    unsigned int rank = 0;
-    uint64_t W = 0;
-    if (i < n) {
-        ki = a[i];
-        for (int j = 0; j < n; ++j) rank += (a[j] > ki) ? 1u : 0u;
-        W = mass(key_float(static_cast<uint32_t>(ki >> 32)), zmax, c2);
-        wv[i] = W;
-        rk[i] = rank;
+    unsigned long long* buf = sm->hist;                                      // [128] scratch masses / prefixes
+    unsigned int* kf = reinterpret_cast<unsigned int*>(sm->hist + 128);      // [128] kept flags
+    unsigned int* ids = kf + 128;                                            // [128] token ids
+    unsigned long long key[4];
+    unsigned int rank[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) key[q] = lane + 32 * q < n ? a[lane + 32 * q] : 0ull;
+    for (int j = 0; j < n; ++j) {
+        const unsigned long long kj = a[j];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) rank[q] += kj > key[q] ? 1u : 0u;
     }
-    const bool in_k = i < n && rank < static_cast<unsigned int>(kk);
-    const uint64_t sk = reduce128(in_k ? W : 0ull, sm->wsum);  // its barriers also publish wv / rk
-    bool kept = in_k;
-    if (pp < 1.f && in_k) {
+    uint64_t W[4];
+    bool in_k[4], kept[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const bool valid = lane + 32 * q < n;
+        W[q] = valid ? mass(key_float(static_cast<uint32_t>(key[q] >> 32)), zmax, c2) : 0ull;
+        in_k[q] = valid && rank[q] < static_cast<unsigned int>(kk);
+        kept[q] = in_k[q];
+    }
+    // top-p on the top-k set in rank order
+#pragma unroll
+    for (int q = 0; q < 4; ++q) buf[4 * lane + q] = 0ull;
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        if (in_k[q]) buf[rank[q]] = W[q];
+    __syncwarp();
+    const uint64_t sk = warp_scan128(buf);
+    if (pp < 1.f) {
         const uint64_t target = ceil_mul_p(pp, sk);
-        uint64_t before = 0;
-        for (int j = 0; j < n; ++j)
-            if (rk[j] < rank) before += wv[j];
-        kept = before < target;  // inside the smallest prefix whose mass reaches target
+#pragma unroll
+        for (int q = 0; q < 4; ++q) kept[q] = in_k[q] && buf[rank[q]] < target;  // prefix before it < target
     }
-    if (i < n) kf[i] = kept ? 1u : 0u;
-    const uint64_t Sp = reduce128(kept ? W : 0ull, sm->wsum);
-    if (kept && W > 0) {
-        const uint64_t u53 = philox_word0(seed, offset) >> 11;
-        const uint64_t X = static_cast<uint64_t>((static_cast<unsigned __int128>(u53) * Sp) >> 53);
-        const int id = sort_key_id(ki);
-        uint64_t before = 0;
-        for (int j = 0; j < n; ++j)
-            if (kf[j] && sort_key_id(a[j]) < id) before += wv[j];
-        if (before <= X && X < before + W) *tok_out = id;
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int i = lane + 32 * q;
+        if (i < n) {
+            kf[i] = kept[q] ? 1u : 0u;
+            ids[i] = static_cast<unsigned int>(sort_key_id(key[q]));
+        }
+        buf[4 * lane + q] = 0ull;
+    }
+    __syncwarp();
+    // draw: kept tokens in id order
+    unsigned int idr[4] = {0u, 0u, 0u, 0u};
+    unsigned int myid[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) myid[q] = static_cast<unsigned int>(sort_key_id(key[q]));
+    for (int j = 0; j < n; ++j) {
+        const unsigned int fj = kf[j], idj = ids[j];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) idr[q] += (fj && idj < myid[q]) ? 1u : 0u;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        if (kept[q]) buf[idr[q]] = W[q];
+    __syncwarp();
+    const uint64_t Sp = warp_scan128(buf);
+    const uint64_t u53 = philox_word0(seed, offset) >> 11;
+    const uint64_t X = static_cast<uint64_t>((static_cast<unsigned __int128>(u53) * Sp) >> 53);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        if (kept[q] && W[q] > 0) {
+            const uint64_t before = buf[idr[q]];
+            if (before <= X && X < before + W[q]) *tok_out = static_cast<int>(myid[q]);
+        }
     }
 }
 
