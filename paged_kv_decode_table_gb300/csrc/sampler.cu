@@ -30,6 +30,10 @@
 #include <limits.h>
 #include <math.h>
 
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "pkv_common.cuh"
 
 namespace cg = cooperative_groups;
@@ -168,6 +172,7 @@ struct View {
     const int* id;  // nullptr: ids are idbase + i
     int n;
     int idbase;
+    bool g16;  // z is a 16-byte aligned global pointer (4-wide loads allowed inside [0, n))
     __device__ __forceinline__ int idat(int i) const { return id ? id[i] : idbase + i; }
 };
 
@@ -374,11 +379,12 @@ struct Bins {
 };
 
 // Four consecutive logits of the slice starting at e (a multiple of 4); entries
-// at or past n read as -inf.  The vector path is used only for the shared-memory
-// copy of the slice, whose buffer is padded to a multiple of 4.
+// at or past n read as -inf.  vec: the slice is the shared-memory copy, padded
+// with -inf up to a multiple of 4 slots.  Otherwise the slice is read from
+// global memory, 16 bytes at a time where aligned and wholly inside the row.
 __device__ __forceinline__ float4 load4(const View& v, int e, bool vec) {
-    // the shared-memory slice is padded with -inf up to a multiple of 4 slots
     if (vec) return *reinterpret_cast<const float4*>(v.z + e);
+    if (v.g16 && e + 4 <= v.n) return __ldg(reinterpret_cast<const float4*>(v.z + e));
     float4 q;
     {
         q.x = e < v.n ? v.z[e] : 0.f;
@@ -394,6 +400,26 @@ __device__ __forceinline__ float4 load4(const View& v, int e, bool vec) {
 }
 __device__ __forceinline__ float f4at(const float4& q, int j) {
     return j == 0 ? q.x : (j == 1 ? q.y : (j == 2 ? q.z : q.w));
+}
+
+// Strided sweep over the 4-wide slots of the slice: slot e = 4 * (tid + kST * i).
+// kU slots are loaded before any is processed, so that a thread keeps kU loads
+// in flight when the slice is read from global memory.  The trip count is the
+// same for every lane of a warp (lanes past the end see -inf), so f may use
+// warp-collective operations.  f(e, q) gets the slot and its four logits.
+template <int kU, typename F>
+__device__ __forceinline__ void sweep4(const View& v, int nvec, bool vec, F&& f) {
+    const int lane = threadIdx.x & 31;
+    for (int e0 = 4 * (static_cast<int>(threadIdx.x) - lane); e0 < nvec; e0 += 4 * kST * kU) {
+        float4 q[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int el = e0 + 4 * lane + 4 * kST * u;
+            q[u] = el < nvec ? load4(v, el, vec) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) f(e0 + 4 * lane + 4 * kST * u, q[u]);
+    }
 }
 
 // Per-thread run length for thread-contiguous passes: a multiple of 4 with an
@@ -473,11 +499,13 @@ __device__ void draw_pass(Ctx& c, const View& v, const Keep& kp, bool vec, float
     auto kept = [&](float z, int id) { return !filt || kp.keep_f(z, id); };
     uint64_t w = 0;
     if (!filt) {
+#pragma unroll 4
         for (int e = b0; e < b1; e += 4) {
             const float4 q = load4(v, e, vec);
             w += mass(q.x, zmax, c2) + mass(q.y, zmax, c2) + mass(q.z, zmax, c2) + mass(q.w, zmax, c2);
         }
     } else {
+#pragma unroll 4
         for (int e = b0; e < b1; e += 4) {
             const float4 q = load4(v, e, vec);
 #pragma unroll
@@ -759,6 +787,7 @@ __global__ void __launch_bounds__(kST, 2)
     v.n = n;
     v.idbase = lo;
     v.z = smem_slice ? zslice : grow;
+    v.g16 = (reinterpret_cast<uintptr_t>(grow) & 15u) == 0;
     const bool vec = smem_slice != 0;
 
     // row parameters first: they decide what the passes must track
@@ -813,7 +842,12 @@ __global__ void __launch_bounds__(kST, 2)
         __syncthreads();  // tail written by every thread is visible
         for (int i = nbulk + tid; i < n; i += kST) stat1(zslice[i]);
     } else {
-        for (int i = tid; i < n; i += kST) stat1(grow[i]);
+        sweep4<4>(v, nvec, false, [&](int, const float4& q) {
+            stat1(q.x);
+            stat1(q.y);
+            stat1(q.z);
+            stat1(q.w);
+        });
     }
     const float tmax = zmx;  // this thread's own maximum
 #pragma unroll
@@ -969,13 +1003,12 @@ __global__ void __launch_bounds__(kST, 2)
             sm->bc[1] = 0;
         }
         __syncthreads();
-        for (int e = 4 * tid; e < nvec; e += 4 * kST) {
-            const float4 q = load4(v, e, vec);
+        sweep4<4>(v, nvec, vec, [&](int, const float4& q) {
             if (q.x > -INFINITY && q.x >= zfloor) atomicAdd(&cnt[kb(q.x)], 1u);
             if (q.y > -INFINITY && q.y >= zfloor) atomicAdd(&cnt[kb(q.y)], 1u);
             if (q.z > -INFINITY && q.z >= zfloor) atomicAdd(&cnt[kb(q.z)], 1u);
             if (q.w > -INFINITY && q.w >= zfloor) atomicAdd(&cnt[kb(q.w)], 1u);
-        }
+        });
         cluster.sync();
         uint32_t g[4] = {0u, 0u, 0u, 0u};
         if (tid * 4 < kb.nb) sum_remote_u4(cluster, cnt, c.nc, g);
@@ -1002,19 +1035,16 @@ __global__ void __launch_bounds__(kST, 2)
                 // every candidate has z >= zlow (two bins of margin for rounding)
                 const float zlow =
                     kb.scale > 0.f ? fmaxf(zfloor, zmax - (static_cast<float>(bk) + 3.0f) / kb.scale) : zfloor;
-                for (int e = 4 * tid - 4 * lane; e < nvec; e += 4 * kST) {  // warp-uniform trip count
-                    const int el = e + 4 * lane;
-                    const float4 q =
-                        el < nvec ? load4(v, el, vec) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                sweep4<4>(v, nvec, vec, [&](int el, const float4& q) {
                     const bool any = q.x >= zlow || q.y >= zlow || q.z >= zlow || q.w >= zlow;
-                    if (!__any_sync(0xffffffffu, any)) continue;
+                    if (!__any_sync(0xffffffffu, any)) return;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const float z = f4at(q, j);
                         const bool pred = z > -INFINITY && z >= zfloor && kb(z) <= bk;
                         gather_push(pred, pred ? sort_key(z, lo + el + j) : 0ull, gcount0, list0);
                     }
-                }
+                });
                 cluster.sync();  // candidates complete in rank 0; no remote access follows
                 if (c.rank != 0) return;
                 solo_finish(sm, static_cast<int>(total), kk, pp, zmax, c2, seed, offset, tok_out);
@@ -1041,8 +1071,7 @@ __global__ void __launch_bounds__(kST, 2)
         }
         __syncthreads();
         uint64_t st = 0;
-        for (int e = 4 * tid; e < nvec; e += 4 * kST) {
-            const float4 q = load4(v, e, vec);
+        sweep4<4>(v, nvec, vec, [&](int, const float4& q) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const float z = f4at(q, j);
@@ -1053,7 +1082,7 @@ __global__ void __launch_bounds__(kST, 2)
                 atomicAdd(&cnt[b], 1u);
                 atomicAdd(&fmass[b], wf);
             }
-        }
+        });
         uint64_t scta;
         block_excl_scan_u64(st, sm->wsum, scta);
         if (tid == 0) sm->xch[c.xb][0] = scta;
@@ -1101,9 +1130,7 @@ __global__ void __launch_bounds__(kST, 2)
         block_excl_scan_u64(wc, sm->wsum, total);
         if (total >= 1 && total <= static_cast<uint64_t>(kListCap)) {
             uint64_t at = 0;
-            for (int e = 4 * tid - 4 * lane; e < nvec; e += 4 * kST) {  // warp-uniform trip count
-                const int el = e + 4 * lane;
-                const float4 q = el < nvec ? load4(v, el, vec) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            sweep4<4>(v, nvec, vec, [&](int el, const float4& q) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const float z = f4at(q, j);
@@ -1113,7 +1140,7 @@ __global__ void __launch_bounds__(kST, 2)
                     const bool pred = fin && b >= blo && b <= bhi;
                     gather_push(pred, pred ? sort_key(z, lo + el + j) : 0ull, gcount0, list0);
                 }
-            }
+            });
             uint64_t acta;
             block_excl_scan_u64(at, sm->wsum, acta);
             if (tid == 0) *cluster.map_shared_rank(&sm->aslot[c.rank], 0) = acta;
@@ -1182,29 +1209,86 @@ __global__ void __launch_bounds__(kST, 2)
 }
 
 // ------------------------------------------------------------------ host side
+// Launch plan: nc CTAs (one cluster) per row, each over a slice of S logits
+// (a multiple of 4), kept in shared memory when smem_slice.
+//
+// A row's work is a short chain of dependent phases (load, bounds, histogram,
+// gather, finish), so the kernel is fastest when every row's cluster is
+// resident at once.  With the slice in shared memory (at most 24576 logits per
+// CTA, so nc = ceil(V / 20480)) a CTA holds up to ~130 KB; once B rows of such
+// clusters no longer fit on the GPU together, the slice is read from global
+// memory instead (the first read streams it from HBM, later passes hit L2),
+// with as many CTAs per row as still lets all B clusters be resident.
 struct SamplerPlan {
     int nc, S, smem_slice;
     size_t smem;
 };
 
-static SamplerPlan plan_sampler(int V) {
+static SamplerPlan make_plan(int V, int nc, bool smem_slice) {
     SamplerPlan p;
-    int nc = (V + 20479) / 20480;
-    if (nc < 1) nc = 1;
-    if (nc > kMaxCluster) nc = kMaxCluster;
     int S = (V + nc - 1) / nc;
     S = (S + 3) & ~3;
     p.nc = nc;
     p.S = S;
-    p.smem_slice = S <= kSliceSmemMax ? 1 : 0;
-    p.smem = sizeof(SampSmem) + (p.smem_slice ? static_cast<size_t>(S) * 4 : 0);  // S is a multiple of 4
+    p.smem_slice = smem_slice ? 1 : 0;
+    p.smem = sizeof(SampSmem) + (smem_slice ? static_cast<size_t>(S) * 4 : 0);  // S is a multiple of 4
     return p;
+}
+
+// Clusters of plan p that can be resident at once on the current device (0 on error).
+static int resident_clusters(const SamplerPlan& p) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, size_t>, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const auto key = std::make_tuple(dev, p.nc, p.smem);
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    if (cudaFuncSetAttribute(sampler_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(p.smem)) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.nc) * 64u, 1, 1);
+    cfg.blockDim = dim3(kST, 1, 1);
+    cfg.dynamicSmemBytes = p.smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = p.nc;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, sampler_kernel, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    cache[key] = n;
+    return n;
+}
+
+static SamplerPlan plan_sampler(int B, int V) {
+    int nc_s = (V + 20479) / 20480;
+    nc_s = nc_s < 1 ? 1 : (nc_s > kMaxCluster ? kMaxCluster : nc_s);
+    const SamplerPlan ps = make_plan(V, nc_s, true);
+    const bool smem_ok = ps.S <= kSliceSmemMax;
+    if (smem_ok && B <= resident_clusters(ps)) return ps;
+    for (int nc = kMaxCluster; nc >= 1; --nc) {
+        if (nc > 1 && (V + nc - 1) / nc < 4096) continue;  // keep slices long enough to be worth a CTA
+        const SamplerPlan pg = make_plan(V, nc, false);
+        if (B <= resident_clusters(pg)) return pg;
+    }
+    return make_plan(V, 1, false);  // more rows than resident CTAs: one CTA per row, in waves
 }
 
 cudaError_t launch_sampler(int32_t* tokens, const float* logits, int B, int V, const float* temperature,
                            const int32_t* top_k, const float* top_p, const uint64_t* seeds, const uint64_t* offsets,
                            int32_t* status, cudaStream_t stream) {
-    const SamplerPlan sp = plan_sampler(V);
+    const SamplerPlan sp = plan_sampler(B, V);
     cudaError_t err = cudaFuncSetAttribute(sampler_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(sp.smem));
     if (err != cudaSuccess) return err;
