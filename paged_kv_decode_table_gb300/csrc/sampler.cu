@@ -45,6 +45,8 @@ constexpr int kSW = kST / 32;      // warps per CTA
 constexpr int kHistBins = 2048;    // widest radix digit (11 bits) and linear bins
 constexpr int kListCap = 2048;     // candidate list capacity (rank 0, gathered)
 constexpr int kTopkBins = 512;     // bins of the bounded top-k histogram
+constexpr int kLocBase = 1024;     // hist[kLocBase..kHistBins): this CTA's top-k candidates
+constexpr int kLocCap = kHistBins - kLocBase;
 constexpr int kMaxCluster = 8;
 constexpr int kSliceSmemMax = 24576;  // floats of a row slice kept in shared memory
 
@@ -59,6 +61,8 @@ struct __align__(16) SampSmem {
     uint64_t bar[4];        // one per chunk of the slice load
     unsigned int gcount;    // rank 0: candidates gathered so far
     int imin;
+    unsigned int lcount;    // this CTA's top-k candidates (sort keys in hist[kLocBase..])
+    int pad_;
 };
 // The row slice follows the struct in shared memory; TMA bulk copies and the
 // 16-byte vector loads need it 16-byte aligned.
@@ -434,7 +438,7 @@ __device__ __forceinline__ int run_len4(int n) {
 // Append the lane's candidate (when pred) to rank 0's gathered list; one remote
 // atomic per warp and element slot.  Every lane of the warp must call this.
 __device__ __forceinline__ void gather_push(bool pred, unsigned long long key, unsigned int* gcount0,
-                                            unsigned long long* list0) {
+                                            unsigned long long* list0, int cap = kListCap) {
     const unsigned int mask = __ballot_sync(0xffffffffu, pred);
     if (mask == 0u) return;
     const int lane = threadIdx.x & 31;
@@ -443,7 +447,7 @@ __device__ __forceinline__ void gather_push(bool pred, unsigned long long key, u
     base = __shfl_sync(0xffffffffu, base, __ffs(mask) - 1);
     if (pred) {
         const unsigned int pos = base + static_cast<unsigned int>(__popc(mask & ((1u << lane) - 1u)));
-        if (pos < static_cast<unsigned int>(kListCap)) list0[pos] = key;
+        if (pos < static_cast<unsigned int>(cap)) list0[pos] = key;
     }
 }
 
@@ -806,7 +810,10 @@ __global__ void __launch_bounds__(kST, 2)
         zmn = fminf(zmn, z > -INFINITY ? z : INFINITY);
         bad |= (z < INFINITY) ? 0u : 1u;  // NaN or +inf
     };
-    if (tid == 0) sm->gcount = 0u;
+    if (tid == 0) {
+        sm->gcount = 0u;
+        sm->lcount = 0u;
+    }
     if (smem_slice) {
         const bool aligned = ((reinterpret_cast<uintptr_t>(grow) & 15u) == 0);
         const int nbulk = aligned ? (n & ~3) : 0;
@@ -1003,11 +1010,20 @@ __global__ void __launch_bounds__(kST, 2)
             sm->bc[1] = 0;
         }
         __syncthreads();
-        sweep4<4>(v, nvec, vec, [&](int, const float4& q) {
-            if (q.x > -INFINITY && q.x >= zfloor) atomicAdd(&cnt[kb(q.x)], 1u);
-            if (q.y > -INFINITY && q.y >= zfloor) atomicAdd(&cnt[kb(q.y)], 1u);
-            if (q.z > -INFINITY && q.z >= zfloor) atomicAdd(&cnt[kb(q.z)], 1u);
-            if (q.w > -INFINITY && q.w >= zfloor) atomicAdd(&cnt[kb(q.w)], 1u);
+        // bounded: the counted logits (usually a few hundred) are also kept as
+        // sort keys in this CTA's candidate list, so the gather below need not
+        // read the slice again
+        unsigned long long* loc = sm->hist + kLocBase;
+        sweep4<4>(v, nvec, vec, [&](int el, const float4& q) {
+            const bool any = q.x >= zfloor || q.y >= zfloor || q.z >= zfloor || q.w >= zfloor;
+            if (!__any_sync(0xffffffffu, any)) return;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float z = f4at(q, j);
+                const bool pred = z > -INFINITY && z >= zfloor;
+                if (pred) atomicAdd(&cnt[kb(z)], 1u);
+                if (bounded) gather_push(pred, pred ? sort_key(z, lo + el + j) : 0ull, &sm->lcount, loc, kLocCap);
+            }
         });
         cluster.sync();
         uint32_t g[4] = {0u, 0u, 0u, 0u};
@@ -1035,16 +1051,28 @@ __global__ void __launch_bounds__(kST, 2)
                 // every candidate has z >= zlow (two bins of margin for rounding)
                 const float zlow =
                     kb.scale > 0.f ? fmaxf(zfloor, zmax - (static_cast<float>(bk) + 3.0f) / kb.scale) : zfloor;
-                sweep4<4>(v, nvec, vec, [&](int el, const float4& q) {
-                    const bool any = q.x >= zlow || q.y >= zlow || q.z >= zlow || q.w >= zlow;
-                    if (!__any_sync(0xffffffffu, any)) return;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float z = f4at(q, j);
-                        const bool pred = z > -INFINITY && z >= zfloor && kb(z) <= bk;
-                        gather_push(pred, pred ? sort_key(z, lo + el + j) : 0ull, gcount0, list0);
+                const int lc = static_cast<int>(sm->lcount);  // read after the cluster barrier above
+                if (bounded && lc <= kLocCap) {
+                    const unsigned long long* loc = sm->hist + kLocBase;
+                    for (int i = tid - lane; i < lc; i += kST) {  // warp-uniform trip count
+                        const int j = i + lane;
+                        const unsigned long long key = j < lc ? loc[j] : 0ull;
+                        const float z = key_float(static_cast<uint32_t>(key >> 32));
+                        const bool pred = j < lc && kb(z) <= bk;
+                        gather_push(pred, key, gcount0, list0);
                     }
-                });
+                } else {
+                    sweep4<4>(v, nvec, vec, [&](int el, const float4& q) {
+                        const bool any = q.x >= zlow || q.y >= zlow || q.z >= zlow || q.w >= zlow;
+                        if (!__any_sync(0xffffffffu, any)) return;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float z = f4at(q, j);
+                            const bool pred = z > -INFINITY && z >= zfloor && kb(z) <= bk;
+                            gather_push(pred, pred ? sort_key(z, lo + el + j) : 0ull, gcount0, list0);
+                        }
+                    });
+                }
                 cluster.sync();  // candidates complete in rank 0; no remote access follows
                 if (c.rank != 0) return;
                 solo_finish(sm, static_cast<int>(total), kk, pp, zmax, c2, seed, offset, tok_out);
