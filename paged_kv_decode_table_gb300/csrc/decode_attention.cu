@@ -12,18 +12,21 @@
 //    [NB, Hkv, BS, D] layout the K (and V) rows of a block for every head are one
 //    contiguous Hkv*BS*256-byte run, fetched by two 128B-swizzled 2-D TMA boxes.
 //  * The sum over sequences of ceil(L/BS) blocks is cut into P = #SM equal
-//    contiguous ranges (plan kernel); CTA c streams range c through an
+//    contiguous ranges; every CTA derives the cut itself from seq_lens (a sum
+//    and a prefix scan over the batch), then streams its range c through an
 //    nst-deep mbarrier ring fed by one producer lane, so each SM keeps
 //    ~128 KB of KV in flight regardless of how lengths are distributed.
 //  * One consumer warp per KV head computes S = Q K^T and O += P V with
 //    mma.sync m16n8k16 (query heads of the group on the M axis, 16 tokens on N/K),
 //    online softmax in the log2 domain, fp32 accumulation.
 //  * A sequence cut by a range boundary leaves per-piece (max, sum, unnormalised
-//    output) partials in the workspace; the combine kernel merges them with the
-//    online-softmax rule.  Sequences wholly inside one range are written directly.
-//  * plan -> main -> combine are chained with programmatic dependent launch: each
-//    kernel launches while its predecessor runs and waits (griddepcontrol.wait)
-//    only before reading the predecessor's results.
+//    output) partials in the workspace, in one of two slots per range (the
+//    range's first sequence when it began in an earlier range, else its last);
+//    the combine kernel merges them with the online-softmax rule.  Sequences
+//    wholly inside one range are written directly.
+//  * main -> combine are chained with programmatic dependent launch: each kernel
+//    launches while its predecessor runs and waits (griddepcontrol.wait) only
+//    before reading the predecessor's results.
 // Generic path (fp32, other shapes): one CTA per (sequence, query head),
 // CUDA-core fp32, chunked online softmax.
 #include <cuda.h>
@@ -36,35 +39,26 @@
 namespace pkv {
 
 // ------------------------------------------------------------------ workspace
-struct SeqInfo {       // 32 bytes per sequence
-    int s;             // first global block index of the sequence in the split order
-    int n;             // number of blocks (0 for an empty or invalid sequence)
-    int first;         // index of the CTA whose range holds block s
-    int pieces;        // number of CTA ranges the sequence spans
-    int base;          // first partial slot of the sequence
-    int L;             // length
-    int valid;         // 0 if the length is out of range
-    int pad;
-};
-struct PlanHdr {
-    int total;         // total blocks
-    int W;             // blocks per CTA range
-    int P;             // number of CTA ranges
+struct SeqInfo {  // 16 bytes per sequence with at least one block
+    int s;        // first global block index of the sequence in the split order
+    int n;        // number of blocks
+    int W;        // blocks per CTA range in this call
     int pad;
 };
 
 struct WsLayout {
-    size_t hdr, info, ml, o, total;
+    size_t info, ml, o, total;
 };
 
 static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// info[B]; then per range two partial slots (2P in all) of (m, l) and o[D] for
+// every query head.
 static WsLayout ws_layout(int B, int Hq, int D, int P) {
     WsLayout w;
-    const size_t slots = static_cast<size_t>(B) + static_cast<size_t>(P);
-    w.hdr = 0;
-    w.info = 256;
-    w.ml = align_up(w.info + sizeof(SeqInfo) * static_cast<size_t>(B), 256);
+    const size_t slots = 2 * static_cast<size_t>(P);
+    w.info = 0;
+    w.ml = align_up(sizeof(SeqInfo) * static_cast<size_t>(B), 256);
     w.o = align_up(w.ml + slots * Hq * 2 * sizeof(float), 256);
     w.total = align_up(w.o + slots * Hq * static_cast<size_t>(D) * sizeof(float), 256);
     return w;
@@ -72,99 +66,37 @@ static WsLayout ws_layout(int B, int Hq, int D, int P) {
 
 size_t decode_workspace_bytes(int B, int Hq, int D, int P) { return ws_layout(B, Hq, D, P).total; }
 
-// ------------------------------------------------------------------ block scan (1024 threads)
-__device__ __forceinline__ int block_excl_scan_1024(int v, int* warp_tot, int& total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Blocks of sequence b (0 for a length outside [0, max_blocks * BS]).
+__device__ __forceinline__ int seq_blocks(const int32_t* seq_lens, int b, int max_blocks, int BS) {
+    const int L = seq_lens[b];
+    return (L >= 0 && static_cast<long long>(L) <= static_cast<long long>(max_blocks) * BS) ? (L + BS - 1) / BS : 0;
+}
+
+// Exclusive prefix sum over the CTA (any blockDim up to 1024); red holds 33 ints.
+__device__ __forceinline__ int cta_excl_scan(int v, int* red, int& total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
     int x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        int y = __shfl_up_sync(0xffffffffu, x, o);
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x += y;
     }
-    if (lane == 31) warp_tot[warp] = x;
+    if (lane == 31) red[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        int t = warp_tot[lane];
+        int t = lane < nw ? red[lane] : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            int y = __shfl_up_sync(0xffffffffu, t, o);
+            const int y = __shfl_up_sync(0xffffffffu, t, o);
             if (lane >= o) t += y;
         }
-        warp_tot[lane] = t;  // inclusive
+        red[lane] = t;  // inclusive
     }
     __syncthreads();
-    const int before = warp ? warp_tot[warp - 1] : 0;
-    total = warp_tot[31];
+    const int before = warp ? red[warp - 1] : 0;
+    total = red[nw - 1];
     __syncthreads();
     return before + x - v;
-}
-
-// ------------------------------------------------------------------ plan kernel
-// Splits the sequence of all (b, logical block) pairs into P equal ranges and
-// records, per sequence, which ranges it spans and where its partials go.
-__global__ void __launch_bounds__(1024)
-    plan_kernel(const int32_t* __restrict__ seq_lens, int B, int max_blocks, int BS, int P,
-                SeqInfo* __restrict__ info, PlanHdr* __restrict__ hdr, int32_t* status) {
-    __shared__ int warp_tot[32];
-    __shared__ int s_carry;
-    // The main kernel may launch now and run its prologue; it waits for this
-    // grid's completion (griddepcontrol.wait) before reading the schedule.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (threadIdx.x == 0) s_carry = 0;
-    __syncthreads();
-    const long long cap = static_cast<long long>(max_blocks) * BS;
-    for (int base = 0; base < B; base += 1024) {
-        const int b = base + threadIdx.x;
-        int n = 0, L = 0, valid = 0;
-        if (b < B) {
-            L = seq_lens[b];
-            valid = (L >= 0 && static_cast<long long>(L) <= cap);
-            if (!valid) report(status, PKV_ERR_DEVICE_BOUNDS);
-            n = valid ? (L + BS - 1) / BS : 0;
-        }
-        int tot;
-        const int ex = block_excl_scan_1024(n, warp_tot, tot);
-        const int carry = s_carry;
-        if (b < B) {
-            info[b].s = carry + ex;
-            info[b].n = n;
-            info[b].L = valid ? L : 0;
-            info[b].valid = valid;
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) s_carry = carry + tot;
-        __syncthreads();
-    }
-    const int total = s_carry;
-    const int W = total > 0 ? (total + P - 1) / P : 1;
-    __syncthreads();
-    if (threadIdx.x == 0) s_carry = 0;
-    __syncthreads();
-    for (int base = 0; base < B; base += 1024) {
-        const int b = base + threadIdx.x;
-        int pieces = 0, first = 0;
-        if (b < B) {
-            const int s = info[b].s, n = info[b].n;
-            first = s / W;
-            pieces = n > 0 ? (s + n - 1) / W - first + 1 : 0;
-        }
-        int tot;
-        const int ex = block_excl_scan_1024(pieces, warp_tot, tot);
-        const int carry = s_carry;
-        if (b < B) {
-            info[b].first = first;
-            info[b].pieces = pieces;
-            info[b].base = carry + ex;
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) s_carry = carry + tot;
-        __syncthreads();
-    }
-    if (threadIdx.x == 0) {
-        hdr->total = total;
-        hdr->W = W;
-        hdr->P = P;
-    }
 }
 
 // ------------------------------------------------------------------ fast kernel
@@ -174,15 +106,17 @@ constexpr int kDim = 128;
 struct StageMeta {
     int b, j, ntok, flags;
 };
-enum : int { kValid = 1, kFirst = 2, kLast = 4, kWhole = 8 };
+// kHead: the sequence began in an earlier range (its partial goes to slot 2c,
+// otherwise to slot 2c + 1 of range c).
+enum : int { kValid = 1, kFirst = 2, kLast = 4, kWhole = 8, kHead = 16 };
 
 // Layout of the dynamic shared memory (base rounded up to 1024 bytes for the
 // 128-byte TMA swizzle): nst stages of [K lo | K hi | V lo | V hi] boxes, each
 // box Hkv*BS rows x 128 bytes; a 2-slot ring of query rows [Hq][128] bf16; the
-// mbarriers; the per-stage metadata.
+// mbarriers; the per-stage metadata; the schedule scratch (40 ints).
 static inline size_t fast_smem_bytes(int nst, int stage_bytes, int q_bytes) {
     return 1024 + static_cast<size_t>(nst) * stage_bytes + 2 * static_cast<size_t>(q_bytes) +
-           (2 * kMaxStages + 4) * sizeof(uint64_t) + kMaxStages * sizeof(StageMeta) + 16;
+           (2 * kMaxStages + 4) * sizeof(uint64_t) + kMaxStages * sizeof(StageMeta) + 40 * sizeof(int) + 16;
 }
 
 constexpr int kFastMaxKvHeads = 8;
@@ -192,9 +126,9 @@ __global__ void __launch_bounds__((kFastMaxKvHeads + 1) * 32, 1)
     decode_attn_fast_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                             const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ out,
                             const int32_t* __restrict__ block_tables, int max_blocks, int B, int Hq, int Hkv,
-                            int BS, int NB, float scale_log2, int nst, const SeqInfo* __restrict__ info,
-                            const PlanHdr* __restrict__ hdr, float* __restrict__ part_ml,
-                            float* __restrict__ part_o, int32_t* status) {
+                            int BS, int NB, float scale_log2, int nst, const int32_t* __restrict__ seq_lens,
+                            SeqInfo* __restrict__ info, float* __restrict__ part_ml, float* __restrict__ part_o,
+                            int32_t* status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int R = Hkv * BS;
@@ -208,12 +142,13 @@ __global__ void __launch_bounds__((kFastMaxKvHeads + 1) * 32, 1)
     uint64_t* qfull = empty + kMaxStages;
     uint64_t* qempty = qfull + 2;
     StageMeta* meta = reinterpret_cast<StageMeta*>(qempty + 2);
+    int* sch = reinterpret_cast<int*>(meta + kMaxStages);  // [0, 33) scan scratch, 33: b0, 34: s0
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int CW = Hkv;  // consumer warps: one per KV head
     const int G = Hq / Hkv;
 
-    // prologue independent of the schedule (overlaps the plan kernel)
+    // prologue independent of the inputs (overlaps the predecessor kernel)
     if (threadIdx.x == 0) {
         for (int s = 0; s < nst; ++s) {
             mbar_init(&full[s], 1);
@@ -227,34 +162,67 @@ __global__ void __launch_bounds__((kFastMaxKvHeads + 1) * 32, 1)
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
     }
-    asm volatile("griddepcontrol.wait;" ::: "memory");  // the plan kernel's results are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the predecessor's writes (KV, lengths) are visible
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the combine kernel may launch
-    const int total = hdr->total, W = hdr->W;
+
+    // ---- schedule: the blocks of all sequences in order, cut into gridDim.x
+    // ranges of W; this CTA takes range blockIdx.x and finds the sequence that
+    // holds its first block with a prefix scan (stopping once past it)
+    const int nthr = blockDim.x;
+    const int n_first = static_cast<int>(threadIdx.x) < B ? seq_blocks(seq_lens, threadIdx.x, max_blocks, BS) : 0;
+    int tsum = n_first;
+    for (int b = threadIdx.x + nthr; b < B; b += nthr) tsum += seq_blocks(seq_lens, b, max_blocks, BS);
+    int total;
+    cta_excl_scan(tsum, sch, total);
+    const int W = total > 0 ? (total + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x) : 1;
     const int start = blockIdx.x * W;
     const int end = min(total, start + W);
-    __syncthreads();
-    if (start >= end) return;
+    if (start >= end) return;  // uniform over the CTA
+    {
+        int carry = 0;
+        for (int base = 0; base < B; base += nthr) {
+            const int b = base + threadIdx.x;
+            const int n = base == 0 ? n_first : (b < B ? seq_blocks(seq_lens, b, max_blocks, BS) : 0);
+            int tot;
+            const int sb = carry + cta_excl_scan(n, sch, tot);
+            if (n > 0 && sb <= start && start < sb + n) {  // exactly one thread of the CTA
+                sch[33] = b;
+                sch[34] = sb;
+            }
+            carry += tot;
+            if (carry > start) break;  // same decision in every thread
+        }
+        __syncthreads();
+    }
 
     if (warp == CW) {
         // ------------------------------------------------ producer (one lane)
         if (lane != 0) return;
-        // first sequence whose block range reaches past `start`: s + n is
-        // non-decreasing in b, and some b < B satisfies it because start < total.
-        int lo = 0, hi = B - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            const SeqInfo si = info[mid];
-            if (si.s + si.n > start) hi = mid; else lo = mid + 1;
-        }
-        int b = lo;
-        SeqInfo cur = info[b];
+        // walk the sequences from the one holding block `start`; empty and
+        // invalid sequences have no blocks and are stepped over
+        int b = sch[33], cs = sch[34];
+        int cn = seq_blocks(seq_lens, b, max_blocks, BS), cL = seq_lens[b];
         int piece = 0;
         for (int i = start, it = 0; i < end; ++i, ++it) {
-            while (cur.s + cur.n <= i) cur = info[++b];
-            const int j = i - cur.s;
+            while (cs + cn <= i) {
+                cs += cn;
+                ++b;
+                cn = seq_blocks(seq_lens, b, max_blocks, BS);
+                cL = seq_lens[b];
+            }
+            const int j = i - cs;
             const bool first = (j == 0) || (i == start);
-            const bool last = (j == cur.n - 1) || (i == end - 1);
-            const bool whole = (cur.s >= start) && (cur.s + cur.n <= end);
+            const bool last = (j == cn - 1) || (i == end - 1);
+            const bool whole = (cs >= start) && (cs + cn <= end);
+            const bool head = cs < start;  // began in an earlier range (set on every stage of the piece)
+            if (j == 0) {
+                SeqInfo si;  // the combine kernel's view of this sequence
+                si.s = cs;
+                si.n = cn;
+                si.W = W;
+                si.pad = 0;
+                info[b] = si;
+            }
             const int stage = it % nst;
             const uint32_t round = static_cast<uint32_t>(it / nst);
             if (!mbar_wait(&empty[stage], (round & 1u) ^ 1u)) {
@@ -278,8 +246,9 @@ __global__ void __launch_bounds__((kFastMaxKvHeads + 1) * 32, 1)
             StageMeta mt;
             mt.b = b;
             mt.j = j;
-            mt.ntok = min(BS, cur.L - j * BS);
-            mt.flags = (valid ? kValid : 0) | (first ? kFirst : 0) | (last ? kLast : 0) | (whole ? kWhole : 0);
+            mt.ntok = min(BS, cL - j * BS);
+            mt.flags = (valid ? kValid : 0) | (first ? kFirst : 0) | (last ? kLast : 0) | (whole ? kWhole : 0) |
+                       (head ? kHead : 0);
             meta[stage] = mt;
             uint64_t* fb = &full[stage];
             if (valid) {
@@ -479,8 +448,7 @@ __global__ void __launch_bounds__((kFastMaxKvHeads + 1) * 32, 1)
                             pack_bf16x2(O[nt][2] * inv1, O[nt][3] * inv1);
                 }
             } else {
-                const SeqInfo si = info[b];
-                const size_t slot = static_cast<size_t>(si.base + (static_cast<int>(blockIdx.x) - si.first));
+                const size_t slot = 2 * static_cast<size_t>(blockIdx.x) + ((mt.flags & kHead) ? 0 : 1);
                 if (r == 0) {
                     if (live0) {
                         part_ml[(slot * Hq + qh0) * 2 + 0] = m0;
@@ -509,66 +477,220 @@ __global__ void __launch_bounds__((kFastMaxKvHeads + 1) * 32, 1)
 // ------------------------------------------------------------------ combine kernel
 // Merges the per-range partials of sequences that span several CTA ranges:
 // M = max m_c, out = sum o_c 2^(m_c - M) / sum l_c 2^(m_c - M) (log2 domain).
-// One CTA per (sequence, query head); the piece weights are computed once into
-// shared memory, then each thread reduces its output dimensions over the pieces.
-// Writes zeros for empty or invalid sequences; skips single-range sequences,
-// which the fast kernel wrote directly.
-constexpr int kCombineThreads = 128;
-constexpr int kCombineMaxPieces = 1024;
+// A sequence spanning ranges f..t left its piece in range f in slot 2f + 1 and
+// its pieces in ranges f+1..t in slots 2c.
+// Two forms.  With many (sequence, query head) units, one warp per unit (four
+// dimensions per lane).  With few units, which then have many pieces each, one
+// CTA of kCombWarps warps per unit: thread p reads piece p's (m, l) and warp w
+// sums the outputs of pieces w, w + kCombWarps, ..., whose loads are issued
+// together with the (m, l) reads, so up to kCombWarps * kCombGroup pieces cost
+// one round trip to memory; the warps' sums meet in shared memory.  Both write
+// zeros for empty, invalid or poisoned sequences and skip single-range
+// sequences, which the fast kernel wrote directly.
+__device__ __forceinline__ void store4(__nv_bfloat16* p, float4 v) {
+    *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+}
+__device__ __forceinline__ void store4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
 
+constexpr int kCombWarps = 4;
+constexpr int kCombThreads = kCombWarps * 32;
+constexpr int kCombGroup = 8;
+constexpr int kCombMaxPieces = 1024;  // per sequence (a range holds >= 1 block, so pieces <= P)
+
+// Many (sequence, head) units: one warp each, four dimensions per lane; the
+// first kCombGroup pieces' outputs are requested together with the (m, l) pairs.
 template <typename T>
-__global__ void __launch_bounds__(kCombineThreads)
-    combine_kernel(const SeqInfo* __restrict__ info, const float* __restrict__ part_ml,
-                   const float* __restrict__ part_o, T* __restrict__ out, int Hq, int D) {
-    __shared__ float wsh[kCombineMaxPieces];
-    __shared__ float red[kCombineThreads / 32];
-    __shared__ int bad_sh;
-    const int b = blockIdx.x / Hq, qh = blockIdx.x - (blockIdx.x / Hq) * Hq;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+__global__ void __launch_bounds__(kCombThreads)
+    combine_warp_kernel(const SeqInfo* __restrict__ info, const int32_t* __restrict__ seq_lens, int max_blocks,
+                        int BS, const float* __restrict__ part_ml, const float* __restrict__ part_o,
+                        T* __restrict__ out, int B, int Hq, int32_t* status) {
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the main kernel's partials are visible
-    const SeqInfo si = info[b];
-    if (si.pieces == 1) return;
-    T* o = out + (static_cast<size_t>(b) * Hq + qh) * D;
-    const int np = min(si.pieces, kCombineMaxPieces);
-    if (tid == 0) bad_sh = (si.pieces == 0 || si.pieces > kCombineMaxPieces) ? 1 : 0;
-    __syncthreads();
-    // max over pieces (and poisoned-piece detection)
-    float M = -INFINITY;
-    for (int c = tid; c < np; c += kCombineThreads) {
-        const float2 ml = *reinterpret_cast<const float2*>(part_ml + ((static_cast<size_t>(si.base) + c) * Hq + qh) * 2);
-        M = fmaxf(M, ml.x);
-        if (ml.y < 0.f) bad_sh = 1;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int lane = threadIdx.x & 31;
+    const long long u = static_cast<long long>(blockIdx.x) * kCombWarps + (threadIdx.x >> 5);
+    if (u >= static_cast<long long>(B) * Hq) return;
+    const int b = static_cast<int>(u / Hq), qh = static_cast<int>(u - static_cast<long long>(b) * Hq);
+    const int L = seq_lens[b];
+    const bool valid = L >= 0 && static_cast<long long>(L) <= static_cast<long long>(max_blocks) * BS;
+    if (!valid && qh == 0 && lane == 0) report(status, PKV_ERR_DEVICE_BOUNDS);
+    const int n = valid ? (L + BS - 1) / BS : 0;
+    int pieces = 0, f = 0;
+    if (n > 0) {
+        const SeqInfo si = info[b];
+        f = si.s / si.W;
+        pieces = (si.s + n - 1) / si.W - f + 1;
     }
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    if (lane == 0) red[warp] = M;
-    __syncthreads();
-    M = red[0];
-    for (int w = 1; w < kCombineThreads / 32; ++w) M = fmaxf(M, red[w]);
-    const bool bad = bad_sh != 0 || M == -INFINITY;
-    __syncthreads();
-    // weights 2^(m_c - M) and the merged denominator
-    float L = 0.f;
-    for (int c = tid; c < np; c += kCombineThreads) {
-        const float2 ml = *reinterpret_cast<const float2*>(part_ml + ((static_cast<size_t>(si.base) + c) * Hq + qh) * 2);
-        const float wgt = bad ? 0.f : exp2f(ml.x - M);
-        wsh[c] = wgt;
-        L += ml.y * wgt;
-    }
-    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-    if (lane == 0) red[warp] = L;
-    __syncthreads();
-    L = 0.f;
-    for (int w = 0; w < kCombineThreads / 32; ++w) L += red[w];
-    const float inv = (!bad && L > 0.f) ? 1.f / L : 0.f;
-    for (int d = tid; d < D; d += kCombineThreads) {
-        float acc = 0.f;
-        if (!bad) {
-            const float* po = part_o + (static_cast<size_t>(si.base) * Hq + qh) * D + d;
-            const size_t stride = static_cast<size_t>(Hq) * D;
-#pragma unroll 8
-            for (int c = 0; c < np; ++c) acc = fmaf(wsh[c], po[c * stride], acc);
+    if (pieces == 1) return;
+    T* o = out + static_cast<size_t>(u) * kDim + 4 * lane;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float inv = 0.f;
+    if (pieces > 1 && pieces <= kCombMaxPieces) {
+        const size_t base = 2 * static_cast<size_t>(f);  // piece p at slot offset 2p + (p == 0)
+        const size_t ml_stride = static_cast<size_t>(Hq) * 2, o_stride = static_cast<size_t>(Hq) * kDim;
+        const float* mlp = part_ml + (base * Hq + qh) * 2;
+        const float* op = part_o + (base * Hq + qh) * kDim + 4 * lane;
+        auto off = [](int p) { return static_cast<size_t>(2 * p + (p == 0 ? 1 : 0)); };
+        float4 og[kCombGroup];
+#pragma unroll
+        for (int j = 0; j < kCombGroup; ++j)
+            og[j] = j < pieces ? __ldg(reinterpret_cast<const float4*>(op + off(j) * o_stride))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        float M = -INFINITY;
+        bool bad = false;
+        for (int c = lane; c < pieces; c += 32) {
+            const float2 ml = __ldg(reinterpret_cast<const float2*>(mlp + off(c) * ml_stride));
+            M = fmaxf(M, ml.x);
+            bad |= ml.y < 0.f;
         }
-        o[d] = from_f32<T>(acc * inv);
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+        bad = __any_sync(0xffffffffu, bad) || M == -INFINITY;
+        if (!bad) {
+            float Lsum = 0.f;
+            for (int c0 = 0; c0 < pieces; c0 += 32) {
+                float wl = 0.f;  // lane c: weight of piece c0 + c
+                if (c0 + lane < pieces) {
+                    const float2 ml = __ldg(reinterpret_cast<const float2*>(mlp + off(c0 + lane) * ml_stride));
+                    wl = exp2f(ml.x - M);
+                    Lsum = fmaf(ml.y, wl, Lsum);
+                }
+                const int nj = min(32, pieces - c0);
+                for (int j0 = 0; j0 < nj; j0 += kCombGroup) {
+                    if (c0 + j0 >= kCombGroup) {  // later groups: fetch now
+#pragma unroll
+                        for (int j = 0; j < kCombGroup; ++j)
+                            og[j] = j0 + j < nj
+                                        ? __ldg(reinterpret_cast<const float4*>(op + off(c0 + j0 + j) * o_stride))
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                    for (int j = 0; j < kCombGroup; ++j) {
+                        const float wj = __shfl_sync(0xffffffffu, wl, (j0 + j) & 31);
+                        if (j0 + j < nj) {
+                            acc.x = fmaf(wj, og[j].x, acc.x);
+                            acc.y = fmaf(wj, og[j].y, acc.y);
+                            acc.z = fmaf(wj, og[j].z, acc.z);
+                            acc.w = fmaf(wj, og[j].w, acc.w);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o2);
+            inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+        }
+    }
+    store4(o, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+}
+
+// Few units (long sequences, many pieces each): one CTA per unit.
+template <typename T>
+__global__ void __launch_bounds__(kCombThreads)
+    combine_kernel(const SeqInfo* __restrict__ info, const int32_t* __restrict__ seq_lens, int max_blocks, int BS,
+                   const float* __restrict__ part_ml, const float* __restrict__ part_o, T* __restrict__ out,
+                   int Hq, int32_t* status) {
+    __shared__ float wsh[kCombMaxPieces];
+    __shared__ float4 accsh[kCombWarps][32];
+    __shared__ float red[2][kCombWarps];
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the main kernel's partials are visible
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b = blockIdx.x / Hq, qh = blockIdx.x - (blockIdx.x / Hq) * Hq;
+    const int L = seq_lens[b];
+    const bool valid = L >= 0 && static_cast<long long>(L) <= static_cast<long long>(max_blocks) * BS;
+    if (!valid && qh == 0 && tid == 0) report(status, PKV_ERR_DEVICE_BOUNDS);
+    const int n = valid ? (L + BS - 1) / BS : 0;
+    int pieces = 0, f = 0;
+    if (n > 0) {
+        const SeqInfo si = info[b];
+        f = si.s / si.W;
+        pieces = (si.s + n - 1) / si.W - f + 1;
+    }
+    if (pieces == 1) return;  // uniform over the CTA
+    T* o = out + (static_cast<size_t>(b) * Hq + qh) * kDim;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float inv = 0.f;
+    if (pieces > 1 && pieces <= kCombMaxPieces) {
+        // piece p sits in slot 2f + 1 (p = 0) or 2(f + p) (p > 0); from slot 2f
+        // that is an offset of 2p + (p == 0) slots
+        const size_t base = 2 * static_cast<size_t>(f);
+        const size_t ml_stride = static_cast<size_t>(Hq) * 2, o_stride = static_cast<size_t>(Hq) * kDim;
+        const float* mlp = part_ml + (base * Hq + qh) * 2;
+        const float* op = part_o + (base * Hq + qh) * kDim + 4 * lane;
+        auto off = [](int p) { return static_cast<size_t>(2 * p + (p == 0 ? 1 : 0)); };
+        float4 og[kCombGroup];
+#pragma unroll
+        for (int j = 0; j < kCombGroup; ++j) {
+            const int p = warp + kCombWarps * j;
+            og[j] = p < pieces ? __ldg(reinterpret_cast<const float4*>(op + off(p) * o_stride))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float M = -INFINITY, Lsum = 0.f;
+        bool bad = false;
+        for (int p = tid; p < pieces; p += kCombThreads) {
+            const float2 ml = __ldg(reinterpret_cast<const float2*>(mlp + off(p) * ml_stride));
+            M = fmaxf(M, ml.x);
+            bad |= ml.y < 0.f;
+            wsh[p] = ml.x;
+        }
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+        bad = __syncthreads_or(bad ? 1 : 0) != 0;  // also publishes wsh
+        if (lane == 0) red[0][warp] = M;
+        __syncthreads();
+        M = red[0][0];
+#pragma unroll
+        for (int w = 1; w < kCombWarps; ++w) M = fmaxf(M, red[0][w]);
+        if (!bad && M > -INFINITY) {
+            for (int p = tid; p < pieces; p += kCombThreads) {
+                const float wgt = exp2f(wsh[p] - M);
+                Lsum = fmaf(__ldg(mlp + off(p) * ml_stride + 1), wgt, Lsum);
+                wsh[p] = wgt;
+            }
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o2);
+            if (lane == 0) red[1][warp] = Lsum;
+            __syncthreads();  // weights and partial sums published
+            float Lt = 0.f;
+#pragma unroll
+            for (int w = 0; w < kCombWarps; ++w) Lt += red[1][w];
+            inv = Lt > 0.f ? 1.f / Lt : 0.f;
+            for (int p0 = 0; p0 < pieces; p0 += kCombWarps * kCombGroup) {
+                if (p0 > 0) {  // later groups: fetch now
+#pragma unroll
+                    for (int j = 0; j < kCombGroup; ++j) {
+                        const int p = p0 + warp + kCombWarps * j;
+                        og[j] = p < pieces ? __ldg(reinterpret_cast<const float4*>(op + off(p) * o_stride))
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < kCombGroup; ++j) {
+                    const int p = p0 + warp + kCombWarps * j;
+                    if (p < pieces) {
+                        const float wj = wsh[p];
+                        acc.x = fmaf(wj, og[j].x, acc.x);
+                        acc.y = fmaf(wj, og[j].y, acc.y);
+                        acc.z = fmaf(wj, og[j].z, acc.z);
+                        acc.w = fmaf(wj, og[j].w, acc.w);
+                    }
+                }
+            }
+        }
+    }
+    // the warps' sums meet in warp 0
+    if (warp > 0) accsh[warp][lane] = acc;
+    __syncthreads();
+    if (warp == 0) {
+#pragma unroll
+        for (int w = 1; w < kCombWarps; ++w) {
+            const float4 t = accsh[w][lane];
+            acc.x += t.x;
+            acc.y += t.y;
+            acc.z += t.z;
+            acc.w += t.w;
+        }
+        store4(o + 4 * lane, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
     }
 }
 
@@ -722,7 +844,7 @@ struct FastPlan {
 };
 
 static FastPlan plan_fast(int Hq, int Hkv, int D, int BS, pkv_dtype dt, const void* k, const void* v,
-                          const void* q) {
+                          const void* q, const void* out) {
     FastPlan fp{false, 0, 0, 0, 0};
     auto aligned16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     if (dt != PKV_BF16 || D != kDim || BS % 16 != 0 || Hkv < 1 || Hkv > kFastMaxKvHeads) return fp;
@@ -730,7 +852,7 @@ static FastPlan plan_fast(int Hq, int Hkv, int D, int BS, pkv_dtype dt, const vo
     if (G < 1 || G > 16) return fp;
     const int R = Hkv * BS;
     if (R > 256) return fp;
-    if (!aligned16(k) || !aligned16(v) || !aligned16(q)) return fp;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(q) || !aligned16(out)) return fp;
     fp.stage_bytes = 4 * R * 128;
     fp.q_bytes = Hq * kDim * 2;
     const long long budget = max_optin_smem();
@@ -749,7 +871,7 @@ cudaError_t launch_decode_attention(void* out, const void* q, const void* k_cach
                                     void* workspace, int P, int32_t* status, cudaStream_t stream,
                                     bool* used_fast) {
     if (scale <= 0.f) scale = 1.0f / sqrtf(static_cast<float>(D));
-    const FastPlan fp = plan_fast(Hq, Hkv, D, BS, dtype, k_cache, v_cache, q);
+    const FastPlan fp = plan_fast(Hq, Hkv, D, BS, dtype, k_cache, v_cache, q, out);
     CUtensorMap tmK, tmV;
     bool fast = fp.ok && encode_pool_map(&tmK, k_cache, NB, Hkv, BS) && encode_pool_map(&tmV, v_cache, NB, Hkv, BS);
     if (used_fast) *used_fast = fast;
@@ -769,11 +891,9 @@ cudaError_t launch_decode_attention(void* out, const void* q, const void* k_cach
     }
     const WsLayout wl = ws_layout(B, Hq, D, P);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    PlanHdr* hdr = reinterpret_cast<PlanHdr*>(ws + wl.hdr);
     SeqInfo* info = reinterpret_cast<SeqInfo*>(ws + wl.info);
     float* part_ml = reinterpret_cast<float*>(ws + wl.ml);
     float* part_o = reinterpret_cast<float*>(ws + wl.o);
-    plan_kernel<<<1, 1024, 0, stream>>>(seq_lens, B, max_blocks, BS, P, info, hdr, status);
     const float scale_log2 = scale * 1.4426950408889634f;
     const int G = Hq / Hkv;
     const unsigned threads = static_cast<unsigned>((Hkv + 1) * 32);
@@ -792,19 +912,26 @@ cudaError_t launch_decode_attention(void* out, const void* q, const void* k_cach
     cfg.numAttrs = 1;
     err = cudaLaunchKernelEx(&cfg, kern, tmK, tmV, static_cast<const __nv_bfloat16*>(q),
                              static_cast<__nv_bfloat16*>(out), block_tables, max_blocks, B, Hq, Hkv, BS, NB,
-                             scale_log2, fp.nst, static_cast<const SeqInfo*>(info), static_cast<const PlanHdr*>(hdr),
-                             part_ml, part_o, status);
+                             scale_log2, fp.nst, seq_lens, info, part_ml, part_o, status);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t ccfg = {};
-    ccfg.gridDim = dim3(static_cast<unsigned>(B) * Hq, 1, 1);
-    ccfg.blockDim = dim3(kCombineThreads, 1, 1);
+    ccfg.blockDim = dim3(kCombThreads, 1, 1);
     ccfg.dynamicSmemBytes = 0;
     ccfg.stream = stream;
     ccfg.attrs = attr;
     ccfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&ccfg, combine_kernel<__nv_bfloat16>, static_cast<const SeqInfo*>(info),
-                             static_cast<const float*>(part_ml), static_cast<const float*>(part_o),
-                             static_cast<__nv_bfloat16*>(out), Hq, D);
+    const long long units = static_cast<long long>(B) * Hq;
+    if (units >= 8LL * P) {
+        ccfg.gridDim = dim3(static_cast<unsigned>((units + kCombWarps - 1) / kCombWarps), 1, 1);
+        err = cudaLaunchKernelEx(&ccfg, combine_warp_kernel<__nv_bfloat16>, static_cast<const SeqInfo*>(info),
+                                 seq_lens, max_blocks, BS, static_cast<const float*>(part_ml),
+                                 static_cast<const float*>(part_o), static_cast<__nv_bfloat16*>(out), B, Hq, status);
+    } else {
+        ccfg.gridDim = dim3(static_cast<unsigned>(units), 1, 1);
+        err = cudaLaunchKernelEx(&ccfg, combine_kernel<__nv_bfloat16>, static_cast<const SeqInfo*>(info), seq_lens,
+                                 max_blocks, BS, static_cast<const float*>(part_ml),
+                                 static_cast<const float*>(part_o), static_cast<__nv_bfloat16*>(out), Hq, status);
+    }
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }

@@ -9,6 +9,9 @@
 // One warp per (sequence, KV head) row; lanes move 16-byte vectors when the row
 // is 16-byte aligned, else elements.  The kernel is a pure bit copy and is
 // latency-bound (a few MB per step); HBM bytes are 2 x (read + write) per row.
+// Launched with programmatic stream serialisation, so it can start while its
+// predecessor drains and the attention kernel after it can start its prologue
+// while it runs; each waits (griddepcontrol.wait) before touching data.
 #include "pkv_common.cuh"
 
 namespace pkv {
@@ -21,6 +24,10 @@ __global__ void __launch_bounds__(kAppendWarps * 32)
                      T* __restrict__ v_cache, const int32_t* __restrict__ block_tables, int max_blocks,
                      const int32_t* __restrict__ seq_lens, int B, int Hkv, int D, int BS, int NB,
                      int vec_ok, int32_t* status) {
+    // launched as a programmatic dependent: wait for the predecessor's writes
+    // (new K/V, lengths, tables), then let the next kernel start its prologue
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row = static_cast<int>(blockIdx.x) * kAppendWarps + warp;  // b * Hkv + h
     if (row >= B * Hkv) return;
@@ -66,17 +73,28 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_cache
     const int vec_ok = ((D * es) % 16 == 0) && aligned16(k_new) && aligned16(v_new) && aligned16(k_cache) &&
                        aligned16(v_cache);
     const long long rows = static_cast<long long>(B) * Hkv;
-    const unsigned grid = static_cast<unsigned>((rows + kAppendWarps - 1) / kAppendWarps);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((rows + kAppendWarps - 1) / kAppendWarps), 1, 1);
+    cfg.blockDim = dim3(kAppendWarps * 32, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t err;
     if (dtype == PKV_F32) {
-        kv_append_kernel<float><<<grid, kAppendWarps * 32, 0, stream>>>(
-            static_cast<const float*>(k_new), static_cast<const float*>(v_new), static_cast<float*>(k_cache),
-            static_cast<float*>(v_cache), block_tables, max_blocks, seq_lens, B, Hkv, D, BS, NB, vec_ok, status);
+        err = cudaLaunchKernelEx(&cfg, kv_append_kernel<float>, static_cast<const float*>(k_new),
+                                 static_cast<const float*>(v_new), static_cast<float*>(k_cache),
+                                 static_cast<float*>(v_cache), block_tables, max_blocks, seq_lens, B, Hkv, D, BS, NB,
+                                 vec_ok, status);
     } else {
-        kv_append_kernel<__nv_bfloat16><<<grid, kAppendWarps * 32, 0, stream>>>(
-            static_cast<const __nv_bfloat16*>(k_new), static_cast<const __nv_bfloat16*>(v_new),
-            static_cast<__nv_bfloat16*>(k_cache), static_cast<__nv_bfloat16*>(v_cache), block_tables,
-            max_blocks, seq_lens, B, Hkv, D, BS, NB, vec_ok, status);
+        err = cudaLaunchKernelEx(&cfg, kv_append_kernel<__nv_bfloat16>, static_cast<const __nv_bfloat16*>(k_new),
+                                 static_cast<const __nv_bfloat16*>(v_new), static_cast<__nv_bfloat16*>(k_cache),
+                                 static_cast<__nv_bfloat16*>(v_cache), block_tables, max_blocks, seq_lens, B, Hkv, D,
+                                 BS, NB, vec_ok, status);
     }
+    if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 

@@ -794,6 +794,10 @@ __global__ void __launch_bounds__(kST, 2)
     v.g16 = (reinterpret_cast<uintptr_t>(grow) & 15u) == 0;
     const bool vec = smem_slice != 0;
 
+    // launched as a programmatic dependent: the logits are read only after the
+    // predecessor grid has finished
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // row parameters first: they decide what the passes must track
     const float T = temperature[row];
     const float pp = top_p[row];
@@ -1325,13 +1329,15 @@ cudaError_t launch_sampler(int32_t* tokens, const float* logits, int B, int V, c
     cfg.blockDim = dim3(kST, 1, 1);
     cfg.dynamicSmemBytes = sp.smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = sp.nc;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, sampler_kernel, tokens, logits, V, sp.S, sp.smem_slice, temperature, top_k,
                               top_p, seeds, offsets, status);
 }
