@@ -8,6 +8,9 @@
  *                               sequence over all cached K/V (split-KV inside);
  *   pkv_sample_tokens           temperature -> top-k -> renormalise -> top-p ->
  *                               renormalise -> seeded per-request draw.
+ * Shared prefixes: a host-side reference-counted block pool (pkv_block_pool_*,
+ * pkv_seq_*) hands out block ids and reports the copy-on-write pairs that
+ * pkv_copy_blocks copies on the GPU before the step's append.
  *
  * Conventions shared by every call
  *  - Every pointer argument is a DEVICE pointer unless stated otherwise.  The
@@ -59,7 +62,8 @@ typedef enum {
     PKV_ERR_CUDA = 3,          /* host: a CUDA runtime call or launch failed */
     PKV_ERR_DEVICE_BOUNDS = 4, /* device: block id or sequence length out of range */
     PKV_ERR_TIMEOUT = 5,       /* device: a bounded wait ran out (kernel returned early) */
-    PKV_ERR_NONFINITE = 6      /* device: NaN / +inf logit, or no finite logit in a row */
+    PKV_ERR_NONFINITE = 6,     /* device: NaN / +inf logit, or no finite logit in a row */
+    PKV_ERR_CAPACITY = 7       /* host: the block pool has too few free blocks */
 } pkv_status;
 
 typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
@@ -180,6 +184,62 @@ pkv_status pkv_sample_tokens(int32_t* tokens, const float* logits, int B, int V,
                              const float* temperature, const int32_t* top_k, const float* top_p,
                              const uint64_t* seeds, const uint64_t* offsets, void* workspace,
                              size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * Copy-on-write block copies ("LLM inference serving tutorial" 4.2; "Suy luan
+ * & Toi uu hoa (Inference)" 3.2).  For i in [0, n_pairs): physical block
+ * dst[i] of k_cache and of v_cache becomes a bit copy of block src[i] (every KV
+ * head, every slot: Hkv * block_size * D elements per pool).  src, dst: device
+ * int32 [n_pairs].  The dst ids must be distinct and none may appear among the
+ * src ids of the same call (the copies run in parallel); a block id outside
+ * [0, num_blocks) skips its pair and records PKV_ERR_DEVICE_BOUNDS.
+ * n_pairs == 0 is a no-op.  Bit copy, no arithmetic.
+ */
+pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst, int n_pairs,
+                           int Hkv, int D, int block_size, int num_blocks, pkv_dtype dtype, int32_t* dev_status,
+                           void* stream);
+
+/*
+ * Reference-counted block pool (host only; "LLM inference serving tutorial"
+ * 4.2, 1.7, appendix A [D07]-[D08]; "Bai Lab tong hop -- Inference
+ * Engineering" block [6]).  Owns the ids 0..num_blocks-1 of a KV pool laid out
+ * as above; never touches device memory.  Sequences are named by caller-chosen
+ * int64 ids.  Every mutating call either succeeds or changes nothing; errors:
+ * PKV_ERR_INVALID_ARG (unknown or duplicate sequence, length beyond
+ * max_blocks_per_seq * block_size, null pointer), PKV_ERR_CAPACITY (no free
+ * block).  Not thread-safe.
+ *   create       all blocks free, reference counts 0; NULL on bad sizes.
+ *   seq_add      a new sequence of `length` tokens gets ceil(length /
+ *                block_size) fresh blocks (count 1 each).
+ *   seq_fork     `child` shares every block of `parent` (each count + 1) and
+ *                has its length: a common prefix or a beam branch.
+ *   seq_append   reserves the slot of one new token at position length: a
+ *                fresh block when the position opens a block; when the tail
+ *                block is shared (count > 1), a fresh block replaces it in this
+ *                sequence's table, the shared block's count drops by one, and
+ *                the pair (shared -> fresh) is written to cow_src[0] /
+ *                cow_dst[0] with *n_cow = 1 (else *n_cow = 0).  The caller
+ *                copies the pairs with pkv_copy_blocks before pkv_kv_append.
+ *   seq_free     every block's count drops by one; a block whose count reaches
+ *                0 returns to the free list.  Freeing an unknown (or already
+ *                freed) sequence is a no-op returning PKV_OK.
+ *   block_tables rows of max_blocks_per_seq block ids for seqs[0..n) (host
+ *                int32 [n, max_blocks_per_seq], unused entries -1) and their
+ *                lengths (host int32 [n]), ready to upload.
+ *   num_free / refcount / seq_length report state (-1 on a bad argument).
+ */
+typedef struct pkv_block_pool pkv_block_pool;
+pkv_block_pool* pkv_block_pool_create(int num_blocks, int block_size, int max_blocks_per_seq);
+void pkv_block_pool_destroy(pkv_block_pool* pool);
+int pkv_block_pool_num_free(const pkv_block_pool* pool);
+int pkv_block_pool_refcount(const pkv_block_pool* pool, int block);
+pkv_status pkv_seq_add(pkv_block_pool* pool, int64_t seq, int length);
+pkv_status pkv_seq_fork(pkv_block_pool* pool, int64_t parent, int64_t child);
+pkv_status pkv_seq_append(pkv_block_pool* pool, int64_t seq, int32_t* cow_src, int32_t* cow_dst, int* n_cow);
+pkv_status pkv_seq_free(pkv_block_pool* pool, int64_t seq);
+int pkv_seq_length(const pkv_block_pool* pool, int64_t seq);
+pkv_status pkv_block_tables(const pkv_block_pool* pool, const int64_t* seqs, int n, int32_t* block_tables,
+                            int32_t* seq_lens);
 
 #ifdef __cplusplus
 }

@@ -20,6 +20,11 @@ What each function follows (web pages cited by title and section):
   tie rules of "LLM inference serving tutorial" section 3.1 and the filter order
   and draw order of the lab's block [8].
 * ``philox4x64_10`` / ``uniform``: Salmon et al., SC'11.
+* ``copy_blocks``: the copy half of copy-on-write, "LLM inference serving
+  tutorial" section 4.2.
+* ``oracle.blocks`` (pure Python): reference-counted block sharing, fork,
+  copy-on-write and idempotent reclaim ("LLM inference serving tutorial"
+  sections 4.1, 4.2, 1.7 and appendix A [D07]-[D08]).
 
 Parity status: every function above is pinned by ``tests/test_oracle_*.py``
 (golden fixtures, closed forms, a library attention routine, brute force over
@@ -88,6 +93,8 @@ def _load():
             lib.oracle_sample_row.restype = i32
             lib.oracle_sample_batch.argtypes = [P, i32, i32, P, P, P, P, P, P, P, P, P, P]
             lib.oracle_sample_batch.restype = i32
+            lib.oracle_copy_blocks.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32]
+            lib.oracle_copy_blocks.restype = i32
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = i32
             _lib = lib
@@ -133,6 +140,15 @@ def kv_append(k_new, v_new, k_cache, v_cache, block_tables, seq_lens, block_size
     return int(_load().oracle_kv_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
                                         _ptr(bt), bt.shape[1], _ptr(sl), B, Hkv, D, BS, NB,
                                         _dtype_code(k_cache)))
+
+
+def copy_blocks(k_cache, v_cache, src, dst) -> int:
+    """In-place copy of whole physical blocks src[i] -> dst[i] in numpy pools [NB, Hkv, BS, D]."""
+    NB, Hkv, BS, D = k_cache.shape
+    s_ = np.ascontiguousarray(src, dtype=np.int32)
+    d_ = np.ascontiguousarray(dst, dtype=np.int32)
+    return int(_load().oracle_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(s_), _ptr(d_), s_.shape[0],
+                                          Hkv, D, BS, NB, _dtype_code(k_cache)))
 
 
 def gather(cache, block_tables, b: int, L: int, h: int) -> np.ndarray:

@@ -159,6 +159,25 @@ int oracle_gather(const void* cache, const int32_t* block_tables, int max_blocks
     return OR_OK;
 }
 
+/* Copy-on-write block copies ("LLM inference serving tutorial" 4.2: a shared
+ * block that must diverge is copied and the writer's table points at the
+ * copy).  For each pair in order, physical block dst[i] of both pools becomes
+ * a byte copy of block src[i]: Hkv * BS * D elements per pool.  Pairs with an
+ * id outside [0, NB) are skipped and reported. */
+int oracle_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst, int n_pairs,
+                       int Hkv, int D, int BS, int NB, int dtype) {
+    size_t block_bytes = (size_t)Hkv * BS * D * elem_size(dtype);
+    int status = OR_OK;
+    for (int i = 0; i < n_pairs; ++i) {
+        if (src[i] < 0 || src[i] >= NB || dst[i] < 0 || dst[i] >= NB) { status = OR_DEVICE_BOUNDS; continue; }
+        memcpy((char*)k_cache + (size_t)dst[i] * block_bytes, (const char*)k_cache + (size_t)src[i] * block_bytes,
+               block_bytes);
+        memcpy((char*)v_cache + (size_t)dst[i] * block_bytes, (const char*)v_cache + (size_t)src[i] * block_bytes,
+               block_bytes);
+    }
+    return status;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Decode attention for one (sequence, query head), two-pass definition ([LAB]
  * block [5] forward: scores = q.K / sqrt(d), causal row covering every cached

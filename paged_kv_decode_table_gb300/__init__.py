@@ -11,6 +11,8 @@ Calls (names follow the C ABI):
   kv_append(k_new, v_new, k_cache, v_cache, block_tables, seq_lens)
   paged_decode_attention(q, k_cache, v_cache, block_tables, seq_lens, out=None, scale=0.0)
   sample_tokens(logits, temperature, top_k, top_p, seeds, offsets, tokens=None)
+  copy_blocks(k_cache, v_cache, src, dst)
+  BlockPool(num_blocks, block_size, max_blocks_per_seq)   host-side refcounted block ids
 """
 from __future__ import annotations
 
@@ -22,10 +24,10 @@ import torch
 
 __all__ = ["PkvError", "load_library", "library_path", "kv_append", "paged_decode_attention",
            "decode_workspace_bytes", "sample_tokens", "sample_workspace_bytes", "status_string",
-           "new_status", "check_status", "STATUS"]
+           "new_status", "check_status", "STATUS", "copy_blocks", "BlockPool"]
 
 STATUS = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED", 3: "PKV_ERR_CUDA",
-          4: "PKV_ERR_DEVICE_BOUNDS", 5: "PKV_ERR_TIMEOUT", 6: "PKV_ERR_NONFINITE"}
+          4: "PKV_ERR_DEVICE_BOUNDS", 5: "PKV_ERR_TIMEOUT", 6: "PKV_ERR_NONFINITE", 7: "PKV_ERR_CAPACITY"}
 PKV_F32, PKV_BF16 = 0, 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -70,6 +72,29 @@ def load_library():
         lib.pkv_sample_workspace_bytes.restype = sz
         lib.pkv_sample_tokens.argtypes = [P, P, i32, i32, P, P, P, P, P, P, sz, P, P]
         lib.pkv_sample_tokens.restype = i32
+        i64 = ctypes.c_int64
+        lib.pkv_copy_blocks.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, P, P]
+        lib.pkv_copy_blocks.restype = i32
+        lib.pkv_block_pool_create.argtypes = [i32, i32, i32]
+        lib.pkv_block_pool_create.restype = P
+        lib.pkv_block_pool_destroy.argtypes = [P]
+        lib.pkv_block_pool_destroy.restype = None
+        lib.pkv_block_pool_num_free.argtypes = [P]
+        lib.pkv_block_pool_num_free.restype = i32
+        lib.pkv_block_pool_refcount.argtypes = [P, i32]
+        lib.pkv_block_pool_refcount.restype = i32
+        lib.pkv_seq_add.argtypes = [P, i64, i32]
+        lib.pkv_seq_add.restype = i32
+        lib.pkv_seq_fork.argtypes = [P, i64, i64]
+        lib.pkv_seq_fork.restype = i32
+        lib.pkv_seq_append.argtypes = [P, i64, P, P, P]
+        lib.pkv_seq_append.restype = i32
+        lib.pkv_seq_free.argtypes = [P, i64]
+        lib.pkv_seq_free.restype = i32
+        lib.pkv_seq_length.argtypes = [P, i64]
+        lib.pkv_seq_length.restype = i32
+        lib.pkv_block_tables.argtypes = [P, P, i32, P, P]
+        lib.pkv_block_tables.restype = i32
         _lib = lib
         return lib
 
@@ -223,3 +248,79 @@ def sample_tokens(logits, temperature, top_k, top_p, seeds, offsets, tokens=None
                                             None, 0, _ptr(status), _stream(dev))
     _raise("pkv_sample_tokens", code)
     return tokens
+
+
+def copy_blocks(k_cache, v_cache, src, dst, status=None):
+    """Copy physical block src[i] onto dst[i] in both pools (copy-on-write);
+    src / dst are int32 device tensors of equal length."""
+    NB, Hkv, BS, D = k_cache.shape
+    dev = k_cache.device
+    _check_cuda("k_cache", k_cache)
+    _check_cuda("v_cache", v_cache, k_cache.dtype, k_cache.shape, dev)
+    n = src.shape[0]
+    _check_cuda("src", src, torch.int32, (n,), dev)
+    _check_cuda("dst", dst, torch.int32, (n,), dev)
+    if status is not None:
+        _check_cuda("status", status, torch.int32, (1,), dev)
+    code = load_library().pkv_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(src), _ptr(dst), n, Hkv, D, BS, NB,
+                                          _dtype_code(k_cache), _ptr(status), _stream(dev))
+    _raise("pkv_copy_blocks", code)
+
+
+class BlockPool:
+    """Host-side reference-counted allocator of physical KV block ids (the
+    library's pkv_block_pool).  Sequences are named by int ids."""
+
+    def __init__(self, num_blocks: int, block_size: int, max_blocks_per_seq: int):
+        self._lib = load_library()
+        self._p = self._lib.pkv_block_pool_create(num_blocks, block_size, max_blocks_per_seq)
+        if not self._p:
+            raise PkvError("pkv_block_pool_create", 1)
+        self.num_blocks, self.block_size, self.max_blocks_per_seq = num_blocks, block_size, max_blocks_per_seq
+
+    def close(self):
+        if self._p:
+            self._lib.pkv_block_pool_destroy(self._p)
+            self._p = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def add(self, seq: int, length: int):
+        _raise("pkv_seq_add", self._lib.pkv_seq_add(self._p, seq, length))
+
+    def fork(self, parent: int, child: int):
+        _raise("pkv_seq_fork", self._lib.pkv_seq_fork(self._p, parent, child))
+
+    def append(self, seq: int):
+        """Reserve the next token's slot; returns the copy-on-write pair
+        (src, dst) or None."""
+        s, d, n = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int()
+        _raise("pkv_seq_append", self._lib.pkv_seq_append(self._p, seq, ctypes.byref(s), ctypes.byref(d),
+                                                             ctypes.byref(n)))
+        return (s.value, d.value) if n.value else None
+
+    def free(self, seq: int):
+        _raise("pkv_seq_free", self._lib.pkv_seq_free(self._p, seq))
+
+    def length(self, seq: int) -> int:
+        return int(self._lib.pkv_seq_length(self._p, seq))
+
+    def num_free(self) -> int:
+        return int(self._lib.pkv_block_pool_num_free(self._p))
+
+    def refcount(self, block: int) -> int:
+        return int(self._lib.pkv_block_pool_refcount(self._p, block))
+
+    def tables(self, seqs):
+        """(block_tables int32 [n, max_blocks_per_seq], seq_lens int32 [n]) as CPU tensors."""
+        n = len(seqs)
+        ids = (ctypes.c_int64 * max(1, n))(*seqs)
+        bt = torch.empty((n, self.max_blocks_per_seq), dtype=torch.int32)
+        sl = torch.empty((n,), dtype=torch.int32)
+        _raise("pkv_block_tables", self._lib.pkv_block_tables(self._p, ids, n, ctypes.c_void_p(bt.data_ptr()),
+                                                               ctypes.c_void_p(sl.data_ptr())))
+        return bt, sl

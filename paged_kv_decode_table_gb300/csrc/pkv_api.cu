@@ -19,6 +19,8 @@ int device_sm_count();
 cudaError_t launch_sampler(int32_t* tokens, const float* logits, int B, int V, const float* temperature,
                            const int32_t* top_k, const float* top_p, const uint64_t* seeds, const uint64_t* offsets,
                            int32_t* status, cudaStream_t stream);
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst, int n_pairs,
+                               long long block_bytes, int NB, int32_t* status, cudaStream_t stream);
 }  // namespace pkv
 
 namespace {
@@ -37,6 +39,7 @@ const char* pkv_status_string(int status) {
         case PKV_ERR_DEVICE_BOUNDS: return "PKV_ERR_DEVICE_BOUNDS";
         case PKV_ERR_TIMEOUT: return "PKV_ERR_TIMEOUT";
         case PKV_ERR_NONFINITE: return "PKV_ERR_NONFINITE";
+        case PKV_ERR_CAPACITY: return "PKV_ERR_CAPACITY";
         default: return "PKV_ERR_UNKNOWN";
     }
 }
@@ -53,6 +56,19 @@ pkv_status pkv_kv_append(const void* k_new, const void* v_new, void* k_cache, vo
     return cuda_status(pkv::launch_kv_append(k_new, v_new, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                              seq_lens, B, Hkv, D, block_size, num_blocks, dtype, dev_status,
                                              static_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst, int n_pairs,
+                           int Hkv, int D, int block_size, int num_blocks, pkv_dtype dtype, int32_t* dev_status,
+                           void* stream) {
+    if (n_pairs < 0 || Hkv < 1 || D < 1 || block_size < 1 || num_blocks < 1 || !dtype_ok(dtype))
+        return PKV_ERR_INVALID_ARG;
+    if (n_pairs == 0) return PKV_OK;
+    if (!k_cache || !v_cache || !src || !dst) return PKV_ERR_INVALID_ARG;
+    const long long es = dtype == PKV_F32 ? 4 : 2;
+    const long long block_bytes = static_cast<long long>(Hkv) * block_size * D * es;
+    return cuda_status(pkv::launch_copy_blocks(k_cache, v_cache, src, dst, n_pairs, block_bytes, num_blocks,
+                                               dev_status, static_cast<cudaStream_t>(stream)));
 }
 
 size_t pkv_decode_workspace_bytes(int B, int Hq, int D, int num_sms) {
