@@ -446,6 +446,123 @@ def run_gpu(args):
     return 0
 
 
+# ---------------------------------------------------------------- extra measurements
+def _time_calls(fn, n: int, flush=None):
+    """Per-call device times (us) with CUDA events on the current stream; when
+    `flush` is given it runs before every call, outside the events (L2 flush)."""
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for e0, e1 in ev:
+        if flush is not None:
+            flush()
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    t = sorted(e0.elapsed_time(e1) * 1e3 for e0, e1 in ev)
+    return {"median_us": t[len(t) // 2], "p90_us": t[min(len(t) - 1, (9 * len(t)) // 10)], "n": n}
+
+
+def run_extras(args):
+    """One JSON line per extra measurement (not part of the default bench line):
+    attention calls on the batch-64, long-context and fragmented workloads, the
+    sampler alone on its three workloads (L2 flushed between calls), block
+    copies, and attention over forked sequences that share prefix blocks."""
+    import paged_kv_decode_table_gb300 as pkv
+    from paged_kv_decode_table_gb300 import build as pkv_build
+    pkv_build.build()
+    pkv.load_library()
+    peak, _ = _peaks()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    scratch = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def flush():
+        scratch.fill_(1)
+
+    def emit(d):
+        print(json.dumps(d), flush=True)
+
+    for num in (2, 3, 4):
+        w = W.workload(num)
+        inp = W.make_decode_inputs(w, dev, with_logits=False)
+        out = torch.empty_like(inp["q"])
+        ws = torch.empty(pkv.decode_workspace_bytes(w.batch, w.n_q_heads, w.head_dim), dtype=torch.uint8,
+                         device=dev)
+        by = W.step_bytes(w, inp["seq_lens"])["attention"]
+        t = _time_calls(lambda: pkv.paged_decode_attention(inp["q"], inp["k_cache"], inp["v_cache"],
+                                                           inp["block_tables"], inp["seq_lens"], out=out,
+                                                           workspace=ws), 50)
+        gbs = by / (t["median_us"] * 1e-6) / 1e9
+        emit({"extra": "paged_decode_attention", "workload": w.name, "bytes": by, **t, "GB/s": gbs,
+              "frac_of_measured": gbs / peak, "frac_of_8TBps": gbs / 8000.0})
+        del inp, out, ws
+        torch.cuda.empty_cache()
+
+    for num, label in ((2, "T0.7 k50 p0.9"), (4, "T1.0 p0.95"), (5, "stress: mixed T / k / p")):
+        w = W.workload(num)
+        si = W.make_sampler_inputs(w, dev)
+        tok = torch.empty(w.batch, dtype=torch.int32, device=dev)
+        t = _time_calls(lambda: pkv.sample_tokens(si["logits"], si["temperature"], si["top_k"], si["top_p"],
+                                                  si["seeds"], si["offsets"], tokens=tok), 50, flush=flush)
+        by = 4 * w.batch * w.vocab
+        emit({"extra": "sample_tokens", "workload": f"{w.batch}x{w.vocab} {label}", **t,
+              "tokens_per_s": w.batch / (t["median_us"] * 1e-6), "logits_GB/s": by / (t["median_us"] * 1e-6) / 1e9,
+              "frac_of_measured": by / (t["median_us"] * 1e-6) / 1e9 / peak})
+        del si
+        torch.cuda.empty_cache()
+
+    # copy-on-write block copies: 1024 pairs of 64 KB blocks (bf16, 8 KV heads, 16 slots, D 128)
+    NB, Hkv, BS, D = 4096, 8, 16, 128
+    K = torch.randn((NB, Hkv, BS, D), device=dev).to(torch.bfloat16)
+    V = torch.randn((NB, Hkv, BS, D), device=dev).to(torch.bfloat16)
+    perm = torch.randperm(NB, generator=torch.Generator().manual_seed(1)).to(torch.int32)
+    src, dst = perm[:1024].to(dev), perm[1024:2048].to(dev)
+    t = _time_calls(lambda: pkv.copy_blocks(K, V, src, dst), 50, flush=flush)
+    by = 1024 * 2 * 2 * Hkv * BS * D * 2   # pools x (read + write) per pair
+    emit({"extra": "copy_blocks", "pairs": 1024, "block_bytes_per_pool": Hkv * BS * D * 2, "bytes": by, **t,
+          "GB/s": by / (t["median_us"] * 1e-6) / 1e9, "frac_of_measured": by / (t["median_us"] * 1e-6) / 1e9 / peak})
+    del K, V
+    torch.cuda.empty_cache()
+
+    # forked sequences: 4 prompts of 2048..4096 tokens, 16 branches each, one decode step
+    # in; attention reads each shared prompt block once from HBM and 15 more times from L2
+    gen = torch.Generator().manual_seed(77)
+    lens = torch.randint(2048, 4097, (4,), generator=gen).tolist()
+    Hq = 32
+    MB = 4200 // BS
+    NB = sum(-(-L // BS) for L in lens) + 4 * 16 * 2 + 8
+    pool = pkv.BlockPool(NB, BS, MB)
+    K = torch.randn((NB, Hkv, BS, D), device=dev).to(torch.bfloat16)
+    V = torch.randn((NB, Hkv, BS, D), device=dev).to(torch.bfloat16)
+    kids = []
+    for p, L in enumerate(lens):
+        pool.add(1000 + p, L)
+        for c in range(16):
+            pool.fork(1000 + p, p * 16 + c)
+            kids.append(p * 16 + c)
+        pool.free(1000 + p)
+    pairs = [x for x in (pool.append(s) for s in kids) if x is not None]
+    if pairs:
+        pkv.copy_blocks(K, V, torch.tensor([x[0] for x in pairs], dtype=torch.int32, device=dev),
+                        torch.tensor([x[1] for x in pairs], dtype=torch.int32, device=dev))
+    bt, sl = pool.tables(kids)
+    bt, sl = bt.to(dev), sl.to(dev)
+    q = torch.randn((len(kids), Hq, D), device=dev).to(torch.bfloat16)
+    out = torch.empty_like(q)
+    t = _time_calls(lambda: pkv.paged_decode_attention(q, K, V, bt, sl, out=out), 50, flush=flush)
+    logical = int(sl.sum()) * Hkv * D * 2 * 2
+    unique = (NB - pool.num_free()) * Hkv * BS * D * 2 * 2
+    emit({"extra": "paged_decode_attention_forked", "workload": f"4 prompts x 16 branches, lengths {lens}",
+          "logical_kv_bytes": logical, "unique_kv_bytes": unique, **t,
+          "logical_GB/s": logical / (t["median_us"] * 1e-6) / 1e9,
+          "unique_GB/s": unique / (t["median_us"] * 1e-6) / 1e9, "cow_pairs": len(pairs)})
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -453,9 +570,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--extras", action="store_true",
+                    help="print extra measurement lines (other workloads, sampler alone, block copies)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.extras:
+        return run_extras(args)
     return run_gpu(args)
 
 
