@@ -58,6 +58,7 @@ struct __align__(16) SampSmem {
     unsigned long long wsum[kSW];
     unsigned long long bc[8];
     unsigned long long aslot[kMaxCluster];
+    unsigned long long bslot[kMaxCluster];
     uint64_t bar[4];        // one per chunk of the slice load
     unsigned int gcount;    // rank 0: candidates gathered so far
     int imin;
@@ -80,10 +81,26 @@ __device__ __forceinline__ float key_float(uint32_t k) {
     const uint32_t u = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
     return __uint_as_float(u);
 }
-// floor(w * 2^40) for w in [0, 1]: scaling by 2^40 is exact, and the float ->
-// u64 conversion truncates (a float carries 24 significant bits, so the
-// integer part is exact).
-__device__ __forceinline__ uint64_t fx40(float w) { return __float2ull_rz(w * 1099511627776.0f); }
+// floor(w * 2^40) for w in [0, 1], from the bits of w with integer ALU
+// operations (a float -> 64-bit integer conversion is a slow multi-cycle
+// operation, and the sampler takes one per logit): a normal w is m * 2^(e-150)
+// with m its 24-bit significand (implicit 1 included), so w * 2^40 =
+// m * 2^(e-110); a left shift (e >= 110) is exact, a right shift drops exactly
+// the fraction, and zero or subnormal w (e = 0) gives 0.  The same value as
+// truncating w * 2^40, which is exact in float.
+__device__ __forceinline__ uint64_t fx40(float w) {
+    const uint32_t u = __float_as_uint(w);
+    const uint64_t m = (u & 0x7fffffu) | 0x800000u;
+    const int sh = static_cast<int>(u >> 23) - 110;
+    return sh >= 0 ? (m << sh) : (sh > -24 ? (m >> -sh) : 0ull);
+}
+// floor(w * 2^24) = fx40(w) >> 16, in 32 bits by the same construction.
+__device__ __forceinline__ uint32_t fx24(float w) {
+    const uint32_t u = __float_as_uint(w);
+    const uint32_t m = (u & 0x7fffffu) | 0x800000u;
+    const int sh = static_cast<int>(u >> 23) - 126;
+    return sh >= 0 ? (m << sh) : (sh > -24 ? (m >> -sh) : 0u);
+}
 // 2^x by the hardware's approximate base-2 exponential (subnormal results flush
 // to zero; they are below 2^-40 and weigh nothing anyway).
 __device__ __forceinline__ float hw_exp2(float x) {
@@ -491,38 +508,65 @@ __device__ __forceinline__ void sum_remote_f4(cg::cluster_group& cl, float* h, i
 // ------------------------------------------------------------------ draw (whole cluster)
 // First kept id (ascending) whose running fixed-point mass exceeds
 // floor(u * S_p), S_p = total kept mass.  The CTA that holds it writes the token.
+// The slice is cut into chunks of 128 * cpw consecutive logits (cpw chosen so
+// that there are at most kHistBins chunks); warp w sums the kept masses of
+// chunks w, w + 16, ... with coalesced 16-byte loads (lane l takes logits
+// 4l..4l+3 of each 128), the chunk sums are scanned in shared memory (hist is
+// free here), the CTA totals are exchanged, and in the CTA that holds the
+// draw one warp walks the single chunk that holds it.
 // Ends with this CTA's arrival on the cluster barrier; the caller waits on it.
 __device__ void draw_pass(Ctx& c, const View& v, const Keep& kp, bool vec, float zmax, float c2, uint64_t seed,
                           uint64_t offset, int32_t* tok_out) {
     SampSmem* sm = c.sm;
-    const int tid = threadIdx.x;
-    const int E = run_len4(v.n);
-    const int b0 = min(v.n, tid * E), b1 = min(v.n, b0 + E);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nvec = (v.n + 3) & ~3;
+    const int cpw = max(1, (nvec + 128 * kHistBins - 1) / (128 * kHistBins));
+    const int csz = 128 * cpw;
+    const int nch = (nvec + csz - 1) / csz;
     const bool filt = kp.k_on || kp.p_on;
     // -inf logits weigh 0, so without a filter every slot is simply summed
-    auto kept = [&](float z, int id) { return !filt || kp.keep_f(z, id); };
-    uint64_t w = 0;
-    if (!filt) {
-#pragma unroll 4
-        for (int e = b0; e < b1; e += 4) {
-            const float4 q = load4(v, e, vec);
-            w += mass(q.x, zmax, c2) + mass(q.y, zmax, c2) + mass(q.z, zmax, c2) + mass(q.w, zmax, c2);
+    auto kmass = [&](float z, int e) -> uint64_t {
+        return (!filt || kp.keep_f(z, v.idbase + e)) ? mass(z, zmax, c2) : 0ull;
+    };
+    auto lane_sum = [&](int e) -> uint64_t {  // this lane's 4 logits at slot e (may lie past the end)
+        if (e >= nvec) return 0ull;
+        const float4 q = load4(v, e, vec);
+        return kmass(q.x, e) + kmass(q.y, e + 1) + kmass(q.z, e + 2) + kmass(q.w, e + 3);
+    };
+    unsigned long long* ctot = sm->hist;
+    for (int ch = warp; ch < nch; ch += kSW) {
+        const int e0 = ch * csz + 4 * lane;
+        uint64_t w = 0;
+        int k = 0;
+        for (; k + 4 <= cpw; k += 4) {
+            const uint64_t a0 = lane_sum(e0 + 128 * k), a1 = lane_sum(e0 + 128 * (k + 1));
+            const uint64_t a2 = lane_sum(e0 + 128 * (k + 2)), a3 = lane_sum(e0 + 128 * (k + 3));
+            w += a0 + a1 + a2 + a3;
         }
-    } else {
-#pragma unroll 4
-        for (int e = b0; e < b1; e += 4) {
-            const float4 q = load4(v, e, vec);
+        for (; k < cpw; ++k) w += lane_sum(e0 + 128 * k);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float z = f4at(q, j);
-                if (kp.keep_f(z, v.idbase + e + j)) w += mass(z, zmax, c2);
-            }
-        }
+        for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
+        if (lane == 0) ctot[ch] = w;
+    }
+    __syncthreads();
+    // exclusive scan of the chunk sums, four consecutive chunks per thread
+    uint64_t t4[4], ts = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int ch = 4 * tid + q;
+        t4[q] = ch < nch ? ctot[ch] : 0ull;
+        ts += t4[q];
     }
     uint64_t tot;
-    const uint64_t ex = block_excl_scan_u64(w, sm->wsum, tot);
+    uint64_t run = block_excl_scan_u64(ts, sm->wsum, tot);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int ch = 4 * tid + q;
+        if (ch < nch) ctot[ch] = run;
+        run += t4[q];
+    }
     if (tid == 0) sm->xch[c.xb][0] = tot;
-    exch(c, 1);
+    exch(c, 1);  // its barriers also publish the scanned chunk sums
     uint64_t Sp = 0, pre = 0;
     for (int j = 0; j < c.nc; ++j) {
         Sp += sm->gath[j][0];
@@ -531,18 +575,52 @@ __device__ void draw_pass(Ctx& c, const View& v, const Keep& kp, bool vec, float
     cluster_arrive();  // all remote reads of this CTA are done
     const uint64_t u53 = philox_word0(seed, offset) >> 11;
     const uint64_t X = static_cast<uint64_t>((static_cast<unsigned __int128>(u53) * Sp) >> 53);  // floor(u*Sp) < Sp
-    if (pre + ex <= X && X < pre + ex + w) {
-        uint64_t cum = pre + ex;
-        for (int e = b0; e < b1; ++e) {
-            const float z = v.z[e];
-            const int id = v.idbase + e;
-            if (!kept(z, id)) continue;
-            cum += mass(z, zmax, c2);
-            if (cum > X) {
-                *tok_out = id;
-                break;
+    if (!(pre <= X && X < pre + tot)) return;  // the draw lies in another CTA
+    const uint64_t Xr = X - pre;
+    // the chunk holding Xr: the last chunk whose exclusive prefix is <= Xr and that
+    // has mass (found by the thread that owns it; a unique match)
+    if (tid == 0) sm->imin = -1;
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int ch = 4 * tid + q;
+        if (ch < nch) {
+            const uint64_t lo = ctot[ch], hi = ch + 1 < nch ? ctot[ch + 1] : tot;
+            if (lo <= Xr && Xr < hi) sm->imin = ch;
+        }
+    }
+    __syncthreads();
+    const int cs = sm->imin;
+    if (warp != 0 || cs < 0) return;
+    uint64_t base = ctot[cs];
+    for (int k = 0; k < cpw; ++k) {
+        const int e = cs * csz + 128 * k + 4 * lane;
+        float4 q = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        if (e < nvec) q = load4(v, e, vec);
+        const uint64_t m0 = kmass(q.x, e), m1 = kmass(q.y, e + 1), m2 = kmass(q.z, e + 2), m3 = kmass(q.w, e + 3);
+        const uint64_t mine = m0 + m1 + m2 + m3;
+        uint64_t inc = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint64_t y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += y;
+        }
+        const uint64_t before = base + inc - mine;
+        if (before <= Xr && Xr < before + mine) {
+            // the 4 logits of this lane: first whose running mass passes Xr
+            uint64_t cum = before;
+            const uint64_t ms[4] = {m0, m1, m2, m3};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                cum += ms[j];
+                if (cum > Xr) {
+                    *tok_out = v.idbase + e + j;
+                    break;
+                }
             }
         }
+        base += __shfl_sync(0xffffffffu, inc, 31);
+        if (base > Xr) break;  // found (warp-uniform)
     }
 }
 
@@ -991,7 +1069,6 @@ __global__ void __launch_bounds__(kST, 2)
         bins.scale = (range > 0.f && sc < INFINITY) ? sc : 0.f;
     }
     unsigned int* cnt = reinterpret_cast<unsigned int*>(sm->hist);
-    float* fmass = reinterpret_cast<float*>(sm->hist) + kHistBins;
     unsigned int* gcount0 = cluster.map_shared_rank(&sm->gcount, 0);
     unsigned long long* list0 = cluster.map_shared_rank(&sm->list[0], 0);
     int kk = 0;  // effective top-k (0: off); set once the finite count is known
@@ -1091,95 +1168,168 @@ __global__ void __launch_bounds__(kST, 2)
     }
 
     if (pp < 1.f) {
-        // ---------------- top-p only: approximate fp32 bin masses locate the cut,
-        // rank 0 resolves it exactly on the gathered bins around it
+        // ---------------- top-p only.  On the 2048 linear bins of (zmax - z), each
+        // bin gets its count and the sums of the high (>> 16) and low (mod 2^16)
+        // parts of its logits' masses floor(w * 2^40), with u32 shared atomics.
+        // Where the sums cannot have wrapped (count * an upper bound of the high
+        // part < 2^32, count < 2^16) they give the bin's exact mass; other bins
+        // are bounded by count times the weights at the bin's edges (1/64 bin of
+        // margin for the rounding of the bin index, 2^-20 relative for the
+        // approximate exponential).  The bounds bracket S and every cumulative
+        // from the top, so the cut lies in the bins [blo, bhi] where they
+        // straddle ceil(p * S); when every bin is exact that is one bin, and the
+        // exact mass above it is already known.  A second pass gathers the
+        // window into rank 0 (summing exact masses above and below it when some
+        // bin was inexact), which sorts it and finds the cut exactly.
+        constexpr int kPer = kHistBins / kST;  // 4 bins per thread
+        unsigned int* pc = reinterpret_cast<unsigned int*>(sm->hist);   // counts
+        unsigned int* ph = pc + kHistBins;                                // sums of mass >> 16
+        unsigned int* pl = reinterpret_cast<unsigned int*>(sm->list);   // sums of mass & 0xffff
         for (int i = tid; i < kHistBins; i += kST) {
-            cnt[i] = 0u;
-            fmass[i] = 0.f;
+            pc[i] = 0u;
+            ph[i] = 0u;
+            pl[i] = 0u;
         }
         if (tid == 0) {
-            sm->bc[2] = kHistBins - 1;
+            sm->bc[2] = 0;
             sm->bc[3] = kHistBins - 1;
+            sm->bc[7] = 0;
         }
         __syncthreads();
-        uint64_t st = 0;
         sweep4<4>(v, nvec, vec, [&](int, const float4& q) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const float z = f4at(q, j);
-                if (!(z > -INFINITY)) continue;
-                const int b = bins(z);
-                const float wf = weight(z, zmax, c2);
-                st += fx40(wf);
-                atomicAdd(&cnt[b], 1u);
-                atomicAdd(&fmass[b], wf);
+                if (z > -INFINITY) {
+                    const int b = bins(z);
+                    const uint64_t m = mass(z, zmax, c2);
+                    atomicAdd(&pc[b], 1u);
+                    atomicAdd(&ph[b], static_cast<unsigned int>(m >> 16));
+                    atomicAdd(&pl[b], static_cast<unsigned int>(m & 0xffffu));
+                }
             }
         });
-        uint64_t scta;
-        block_excl_scan_u64(st, sm->wsum, scta);
-        if (tid == 0) sm->xch[c.xb][0] = scta;
-        exch(c, 1);  // also publishes every CTA's histograms
-        uint64_t S = 0;
-        for (int j = 0; j < c.nc; ++j) S += sm->gath[j][0];
-        const uint64_t target = ceil_mul_p(pp, S);
-        const uint64_t eps = S / 10000 + 1;
-        const uint64_t lo_t = target > eps ? target - eps : 0;
-        const uint64_t hi_t = target + eps;
-        float fs[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t gcn[4] = {0u, 0u, 0u, 0u};
-        sum_remote_f4(cluster, fmass, c.nc, fs);
-        sum_remote_u4(cluster, cnt, c.nc, gcn);
-        uint64_t gm[4];
-        uint64_t tsum = 0;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            gm[q] = static_cast<uint64_t>(static_cast<double>(fs[q]) * 1099511627776.0);
-            tsum += gm[q];
+        cluster.sync();  // every CTA's bins are complete
+        // this thread's bins [4*tid, 4*tid + 4), summed over the cluster
+        uint32_t gc[kPer] = {0u, 0u, 0u, 0u}, gh[kPer] = {0u, 0u, 0u, 0u}, gl[kPer] = {0u, 0u, 0u, 0u};
+        for (int r = 0; r < c.nc; ++r) {
+            const uint4 cc = reinterpret_cast<const uint4*>(cluster.map_shared_rank(pc, r))[tid];
+            const uint4 hh = reinterpret_cast<const uint4*>(cluster.map_shared_rank(ph, r))[tid];
+            const uint4 ll = reinterpret_cast<const uint4*>(cluster.map_shared_rank(pl, r))[tid];
+            gc[0] += cc.x; gc[1] += cc.y; gc[2] += cc.z; gc[3] += cc.w;
+            gh[0] += hh.x; gh[1] += hh.y; gh[2] += hh.z; gh[3] += hh.w;
+            gl[0] += ll.x; gl[1] += ll.y; gl[2] += ll.z; gl[3] += ll.w;
         }
-        uint64_t tot;
-        const uint64_t ex = block_excl_scan_u64(tsum, sm->wsum, tot);
+        cluster_arrive();  // remote reads of the bins are done (waited on before reuse)
+        auto bin_bounds = [&](int q, uint64_t& mh, uint64_t& ml) {
+            const uint64_t n = gc[q];
+            mh = ml = 0;
+            if (n == 0) return;
+            const int bq = kPer * tid + q;
+            // weights at the bin's edges: bin b holds (zmax - (b+1)/s, zmax - b/s]
+            const float dh = bins.scale > 0.f ? (static_cast<float>(bq) - 0.015625f) / bins.scale : 0.f;
+            const float dl = bins.scale > 0.f ? (static_cast<float>(bq + 1) + 0.015625f) / bins.scale : zmax - zmin;
+            uint64_t hi = fx40(hw_exp2(fminf(-dh * c2, 0.f)));
+            hi += (hi >> 20) + 1;
+            if (n < 65536u && n * ((hi >> 16) + 1) < (1ull << 32)) {
+                ml = mh = (static_cast<uint64_t>(gh[q]) << 16) + gl[q];  // the sums did not wrap: exact
+                return;
+            }
+            uint64_t lo = fx40(hw_exp2(-dl * c2));
+            lo = lo > (lo >> 20) + 1 ? lo - (lo >> 20) - 1 : 0ull;
+            mh = n * hi;
+            ml = n * lo;
+        };
+        uint64_t tlo = 0, thi = 0;
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            uint64_t mh, ml;
+            bin_bounds(q, mh, ml);
+            thi += mh;
+            tlo += ml;
+        }
+        uint64_t Shi, Slo;
+        const uint64_t exh = block_excl_scan_u64(thi, sm->wsum, Shi);
+        const uint64_t exl = block_excl_scan_u64(tlo, sm->wsum, Slo);
+        const uint64_t tgt_lo = ceil_mul_p(pp, Slo), tgt_hi = ceil_mul_p(pp, Shi);
         {
-            uint64_t cc = ex;
-            for (int q = 0; q < 4; ++q) {
-                // first bin whose inclusive approximate cumulative reaches lo_t / hi_t
-                const int b = tid * 4 + q;
-                const uint64_t nx = cc + gm[q];
-                if (nx >= lo_t && (b == 0 || cc < lo_t)) sm->bc[2] = static_cast<unsigned long long>(b);
-                if (nx >= hi_t && (b == 0 || cc < hi_t)) sm->bc[3] = static_cast<unsigned long long>(b);
-                cc = nx;
+            uint64_t ch = exh, cl = exl;
+#pragma unroll
+            for (int q = 0; q < kPer; ++q) {
+                const int bq = kPer * tid + q;
+                uint64_t mh, ml;
+                bin_bounds(q, mh, ml);
+                const uint64_t nh = ch + mh, nl = cl + ml;
+                if (nh >= tgt_lo && (bq == 0 || ch < tgt_lo)) {
+                    sm->bc[2] = static_cast<unsigned long long>(bq);
+                    sm->bc[7] = ch;  // mass above bin blo (exact when every bin is)
+                }
+                if (nl >= tgt_hi && (bq == 0 || cl < tgt_hi)) sm->bc[3] = static_cast<unsigned long long>(bq);
+                ch = nh;
+                cl = nl;
             }
         }
         __syncthreads();
         const int blo = static_cast<int>(sm->bc[2]);
         const int bhi = max(blo, static_cast<int>(sm->bc[3]));
-        // exact count of the window from the summed histograms
+        const bool exact = Shi == Slo;  // every bin's mass is known exactly
+        const uint64_t A_known = sm->bc[7];
         uint64_t wc = 0;
-        for (int q = 0; q < 4; ++q) {
-            const int b = tid * 4 + q;
-            if (b >= blo && b <= bhi) wc += gcn[q];
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const int bq = kPer * tid + q;
+            if (bq >= blo && bq <= bhi) wc += gc[q];
         }
         uint64_t total;
         block_excl_scan_u64(wc, sm->wsum, total);
+        cluster_wait();  // no CTA still reads another's counts
         if (total >= 1 && total <= static_cast<uint64_t>(kListCap)) {
-            uint64_t at = 0;
-            sweep4<4>(v, nvec, vec, [&](int el, const float4& q) {
+            uint64_t at = 0, bt = 0;  // exact masses above and below the window
+            if (exact) {
+                sweep4<4>(v, nvec, vec, [&](int el, const float4& q) {
+                    bool in[4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float z = f4at(q, j);
-                    const bool fin = z > -INFINITY;
-                    const int b = fin ? bins(z) : kHistBins;
-                    if (fin && b < blo) at += mass(z, zmax, c2);
-                    const bool pred = fin && b >= blo && b <= bhi;
-                    gather_push(pred, pred ? sort_key(z, lo + el + j) : 0ull, gcount0, list0);
-                }
-            });
-            uint64_t acta;
+                    for (int j = 0; j < 4; ++j) {
+                        const float z = f4at(q, j);
+                        const int b = bins(z);
+                        in[j] = z > -INFINITY && b >= blo && b <= bhi;
+                    }
+                    if (!__any_sync(0xffffffffu, in[0] || in[1] || in[2] || in[3])) return;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        gather_push(in[j], in[j] ? sort_key(f4at(q, j), lo + el + j) : 0ull, gcount0, list0);
+                });
+            } else {
+                sweep4<4>(v, nvec, vec, [&](int el, const float4& q) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float z = f4at(q, j);
+                        const bool fin = z > -INFINITY;
+                        const int b = fin ? bins(z) : kHistBins;
+                        if (fin && (b < blo || b > bhi)) {
+                            const uint64_t m = mass(z, zmax, c2);
+                            if (b < blo) at += m; else bt += m;
+                        }
+                        const bool pred = fin && b >= blo && b <= bhi;
+                        gather_push(pred, pred ? sort_key(z, lo + el + j) : 0ull, gcount0, list0);
+                    }
+                });
+            }
+            uint64_t acta, bcta;
             block_excl_scan_u64(at, sm->wsum, acta);
-            if (tid == 0) *cluster.map_shared_rank(&sm->aslot[c.rank], 0) = acta;
-            cluster.sync();  // window gathered and exact masses above it posted in rank 0
+            block_excl_scan_u64(bt, sm->wsum, bcta);
+            if (tid == 0) {
+                *cluster.map_shared_rank(&sm->aslot[c.rank], 0) = acta;
+                *cluster.map_shared_rank(&sm->bslot[c.rank], 0) = bcta;
+            }
+            cluster.sync();  // window gathered and exact masses around it posted in rank 0
             if (c.rank == 0) {
-                uint64_t A = 0;
-                for (int r = 0; r < c.nc; ++r) A += sm->aslot[r];
+                uint64_t A = 0, Bm = 0;
+                for (int r = 0; r < c.nc; ++r) {
+                    A += sm->aslot[r];
+                    Bm += sm->bslot[r];
+                }
+                if (exact) A = A_known;  // and Bm stays 0: S is known
                 unsigned long long* a = sm->list;
                 const int nw = static_cast<int>(total);
                 const int np2 = pow2_ceil(nw);
@@ -1197,6 +1347,7 @@ __global__ void __launch_bounds__(kST, 2)
                 for (int j = b0; j < b1; ++j) w += mass(key_float(static_cast<uint32_t>(a[j] >> 32)), zmax, c2);
                 uint64_t wtot;
                 const uint64_t wex = block_excl_scan_u64(w, sm->wsum, wtot);
+                const uint64_t target = ceil_mul_p(pp, exact ? Shi : A + wtot + Bm);  // exact S
                 if (A < target && A + wtot >= target && A + wex < target && A + wex + w >= target) {
                     uint64_t cum = A + wex;
                     for (int j = b0; j < b1; ++j) {
@@ -1227,8 +1378,6 @@ __global__ void __launch_bounds__(kST, 2)
                 cluster_wait();
                 return;
             }
-        } else {
-            cluster.sync();  // remote histogram reads are done before the fallback reuses it
         }
         fallback_select_and_draw(c, v, kp, vec, 0, pp, zmax, c2, seed, offset, tok_out);
         cluster_wait();
