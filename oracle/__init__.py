@@ -20,6 +20,11 @@ What each function follows (web pages cited by title and section):
   tie rules of "LLM inference serving tutorial" section 3.1 and the filter order
   and draw order of the lab's block [8].
 * ``philox4x64_10`` / ``uniform``: Salmon et al., SC'11.
+* ``spec_verify_row`` / ``uniform_at``: speculative rejection sampling of
+  "Suy luan & Toi uu hoa (Inference)" section 5.2 (accept with probability
+  min(1, p/q), residual max(0, p - q) on rejection, a bonus token when all
+  drafts are accepted), with the KV roll-back of "LLM inference serving
+  tutorial" section 7 / Q16.
 * ``copy_blocks``: the copy half of copy-on-write, "LLM inference serving
   tutorial" section 4.2.
 * ``oracle.blocks`` (pure Python): reference-counted block sharing, fork,
@@ -95,6 +100,10 @@ def _load():
             lib.oracle_sample_batch.restype = i32
             lib.oracle_copy_blocks.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32]
             lib.oracle_copy_blocks.restype = i32
+            lib.oracle_uniform_at.argtypes = [u64, u64, u64]
+            lib.oracle_uniform_at.restype = f64
+            lib.oracle_spec_verify_row.argtypes = [P, P, P, i32, i32, f32, u64, u64, i32, P, P, P, P, P]
+            lib.oracle_spec_verify_row.restype = i32
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = i32
             _lib = lib
@@ -149,6 +158,33 @@ def copy_blocks(k_cache, v_cache, src, dst) -> int:
     d_ = np.ascontiguousarray(dst, dtype=np.int32)
     return int(_load().oracle_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(s_), _ptr(d_), s_.shape[0],
                                           Hkv, D, BS, NB, _dtype_code(k_cache)))
+
+
+def uniform_at(seed: int, offset: int, j: int) -> float:
+    """Uniform number j of the request stream (seed, offset); j = 0 is uniform()."""
+    return float(_load().oracle_uniform_at(int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), int(j)))
+
+
+def spec_verify_row(target_logits, draft_logits, draft_tokens, temperature: float, seed: int, offset: int,
+                    seq_len: int):
+    """Speculative verification of one request.  target_logits [gamma+1, V],
+    draft_logits [gamma, V] float32, draft_tokens [gamma] int32.  Returns dict
+    (status, tokens [gamma+1], n_acc, seq_len_out, test_margin, draw_margin)."""
+    zt = np.ascontiguousarray(target_logits, dtype=np.float32)
+    g1, V = zt.shape
+    gamma = g1 - 1
+    zd = np.ascontiguousarray(draft_logits, dtype=np.float32).reshape(max(gamma, 0), V)
+    x = np.ascontiguousarray(draft_tokens, dtype=np.int32).reshape(gamma)
+    tok = np.zeros(gamma + 1, np.int32)
+    n = ctypes.c_int32()
+    so = ctypes.c_int32()
+    tm, dm = ctypes.c_double(), ctypes.c_double()
+    st = _load().oracle_spec_verify_row(_ptr(zt), _ptr(zd) if gamma else None, _ptr(x) if gamma else None, gamma,
+                                        V, float(temperature), int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
+                                        int(seq_len), _ptr(tok), ctypes.byref(n), ctypes.byref(so),
+                                        ctypes.byref(tm), ctypes.byref(dm))
+    return dict(status=int(st), tokens=tok, n_acc=n.value, seq_len_out=so.value, test_margin=tm.value,
+                draw_margin=dm.value)
 
 
 def gather(cache, block_tables, b: int, L: int, h: int) -> np.ndarray:

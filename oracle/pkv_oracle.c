@@ -95,6 +95,16 @@ double oracle_uniform(uint64_t seed, uint64_t offset) {
     return (double)(out[0] >> 11) * (1.0 / 9007199254740992.0); /* 2^-53 */
 }
 
+/* Uniform number j of a request's stream: counter (offset, j, 0, 0) under key
+ * (seed, 0); j = 0 is oracle_uniform. */
+double oracle_uniform_at(uint64_t seed, uint64_t offset, uint64_t j) {
+    uint64_t ctr[4] = {offset, j, 0, 0};
+    uint64_t key[2] = {seed, 0};
+    uint64_t out[4];
+    oracle_philox4x64_10(ctr, key, out);
+    return (double)(out[0] >> 11) * (1.0 / 9007199254740992.0); /* 2^-53 */
+}
+
 /* ------------------------------------------------------------------------ */
 /* Element access: bf16 is the top half of an IEEE float32. */
 static double load_elem(const void* base, size_t idx, int dtype) {
@@ -470,6 +480,135 @@ int oracle_sample_batch(const float* logits, int B, int V, const float* temperat
         }
     }
     return status;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Speculative-decoding verification ("Suy luan & Toi uu hoa (Inference)" 5.2,
+ * speculative rejection sampling after Leviathan & Matias; "LLM inference
+ * serving tutorial" section 7 and Q16: a variable number of accepted tokens,
+ * and the KV of rejected candidates rolled back).  One request:
+ *   target logits zt[gamma+1][V] (the target model's distributions p_1..p_{g+1}
+ *   at the g draft positions and the one after), draft logits zd[gamma][V]
+ *   (q_1..q_g), draft tokens x[gamma], temperature T, stream (seed, offset).
+ *   p_i = softmax(zt[i] / T), q_i = softmax(zd[i] / T) over finite logits.
+ *   T == 0: accept while x[i] is the target argmax of row i (lowest id among
+ *     ties); the token after the accepted ones is the argmax of the first
+ *     rejected row, or of row gamma when all are accepted.
+ *   T > 0: for i = 0.. in order, u_i = uniform number i + 1 of the stream;
+ *     accept x[i] iff u_i * q_i(x[i]) < p_i(x[i]) (probability min(1, p/q));
+ *     stop at the first rejection.  Rejected at n: draw from the residual
+ *     max(0, p_n - q_n) normalised (p_n when the residual is all zero); all
+ *     accepted: draw from p_{gamma+1}.  The draw uses uniform number 0 and walks
+ *     token ids in ascending order (first id whose running CDF exceeds u).
+ * Outputs: tokens[0..n_acc) = accepted drafts, tokens[n_acc] = the drawn
+ * token, tokens past it = -1; *n_acc; *seq_len_out = seq_len - gamma + n_acc
+ * (seq_len counts the gamma draft positions whose KV the target pass wrote;
+ * the rejected ones are rolled back).
+ * Diagnostics: *test_margin = min over the tests made of |u_i - p/q| (1 when
+ * none or T == 0); *draw_margin = distance from u to the nearer CDF edge of
+ * the drawn token (1 for T == 0).
+ * Errors: NaN / +inf logit or a row with no finite logit -> OR_NONFINITE;
+ * T < 0 or NaN, a draft token outside [0, V), seq_len < gamma ->
+ * OR_INVALID_ARG; then tokens are -1, n_acc = 0 and seq_len_out = seq_len. */
+static int row_check(const float* z, int V) {
+    int fin = 0;
+    for (int i = 0; i < V; ++i) {
+        if (isnan(z[i]) || (isinf(z[i]) && z[i] > 0)) return OR_NONFINITE;
+        if (isfinite(z[i])) ++fin;
+    }
+    return fin ? OR_OK : OR_NONFINITE;
+}
+
+static int row_argmax(const float* z, int V) {
+    int best = -1;
+    for (int i = 0; i < V; ++i)
+        if (isfinite(z[i]) && (best < 0 || z[i] > z[best])) best = i;
+    return best;
+}
+
+/* probabilities softmax(z / T) over finite logits into pr[V] */
+static void row_softmax(const float* z, int V, double T, double* pr) {
+    double zmax = -INFINITY;
+    for (int i = 0; i < V; ++i) if (isfinite(z[i]) && z[i] > zmax) zmax = z[i];
+    double S = 0.0;
+    for (int i = 0; i < V; ++i) { pr[i] = isfinite(z[i]) ? exp(((double)z[i] - zmax) / T) : 0.0; S += pr[i]; }
+    for (int i = 0; i < V; ++i) pr[i] /= S;
+}
+
+/* inverse CDF in token-id order of the (unnormalised) weights w[V] */
+static int draw_id_order(const double* w, int V, double u, double* margin) {
+    double S = 0.0;
+    for (int i = 0; i < V; ++i) S += w[i];
+    double c = 0.0, cprev = 0.0;
+    int last = -1;
+    for (int i = 0; i < V; ++i) {
+        if (w[i] <= 0.0) continue;
+        last = i;
+        cprev = c;
+        c += w[i] / S;
+        if (c > u) {
+            double a = u - cprev, b = c - u;
+            *margin = a < b ? a : b;
+            return i;
+        }
+    }
+    *margin = 0.0;
+    return last;
+}
+
+int oracle_spec_verify_row(const float* zt, const float* zd, const int32_t* x, int gamma, int V,
+                           float temperature, uint64_t seed, uint64_t offset, int32_t seq_len,
+                           int32_t* tokens, int32_t* n_acc, int32_t* seq_len_out,
+                           double* test_margin, double* draw_margin) {
+    for (int i = 0; i <= gamma; ++i) tokens[i] = -1;
+    *n_acc = 0;
+    *seq_len_out = seq_len;
+    *test_margin = 1.0;
+    *draw_margin = 1.0;
+    for (int i = 0; i <= gamma; ++i) { int st = row_check(zt + (size_t)i * V, V); if (st) return st; }
+    for (int i = 0; i < gamma; ++i) { int st = row_check(zd + (size_t)i * V, V); if (st) return st; }
+    if (!(temperature >= 0.0f) || seq_len < gamma) return OR_INVALID_ARG;
+    for (int i = 0; i < gamma; ++i) if (x[i] < 0 || x[i] >= V) return OR_INVALID_ARG;
+    int n = 0;
+    if (temperature == 0.0f) {
+        while (n < gamma && x[n] == row_argmax(zt + (size_t)n * V, V)) ++n;
+        for (int i = 0; i < n; ++i) tokens[i] = x[i];
+        tokens[n] = row_argmax(zt + (size_t)n * V, V);
+    } else {
+        double T = (double)temperature;
+        double* p = (double*)malloc(sizeof(double) * (size_t)V);
+        double* q = (double*)malloc(sizeof(double) * (size_t)V);
+        int rejected = 0;
+        while (n < gamma) {
+            row_softmax(zt + (size_t)n * V, V, T, p);
+            row_softmax(zd + (size_t)n * V, V, T, q);
+            double u = oracle_uniform_at(seed, offset, (uint64_t)n + 1);
+            double px = p[x[n]], qx = q[x[n]];
+            if (qx > 0.0) {
+                double mg = fabs(u - px / qx);
+                if (mg < *test_margin) *test_margin = mg;
+            }
+            if (u * qx < px) { ++n; continue; }
+            rejected = 1;
+            break;
+        }
+        double u = oracle_uniform_at(seed, offset, 0);
+        if (rejected) {
+            /* p, q hold row n */
+            double R = 0.0;
+            for (int i = 0; i < V; ++i) { double d = p[i] - q[i]; q[i] = d > 0.0 ? d : 0.0; R += q[i]; }
+            tokens[n] = draw_id_order(R > 0.0 ? q : p, V, u, draw_margin);
+        } else {
+            row_softmax(zt + (size_t)gamma * V, V, T, p);
+            tokens[n] = draw_id_order(p, V, u, draw_margin);
+        }
+        for (int i = 0; i < n; ++i) tokens[i] = x[i];
+        free(p);
+        free(q);
+    }
+    *n_acc = n;
+    *seq_len_out = seq_len - gamma + n;
+    return OR_OK;
 }
 
 int oracle_num_threads(void) {
