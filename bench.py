@@ -469,8 +469,9 @@ def _time_calls(fn, n: int, flush=None):
 def run_extras(args):
     """One JSON line per extra measurement (not part of the default bench line):
     attention calls on the batch-64, long-context and fragmented workloads, the
-    sampler alone on its three workloads (L2 flushed between calls), block
-    copies, and attention over forked sequences that share prefix blocks."""
+    sampler alone on its three workloads (L2 flushed between calls), speculative
+    verification, block copies, and attention over forked sequences that share
+    prefix blocks."""
     import paged_kv_decode_table_gb300 as pkv
     from paged_kv_decode_table_gb300 import build as pkv_build
     pkv_build.build()
@@ -514,6 +515,28 @@ def run_extras(args):
               "frac_of_measured": by / (t["median_us"] * 1e-6) / 1e9 / peak})
         del si
         torch.cuda.empty_cache()
+
+    # speculative verification: 64 requests, 4 drafts each, 128256-token vocabulary
+    B, gamma, V = 64, 4, 128256
+    g = torch.Generator(device=dev)
+    g.manual_seed(2024)
+    tgt = torch.randn((B, gamma + 1, V), generator=g, device=dev) * 2.0
+    drf = (tgt[:, :gamma] + 0.5 * torch.randn((B, gamma, V), generator=g, device=dev)).contiguous()
+    x = torch.topk(drf, 4, dim=2).indices[..., 1].to(torch.int32).contiguous()
+    seq = torch.full((B,), 2048, dtype=torch.int32, device=dev)
+    temp = torch.full((B,), 0.8, dtype=torch.float32, device=dev)
+    sd = torch.arange(B, dtype=torch.int64, device=dev)
+    off = torch.zeros(B, dtype=torch.int64, device=dev)
+    wsv = torch.empty(pkv.spec_verify_workspace_bytes(B, gamma), dtype=torch.uint8, device=dev)
+    t = _time_calls(lambda: pkv.spec_verify(tgt, drf, x, seq, temp, sd, off, workspace=wsv), 50, flush=flush)
+    _, nacc, _ = pkv.spec_verify(tgt, drf, x, seq, temp, sd, off, workspace=wsv)
+    emitted = int(nacc.sum()) + B
+    by = B * (2 * gamma + 1) * V * 4
+    emit({"extra": "spec_verify", "workload": f"{B} requests x {gamma} drafts, V {V}, T 0.8", "bytes": by, **t,
+          "GB/s": by / (t["median_us"] * 1e-6) / 1e9, "frac_of_measured": by / (t["median_us"] * 1e-6) / 1e9 / peak,
+          "accepted_drafts": int(nacc.sum()), "emitted_tokens_per_s": emitted / (t["median_us"] * 1e-6)})
+    del tgt, drf
+    torch.cuda.empty_cache()
 
     # copy-on-write block copies: 1024 pairs of 64 KB blocks (bf16, 8 KV heads, 16 slots, D 128)
     NB, Hkv, BS, D = 4096, 8, 16, 128

@@ -11,6 +11,8 @@
  * Shared prefixes: a host-side reference-counted block pool (pkv_block_pool_*,
  * pkv_seq_*) hands out block ids and reports the copy-on-write pairs that
  * pkv_copy_blocks copies on the GPU before the step's append.
+ * Speculative decoding: pkv_spec_verify accepts or rejects draft tokens,
+ * draws the correction or bonus token and returns the rolled-back lengths.
  *
  * Conventions shared by every call
  *  - Every pointer argument is a DEVICE pointer unless stated otherwise.  The
@@ -198,6 +200,48 @@ pkv_status pkv_sample_tokens(int32_t* tokens, const float* logits, int B, int V,
 pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst, int n_pairs,
                            int Hkv, int D, int block_size, int num_blocks, pkv_dtype dtype, int32_t* dev_status,
                            void* stream);
+
+/*
+ * Workspace bytes pkv_spec_verify needs: 32 bytes per logits row,
+ * B * (2 * gamma + 1) rows.  Pure host arithmetic.
+ */
+size_t pkv_spec_verify_workspace_bytes(int B, int gamma);
+
+/*
+ * Speculative-decoding verification ("Suy luan & Toi uu hoa (Inference)" 5.2;
+ * "LLM inference serving tutorial" section 7 and Q16).  Per request b with
+ * gamma draft tokens x_i (draft_tokens int32 [B, gamma]), the target model's
+ * logits at the gamma draft positions and the next one (target_logits fp32
+ * [B, gamma + 1, V]) and the draft model's logits at the draft positions
+ * (draft_logits fp32 [B, gamma, V]):
+ *   p_i = softmax(target_logits[b][i] / T), q_i = softmax(draft_logits[b][i] / T)
+ *   over finite logits, T = temperature[b].
+ *   T == 0: x_i is accepted while it is the target argmax of row i (lowest id
+ *     among ties); the next token is the argmax of the first rejected row (row
+ *     gamma when every draft is accepted).
+ *   T > 0: u_i = Philox4x64-10(key (seeds[b], 0), counter (offsets[b], i + 1,
+ *     0, 0)) word 0, top 53 bits * 2^-53; x_i is accepted iff u_i * q_i(x_i) <
+ *     p_i(x_i), in order, up to the first rejection n.  The next token is drawn
+ *     with u = the same generator at counter (offsets[b], 0, 0, 0), walking ids
+ *     in ascending order: from max(0, p_n - q_n) normalised (p_n if that is all
+ *     zero) when n < gamma, else from p_{gamma+1}.
+ * Outputs (device): tokens_out int32 [B, gamma + 1] = the accepted drafts, the
+ * drawn token, then -1; n_accepted int32 [B]; seq_lens_out int32 [B] =
+ * seq_lens[b] - gamma + n_accepted[b], where seq_lens counts the gamma draft
+ * positions whose KV the target pass appended (the rejected ones are rolled
+ * back).  Probabilities are float32 exponentials with exact 2^-40 fixed-point
+ * row sums; a decision can differ from a float64 evaluation only when u lies
+ * within ~1e-6 of p/q or of a CDF edge.  Errors per request (tokens -1,
+ * n_accepted 0, seq_lens_out = seq_lens): NaN / +inf logit or a row without a
+ * finite logit -> PKV_ERR_NONFINITE; T < 0 or NaN, a draft token outside
+ * [0, V), seq_lens < gamma -> PKV_ERR_INVALID_ARG.  0 <= gamma <= 32,
+ * 1 <= V <= 2^23; workspace >= pkv_spec_verify_workspace_bytes(B, gamma).
+ */
+pkv_status pkv_spec_verify(int32_t* tokens_out, int32_t* n_accepted, int32_t* seq_lens_out,
+                           const float* target_logits, const float* draft_logits, const int32_t* draft_tokens,
+                           const int32_t* seq_lens, int B, int gamma, int V, const float* temperature,
+                           const uint64_t* seeds, const uint64_t* offsets, void* workspace, size_t workspace_bytes,
+                           int32_t* dev_status, void* stream);
 
 /*
  * Reference-counted block pool (host only; "LLM inference serving tutorial"

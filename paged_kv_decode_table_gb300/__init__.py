@@ -12,6 +12,7 @@ Calls (names follow the C ABI):
   paged_decode_attention(q, k_cache, v_cache, block_tables, seq_lens, out=None, scale=0.0)
   sample_tokens(logits, temperature, top_k, top_p, seeds, offsets, tokens=None)
   copy_blocks(k_cache, v_cache, src, dst)
+  spec_verify(target_logits, draft_logits, draft_tokens, seq_lens, temperature, seeds, offsets)
   BlockPool(num_blocks, block_size, max_blocks_per_seq)   host-side refcounted block ids
 """
 from __future__ import annotations
@@ -24,7 +25,8 @@ import torch
 
 __all__ = ["PkvError", "load_library", "library_path", "kv_append", "paged_decode_attention",
            "decode_workspace_bytes", "sample_tokens", "sample_workspace_bytes", "status_string",
-           "new_status", "check_status", "STATUS", "copy_blocks", "BlockPool"]
+           "new_status", "check_status", "STATUS", "copy_blocks", "BlockPool", "spec_verify",
+           "spec_verify_workspace_bytes"]
 
 STATUS = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED", 3: "PKV_ERR_CUDA",
           4: "PKV_ERR_DEVICE_BOUNDS", 5: "PKV_ERR_TIMEOUT", 6: "PKV_ERR_NONFINITE", 7: "PKV_ERR_CAPACITY"}
@@ -73,6 +75,10 @@ def load_library():
         lib.pkv_sample_tokens.argtypes = [P, P, i32, i32, P, P, P, P, P, P, sz, P, P]
         lib.pkv_sample_tokens.restype = i32
         i64 = ctypes.c_int64
+        lib.pkv_spec_verify_workspace_bytes.argtypes = [i32, i32]
+        lib.pkv_spec_verify_workspace_bytes.restype = sz
+        lib.pkv_spec_verify.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, P, P, P, P, sz, P, P]
+        lib.pkv_spec_verify.restype = i32
         lib.pkv_copy_blocks.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, P, P]
         lib.pkv_copy_blocks.restype = i32
         lib.pkv_block_pool_create.argtypes = [i32, i32, i32]
@@ -324,3 +330,45 @@ class BlockPool:
         _raise("pkv_block_tables", self._lib.pkv_block_tables(self._p, ids, n, ctypes.c_void_p(bt.data_ptr()),
                                                                ctypes.c_void_p(sl.data_ptr())))
         return bt, sl
+
+
+def spec_verify_workspace_bytes(B: int, gamma: int) -> int:
+    return int(load_library().pkv_spec_verify_workspace_bytes(B, gamma))
+
+
+def spec_verify(target_logits, draft_logits, draft_tokens, seq_lens, temperature, seeds, offsets,
+                workspace=None, status=None):
+    """Speculative verification of B requests with gamma drafts each.
+
+    target_logits [B, gamma+1, V] float32, draft_logits [B, gamma, V] float32,
+    draft_tokens [B, gamma] int32, seq_lens [B] int32 (including the drafts'
+    KV), temperature [B] float32, seeds / offsets [B] 64-bit.  Returns
+    (tokens [B, gamma+1] int32, n_accepted [B] int32, seq_lens_out [B] int32)."""
+    B, g1, V = target_logits.shape
+    gamma = g1 - 1
+    dev = target_logits.device
+    _check_cuda("target_logits", target_logits, torch.float32)
+    _check_cuda("draft_logits", draft_logits, torch.float32, (B, gamma, V), dev)
+    _check_cuda("draft_tokens", draft_tokens, torch.int32, (B, gamma), dev)
+    _check_cuda("seq_lens", seq_lens, torch.int32, (B,), dev)
+    _check_cuda("temperature", temperature, torch.float32, (B,), dev)
+    if seeds.dtype not in (torch.int64, torch.uint64) or offsets.dtype not in (torch.int64, torch.uint64):
+        raise TypeError("seeds and offsets must be 64-bit integer tensors")
+    _check_cuda("seeds", seeds, shape=(B,), device=dev)
+    _check_cuda("offsets", offsets, shape=(B,), device=dev)
+    lib = load_library()
+    need = int(lib.pkv_spec_verify_workspace_bytes(B, gamma))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    _check_cuda("workspace", workspace, device=dev)
+    if status is not None:
+        _check_cuda("status", status, torch.int32, (1,), dev)
+    tokens = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
+    n_acc = torch.empty((B,), dtype=torch.int32, device=dev)
+    sl_out = torch.empty((B,), dtype=torch.int32, device=dev)
+    code = lib.pkv_spec_verify(_ptr(tokens), _ptr(n_acc), _ptr(sl_out), _ptr(target_logits), _ptr(draft_logits),
+                               _ptr(draft_tokens), _ptr(seq_lens), B, gamma, V, _ptr(temperature), _ptr(seeds),
+                               _ptr(offsets), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                               _ptr(status), _stream(dev))
+    _raise("pkv_spec_verify", code)
+    return tokens, n_acc, sl_out

@@ -19,6 +19,11 @@ int device_sm_count();
 cudaError_t launch_sampler(int32_t* tokens, const float* logits, int B, int V, const float* temperature,
                            const int32_t* top_k, const float* top_p, const uint64_t* seeds, const uint64_t* offsets,
                            int32_t* status, cudaStream_t stream);
+size_t spec_verify_workspace_bytes(int B, int gamma);
+cudaError_t launch_spec_verify(int32_t* tokens_out, int32_t* n_accepted, int32_t* seq_lens_out, const float* target,
+                               const float* draft, const int32_t* draft_tokens, const int32_t* seq_lens, int B,
+                               int gamma, int V, const float* temperature, const uint64_t* seeds,
+                               const uint64_t* offsets, void* workspace, int32_t* status, cudaStream_t stream);
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst, int n_pairs,
                                long long block_bytes, int NB, int32_t* status, cudaStream_t stream);
 }  // namespace pkv
@@ -69,6 +74,28 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, con
     const long long block_bytes = static_cast<long long>(Hkv) * block_size * D * es;
     return cuda_status(pkv::launch_copy_blocks(k_cache, v_cache, src, dst, n_pairs, block_bytes, num_blocks,
                                                dev_status, static_cast<cudaStream_t>(stream)));
+}
+
+size_t pkv_spec_verify_workspace_bytes(int B, int gamma) {
+    if (B < 0 || gamma < 0 || gamma > 32) return 0;
+    return pkv::spec_verify_workspace_bytes(B, gamma);
+}
+
+pkv_status pkv_spec_verify(int32_t* tokens_out, int32_t* n_accepted, int32_t* seq_lens_out, const float* target_logits,
+                           const float* draft_logits, const int32_t* draft_tokens, const int32_t* seq_lens, int B,
+                           int gamma, int V, const float* temperature, const uint64_t* seeds, const uint64_t* offsets,
+                           void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    if (B < 0 || gamma < 0 || gamma > 32 || V < 1 || V > (1 << 23)) return PKV_ERR_INVALID_ARG;
+    if (B == 0) return PKV_OK;
+    if (!tokens_out || !n_accepted || !seq_lens_out || !target_logits || !seq_lens || !temperature || !seeds ||
+        !offsets || !workspace)
+        return PKV_ERR_INVALID_ARG;
+    if (gamma > 0 && (!draft_logits || !draft_tokens)) return PKV_ERR_INVALID_ARG;
+    if (workspace_bytes < pkv::spec_verify_workspace_bytes(B, gamma)) return PKV_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return PKV_ERR_INVALID_ARG;
+    return cuda_status(pkv::launch_spec_verify(tokens_out, n_accepted, seq_lens_out, target_logits, draft_logits,
+                                               draft_tokens, seq_lens, B, gamma, V, temperature, seeds, offsets,
+                                               workspace, dev_status, static_cast<cudaStream_t>(stream)));
 }
 
 size_t pkv_decode_workspace_bytes(int B, int Hq, int D, int num_sms) {

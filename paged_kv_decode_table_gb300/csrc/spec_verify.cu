@@ -1,0 +1,393 @@
+// spec_verify.cu -- speculative-decoding verification (accept / reject the draft
+// tokens of every request, draw the correction or bonus token, roll back KV).
+//
+// "Suy luan & Toi uu hoa (Inference)" 5.2 (speculative rejection sampling after
+// Leviathan & Matias): at draft position i the draft token x_i ~ q_i is kept
+// with probability min(1, p_i(x_i) / q_i(x_i)); the first rejection ends the
+// cycle with a token drawn from the residual max(0, p_i - q_i) normalised; when
+// every draft is kept, one more token comes from p_{gamma+1}.  Greedy decoding
+// (T = 0) keeps drafts while they equal the target argmax.  "LLM inference
+// serving tutorial" section 7 / Q16: the number of accepted tokens varies per
+// request, and the KV written for rejected drafts is rolled back, here by
+// returning the committed length seq_len - gamma + n_accepted.
+//
+// p_i = softmax(z_target[i] / T) and q_i = softmax(z_draft[i] / T) over finite
+// logits, represented as in the sampler: fixed-point masses floor(w * 2^40) of
+// w = 2^((z - zmax) log2(e) / T), with exact integer row sums.  Uniform
+// number j of a request is Philox4x64-10 word 0 at counter (offset, j, 0, 0)
+// under key (seed, 0), top 53 bits: j = i + 1 for the test at draft position i,
+// j = 0 for the final draw, which walks token ids in ascending order.
+//
+// Two kernels: row statistics (max, lowest argmax, mass sum) with one CTA per
+// logits row; then one CTA per request for the tests (one thread per draft
+// position) and the final draw (chunked inverse CDF over the vocabulary).
+#include <limits.h>
+#include <math.h>
+
+#include "pkv_common.cuh"
+#include "sampling_math.cuh"
+
+namespace pkv {
+
+constexpr int kVT = 512;             // threads per CTA
+constexpr int kVW = kVT / 32;
+constexpr int kDrawChunks = 2048;    // chunk sums kept in shared memory
+
+struct RowStat {   // 32 bytes per logits row
+    float zmax;
+    int argmax;    // lowest id holding zmax (-1: no finite logit)
+    int bad;       // NaN or +inf present
+    int pad;
+    unsigned long long S;  // sum of floor(2^40 * 2^((z - zmax) c2)) (T > 0)
+    unsigned long long pad2;
+};
+
+__device__ __forceinline__ float4 load4_row(const float* row, int e, int n, bool al) {
+    if (al && e + 4 <= n) return __ldg(reinterpret_cast<const float4*>(row + e));
+    float4 q;
+    q.x = e < n ? row[e] : -INFINITY;
+    q.y = e + 1 < n ? row[e + 1] : -INFINITY;
+    q.z = e + 2 < n ? row[e + 2] : -INFINITY;
+    q.w = e + 3 < n ? row[e + 3] : -INFINITY;
+    return q;
+}
+
+__device__ __forceinline__ uint64_t block_sum_u64(uint64_t v, unsigned long long* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    uint64_t t = 0;
+    for (int w = 0; w < kVW; ++w) t += red[w];
+    __syncthreads();
+    return t;
+}
+
+// ------------------------------------------------------------------ row statistics
+// Row r of request b: r < gamma + 1 is target row r, else draft row r - gamma - 1.
+__global__ void __launch_bounds__(kVT)
+    spec_stats_kernel(const float* __restrict__ target, const float* __restrict__ draft, int gamma, int V,
+                      const float* __restrict__ temperature, RowStat* __restrict__ stats) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    __shared__ float smax[kVW];
+    __shared__ int sid[kVW], sbad[kVW];
+    __shared__ unsigned long long red[kVW];
+    const int rows = 2 * gamma + 1;
+    const int b = blockIdx.x / rows, r = blockIdx.x - (blockIdx.x / rows) * rows;
+    const float* row = r <= gamma ? target + (static_cast<size_t>(b) * (gamma + 1) + r) * V
+                                  : draft + (static_cast<size_t>(b) * gamma + (r - gamma - 1)) * V;
+    const bool al = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(row) & 15u) == 0);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float m = -INFINITY;
+    int id = INT_MAX;
+    int bad = 0;
+    for (int e = 4 * tid; e < V; e += 4 * kVT) {
+        const float4 q = load4_row(row, e, V, al);
+        const float zz[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float z = zz[j];
+            bad |= (z < INFINITY) ? 0 : 1;  // NaN or +inf (slots past V read -inf)
+            if (z > m) {                     // ids grow within a thread: first max wins
+                m = z;
+                id = e + j;
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const int id2 = __shfl_xor_sync(0xffffffffu, id, o);
+        if (m2 > m || (m2 == m && id2 < id)) {
+            m = m2;
+            id = id2;
+        }
+        bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+    }
+    if (lane == 0) {
+        smax[warp] = m;
+        sid[warp] = id;
+        sbad[warp] = bad;
+    }
+    __syncthreads();
+    m = smax[0];
+    id = sid[0];
+    bad = sbad[0];
+    for (int w = 1; w < kVW; ++w) {
+        if (smax[w] > m || (smax[w] == m && sid[w] < id)) {
+            m = smax[w];
+            id = sid[w];
+        }
+        bad |= sbad[w];
+    }
+    const float T = temperature[b];
+    uint64_t S = 0;
+    if (!bad && m > -INFINITY && T > 0.f) {
+        const float c2 = fminf(1.4426950408889634f / T, 1.0e30f);
+        uint64_t s = 0;
+        for (int e = 4 * tid; e < V; e += 4 * kVT) {
+            const float4 q = load4_row(row, e, V, al);
+            s += mass(q.x, m, c2) + mass(q.y, m, c2) + mass(q.z, m, c2) + mass(q.w, m, c2);
+        }
+        S = block_sum_u64(s, red);
+    }
+    if (tid == 0) {
+        RowStat st;
+        st.zmax = m;
+        st.argmax = m > -INFINITY ? id : -1;
+        st.bad = bad;
+        st.pad = 0;
+        st.S = S;
+        st.pad2 = 0;
+        stats[blockIdx.x] = st;
+    }
+}
+
+// ------------------------------------------------------------------ CTA inverse-CDF draw
+// First element e (ascending) of [0, n) whose running mass exceeds
+// floor(u * total), masses given four at a time by m4(e, out[4]).  Chunks of
+// 128 * cpw elements: warp w sums chunks w, w + 16, ... (lane l takes elements
+// 4l..4l+3 of each 128), the chunk sums are scanned in shared memory, and warp
+// 0 walks the chunk that holds the draw.  Returns -1 when the total is 0.
+template <typename M4>
+__device__ int cta_draw(int n, M4 m4, uint64_t u53, unsigned long long* ctot, unsigned long long* red, int* sel) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nv = (n + 3) & ~3;
+    const int cpw = max(1, (nv + 128 * kDrawChunks - 1) / (128 * kDrawChunks));
+    const int csz = 128 * cpw;
+    const int nch = (nv + csz - 1) / csz;
+    for (int ch = warp; ch < nch; ch += kVW) {
+        uint64_t w = 0;
+        for (int k = 0; k < cpw; ++k) {
+            const int e = ch * csz + 128 * k + 4 * lane;
+            if (e < nv) {
+                uint64_t m[4];
+                m4(e, m);
+                w += m[0] + m[1] + m[2] + m[3];
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
+        if (lane == 0) ctot[ch] = w;
+    }
+    __syncthreads();
+    uint64_t t4[4], ts = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int ch = 4 * tid + q;
+        t4[q] = ch < nch ? ctot[ch] : 0ull;
+        ts += t4[q];
+    }
+    // exclusive scan over the CTA
+    uint64_t x = ts;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) red[warp] = x;
+    if (tid == 0) *sel = -1;
+    __syncthreads();
+    uint64_t before = 0, total = 0;
+    for (int w = 0; w < kVW; ++w) {
+        if (w < warp) before += red[w];
+        total += red[w];
+    }
+    uint64_t run = before + x - ts;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int ch = 4 * tid + q;
+        if (ch < nch) ctot[ch] = run;
+        run += t4[q];
+    }
+    __syncthreads();
+    if (total == 0) return -1;
+    const uint64_t X = static_cast<uint64_t>((static_cast<unsigned __int128>(u53) * total) >> 53);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int ch = 4 * tid + q;
+        if (ch < nch) {
+            const uint64_t lo = ctot[ch], hi = ch + 1 < nch ? ctot[ch + 1] : total;
+            if (lo <= X && X < hi) *sel = ch;
+        }
+    }
+    __syncthreads();
+    const int cs = *sel;
+    __shared__ int found;
+    if (tid == 0) found = -1;
+    __syncthreads();
+    if (warp == 0 && cs >= 0) {
+        uint64_t base = ctot[cs];
+        for (int k = 0; k < cpw; ++k) {
+            const int e = cs * csz + 128 * k + 4 * lane;
+            uint64_t m[4] = {0ull, 0ull, 0ull, 0ull};
+            if (e < nv) m4(e, m);
+            const uint64_t mine = m[0] + m[1] + m[2] + m[3];
+            uint64_t inc = mine;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint64_t y = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += y;
+            }
+            const uint64_t bl = base + inc - mine;
+            if (bl <= X && X < bl + mine) {
+                uint64_t cum = bl;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    cum += m[j];
+                    if (cum > X) {
+                        found = e + j;
+                        break;
+                    }
+                }
+            }
+            base += __shfl_sync(0xffffffffu, inc, 31);
+            if (base > X) break;
+        }
+    }
+    __syncthreads();
+    return found;
+}
+
+// ------------------------------------------------------------------ verification
+__global__ void __launch_bounds__(kVT)
+    spec_verify_kernel(int32_t* __restrict__ tokens_out, int32_t* __restrict__ n_accepted,
+                       int32_t* __restrict__ seq_lens_out, const float* __restrict__ target,
+                       const float* __restrict__ draft, const int32_t* __restrict__ draft_tokens,
+                       const int32_t* __restrict__ seq_lens, int gamma, int V, const float* __restrict__ temperature,
+                       const uint64_t* __restrict__ seeds, const uint64_t* __restrict__ offsets,
+                       const RowStat* __restrict__ stats, int32_t* status) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the row statistics are complete
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    __shared__ unsigned long long ctot[kDrawChunks];
+    __shared__ unsigned long long red[kVW];
+    __shared__ int sel, nrej, err;
+    const int b = blockIdx.x, tid = threadIdx.x;
+    const int rows = 2 * gamma + 1;
+    const RowStat* st = stats + static_cast<size_t>(b) * rows;
+    const float T = temperature[b];
+    const uint64_t seed = seeds[b], offset = offsets[b];
+    const int L = seq_lens[b];
+    int32_t* tok = tokens_out + static_cast<size_t>(b) * (gamma + 1);
+    if (tid == 0) {
+        int e = 0;
+        for (int r = 0; r < rows; ++r)
+            if (st[r].bad || st[r].argmax < 0) e = PKV_ERR_NONFINITE;
+        if (!e) {
+            if (!(T >= 0.f) || L < gamma) e = PKV_ERR_INVALID_ARG;
+            for (int i = 0; i < gamma; ++i) {
+                const int x = draft_tokens[static_cast<size_t>(b) * gamma + i];
+                if (x < 0 || x >= V) e = PKV_ERR_INVALID_ARG;
+            }
+        }
+        err = e;
+        nrej = gamma;
+    }
+    __syncthreads();
+    if (err) {
+        for (int i = tid; i <= gamma; i += kVT) tok[i] = -1;
+        if (tid == 0) {
+            n_accepted[b] = 0;
+            seq_lens_out[b] = L;
+            report(status, err);
+        }
+        return;
+    }
+    const float c2 = fminf(1.4426950408889634f / T, 1.0e30f);
+    // the tests: thread i decides draft position i; the first rejection ends the cycle
+    if (tid < gamma) {
+        const int x = draft_tokens[static_cast<size_t>(b) * gamma + tid];
+        const float* zt = target + (static_cast<size_t>(b) * (gamma + 1) + tid) * V;
+        const float* zd = draft + (static_cast<size_t>(b) * gamma + tid) * V;
+        bool accept;
+        if (T == 0.f) {
+            accept = x == st[tid].argmax;
+        } else {
+            const RowStat& sp = st[tid];
+            const RowStat& sq = st[gamma + 1 + tid];
+            const double p = static_cast<double>(mass(zt[x], sp.zmax, c2)) / static_cast<double>(sp.S);
+            const double q = static_cast<double>(mass(zd[x], sq.zmax, c2)) / static_cast<double>(sq.S);
+            const double u = static_cast<double>(philox_word0(seed, offset, static_cast<uint64_t>(tid) + 1) >> 11) *
+                             (1.0 / 9007199254740992.0);
+            accept = u * q < p;
+        }
+        if (!accept) atomicMin(&nrej, tid);
+    }
+    __syncthreads();
+    const int n = nrej;
+    int final_tok;
+    if (T == 0.f) {
+        final_tok = st[n].argmax;
+    } else {
+        const uint64_t u53 = philox_word0(seed, offset, 0) >> 11;
+        const float* zt = target + (static_cast<size_t>(b) * (gamma + 1) + n) * V;
+        const bool alt = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(zt) & 15u) == 0);
+        const float mt = st[n].zmax;
+        auto target_mass = [&](int e, uint64_t* m) {
+            const float4 q = load4_row(zt, e, V, alt);
+            m[0] = mass(q.x, mt, c2);
+            m[1] = mass(q.y, mt, c2);
+            m[2] = mass(q.z, mt, c2);
+            m[3] = mass(q.w, mt, c2);
+        };
+        final_tok = -1;
+        if (n < gamma) {
+            // residual max(0, p - q) in 2^-40 fixed point of probability
+            const float* zd = draft + (static_cast<size_t>(b) * gamma + n) * V;
+            const bool ald = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(zd) & 15u) == 0);
+            const float mq = st[gamma + 1 + n].zmax;
+            const float at = static_cast<float>(1099511627776.0 / static_cast<double>(st[n].S));
+            const float aq = static_cast<float>(1099511627776.0 / static_cast<double>(st[gamma + 1 + n].S));
+            auto resid_mass = [&](int e, uint64_t* m) {
+                const float4 a = load4_row(zt, e, V, alt);
+                const float4 d = load4_row(zd, e, V, ald);
+                const float pa[4] = {a.x, a.y, a.z, a.w}, pd[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float r = weight(pa[j], mt, c2) * at - weight(pd[j], mq, c2) * aq;
+                    m[j] = fx40(fminf(fmaxf(r, 0.f), 1.f));
+                }
+            };
+            final_tok = cta_draw(V, resid_mass, u53, ctot, red, &sel);
+        }
+        if (final_tok < 0) final_tok = cta_draw(V, target_mass, u53, ctot, red, &sel);
+    }
+    for (int i = tid; i <= gamma; i += kVT)
+        tok[i] = i < n ? draft_tokens[static_cast<size_t>(b) * gamma + i] : (i == n ? final_tok : -1);
+    if (tid == 0) {
+        n_accepted[b] = n;
+        seq_lens_out[b] = L - gamma + n;
+    }
+}
+
+size_t spec_verify_workspace_bytes(int B, int gamma) {
+    return static_cast<size_t>(B) * (2 * static_cast<size_t>(gamma) + 1) * sizeof(RowStat);
+}
+
+cudaError_t launch_spec_verify(int32_t* tokens_out, int32_t* n_accepted, int32_t* seq_lens_out, const float* target,
+                               const float* draft, const int32_t* draft_tokens, const int32_t* seq_lens, int B,
+                               int gamma, int V, const float* temperature, const uint64_t* seeds,
+                               const uint64_t* offsets, void* workspace, int32_t* status, cudaStream_t stream) {
+    RowStat* stats = static_cast<RowStat*>(workspace);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(B) * (2 * gamma + 1), 1, 1);
+    cfg.blockDim = dim3(kVT, 1, 1);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t err = cudaLaunchKernelEx(&cfg, spec_stats_kernel, target, draft, gamma, V, temperature, stats);
+    if (err != cudaSuccess) return err;
+    cfg.gridDim = dim3(static_cast<unsigned>(B), 1, 1);
+    err = cudaLaunchKernelEx(&cfg, spec_verify_kernel, tokens_out, n_accepted, seq_lens_out, target, draft,
+                             draft_tokens, seq_lens, gamma, V, temperature, seeds, offsets,
+                             static_cast<const RowStat*>(stats), status);
+    if (err != cudaSuccess) return err;
+    return cudaGetLastError();
+}
+
+}  // namespace pkv
