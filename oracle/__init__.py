@@ -25,6 +25,10 @@ What each function follows (web pages cited by title and section):
   min(1, p/q), residual max(0, p - q) on rejection, a bonus token when all
   drafts are accepted), with the KV roll-back of "LLM inference serving
   tutorial" section 7 / Q16.
+* ``process_logits``: hard constraint masks and the frequency / presence /
+  sign-aware repetition penalties of "LLM inference serving tutorial" sections
+  3.2-3.3, in the section 3.1 pipeline order; ``sample_row(min_p=...)`` adds
+  min-p (section 3.1 and Q4) after top-p.
 * ``copy_blocks``: the copy half of copy-on-write, "LLM inference serving
   tutorial" section 4.2.
 * ``oracle.blocks`` (pure Python): reference-counted block sharing, fork,
@@ -104,6 +108,10 @@ def _load():
             lib.oracle_uniform_at.restype = f64
             lib.oracle_spec_verify_row.argtypes = [P, P, P, i32, i32, f32, u64, u64, i32, P, P, P, P, P]
             lib.oracle_spec_verify_row.restype = i32
+            lib.oracle_sample_row_ex.argtypes = [P, i32, f32, i32, f32, f32, u64, u64, P, P, P, P, P]
+            lib.oracle_sample_row_ex.restype = i32
+            lib.oracle_process_logits.argtypes = [P, i32, i32, P, P, P, P, P, P, P]
+            lib.oracle_process_logits.restype = i32
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = i32
             _lib = lib
@@ -239,8 +247,9 @@ def attention_split_row(q, k_cache, v_cache, block_tables, seq_lens, b: int, qh:
 
 
 def sample_row(z, temperature: float, top_k: int, top_p: float, seed: int, offset: int,
-               want_probs: bool = False):
-    """One row. Returns dict(token, status, draw_margin, cut_margin, n_kept[, probs])."""
+               want_probs: bool = False, min_p: float = 0.0):
+    """One row (min_p > 0: min-p after top-p). Returns dict(token, status,
+    draw_margin, cut_margin, n_kept[, probs])."""
     z = np.ascontiguousarray(z, dtype=np.float32)
     V = z.shape[0]
     tok = ctypes.c_int32(0)
@@ -248,7 +257,7 @@ def sample_row(z, temperature: float, top_k: int, top_p: float, seed: int, offse
     cm = ctypes.c_double(0)
     nk = ctypes.c_int32(0)
     probs = np.zeros(V, dtype=np.float64) if want_probs else None
-    st = _load().oracle_sample_row(_ptr(z), V, float(temperature), int(top_k), float(top_p),
+    st = _load().oracle_sample_row_ex(_ptr(z), V, float(temperature), int(top_k), float(top_p), float(min_p),
                                    int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
                                    ctypes.byref(tok), ctypes.byref(dm), ctypes.byref(cm),
                                    ctypes.byref(nk), _ptr(probs) if want_probs else None)
@@ -257,6 +266,16 @@ def sample_row(z, temperature: float, top_k: int, top_p: float, seed: int, offse
     if want_probs:
         res["probs"] = probs
     return res
+
+
+def process_logits(logits, mask=None, row_ptr=None, tokens=None, counts=None, rep=None, freq=None, pres=None):
+    """Masks and penalties in place on float32 logits [B, V]; returns the status."""
+    B, V = logits.shape
+    arr = lambda a, t: None if a is None else np.ascontiguousarray(a, dtype=t)
+    m, rp, tk, ct = arr(mask, np.uint32), arr(row_ptr, np.int32), arr(tokens, np.int32), arr(counts, np.int32)
+    r, f, p = arr(rep, np.float32), arr(freq, np.float32), arr(pres, np.float32)
+    P = lambda a: None if a is None else _ptr(a)
+    return int(_load().oracle_process_logits(_ptr(logits), B, V, P(m), P(rp), P(tk), P(ct), P(r), P(f), P(p)))
 
 
 def sample_batch(logits, temperature, top_k, top_p, seeds, offsets):

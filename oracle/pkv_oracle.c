@@ -375,9 +375,9 @@ static int cmp_zid(const void* a, const void* b) {
  * cumulative sums that bracket the top-p cut (1.0 when top-p is off);
  * n_kept = size of the final support; probs (optional, length V) = final
  * renormalised distribution in token-id order. */
-int oracle_sample_row(const float* z, int V, float temperature, int top_k, float top_p,
-                      uint64_t seed, uint64_t offset, int32_t* token, double* draw_margin,
-                      double* cut_margin, int32_t* n_kept, double* probs) {
+int oracle_sample_row_ex(const float* z, int V, float temperature, int top_k, float top_p, float min_p,
+                         uint64_t seed, uint64_t offset, int32_t* token, double* draw_margin,
+                         double* cut_margin, int32_t* n_kept, double* probs) {
     *token = -1;
     *draw_margin = 0.0;
     *cut_margin = 1.0;
@@ -401,6 +401,7 @@ int oracle_sample_row(const float* z, int V, float temperature, int top_k, float
         return OR_OK;
     }
     if (!(top_p > 0.0f)) return OR_INVALID_ARG; /* p <= 0 or NaN */
+    if (isnan(min_p) || min_p > 1.0f) return OR_INVALID_ARG;
 
     zid_t* ord = (zid_t*)malloc(sizeof(zid_t) * (size_t)n_fin);
     int n = 0;
@@ -433,6 +434,23 @@ int oracle_sample_row(const float* z, int V, float temperature, int top_k, float
         *cut_margin = d1 < d0 ? d1 : d0;
     }
 
+    /* min-p ("LLM inference serving tutorial" 3.1, Q4): keep the tokens whose
+     * probability is at least min_p times the largest, i.e. whose weight
+     * exp((z - zmax) / T) relative to the maximum is >= min_p; the maximum is
+     * always kept.  Applied after top-p (a prefix of the same order).  The
+     * margin to that threshold joins cut_margin. */
+    if (min_p > 0.0f) {
+        double a = (double)min_p;
+        int keep = 0;
+        for (int j = 0; j < m; ++j) {
+            double w = exp(((double)ord[j].z - zmax) / T);
+            double d = fabs(w - a);
+            if (d < *cut_margin) *cut_margin = d;
+            if (w >= a) keep = j + 1;
+        }
+        m = keep;
+    }
+
     /* renormalise over the nucleus; draw in token-id order */
     double Sp = 0.0;
     for (int j = 0; j < m; ++j) Sp += q[j];
@@ -459,6 +477,56 @@ int oracle_sample_row(const float* z, int V, float temperature, int top_k, float
     if (probs) for (int i = 0; i < V; ++i) probs[i] = pi[i];
     free(ord); free(q); free(pi); free(kept);
     return OR_OK;
+}
+
+int oracle_sample_row(const float* z, int V, float temperature, int top_k, float top_p,
+                      uint64_t seed, uint64_t offset, int32_t* token, double* draw_margin,
+                      double* cut_margin, int32_t* n_kept, double* probs) {
+    return oracle_sample_row_ex(z, V, temperature, top_k, top_p, 0.0f, seed, offset, token, draw_margin,
+                                cut_margin, n_kept, probs);
+}
+
+/* Logits processors before the sampler ("LLM inference serving tutorial" 3.1
+ * pipeline: hard constraints, then penalties, then temperature and filters;
+ * 3.2 penalty definitions; 3.3 constraint masks), in place on logits [B, V]:
+ *  1. mask (optional, uint32 [B, ceil(V/32)]): token i of row b is allowed iff
+ *     bit (i % 32) of word i / 32 is set; a disallowed logit becomes -inf;
+ *  2. for each (token, count c >= 1) listed for row b (CSR: row_ptr [B+1],
+ *     tokens / counts [nnz]; each token at most once per row) whose logit is
+ *     finite: the sign-aware repetition penalty r = rep[b] (z / r for z > 0,
+ *     z * r for z < 0, z = 0 unchanged; r == 1 is a no-op), then
+ *     z - freq[b] * c - pres[b], in double, rounded once to float.
+ * rep, freq, pres may be NULL (off).  Errors: a listed token outside [0, V) or
+ * r <= 0 / NaN -> OR_INVALID_ARG (that entry, or the row's penalties, skipped). */
+int oracle_process_logits(float* logits, int B, int V, const uint32_t* mask, const int32_t* row_ptr,
+                          const int32_t* tokens, const int32_t* counts, const float* rep, const float* freq,
+                          const float* pres) {
+    int status = OR_OK;
+    int words = (V + 31) / 32;
+    for (int b = 0; b < B; ++b) {
+        float* z = logits + (size_t)b * V;
+        if (mask) {
+            const uint32_t* mrow = mask + (size_t)b * words;
+            for (int i = 0; i < V; ++i)
+                if (!((mrow[i / 32] >> (i % 32)) & 1u)) z[i] = -INFINITY;
+        }
+        if (!row_ptr) continue;
+        double r = rep ? (double)rep[b] : 1.0;
+        double f = freq ? (double)freq[b] : 0.0;
+        double pr = pres ? (double)pres[b] : 0.0;
+        if (!(r > 0.0)) { status = OR_INVALID_ARG; continue; }
+        for (int e = row_ptr[b]; e < row_ptr[b + 1]; ++e) {
+            int t = tokens[e], c = counts[e];
+            if (t < 0 || t >= V) { status = OR_INVALID_ARG; continue; }
+            if (c < 1 || !isfinite(z[t])) continue;
+            double zd = (double)z[t];
+            if (r != 1.0) zd = zd > 0.0 ? zd / r : (zd < 0.0 ? zd * r : zd);
+            zd = zd - f * (double)c;
+            zd = zd - pr;
+            z[t] = (float)zd;
+        }
+    }
+    return status;
 }
 
 /* Batched sampler over B rows of logits [B, V] (rows independent).  Per-row
