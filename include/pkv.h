@@ -202,6 +202,42 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, con
                            void* stream);
 
 /*
+ * pkv_sample_tokens with min-p ("LLM inference serving tutorial" 3.1, Q4):
+ * after top-p, a token stays in the support only if its probability is at
+ * least min_p[b] times the largest one, i.e. its weight 2^((z - zmax) log2(e) /
+ * T) is >= min_p[b] (taken in 2^-40 fixed point: mass >= ceil(min_p * 2^40));
+ * the most probable token always stays.  min_p: float32 [B], or NULL (off);
+ * min_p[b] <= 0 turns it off for row b; NaN or > 1 is PKV_ERR_INVALID_ARG
+ * (token -1).  Everything else as pkv_sample_tokens (no workspace).
+ */
+pkv_status pkv_sample_tokens_ex(int32_t* tokens, const float* logits, int B, int V, const float* temperature,
+                                const int32_t* top_k, const float* top_p, const float* min_p, const uint64_t* seeds,
+                                const uint64_t* offsets, int32_t* dev_status, void* stream);
+
+/*
+ * Logits processors, in place on logits float32 [B, V], in the order of the
+ * "LLM inference serving tutorial" 3.1 pipeline (before temperature and the
+ * filters of pkv_sample_tokens):
+ *  1. constraint mask (3.3): allow_mask uint32 [B, ceil(V/32)] or NULL; token
+ *     i of row b is allowed iff bit i % 32 of word i / 32 is set, else its
+ *     logit becomes -inf;
+ *  2. penalties (3.2) on the tokens listed for row b in CSR form (row_ptr int32
+ *     [B + 1] or NULL, tokens / counts int32 [row_ptr[B]], each token at most
+ *     once per row) with count c >= 1, an allowed mask bit and a finite logit:
+ *     the sign-aware repetition penalty r = repetition[b] (z / r for z > 0,
+ *     r * z for z < 0, 0 unchanged; r == 1 is a no-op), then
+ *     z - frequency[b] * c - presence[b]; computed in double, each operation
+ *     rounded on its own, then rounded once to float.
+ * repetition / frequency / presence: float32 [B] or NULL (off).  Errors: a
+ * listed token outside [0, V) (that entry skipped) or repetition <= 0 / NaN
+ * (that row's penalties skipped) -> PKV_ERR_INVALID_ARG in dev_status.
+ */
+pkv_status pkv_apply_logits_processors(float* logits, int B, int V, const uint32_t* allow_mask,
+                                       const int32_t* row_ptr, const int32_t* tokens, const int32_t* counts,
+                                       const float* repetition, const float* frequency, const float* presence,
+                                       int32_t* dev_status, void* stream);
+
+/*
  * Workspace bytes pkv_spec_verify needs: 32 bytes per logits row,
  * B * (2 * gamma + 1) rows.  Pure host arithmetic.
  */

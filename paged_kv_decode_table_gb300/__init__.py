@@ -13,6 +13,7 @@ Calls (names follow the C ABI):
   sample_tokens(logits, temperature, top_k, top_p, seeds, offsets, tokens=None)
   copy_blocks(k_cache, v_cache, src, dst)
   spec_verify(target_logits, draft_logits, draft_tokens, seq_lens, temperature, seeds, offsets)
+  apply_logits_processors(logits, allow_mask=None, row_ptr=None, tokens=None, counts=None, ...)
   BlockPool(num_blocks, block_size, max_blocks_per_seq)   host-side refcounted block ids
 """
 from __future__ import annotations
@@ -26,7 +27,7 @@ import torch
 __all__ = ["PkvError", "load_library", "library_path", "kv_append", "paged_decode_attention",
            "decode_workspace_bytes", "sample_tokens", "sample_workspace_bytes", "status_string",
            "new_status", "check_status", "STATUS", "copy_blocks", "BlockPool", "spec_verify",
-           "spec_verify_workspace_bytes"]
+           "spec_verify_workspace_bytes", "apply_logits_processors"]
 
 STATUS = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED", 3: "PKV_ERR_CUDA",
           4: "PKV_ERR_DEVICE_BOUNDS", 5: "PKV_ERR_TIMEOUT", 6: "PKV_ERR_NONFINITE", 7: "PKV_ERR_CAPACITY"}
@@ -75,6 +76,10 @@ def load_library():
         lib.pkv_sample_tokens.argtypes = [P, P, i32, i32, P, P, P, P, P, P, sz, P, P]
         lib.pkv_sample_tokens.restype = i32
         i64 = ctypes.c_int64
+        lib.pkv_sample_tokens_ex.argtypes = [P, P, i32, i32, P, P, P, P, P, P, P, P]
+        lib.pkv_sample_tokens_ex.restype = i32
+        lib.pkv_apply_logits_processors.argtypes = [P, i32, i32, P, P, P, P, P, P, P, P, P]
+        lib.pkv_apply_logits_processors.restype = i32
         lib.pkv_spec_verify_workspace_bytes.argtypes = [i32, i32]
         lib.pkv_spec_verify_workspace_bytes.restype = sz
         lib.pkv_spec_verify.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, P, P, P, P, sz, P, P]
@@ -230,10 +235,11 @@ def sample_workspace_bytes(B: int, V: int) -> int:
     return int(load_library().pkv_sample_workspace_bytes(B, V))
 
 
-def sample_tokens(logits, temperature, top_k, top_p, seeds, offsets, tokens=None, status=None):
+def sample_tokens(logits, temperature, top_k, top_p, seeds, offsets, tokens=None, status=None, min_p=None):
     """One token per row of logits [B, V] (float32); returns tokens [B] int32.
 
-    seeds / offsets are int64 tensors holding uint64 bit patterns."""
+    seeds / offsets are int64 tensors holding uint64 bit patterns; min_p
+    (float32 [B], optional) adds the min-p filter after top-p."""
     B, V = logits.shape
     dev = logits.device
     _check_cuda("logits", logits, torch.float32)
@@ -249,6 +255,13 @@ def sample_tokens(logits, temperature, top_k, top_p, seeds, offsets, tokens=None
     _check_cuda("tokens", tokens, torch.int32, (B,), dev)
     if status is not None:
         _check_cuda("status", status, torch.int32, (1,), dev)
+    if min_p is not None:
+        _check_cuda("min_p", min_p, torch.float32, (B,), dev)
+        code = load_library().pkv_sample_tokens_ex(_ptr(tokens), _ptr(logits), B, V, _ptr(temperature),
+                                                   _ptr(top_k), _ptr(top_p), _ptr(min_p), _ptr(seeds),
+                                                   _ptr(offsets), _ptr(status), _stream(dev))
+        _raise("pkv_sample_tokens_ex", code)
+        return tokens
     code = load_library().pkv_sample_tokens(_ptr(tokens), _ptr(logits), B, V, _ptr(temperature),
                                             _ptr(top_k), _ptr(top_p), _ptr(seeds), _ptr(offsets),
                                             None, 0, _ptr(status), _stream(dev))
@@ -372,3 +385,30 @@ def spec_verify(target_logits, draft_logits, draft_tokens, seq_lens, temperature
                                _ptr(status), _stream(dev))
     _raise("pkv_spec_verify", code)
     return tokens, n_acc, sl_out
+
+
+def apply_logits_processors(logits, allow_mask=None, row_ptr=None, tokens=None, counts=None, repetition=None,
+                            frequency=None, presence=None, status=None):
+    """Constraint mask (uint32 [B, ceil(V/32)], set bit = allowed) and CSR
+    repetition / frequency / presence penalties, in place on logits [B, V]."""
+    B, V = logits.shape
+    dev = logits.device
+    _check_cuda("logits", logits, torch.float32)
+    if allow_mask is not None:
+        if allow_mask.dtype not in (torch.int32, torch.uint32):
+            raise TypeError("allow_mask must hold 32-bit words")
+        _check_cuda("allow_mask", allow_mask, shape=(B, (V + 31) // 32), device=dev)
+    if row_ptr is not None:
+        _check_cuda("row_ptr", row_ptr, torch.int32, (B + 1,), dev)
+        _check_cuda("tokens", tokens, torch.int32, device=dev)
+        _check_cuda("counts", counts, torch.int32, tokens.shape, dev)
+    for name, t in (("repetition", repetition), ("frequency", frequency), ("presence", presence)):
+        if t is not None:
+            _check_cuda(name, t, torch.float32, (B,), dev)
+    if status is not None:
+        _check_cuda("status", status, torch.int32, (1,), dev)
+    code = load_library().pkv_apply_logits_processors(_ptr(logits), B, V, _ptr(allow_mask), _ptr(row_ptr),
+                                                      _ptr(tokens), _ptr(counts), _ptr(repetition),
+                                                      _ptr(frequency), _ptr(presence), _ptr(status), _stream(dev))
+    _raise("pkv_apply_logits_processors", code)
+    return logits

@@ -17,8 +17,11 @@ cudaError_t launch_decode_attention(void* out, const void* q, const void* k_cach
 size_t decode_workspace_bytes(int B, int Hq, int D, int P);
 int device_sm_count();
 cudaError_t launch_sampler(int32_t* tokens, const float* logits, int B, int V, const float* temperature,
-                           const int32_t* top_k, const float* top_p, const uint64_t* seeds, const uint64_t* offsets,
-                           int32_t* status, cudaStream_t stream);
+                           const int32_t* top_k, const float* top_p, const float* min_p, const uint64_t* seeds,
+                           const uint64_t* offsets, int32_t* status, cudaStream_t stream);
+cudaError_t launch_logits_processors(float* logits, int B, int V, const uint32_t* mask, const int32_t* row_ptr,
+                                     const int32_t* tokens, const int32_t* counts, const float* rep,
+                                     const float* freq, const float* pres, int32_t* status, cudaStream_t stream);
 size_t spec_verify_workspace_bytes(int B, int gamma);
 cudaError_t launch_spec_verify(int32_t* tokens_out, int32_t* n_accepted, int32_t* seq_lens_out, const float* target,
                                const float* draft, const int32_t* draft_tokens, const int32_t* seq_lens, int B,
@@ -139,8 +142,30 @@ pkv_status pkv_sample_tokens(int32_t* tokens, const float* logits, int B, int V,
     if (B < 0 || V < 1 || V > (1 << 23)) return PKV_ERR_INVALID_ARG;
     if (B == 0) return PKV_OK;
     if (!tokens || !logits || !temperature || !top_k || !top_p || !seeds || !offsets) return PKV_ERR_INVALID_ARG;
-    return cuda_status(pkv::launch_sampler(tokens, logits, B, V, temperature, top_k, top_p, seeds, offsets, dev_status,
-                                           static_cast<cudaStream_t>(stream)));
+    return cuda_status(pkv::launch_sampler(tokens, logits, B, V, temperature, top_k, top_p, nullptr, seeds, offsets,
+                                           dev_status, static_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_sample_tokens_ex(int32_t* tokens, const float* logits, int B, int V, const float* temperature,
+                                const int32_t* top_k, const float* top_p, const float* min_p, const uint64_t* seeds,
+                                const uint64_t* offsets, int32_t* dev_status, void* stream) {
+    if (B < 0 || V < 1 || V > (1 << 23)) return PKV_ERR_INVALID_ARG;
+    if (B == 0) return PKV_OK;
+    if (!tokens || !logits || !temperature || !top_k || !top_p || !seeds || !offsets) return PKV_ERR_INVALID_ARG;
+    return cuda_status(pkv::launch_sampler(tokens, logits, B, V, temperature, top_k, top_p, min_p, seeds, offsets,
+                                           dev_status, static_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_apply_logits_processors(float* logits, int B, int V, const uint32_t* allow_mask,
+                                       const int32_t* row_ptr, const int32_t* tokens, const int32_t* counts,
+                                       const float* repetition, const float* frequency, const float* presence,
+                                       int32_t* dev_status, void* stream) {
+    if (B < 0 || V < 1 || V > (1 << 23)) return PKV_ERR_INVALID_ARG;
+    if (B == 0 || (!allow_mask && !row_ptr)) return PKV_OK;
+    if (!logits || (row_ptr && (!tokens || !counts))) return PKV_ERR_INVALID_ARG;
+    return cuda_status(pkv::launch_logits_processors(logits, B, V, allow_mask, row_ptr, tokens, counts, repetition,
+                                                     frequency, presence, dev_status,
+                                                     static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -116,6 +116,7 @@ struct View {
 
 struct Keep {
     bool k_on, p_on;
+    uint64_t mth;  // min-p: a kept token's mass must be >= mth (0: off)
     uint32_t tauk, taup;
     int idk, idp;
     float zk, zp;  // key_float(tauk), key_float(taup)
@@ -443,7 +444,8 @@ __device__ void draw_pass(Ctx& c, const View& v, const Keep& kp, bool vec, float
     const bool filt = kp.k_on || kp.p_on;
     // -inf logits weigh 0, so without a filter every slot is simply summed
     auto kmass = [&](float z, int e) -> uint64_t {
-        return (!filt || kp.keep_f(z, v.idbase + e)) ? mass(z, zmax, c2) : 0ull;
+        const uint64_t m = (!filt || kp.keep_f(z, v.idbase + e)) ? mass(z, zmax, c2) : 0ull;
+        return m >= kp.mth ? m : 0ull;
     };
     auto lane_sum = [&](int e) -> uint64_t {  // this lane's 4 logits at slot e (may lie past the end)
         if (e >= nvec) return 0ull;
@@ -575,8 +577,8 @@ __device__ __forceinline__ uint64_t warp_scan128(unsigned long long* buf) {
     return total;
 }
 
-__device__ void solo_finish_small(SampSmem* sm, int n, int kk, float pp, float zmax, float c2, uint64_t seed,
-                                  uint64_t offset, int32_t* tok_out) {
+__device__ void solo_finish_small(SampSmem* sm, int n, int kk, float pp, uint64_t mth, float zmax, float c2,
+                                  uint64_t seed, uint64_t offset, int32_t* tok_out) {
     if (threadIdx.x >= 32) return;
     const int lane = threadIdx.x;
     const unsigned long long* a = sm->list;
@@ -615,6 +617,8 @@ __device__ void solo_finish_small(SampSmem* sm, int n, int kk, float pp, float z
 #pragma unroll
         for (int q = 0; q < 4; ++q) kept[q] = in_k[q] && buf[rank[q]] < target;  // prefix before it < target
     }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) kept[q] = kept[q] && W[q] >= mth;  // min-p, after top-p
     __syncwarp();
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -654,10 +658,10 @@ __device__ void solo_finish_small(SampSmem* sm, int n, int kk, float pp, float z
 
 // Larger lists: bitonic sort by (z desc, id asc), keep the first kk, apply
 // top-p exactly, re-sort the kept tokens by id and draw.
-__device__ void solo_finish(SampSmem* sm, int n, int kk, float pp, float zmax, float c2, uint64_t seed,
-                            uint64_t offset, int32_t* tok_out) {
+__device__ void solo_finish(SampSmem* sm, int n, int kk, float pp, uint64_t mth, float zmax, float c2,
+                            uint64_t seed, uint64_t offset, int32_t* tok_out) {
     if (n <= kSmallList) {
-        solo_finish_small(sm, n, kk, pp, zmax, c2, seed, offset, tok_out);
+        solo_finish_small(sm, n, kk, pp, mth, zmax, c2, seed, offset, tok_out);
         return;
     }
     const int tid = threadIdx.x;
@@ -696,7 +700,8 @@ __device__ void solo_finish(SampSmem* sm, int n, int kk, float pp, float zmax, f
     // kept tokens re-keyed as (id << 41 | mass) and sorted by id
     for (int j = tid; j < m; j += kST) {
         const unsigned long long k = a[j];
-        const uint64_t W = mass(key_float(static_cast<uint32_t>(k >> 32)), zmax, c2);
+        uint64_t W = mass(key_float(static_cast<uint32_t>(k >> 32)), zmax, c2);
+        W = W >= mth ? W : 0ull;  // min-p, after top-p: weighs nothing in the draw
         a[j] = (static_cast<unsigned long long>(sort_key_id(k)) << 41) | W;
     }
     const int mp2 = pow2_ceil(m);
@@ -763,8 +768,8 @@ constexpr int kLoadChunks = 4;
 __global__ void __launch_bounds__(kST, 2)
     sampler_kernel(int32_t* __restrict__ tokens, const float* __restrict__ logits, int V, int S, int smem_slice,
                    const float* __restrict__ temperature, const int32_t* __restrict__ top_k,
-                   const float* __restrict__ top_p, const uint64_t* __restrict__ seeds,
-                   const uint64_t* __restrict__ offsets, int32_t* status) {
+                   const float* __restrict__ top_p, const float* __restrict__ min_p,
+                   const uint64_t* __restrict__ seeds, const uint64_t* __restrict__ offsets, int32_t* status) {
     extern __shared__ __align__(16) uint8_t samp_smem_raw[];
     SampSmem* sm = reinterpret_cast<SampSmem*>(samp_smem_raw);
     float* zslice = reinterpret_cast<float*>(samp_smem_raw + sizeof(SampSmem));
@@ -796,6 +801,7 @@ __global__ void __launch_bounds__(kST, 2)
     // row parameters first: they decide what the passes must track
     const float T = temperature[row];
     const float pp = top_p[row];
+    const float mp = min_p ? min_p[row] : 0.f;
     const int kk_in = top_k[row];
     const uint64_t seed = seeds[row], offset = offsets[row];
     const int nvec = (n + 3) & ~3;  // element slots visited by the 4-wide loops
@@ -934,6 +940,7 @@ __global__ void __launch_bounds__(kST, 2)
     if (gbad || !(zmax > -INFINITY)) err = PKV_ERR_NONFINITE;  // NaN / +inf, or no finite logit
     else if (!(T >= 0.f)) err = PKV_ERR_INVALID_ARG;
     else if (T != 0.f && !(pp > 0.f)) err = PKV_ERR_INVALID_ARG;
+    else if (T != 0.f && (mp != mp || mp > 1.f)) err = PKV_ERR_INVALID_ARG;  // min_p NaN or > 1
     if (err) {
         if (c.rank == 0 && tid == 0) {
             *tok_out = -1;
@@ -974,6 +981,7 @@ __global__ void __launch_bounds__(kST, 2)
     Keep kp;
     kp.k_on = false;
     kp.p_on = false;
+    kp.mth = mp > 0.f ? ceil_mul_p(mp, 1ull << 40) : 0ull;  // min-p: mass >= ceil(min_p * 2^40)
     kp.tauk = kp.taup = 0u;
     kp.idk = kp.idp = INT_MAX;
     kp.zk = kp.zp = 0.f;
@@ -1073,7 +1081,7 @@ __global__ void __launch_bounds__(kST, 2)
                 }
                 cluster.sync();  // candidates complete in rank 0; no remote access follows
                 if (c.rank != 0) return;
-                solo_finish(sm, static_cast<int>(total), kk, pp, zmax, c2, seed, offset, tok_out);
+                solo_finish(sm, static_cast<int>(total), kk, pp, kp.mth, zmax, c2, seed, offset, tok_out);
                 return;
             }
             cluster.sync();  // remote histogram reads are done before the fallback reuses it
@@ -1384,8 +1392,8 @@ static SamplerPlan plan_sampler(int B, int V) {
 }
 
 cudaError_t launch_sampler(int32_t* tokens, const float* logits, int B, int V, const float* temperature,
-                           const int32_t* top_k, const float* top_p, const uint64_t* seeds, const uint64_t* offsets,
-                           int32_t* status, cudaStream_t stream) {
+                           const int32_t* top_k, const float* top_p, const float* min_p, const uint64_t* seeds,
+                           const uint64_t* offsets, int32_t* status, cudaStream_t stream) {
     const SamplerPlan sp = plan_sampler(B, V);
     cudaError_t err = cudaFuncSetAttribute(sampler_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(sp.smem));
@@ -1405,7 +1413,7 @@ cudaError_t launch_sampler(int32_t* tokens, const float* logits, int B, int V, c
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, sampler_kernel, tokens, logits, V, sp.S, sp.smem_slice, temperature, top_k,
-                              top_p, seeds, offsets, status);
+                              top_p, min_p, seeds, offsets, status);
 }
 
 }  // namespace pkv
