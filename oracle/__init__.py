@@ -29,6 +29,10 @@ What each function follows (web pages cited by title and section):
   sign-aware repetition penalties of "LLM inference serving tutorial" sections
   3.2-3.3, in the section 3.1 pipeline order; ``sample_row(min_p=...)`` adds
   min-p (section 3.1 and Q4) after top-p.
+* ``kv_append_chunk`` / ``prefill_attention``: a prefill chunk of several
+  tokens per sequence written through the block table and its causal attention
+  over the cached prefix and the chunk ("Suy luan & Toi uu hoa (Inference)"
+  2.1; "LLM inference serving tutorial" 5.4; the lab's prefill).
 * ``copy_blocks``: the copy half of copy-on-write, "LLM inference serving
   tutorial" section 4.2.
 * ``oracle.blocks`` (pure Python): reference-counted block sharing, fork,
@@ -112,6 +116,11 @@ def _load():
             lib.oracle_sample_row_ex.restype = i32
             lib.oracle_process_logits.argtypes = [P, i32, i32, P, P, P, P, P, P, P]
             lib.oracle_process_logits.restype = i32
+            lib.oracle_kv_append_chunk.argtypes = [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32]
+            lib.oracle_kv_append_chunk.restype = i32
+            lib.oracle_prefill_attention.argtypes = [P, P, P, P, i32, P, i32, P, P, i32, i32, i32, i32, i32, i32,
+                                                     f64, P, i64, P]
+            lib.oracle_prefill_attention.restype = i32
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = i32
             _lib = lib
@@ -193,6 +202,38 @@ def spec_verify_row(target_logits, draft_logits, draft_tokens, temperature: floa
                                         ctypes.byref(tm), ctypes.byref(dm))
     return dict(status=int(st), tokens=tok, n_acc=n.value, seq_len_out=so.value, test_margin=tm.value,
                 draw_margin=dm.value)
+
+
+def kv_append_chunk(k_new, v_new, k_cache, v_cache, block_tables, seq_lens, q_start) -> int:
+    """In-place append of n_b = q_start[b+1] - q_start[b] tokens per sequence (rows of the packed
+    [T, Hkv, D] k_new / v_new) at positions seq_lens[b] - n_b .. seq_lens[b] - 1."""
+    NB, Hkv, BS, D = k_cache.shape
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    qs = np.ascontiguousarray(q_start, dtype=np.int32)
+    B = sl.shape[0]
+    return int(_load().oracle_kv_append_chunk(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(bt),
+                                              bt.shape[1], _ptr(sl), _ptr(qs), B, Hkv, D, BS, NB,
+                                              _dtype_code(k_cache)))
+
+
+def prefill_attention(q, k_cache, v_cache, block_tables, seq_lens, q_start, scale: float = 0.0, rows=None):
+    """Causal chunk attention; q [T, Hq, D].  Returns (out float64 [n, D], status, max |sum w - 1|)."""
+    T, Hq, D = q.shape
+    NB, Hkv, BS, D2 = k_cache.shape
+    assert D == D2
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    qs = np.ascontiguousarray(q_start, dtype=np.int32)
+    B = sl.shape[0]
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    n = T * Hq if r is None else r.shape[0]
+    out = np.zeros((n, D), dtype=np.float64)
+    werr = ctypes.c_double(0.0)
+    st = _load().oracle_prefill_attention(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _dtype_code(q), _ptr(bt),
+                                          bt.shape[1], _ptr(sl), _ptr(qs), B, Hq, Hkv, D, BS, NB, float(scale),
+                                          None if r is None else _ptr(r), n, ctypes.byref(werr))
+    return out, int(st), float(werr.value)
 
 
 def gather(cache, block_tables, b: int, L: int, h: int) -> np.ndarray:

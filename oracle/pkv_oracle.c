@@ -194,7 +194,7 @@ int oracle_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const i
  * position including the new one, softmax with the max subtracted, weights times
  * V; [CH5] 3.1: query head qh uses KV head qh / G).  out[D] in float64.
  * Writes sum(weights) - 1 to *wsum_err.  L = 0 gives zeros. */
-static int attention_row(const void* q, const void* k_cache, const void* v_cache, int dtype,
+static int attention_row(const void* q, size_t qrow, const void* k_cache, const void* v_cache, int dtype,
                          const int32_t* block_tables, int max_blocks, int b, int qh, int L,
                          int Hq, int Hkv, int D, int BS, int NB, double scale, double* out,
                          double* wsum_err) {
@@ -210,7 +210,7 @@ static int attention_row(const void* q, const void* k_cache, const void* v_cache
     int st = oracle_gather(k_cache, block_tables, max_blocks, b, L, h, Hkv, D, BS, NB, dtype, K);
     if (st == OR_OK) st = oracle_gather(v_cache, block_tables, max_blocks, b, L, h, Hkv, D, BS, NB, dtype, V);
     if (st == OR_OK) {
-        for (int d = 0; d < D; ++d) qv[d] = load_elem(q, ((size_t)b * Hq + qh) * D + d, dtype);
+        for (int d = 0; d < D; ++d) qv[d] = load_elem(q, (qrow * Hq + qh) * D + d, dtype);
         double mx = -INFINITY;
         for (int j = 0; j < L; ++j) {
             double acc = 0.0;
@@ -260,7 +260,7 @@ int oracle_paged_attention(double* out, const void* q, const void* k_cache, cons
             for (int d = 0; d < D; ++d) out[i * D + d] = 0.0;
             st = OR_DEVICE_BOUNDS;
         } else {
-            st = attention_row(q, k_cache, v_cache, dtype, block_tables, max_blocks, b, qh, L, Hq,
+            st = attention_row(q, (size_t)b, k_cache, v_cache, dtype, block_tables, max_blocks, b, qh, L, Hq,
                                Hkv, D, BS, NB, scale, out + i * D, &e);
         }
         if (st != OR_OK) {
@@ -547,6 +547,86 @@ int oracle_sample_batch(const float* logits, int B, int V, const float* temperat
             status = st;
         }
     }
+    return status;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Chunked prefill ("Bai Lab tong hop -- Inference Engineering" prefill of a
+ * prompt through the same block table; "Suy luan & Toi uu hoa (Inference)"
+ * 2.1: a chunk's queries attend causally to the whole cached prefix and to the
+ * chunk itself; "LLM inference serving tutorial" 5.4 chunked prefill).  Sequence
+ * b appends n_b = q_start[b+1] - q_start[b] new tokens (rows q_start[b] ..
+ * q_start[b+1]-1 of the packed [T, Hkv, D] / [T, Hq, D] arrays); seq_lens[b]
+ * is the length after the append, so new token i sits at position
+ * L_b - n_b + i. */
+static int seq_of_row(const int32_t* q_start, int B, int t) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {  /* last b with q_start[b] <= t */
+        int mid = (lo + hi + 1) / 2;
+        if (q_start[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+int oracle_kv_append_chunk(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                           const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
+                           const int32_t* q_start, int B, int Hkv, int D, int BS, int NB, int dtype) {
+    size_t es = elem_size(dtype);
+    int status = OR_OK;
+    for (int b = 0; b < B; ++b) {
+        int n = q_start[b + 1] - q_start[b], L = seq_lens[b];
+        if (n < 0 || L < n || (long long)L > (long long)max_blocks * BS) { status = OR_DEVICE_BOUNDS; continue; }
+        for (int i = 0; i < n; ++i) {
+            int pos = L - n + i;
+            size_t t = (size_t)q_start[b] + i;
+            for (int h = 0; h < Hkv; ++h) {
+                long long off = pool_offset(block_tables, max_blocks, b, pos, h, Hkv, BS, D, NB);
+                if (off < 0) { status = OR_DEVICE_BOUNDS; continue; }
+                size_t src = (t * Hkv + h) * D;
+                memcpy((char*)k_cache + (size_t)off * es, (const char*)k_new + src * es, D * es);
+                memcpy((char*)v_cache + (size_t)off * es, (const char*)v_new + src * es, D * es);
+            }
+        }
+    }
+    return status;
+}
+
+/* Causal attention of the chunk's queries: row (t, qh) of the packed q [T, Hq,
+ * D] attends to positions 0 .. pos_t of its sequence through the table.  rows
+ * (length nrows, values t * Hq + qh) selects the rows computed (NULL: all T *
+ * Hq); out is [nrows, D] float64. */
+int oracle_prefill_attention(double* out, const void* q, const void* k_cache, const void* v_cache, int dtype,
+                             const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
+                             const int32_t* q_start, int B, int Hq, int Hkv, int D, int BS, int NB, double scale,
+                             const int64_t* rows, int64_t nrows, double* max_wsum_err) {
+    if (scale <= 0.0) scale = 1.0 / sqrt((double)D);
+    int T = q_start[B];
+    if (!rows) nrows = (int64_t)T * Hq;
+    int status = OR_OK;
+    double werr = 0.0;
+#pragma omp parallel for schedule(dynamic, 4) reduction(max : werr)
+    for (int64_t i = 0; i < nrows; ++i) {
+        int64_t flat = rows ? rows[i] : i;
+        int t = (int)(flat / Hq), qh = (int)(flat % Hq);
+        int b = seq_of_row(q_start, B, t);
+        int n = q_start[b + 1] - q_start[b], L = seq_lens[b];
+        double e = 0.0;
+        int st;
+        if (n < 1 || L < n || (long long)L > (long long)max_blocks * BS) {
+            for (int d = 0; d < D; ++d) out[i * D + d] = 0.0;
+            st = OR_DEVICE_BOUNDS;
+        } else {
+            int pos = L - n + (t - q_start[b]);
+            st = attention_row(q, (size_t)t, k_cache, v_cache, dtype, block_tables, max_blocks, b, qh, pos + 1,
+                               Hq, Hkv, D, BS, NB, scale, out + i * D, &e);
+        }
+        if (st != OR_OK) {
+#pragma omp atomic write
+            status = st;
+        }
+        if (fabs(e) > werr) werr = fabs(e);
+    }
+    if (max_wsum_err) *max_wsum_err = werr;
     return status;
 }
 
