@@ -11,6 +11,7 @@
  * Shared prefixes: a host-side reference-counted block pool (pkv_block_pool_*,
  * pkv_seq_*) hands out block ids and reports the copy-on-write pairs that
  * pkv_copy_blocks copies on the GPU before the step's append.
+ * Chunked prefill: pkv_kv_append_chunk and pkv_paged_prefill_attention.
  * Speculative decoding: pkv_spec_verify accepts or rejects draft tokens,
  * draws the correction or bonus token and returns the rolled-back lengths.
  *
@@ -200,6 +201,43 @@ pkv_status pkv_sample_tokens(int32_t* tokens, const float* logits, int B, int V,
 pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst, int n_pairs,
                            int Hkv, int D, int block_size, int num_blocks, pkv_dtype dtype, int32_t* dev_status,
                            void* stream);
+
+/*
+ * Chunked prefill, append half ("Bai Lab tong hop -- Inference Engineering"
+ * prefill chunks written with KVPool.write; "LLM inference serving tutorial"
+ * 5.4).  Sequence b appends n_b = q_start[b+1] - q_start[b] tokens: rows
+ * q_start[b] .. q_start[b+1] - 1 of the packed k_new / v_new [T_new, Hkv, D]
+ * (T_new = q_start[B]); seq_lens[b] is the length after the append, so row
+ * q_start[b] + i goes to position seq_lens[b] - n_b + i through the table.
+ * q_start: device int32 [B + 1], non-decreasing, q_start[0] = 0.  A sequence
+ * with seq_lens[b] < n_b or beyond the table, or a block id outside [0,
+ * num_blocks), is skipped and PKV_ERR_DEVICE_BOUNDS recorded.  Bit copy.
+ */
+pkv_status pkv_kv_append_chunk(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                               const int32_t* q_start, int B, int T_new, int Hkv, int D, int block_size,
+                               int num_blocks, pkv_dtype dtype, int32_t* dev_status, void* stream);
+
+/*
+ * Chunked prefill, attention half ("Suy luan & Toi uu hoa (Inference)" 2.1;
+ * the lab's forward over a prompt chunk; "LLM inference serving tutorial"
+ * 5.4): for packed query row t of sequence b (q [T_new, Hq, D], rows laid out
+ * as in pkv_kv_append_chunk), at position pos = seq_lens[b] - n_b + (t -
+ * q_start[b]), query head qh attends to K/V head qh / (Hq / Hkv) at positions
+ * 0 .. pos (causal), read through the table:
+ *   out[t][qh] = sum_{j <= pos} softmax_j(scale * <q[t][qh], K_j>) V_j.
+ * The chunk's own K/V must already be in the cache (pkv_kv_append_chunk first).
+ * scale <= 0 selects 1/sqrt(D).  bf16 only, D = 128, block_size a multiple of
+ * 16, Hq / Hkv <= 8, 16-byte aligned pools and 4-byte aligned q / out (else
+ * PKV_ERR_UNSUPPORTED).  fp32 accumulation; one CTA per (16 chunk tokens, KV
+ * head) with tensor-core MMAs.  A sequence with an invalid length or block id
+ * gets zero output and PKV_ERR_DEVICE_BOUNDS.
+ */
+pkv_status pkv_paged_prefill_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                                       const int32_t* q_start, int B, int T_new, int Hq, int Hkv, int D,
+                                       int block_size, int num_blocks, float scale, pkv_dtype dtype,
+                                       int32_t* dev_status, void* stream);
 
 /*
  * pkv_sample_tokens with min-p ("LLM inference serving tutorial" 3.1, Q4):

@@ -14,6 +14,8 @@ Calls (names follow the C ABI):
   copy_blocks(k_cache, v_cache, src, dst)
   spec_verify(target_logits, draft_logits, draft_tokens, seq_lens, temperature, seeds, offsets)
   apply_logits_processors(logits, allow_mask=None, row_ptr=None, tokens=None, counts=None, ...)
+  kv_append_chunk(k_new, v_new, k_cache, v_cache, block_tables, seq_lens, q_start)
+  paged_prefill_attention(q, k_cache, v_cache, block_tables, seq_lens, q_start, out=None, scale=0.0)
   BlockPool(num_blocks, block_size, max_blocks_per_seq)   host-side refcounted block ids
 """
 from __future__ import annotations
@@ -27,7 +29,8 @@ import torch
 __all__ = ["PkvError", "load_library", "library_path", "kv_append", "paged_decode_attention",
            "decode_workspace_bytes", "sample_tokens", "sample_workspace_bytes", "status_string",
            "new_status", "check_status", "STATUS", "copy_blocks", "BlockPool", "spec_verify",
-           "spec_verify_workspace_bytes", "apply_logits_processors"]
+           "spec_verify_workspace_bytes", "apply_logits_processors", "kv_append_chunk",
+           "paged_prefill_attention"]
 
 STATUS = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED", 3: "PKV_ERR_CUDA",
           4: "PKV_ERR_DEVICE_BOUNDS", 5: "PKV_ERR_TIMEOUT", 6: "PKV_ERR_NONFINITE", 7: "PKV_ERR_CAPACITY"}
@@ -76,6 +79,11 @@ def load_library():
         lib.pkv_sample_tokens.argtypes = [P, P, i32, i32, P, P, P, P, P, P, sz, P, P]
         lib.pkv_sample_tokens.restype = i32
         i64 = ctypes.c_int64
+        lib.pkv_kv_append_chunk.argtypes = [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32, i32, P, P]
+        lib.pkv_kv_append_chunk.restype = i32
+        lib.pkv_paged_prefill_attention.argtypes = [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                                    f32, i32, P, P]
+        lib.pkv_paged_prefill_attention.restype = i32
         lib.pkv_sample_tokens_ex.argtypes = [P, P, i32, i32, P, P, P, P, P, P, P, P]
         lib.pkv_sample_tokens_ex.restype = i32
         lib.pkv_apply_logits_processors.argtypes = [P, i32, i32, P, P, P, P, P, P, P, P, P]
@@ -412,3 +420,54 @@ def apply_logits_processors(logits, allow_mask=None, row_ptr=None, tokens=None, 
                                                       _ptr(frequency), _ptr(presence), _ptr(status), _stream(dev))
     _raise("pkv_apply_logits_processors", code)
     return logits
+
+
+def kv_append_chunk(k_new, v_new, k_cache, v_cache, block_tables, seq_lens, q_start, status=None):
+    """Append n_b = q_start[b+1] - q_start[b] rows of k_new / v_new [T_new, Hkv, D]
+    per sequence at positions seq_lens[b] - n_b .. seq_lens[b] - 1."""
+    NB, Hkv, BS, D = k_cache.shape
+    B = seq_lens.shape[0]
+    T = k_new.shape[0]
+    dev = k_cache.device
+    _check_cuda("k_cache", k_cache)
+    _check_cuda("v_cache", v_cache, k_cache.dtype, k_cache.shape, dev)
+    _check_cuda("k_new", k_new, k_cache.dtype, (T, Hkv, D), dev)
+    _check_cuda("v_new", v_new, k_cache.dtype, (T, Hkv, D), dev)
+    _check_cuda("block_tables", block_tables, torch.int32, device=dev)
+    _check_cuda("seq_lens", seq_lens, torch.int32, (B,), dev)
+    _check_cuda("q_start", q_start, torch.int32, (B + 1,), dev)
+    if status is not None:
+        _check_cuda("status", status, torch.int32, (1,), dev)
+    code = load_library().pkv_kv_append_chunk(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                              _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
+                                              _ptr(q_start), B, T, Hkv, D, BS, NB, _dtype_code(k_cache),
+                                              _ptr(status), _stream(dev))
+    _raise("pkv_kv_append_chunk", code)
+
+
+def paged_prefill_attention(q, k_cache, v_cache, block_tables, seq_lens, q_start, out=None, scale: float = 0.0,
+                            status=None):
+    """Causal attention of the packed chunk queries q [T_new, Hq, D]; returns out [T_new, Hq, D]."""
+    T, Hq, D = q.shape
+    NB, Hkv, BS, D2 = k_cache.shape
+    B = seq_lens.shape[0]
+    dev = q.device
+    if D2 != D:
+        raise ValueError("head_dim of q and the cache differ")
+    _check_cuda("q", q)
+    _check_cuda("k_cache", k_cache, q.dtype, device=dev)
+    _check_cuda("v_cache", v_cache, q.dtype, k_cache.shape, dev)
+    _check_cuda("block_tables", block_tables, torch.int32, device=dev)
+    _check_cuda("seq_lens", seq_lens, torch.int32, (B,), dev)
+    _check_cuda("q_start", q_start, torch.int32, (B + 1,), dev)
+    if out is None:
+        out = torch.empty_like(q)
+    _check_cuda("out", out, q.dtype, q.shape, dev)
+    if status is not None:
+        _check_cuda("status", status, torch.int32, (1,), dev)
+    code = load_library().pkv_paged_prefill_attention(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                                      _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
+                                                      _ptr(q_start), B, T, Hq, Hkv, D, BS, NB, float(scale),
+                                                      _dtype_code(q), _ptr(status), _stream(dev))
+    _raise("pkv_paged_prefill_attention", code)
+    return out

@@ -3,6 +3,7 @@
 // Host-side argument validation, then one or more kernel launches on the
 // caller's stream.  Nothing here allocates device memory or synchronises.
 #include <cuda_runtime.h>
+#include <math.h>
 
 #include "pkv_common.cuh"
 
@@ -27,6 +28,14 @@ cudaError_t launch_spec_verify(int32_t* tokens_out, int32_t* n_accepted, int32_t
                                const float* draft, const int32_t* draft_tokens, const int32_t* seq_lens, int B,
                                int gamma, int V, const float* temperature, const uint64_t* seeds,
                                const uint64_t* offsets, void* workspace, int32_t* status, cudaStream_t stream);
+cudaError_t launch_kv_append_chunk(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                                   const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
+                                   const int32_t* q_start, int B, int T_new, int Hkv, int D, int BS, int NB,
+                                   pkv_dtype dtype, int32_t* status, cudaStream_t stream);
+cudaError_t launch_prefill_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
+                                     const int32_t* q_start, int B, int T_new, int Hq, int Hkv, int BS, int NB,
+                                     float scale, int32_t* status, cudaStream_t stream);
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst, int n_pairs,
                                long long block_bytes, int NB, int32_t* status, cudaStream_t stream);
 }  // namespace pkv
@@ -99,6 +108,41 @@ pkv_status pkv_spec_verify(int32_t* tokens_out, int32_t* n_accepted, int32_t* se
     return cuda_status(pkv::launch_spec_verify(tokens_out, n_accepted, seq_lens_out, target_logits, draft_logits,
                                                draft_tokens, seq_lens, B, gamma, V, temperature, seeds, offsets,
                                                workspace, dev_status, static_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_kv_append_chunk(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                               const int32_t* q_start, int B, int T_new, int Hkv, int D, int block_size,
+                               int num_blocks, pkv_dtype dtype, int32_t* dev_status, void* stream) {
+    if (B < 0 || T_new < 0 || Hkv < 1 || D < 1 || block_size < 1 || num_blocks < 1 || max_blocks_per_seq < 1 ||
+        !dtype_ok(dtype))
+        return PKV_ERR_INVALID_ARG;
+    if (B == 0 || T_new == 0) return PKV_OK;
+    if (!k_new || !v_new || !k_cache || !v_cache || !block_tables || !seq_lens || !q_start) return PKV_ERR_INVALID_ARG;
+    return cuda_status(pkv::launch_kv_append_chunk(k_new, v_new, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                                   seq_lens, q_start, B, T_new, Hkv, D, block_size, num_blocks, dtype,
+                                                   dev_status, static_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_paged_prefill_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                                       const int32_t* q_start, int B, int T_new, int Hq, int Hkv, int D,
+                                       int block_size, int num_blocks, float scale, pkv_dtype dtype,
+                                       int32_t* dev_status, void* stream) {
+    if (B < 0 || T_new < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || block_size < 1 || num_blocks < 1 ||
+        max_blocks_per_seq < 1 || !dtype_ok(dtype))
+        return PKV_ERR_INVALID_ARG;
+    if (B == 0 || T_new == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !q_start) return PKV_ERR_INVALID_ARG;
+    if (dtype != PKV_BF16 || D != 128 || block_size % 16 != 0 || Hq / Hkv > 8) return PKV_ERR_UNSUPPORTED;
+    auto aligned16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (!aligned16(k_cache) || !aligned16(v_cache) || (reinterpret_cast<uintptr_t>(q) & 3u) ||
+        (reinterpret_cast<uintptr_t>(out) & 3u))
+        return PKV_ERR_UNSUPPORTED;
+    if (scale <= 0.f) scale = 1.0f / sqrtf(static_cast<float>(D));
+    return cuda_status(pkv::launch_prefill_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                                     seq_lens, q_start, B, T_new, Hq, Hkv, block_size, num_blocks,
+                                                     scale, dev_status, static_cast<cudaStream_t>(stream)));
 }
 
 size_t pkv_decode_workspace_bytes(int B, int Hq, int D, int num_sms) {
