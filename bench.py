@@ -52,6 +52,18 @@ def _peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def _bf16_peak():
+    """Measured dense bf16 TFLOP/s (burst) from MEASURED_PEAKS.json, else the fallback 1900."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        for k in ("bf16_tflops", "bf16_tflops_burst"):
+            if k in d:
+                return float(d[k])
+    return 1900.0
+
+
 def _source_hash():
     h = hashlib.sha256()
     for rel in ("paged_kv_decode_table_gb300/csrc/decode_attention.cu",
@@ -536,6 +548,38 @@ def run_extras(args):
           "GB/s": by / (t["median_us"] * 1e-6) / 1e9, "frac_of_measured": by / (t["median_us"] * 1e-6) / 1e9 / peak,
           "accepted_drafts": int(nacc.sum()), "emitted_tokens_per_s": emitted / (t["median_us"] * 1e-6)})
     del tgt, drf
+    torch.cuda.empty_cache()
+
+    # chunked prefill: 16 sequences, a 512-token chunk each after a 1024..4096-token prefix
+    Bp, chunk, Hq, Hkv_p, Dp, BSp = 16, 512, 32, 8, 128, 16
+    gen = torch.Generator().manual_seed(5)
+    prefix = torch.randint(1024, 4097, (Bp,), generator=gen)
+    Lp = (prefix + chunk).to(torch.int32)
+    nbp = (Lp + BSp - 1) // BSp
+    NBp = int(nbp.sum())
+    permp = torch.randperm(NBp, generator=gen).to(torch.int32)
+    MBp = int(nbp.max())
+    btp = torch.full((Bp, MBp), -1, dtype=torch.int32)
+    o = 0
+    for b in range(Bp):
+        btp[b, :nbp[b]] = permp[o:o + int(nbp[b])]
+        o += int(nbp[b])
+    Kp = torch.randn((NBp, Hkv_p, BSp, Dp), device=dev).to(torch.bfloat16)
+    Vp = torch.randn((NBp, Hkv_p, BSp, Dp), device=dev).to(torch.bfloat16)
+    qp = torch.randn((Bp * chunk, Hq, Dp), device=dev).to(torch.bfloat16)
+    qs = torch.arange(0, Bp * chunk + 1, chunk, dtype=torch.int32, device=dev)
+    btp, Lpd = btp.to(dev), Lp.to(dev)
+    outp = torch.empty_like(qp)
+    t = _time_calls(lambda: pkv.paged_prefill_attention(qp, Kp, Vp, btp, Lpd, qs, out=outp), 20, flush=flush)
+    # causal pairs: token i of a chunk sees prefix + i + 1 positions
+    pairs = sum(int(prefix[b]) * chunk + chunk * (chunk + 1) // 2 for b in range(Bp))
+    flops = 4 * Hq * Dp * pairs
+    kv_bytes = int(Lp.sum()) * Hkv_p * Dp * 2 * 2
+    tf = flops / (t["median_us"] * 1e-6) / 1e12
+    emit({"extra": "paged_prefill_attention", "workload": f"{Bp} x {chunk}-token chunks, prefix 1024..4096, "
+          f"{Hq}q/{Hkv_p}kv, D {Dp}", "flops": flops, "kv_bytes": kv_bytes, **t, "TFLOP/s": tf,
+          "frac_of_bf16_dense": tf / _bf16_peak(), "kv_GB/s": kv_bytes / (t["median_us"] * 1e-6) / 1e9})
+    del Kp, Vp, qp, outp
     torch.cuda.empty_cache()
 
     # copy-on-write block copies: 1024 pairs of 64 KB blocks (bf16, 8 KV heads, 16 slots, D 128)

@@ -14,9 +14,9 @@
 // Attention (bf16, D = 128, block_size a multiple of 16): one CTA per (tile of
 // 16 chunk tokens of one sequence, KV head h), one warp per query head of the
 // group.  A warp holds its 16 query rows as mma.sync A fragments (tokens on M);
-// the CTA streams the 16-key sub-tiles of head h's K and V through a two-stage
-// cp.async ring in shared memory (128-byte-swizzled rows; rows past the
-// sequence end are zero-filled) shared by the G warps; S = Q K^T and O += P V
+// the CTA streams head h's K and V in 32-key steps through a four-step
+// cp.async ring in shared memory (128-byte-swizzled rows; rows past the tile's
+// last position are zero-filled) shared by the G warps; S = Q K^T and O += P V
 // by m16n8k16 bf16 MMAs with fp32 accumulation, causal mask and online softmax
 // in the log2 domain.  Each K/V sub-tile is used by 16 tokens x G heads.
 #include <math.h>
@@ -88,6 +88,18 @@ __global__ void __launch_bounds__(kPAppendWarps * 32)
 constexpr int kPBox = 16 * 128;      // one 64-dim half of a 16-row sub-tile, 128 B per row
 constexpr int kPTile = 2 * kPBox;    // a K (or V) sub-tile: 16 rows x 128 dims bf16
 constexpr int kPStage = 2 * kPTile;  // K and V
+constexpr int kPRing = 4;            // pair slots (2 sub-tiles each): three pairs in flight while one is used
+constexpr int kPSmem = kPRing * 2 * kPStage;  // 64 KB of dynamic shared memory
+constexpr int kPTableWin = 512;  // block-table entries kept in shared memory at a time
+
+// 2^x by the hardware's approximate base-2 exponential (P and the rescale
+// factors of the online softmax, which are rounded to bf16 or only scale fp32
+// accumulators).
+__device__ __forceinline__ float ex2a(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
@@ -106,8 +118,9 @@ __global__ void __launch_bounds__(256)
                         float scale_log2, int32_t* status) {
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the chunk's K/V appended, lengths final
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    __shared__ __align__(1024) uint8_t ring[2 * kPStage];
+    extern __shared__ __align__(1024) uint8_t ring[];  // kPSmem bytes
     __shared__ int s_b, s_tile, s_bad;
+    __shared__ int tblk[kPTableWin];  // block ids of logical blocks win0 .. win0 + kPTableWin - 1
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nthr = blockDim.x;
     const int G = Hq / Hkv, h = blockIdx.y;
@@ -186,103 +199,158 @@ __global__ void __launch_bounds__(256)
 
     const uint32_t ring_u32 = smem_u32(ring);
     const int32_t* trow = block_tables + static_cast<size_t>(b) * max_blocks;
-    // 16-byte chunks of sub-tile sub into stage st: K then V, 16 rows x 16 chunks each
-    auto load = [&](int sub, int st) {
-        for (int c = tid; c < 512; c += nthr) {
-            const int which = c >> 8, rem = c & 255, row = rem >> 4, ch = rem & 15;
-            const int pos = sub * 16 + row;
-            bool ok = pos < L;
+    // The block ids come from a window of the table in shared memory, so that
+    // issuing a step's copies waits on no global load.  A step never spans more
+    // than 3 logical blocks (32 keys, blocks of >= 16), so the window is moved
+    // when the step's blocks would run past it.
+    const int nblk_used = plast / BS + 1;
+    int win0 = -kPTableWin;
+    auto ensure_window = [&](int pr) {  // called by every thread with the same pr
+        const int first = pr * 32 / BS, last = min(nblk_used - 1, (pr * 32 + 31) / BS);
+        if (first >= win0 && last < win0 + kPTableWin) return;
+        __syncthreads();  // nobody still reads the old window
+        win0 = first;
+        for (int i = tid; i < kPTableWin; i += nthr) tblk[i] = win0 + i < nblk_used ? trow[win0 + i] : -1;
+        __syncthreads();
+    };
+    // a pair of 16-key sub-tiles (keys 32 * pr .. 32 * pr + 31) into slot st:
+    // [sub-tile 0: K | V][sub-tile 1: K | V], 16 rows x 16 chunks of 16 bytes each
+    auto load_pair = [&](int pr, int st) {
+        // thread: 16-byte column ch of rows rsel, rsel + nthr/16, ... of the 32
+        // rows (keys) of the step; K and V of a row share its block lookup
+        const int ch = tid & 15;
+        for (int row32 = tid >> 4; row32 < 32; row32 += nthr >> 4) {
+            const int half = row32 >> 4, row = row32 & 15;
+            const int pos = pr * 32 + row32;
+            bool ok = pos <= plast;  // later keys are masked for every row of the tile
             int blk = 0;
             if (ok) {
-                blk = trow[pos / BS];
+                blk = tblk[pos / BS - win0];
                 if (blk < 0 || blk >= NB) {
                     s_bad = 1;
                     ok = false;
                 }
             }
-            const __nv_bfloat16* base = which ? v_cache : k_cache;
-            const __nv_bfloat16* src =
-                ok ? base + ((static_cast<size_t>(blk) * Hkv + h) * BS + pos % BS) * kPDim + ch * 8 : base;
-            const uint32_t dst = ring_u32 + st * kPStage + which * kPTile + (ch >> 3) * kPBox + row * 128 +
+            const size_t eoff = ok ? ((static_cast<size_t>(blk) * Hkv + h) * BS + pos % BS) * kPDim + ch * 8 : 0;
+            const uint32_t dst = ring_u32 + (2 * st + half) * kPStage + (ch >> 3) * kPBox + row * 128 +
                                  (((ch & 7) ^ (row & 7)) << 4);
-            cp_async16(dst, src, ok ? 16 : 0);  // rows past the end (and bad blocks) are zero-filled
+            cp_async16(dst, k_cache + eoff, ok ? 16 : 0);  // rows past the end (and bad blocks) are zero-filled
+            cp_async16(dst + kPTile, v_cache + eoff, ok ? 16 : 0);
         }
         cp_async_commit();
     };
-    load(0, 0);
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    for (int sub = 0; sub < nsub; ++sub) {
-        if (sub + 1 < nsub) {
-            load(sub + 1, (sub + 1) & 1);
-            cp_async_wait<1>();
+    // ring of kPRing pair slots: pair p lives in slot p % kPRing; one commit
+    // group per pair (empty past the end), so that waiting for all but the
+    // kPRing - 2 newest groups means pair p has landed
+    const int npair = (nsub + 1) >> 1;
+    for (int s0 = 0; s0 < kPRing - 1; ++s0) {
+        if (s0 < npair) {
+            ensure_window(s0);
+            load_pair(s0, s0);
         } else {
-            cp_async_wait<0>();
+            cp_async_commit();
         }
-        __syncthreads();  // sub-tile sub is in shared memory for every warp
+    }
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    for (int pr = 0; pr < npair; ++pr) {
+        cp_async_wait<kPRing - 2>();
+        __syncthreads();  // pair pr is in shared memory for every warp, and every
+                          // warp is done with pair pr - 1, whose slot is refilled next
+        if (pr + kPRing - 1 < npair) {
+            ensure_window(pr + kPRing - 1);
+            load_pair(pr + kPRing - 1, (pr + kPRing - 1) % kPRing);
+        } else {
+            cp_async_commit();
+        }
         if (warp < G) {
-            const uint32_t kb = ring_u32 + (sub & 1) * kPStage, vb = kb + kPTile;
-            float s[2][4];
+            const uint32_t k0 = ring_u32 + (2 * (pr % kPRing)) * kPStage, k1 = k0 + kPStage;
+            // ---- S = Q K^T for 32 keys: four independent n-tiles of 8
+            float s[4][4];
 #pragma unroll
-            for (int t = 0; t < 2; ++t) s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
+            for (int t = 0; t < 4; ++t) s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const int row = (mi >> 1) * 8 + rr;
                 const int dc = kk * 2 + (mi & 1);
-                const uint32_t addr = kb + static_cast<uint32_t>(dc >> 3) * kPBox + static_cast<uint32_t>(row) * 128u +
-                                      (static_cast<uint32_t>((dc & 7) ^ (row & 7)) << 4);
-                uint32_t b0, b1, b2, b3;
-                ldmatrix_x4(b0, b1, b2, b3, addr);
+                const uint32_t off = static_cast<uint32_t>(dc >> 3) * kPBox + static_cast<uint32_t>(row) * 128u +
+                                     (static_cast<uint32_t>((dc & 7) ^ (row & 7)) << 4);
+                uint32_t b0, b1, b2, b3, c0, c1, c2, c3;
+                ldmatrix_x4(b0, b1, b2, b3, k0 + off);
+                ldmatrix_x4(c0, c1, c2, c3, k1 + off);
                 mma_bf16_16816(s[0], qa[kk], b0, b1);
                 mma_bf16_16816(s[1], qa[kk], b2, b3);
+                mma_bf16_16816(s[2], qa[kk], c0, c1);
+                mma_bf16_16816(s[3], qa[kk], c2, c3);
             }
-            // causal mask: key position <= the row's position
+            // causal mask: key position <= the row's position (only steps that
+            // reach past the tile's first position need it)
+            if (pr * 32 + 31 > p0) {
 #pragma unroll
-            for (int t = 0; t < 2; ++t)
+                for (int t = 0; t < 4; ++t)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int kp = sub * 16 + t * 8 + 2 * r + (e & 1);
-                    const int rp = e < 2 ? rpos0 : rpos1;
-                    s[t][e] = kp <= rp ? s[t][e] * scale_log2 : -INFINITY;
-                }
-            float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
-            float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+                    for (int e = 0; e < 4; ++e) {
+                        const int kp = pr * 32 + t * 8 + 2 * r + (e & 1);
+                        const int rp = e < 2 ? rpos0 : rpos1;
+                        s[t][e] = kp <= rp ? s[t][e] * scale_log2 : -INFINITY;
+                    }
+            } else {
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) s[t][e] *= scale_log2;
+            }
+            float mx0 = fmaxf(fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1])),
+                              fmaxf(fmaxf(s[2][0], s[2][1]), fmaxf(s[3][0], s[3][1])));
+            float mx1 = fmaxf(fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3])),
+                              fmaxf(fmaxf(s[2][2], s[2][3]), fmaxf(s[3][2], s[3][3])));
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
             const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
             const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
-            const float a0 = exp2f(m0 - mu0), a1 = exp2f(m1 - mu1);
+            const float a0 = ex2a(m0 - mu0), a1 = ex2a(m1 - mu1);
             m0 = mn0;
             m1 = mn1;
-            uint32_t pa[4];
-            pa[0] = pack_bf16x2(exp2f(s[0][0] - mu0), exp2f(s[0][1] - mu0));
-            pa[2] = pack_bf16x2(exp2f(s[1][0] - mu0), exp2f(s[1][1] - mu0));
-            pa[1] = pack_bf16x2(exp2f(s[0][2] - mu1), exp2f(s[0][3] - mu1));
-            pa[3] = pack_bf16x2(exp2f(s[1][2] - mu1), exp2f(s[1][3] - mu1));
-            l0 = l0 * a0 + ((bf16_lo(pa[0]) + bf16_hi(pa[0])) + (bf16_lo(pa[2]) + bf16_hi(pa[2])));
-            l1 = l1 * a1 + ((bf16_lo(pa[1]) + bf16_hi(pa[1])) + (bf16_lo(pa[3]) + bf16_hi(pa[3])));
+            uint32_t pa[2][4];  // P for keys 0..15 and 16..31, A-fragment layout
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                O[c][0] *= a0;
-                O[c][1] *= a0;
-                O[c][2] *= a1;
-                O[c][3] *= a1;
+            for (int hh = 0; hh < 2; ++hh) {
+                pa[hh][0] = pack_bf16x2(ex2a(s[2 * hh][0] - mu0), ex2a(s[2 * hh][1] - mu0));
+                pa[hh][2] = pack_bf16x2(ex2a(s[2 * hh + 1][0] - mu0), ex2a(s[2 * hh + 1][1] - mu0));
+                pa[hh][1] = pack_bf16x2(ex2a(s[2 * hh][2] - mu1), ex2a(s[2 * hh][3] - mu1));
+                pa[hh][3] = pack_bf16x2(ex2a(s[2 * hh + 1][2] - mu1), ex2a(s[2 * hh + 1][3] - mu1));
             }
+            l0 = l0 * a0 + (((bf16_lo(pa[0][0]) + bf16_hi(pa[0][0])) + (bf16_lo(pa[0][2]) + bf16_hi(pa[0][2]))) +
+                            ((bf16_lo(pa[1][0]) + bf16_hi(pa[1][0])) + (bf16_lo(pa[1][2]) + bf16_hi(pa[1][2]))));
+            l1 = l1 * a1 + (((bf16_lo(pa[0][1]) + bf16_hi(pa[0][1])) + (bf16_lo(pa[0][3]) + bf16_hi(pa[0][3]))) +
+                            ((bf16_lo(pa[1][1]) + bf16_hi(pa[1][1])) + (bf16_lo(pa[1][3]) + bf16_hi(pa[1][3]))));
+            if (a0 != 1.f || a1 != 1.f) {  // the running maximum moved: rescale
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    O[c][0] *= a0;
+                    O[c][1] *= a0;
+                    O[c][2] *= a1;
+                    O[c][3] *= a1;
+                }
+            }
+            // ---- O += P V over the 32 keys
 #pragma unroll
             for (int dp = 0; dp < 8; ++dp) {
                 const int row = (mi & 1) * 8 + rr;
                 const int dc = dp * 2 + (mi >> 1);
-                const uint32_t addr = vb + static_cast<uint32_t>(dc >> 3) * kPBox + static_cast<uint32_t>(row) * 128u +
-                                      (static_cast<uint32_t>((dc & 7) ^ (row & 7)) << 4);
-                uint32_t v0, v1, v2, v3;
-                ldmatrix_x4_trans(v0, v1, v2, v3, addr);
-                mma_bf16_16816(O[2 * dp], pa, v0, v1);
-                mma_bf16_16816(O[2 * dp + 1], pa, v2, v3);
+                const uint32_t off = kPTile + static_cast<uint32_t>(dc >> 3) * kPBox + static_cast<uint32_t>(row) * 128u +
+                                     (static_cast<uint32_t>((dc & 7) ^ (row & 7)) << 4);
+                uint32_t v0, v1, v2, v3, w0, w1, w2, w3;
+                ldmatrix_x4_trans(v0, v1, v2, v3, k0 + off);
+                ldmatrix_x4_trans(w0, w1, w2, w3, k1 + off);
+                mma_bf16_16816(O[2 * dp], pa[0], v0, v1);
+                mma_bf16_16816(O[2 * dp + 1], pa[0], v2, v3);
+                mma_bf16_16816(O[2 * dp], pa[1], w0, w1);
+                mma_bf16_16816(O[2 * dp + 1], pa[1], w2, w3);
             }
         }
-        __syncthreads();  // every warp is done with this stage before it is refilled
     }
+    cp_async_wait<0>();
     if (warp >= G) return;
     float t0l = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
     t0l += __shfl_xor_sync(0xffffffffu, t0l, 2);
@@ -341,7 +409,10 @@ cudaError_t launch_prefill_attention(void* out, const void* q, const void* k_cac
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(Hkv), 1);
     cfg.blockDim = dim3(static_cast<unsigned>(32 * (Hq / Hkv)), 1, 1);
+    cfg.dynamicSmemBytes = kPSmem;
     cfg.stream = stream;
+    cudaError_t aerr = cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmem);
+    if (aerr != cudaSuccess) return aerr;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;

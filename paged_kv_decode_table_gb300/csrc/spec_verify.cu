@@ -13,13 +13,15 @@
 //
 // p_i = softmax(z_target[i] / T) and q_i = softmax(z_draft[i] / T) over finite
 // logits, represented as in the sampler: fixed-point masses floor(w * 2^40) of
-// w = 2^((z - zmax) log2(e) / T), with exact integer row sums.  Uniform
+// w = 2^((z - zmax) log2(e) / T).  The row sums for the tests come from one
+// pass (relative error ~1e-7); the final draw sums its own masses exactly.  Uniform
 // number j of a request is Philox4x64-10 word 0 at counter (offset, j, 0, 0)
 // under key (seed, 0), top 53 bits: j = i + 1 for the test at draft position i,
 // j = 0 for the final draw, which walks token ids in ascending order.
 //
-// Two kernels: row statistics (max, lowest argmax, mass sum) with one CTA per
-// logits row; then one CTA per request for the tests (one thread per draft
+// Two kernels: row statistics (max, lowest argmax, mass sum in one pass over
+// the row, the sum kept relative to a running maximum) with one CTA per logits
+// row; then one CTA per request for the tests (one thread per draft
 // position) and the final draw (chunked inverse CDF over the vocabulary).
 #include <limits.h>
 #include <math.h>
@@ -38,7 +40,7 @@ struct RowStat {   // 32 bytes per logits row
     int argmax;    // lowest id holding zmax (-1: no finite logit)
     int bad;       // NaN or +inf present
     int pad;
-    unsigned long long S;  // sum of floor(2^40 * 2^((z - zmax) c2)) (T > 0)
+    unsigned long long S;  // ~ sum of floor(2^40 * 2^((z - zmax) c2)) (T > 0), relative error ~1e-7
     unsigned long long pad2;
 };
 
@@ -52,13 +54,13 @@ __device__ __forceinline__ float4 load4_row(const float* row, int e, int n, bool
     return q;
 }
 
-__device__ __forceinline__ uint64_t block_sum_u64(uint64_t v, unsigned long long* red) {
+__device__ __forceinline__ double block_sum_f64(double v, double* red) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     if (lane == 0) red[warp] = v;
     __syncthreads();
-    uint64_t t = 0;
+    double t = 0.0;
     for (int w = 0; w < kVW; ++w) t += red[w];
     __syncthreads();
     return t;
@@ -73,29 +75,56 @@ __global__ void __launch_bounds__(kVT)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ float smax[kVW];
     __shared__ int sid[kVW], sbad[kVW];
-    __shared__ unsigned long long red[kVW];
+    __shared__ double dred[kVW];
     const int rows = 2 * gamma + 1;
     const int b = blockIdx.x / rows, r = blockIdx.x - (blockIdx.x / rows) * rows;
     const float* row = r <= gamma ? target + (static_cast<size_t>(b) * (gamma + 1) + r) * V
                                   : draft + (static_cast<size_t>(b) * gamma + (r - gamma - 1)) * V;
     const bool al = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(row) & 15u) == 0);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float T = temperature[b];
+    const bool sum = T > 0.f;
+    const float c2 = sum ? fminf(1.4426950408889634f / T, 1.0e30f) : 0.f;
+    // one pass: running maximum (lowest id among equals) and the fixed-point
+    // mass sum relative to it.  The thread takes its logits in batches of 32;
+    // a batch's maximum is found first, the sum so far is rescaled to it if it
+    // is larger (at most once per batch), then the batch's masses are added.
+    constexpr int kU = 8;  // float4 slots per batch
     float m = -INFINITY;
     int id = INT_MAX;
     int bad = 0;
-    for (int e = 4 * tid; e < V; e += 4 * kVT) {
-        const float4 q = load4_row(row, e, V, al);
-        const float zz[4] = {q.x, q.y, q.z, q.w};
+    uint64_t acc = 0;
+    for (int e0 = 4 * tid; e0 < V; e0 += 4 * kVT * kU) {
+        float4 q[kU];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float z = zz[j];
-            bad |= (z < INFINITY) ? 0 : 1;  // NaN or +inf (slots past V read -inf)
-            if (z > m) {                     // ids grow within a thread: first max wins
-                m = z;
-                id = e + j;
+        for (int u = 0; u < kU; ++u) q[u] = load4_row(row, e0 + 4 * kVT * u, V, al);
+        float bm = -INFINITY;
+        int bid = INT_MAX;
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const float zz[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                bad |= (zz[j] < INFINITY) ? 0 : 1;  // NaN or +inf (slots past V read -inf)
+                if (zz[j] > bm) {                   // ids grow within a batch: first max wins
+                    bm = zz[j];
+                    bid = e0 + 4 * kVT * u + j;
+                }
             }
         }
+        if (bm > m) {  // earlier batches hold lower ids, so an equal maximum keeps id
+            if (sum && acc)
+                acc = static_cast<uint64_t>(static_cast<double>(acc) * static_cast<double>(hw_exp2((m - bm) * c2)));
+            m = bm;
+            id = bid;
+        }
+        if (sum && m > -INFINITY) {
+#pragma unroll
+            for (int u = 0; u < kU; ++u)
+                acc += mass(q[u].x, m, c2) + mass(q[u].y, m, c2) + mass(q[u].z, m, c2) + mass(q[u].w, m, c2);
+        }
     }
+    const float mt = m;  // this thread's maximum, the reference of acc
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
@@ -122,16 +151,11 @@ __global__ void __launch_bounds__(kVT)
         }
         bad |= sbad[w];
     }
-    const float T = temperature[b];
     uint64_t S = 0;
-    if (!bad && m > -INFINITY && T > 0.f) {
-        const float c2 = fminf(1.4426950408889634f / T, 1.0e30f);
-        uint64_t s = 0;
-        for (int e = 4 * tid; e < V; e += 4 * kVT) {
-            const float4 q = load4_row(row, e, V, al);
-            s += mass(q.x, m, c2) + mass(q.y, m, c2) + mass(q.z, m, c2) + mass(q.w, m, c2);
-        }
-        S = block_sum_u64(s, red);
+    if (!bad && m > -INFINITY && sum) {
+        // each thread's sum moved to the row maximum (relative error ~1e-7)
+        const double part = acc ? static_cast<double>(acc) * static_cast<double>(hw_exp2((mt - m) * c2)) : 0.0;
+        S = static_cast<uint64_t>(block_sum_f64(part, dred) + 0.5);
     }
     if (tid == 0) {
         RowStat st;
