@@ -88,8 +88,8 @@ __global__ void __launch_bounds__(kPAppendWarps * 32)
 constexpr int kPBox = 16 * 128;      // one 64-dim half of a 16-row sub-tile, 128 B per row
 constexpr int kPTile = 2 * kPBox;    // a K (or V) sub-tile: 16 rows x 128 dims bf16
 constexpr int kPStage = 2 * kPTile;  // K and V
-constexpr int kPRing = 4;            // pair slots (2 sub-tiles each): three pairs in flight while one is used
-constexpr int kPSmem = kPRing * 2 * kPStage;  // 64 KB of dynamic shared memory
+constexpr int kPRing = 2;            // pair slots (2 sub-tiles each): one pair in flight while one is used
+constexpr int kPRingBytes = kPRing * 2 * kPStage;  // 32 KB, then each warp's 4 KB query tile
 constexpr int kPTableWin = 512;  // block-table entries kept in shared memory at a time
 
 // 2^x by the hardware's approximate base-2 exponential (P and the rescale
@@ -110,7 +110,8 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-__global__ void __launch_bounds__(256)
+template <int kThreads, int kMinBlocks>
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
     prefill_attn_kernel(const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ out,
                         const __nv_bfloat16* __restrict__ k_cache, const __nv_bfloat16* __restrict__ v_cache,
                         const int32_t* __restrict__ block_tables, int max_blocks, const int32_t* __restrict__ seq_lens,
@@ -118,7 +119,7 @@ __global__ void __launch_bounds__(256)
                         float scale_log2, int32_t* status) {
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the chunk's K/V appended, lengths final
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    extern __shared__ __align__(1024) uint8_t ring[];  // kPSmem bytes
+    extern __shared__ __align__(1024) uint8_t ring[];  // kPRingBytes + 4 KB per warp
     __shared__ int s_b, s_tile, s_bad;
     __shared__ int tblk[kPTableWin];  // block ids of logical blocks win0 .. win0 + kPTableWin - 1
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -184,19 +185,17 @@ __global__ void __launch_bounds__(256)
     const int nsub = plast / 16 + 1;   // 16-key sub-tiles covering positions 0 .. plast
     const int rpos0 = g < nt ? p0 + g : plast, rpos1 = g + 8 < nt ? p0 + g + 8 : plast;
 
-    // query fragments: rows = tokens g and g + 8 of the tile, head qh
-    uint32_t qa[8][4];
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-        const int c0 = kk * 16 + 2 * r;
-        const __nv_bfloat16* q0 = q + (static_cast<size_t>(t0 + g) * Hq + qh) * kPDim;
-        const __nv_bfloat16* q1 = q + (static_cast<size_t>(t0 + g + 8) * Hq + qh) * kPDim;
-        qa[kk][0] = g < nt ? *reinterpret_cast<const uint32_t*>(q0 + c0) : 0u;
-        qa[kk][2] = g < nt ? *reinterpret_cast<const uint32_t*>(q0 + c0 + 8) : 0u;
-        qa[kk][1] = g + 8 < nt ? *reinterpret_cast<const uint32_t*>(q1 + c0) : 0u;
-        qa[kk][3] = g + 8 < nt ? *reinterpret_cast<const uint32_t*>(q1 + c0 + 8) : 0u;
+    // this warp's query tile (16 tokens x 128 dims of head qh) in shared memory,
+    // 128-byte-swizzled like the K tiles; rows past the chunk are zero
+    uint8_t* qtile = ring + kPRingBytes + warp * 4096;
+    for (int c = lane; c < 256; c += 32) {
+        const int row = c >> 4, ch = c & 15;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (row < nt) v = __ldg(reinterpret_cast<const uint4*>(q + (static_cast<size_t>(t0 + row) * Hq + qh) * kPDim) + ch);
+        *reinterpret_cast<uint4*>(qtile + (ch >> 3) * kPBox + row * 128 + (((ch & 7) ^ (row & 7)) << 4)) = v;
     }
-
+    __syncwarp();
+    const uint32_t qtile_u32 = smem_u32(qtile);
     const uint32_t ring_u32 = smem_u32(ring);
     const int32_t* trow = block_tables + static_cast<size_t>(b) * max_blocks;
     // The block ids come from a window of the table in shared memory, so that
@@ -274,13 +273,19 @@ __global__ void __launch_bounds__(256)
                 const int dc = kk * 2 + (mi & 1);
                 const uint32_t off = static_cast<uint32_t>(dc >> 3) * kPBox + static_cast<uint32_t>(row) * 128u +
                                      (static_cast<uint32_t>((dc & 7) ^ (row & 7)) << 4);
+                // A fragments of the query tile: lane l reads row l % 16, 16-byte column 2 kk + l / 16
+                const int qrow = lane & 15, qdc = kk * 2 + (lane >> 4);
+                uint32_t qa[4];
+                ldmatrix_x4(qa[0], qa[1], qa[2], qa[3],
+                            qtile_u32 + static_cast<uint32_t>(qdc >> 3) * kPBox + static_cast<uint32_t>(qrow) * 128u +
+                                (static_cast<uint32_t>((qdc & 7) ^ (qrow & 7)) << 4));
                 uint32_t b0, b1, b2, b3, c0, c1, c2, c3;
                 ldmatrix_x4(b0, b1, b2, b3, k0 + off);
                 ldmatrix_x4(c0, c1, c2, c3, k1 + off);
-                mma_bf16_16816(s[0], qa[kk], b0, b1);
-                mma_bf16_16816(s[1], qa[kk], b2, b3);
-                mma_bf16_16816(s[2], qa[kk], c0, c1);
-                mma_bf16_16816(s[3], qa[kk], c2, c3);
+                mma_bf16_16816(s[0], qa, b0, b1);
+                mma_bf16_16816(s[1], qa, b2, b3);
+                mma_bf16_16816(s[2], qa, c0, c1);
+                mma_bf16_16816(s[3], qa, c2, c3);
             }
             // causal mask: key position <= the row's position (only steps that
             // reach past the tile's first position need it)
@@ -409,9 +414,13 @@ cudaError_t launch_prefill_attention(void* out, const void* q, const void* k_cac
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(Hkv), 1);
     cfg.blockDim = dim3(static_cast<unsigned>(32 * (Hq / Hkv)), 1, 1);
-    cfg.dynamicSmemBytes = kPSmem;
+    const int G = Hq / Hkv;
+    const int smem = kPRingBytes + 4096 * G;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaError_t aerr = cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmem);
+    // up to 4 query heads per KV head: 128-thread CTAs, four per SM; else 256 threads, two per SM
+    auto kern = G <= 4 ? prefill_attn_kernel<128, 4> : prefill_attn_kernel<256, 2>;
+    cudaError_t aerr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (aerr != cudaSuccess) return aerr;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -419,7 +428,7 @@ cudaError_t launch_prefill_attention(void* out, const void* q, const void* k_cac
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const float scale_log2 = scale * 1.4426950408889634f;
-    cudaError_t err = cudaLaunchKernelEx(&cfg, prefill_attn_kernel, static_cast<const __nv_bfloat16*>(q),
+    cudaError_t err = cudaLaunchKernelEx(&cfg, kern, static_cast<const __nv_bfloat16*>(q),
                                          static_cast<__nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(k_cache),
                                          static_cast<const __nv_bfloat16*>(v_cache), block_tables, max_blocks,
                                          seq_lens, q_start, B, Hq, Hkv, BS, NB, scale_log2, status);

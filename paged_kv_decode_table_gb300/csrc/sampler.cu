@@ -48,6 +48,7 @@ constexpr int kListCap = 2048;     // candidate list capacity (rank 0, gathered)
 constexpr int kTopkBins = 512;     // bins of the bounded top-k histogram
 constexpr int kLocBase = 1024;     // hist[kLocBase..kHistBins): this CTA's top-k candidates
 constexpr int kLocCap = kHistBins - kLocBase;
+constexpr int kRegTopk = 256;      // largest top-k taken from the first pass's thread maxima
 constexpr int kMaxCluster = 8;
 constexpr int kSliceSmemMax = 24576;  // floats of a row slice kept in shared memory
 
@@ -63,8 +64,10 @@ struct __align__(16) SampSmem {
     uint64_t bar[4];        // one per chunk of the slice load
     unsigned int gcount;    // rank 0: candidates gathered so far
     int imin;
-    unsigned int lcount;    // this CTA's top-k candidates (sort keys in hist[kLocBase..])
+    unsigned int lcount;    // this CTA's top-k candidates (sort keys in hist[kLocBase..]), or its rescanning threads
     int pad_;
+    unsigned long long u53;  // the row's uniform draw, top 53 bits of Philox word 0
+    unsigned long long pad2_;
 };
 // The row slice follows the struct in shared memory; TMA bulk copies and the
 // 16-byte vector loads need it 16-byte aligned.
@@ -428,13 +431,13 @@ __device__ __forceinline__ void sum_remote_f4(cg::cluster_group& cl, float* h, i
 // floor(u * S_p), S_p = total kept mass.  The CTA that holds it writes the token.
 // The slice is cut into chunks of 128 * cpw consecutive logits (cpw chosen so
 // that there are at most kHistBins chunks); warp w sums the kept masses of
-// chunks w, w + 16, ... with coalesced 16-byte loads (lane l takes logits
-// 4l..4l+3 of each 128), the chunk sums are scanned in shared memory (hist is
-// free here), the CTA totals are exchanged, and in the CTA that holds the
-// draw one warp walks the single chunk that holds it.
+// chunks w, w + 16, ..., four chunks at a time, with coalesced 16-byte loads
+// (lane l takes logits 4l..4l+3 of each 128), the chunk sums are scanned in
+// shared memory (hist is free here), the CTA totals are exchanged, and in the
+// CTA that holds the draw one warp walks the single chunk that holds it.
 // Ends with this CTA's arrival on the cluster barrier; the caller waits on it.
-__device__ void draw_pass(Ctx& c, const View& v, const Keep& kp, bool vec, float zmax, float c2, uint64_t seed,
-                          uint64_t offset, int32_t* tok_out) {
+__device__ void draw_pass(Ctx& c, const View& v, const Keep& kp, bool vec, float zmax, float c2,
+                          int32_t* tok_out) {
     SampSmem* sm = c.sm;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nvec = (v.n + 3) & ~3;
@@ -447,25 +450,35 @@ __device__ void draw_pass(Ctx& c, const View& v, const Keep& kp, bool vec, float
         const uint64_t m = (!filt || kp.keep_f(z, v.idbase + e)) ? mass(z, zmax, c2) : 0ull;
         return m >= kp.mth ? m : 0ull;
     };
-    auto lane_sum = [&](int e) -> uint64_t {  // this lane's 4 logits at slot e (may lie past the end)
-        if (e >= nvec) return 0ull;
-        const float4 q = load4(v, e, vec);
-        return kmass(q.x, e) + kmass(q.y, e + 1) + kmass(q.z, e + 2) + kmass(q.w, e + 3);
-    };
+    // warp w takes chunks w, w + 16, w + 32, w + 48 together (four loads in
+    // flight per lane), then w + 64, ...; slots past the end read as -inf (mass 0)
+    constexpr int kDU = 4;
     unsigned long long* ctot = sm->hist;
-    for (int ch = warp; ch < nch; ch += kSW) {
-        const int e0 = ch * csz + 4 * lane;
-        uint64_t w = 0;
-        int k = 0;
-        for (; k + 4 <= cpw; k += 4) {
-            const uint64_t a0 = lane_sum(e0 + 128 * k), a1 = lane_sum(e0 + 128 * (k + 1));
-            const uint64_t a2 = lane_sum(e0 + 128 * (k + 2)), a3 = lane_sum(e0 + 128 * (k + 3));
-            w += a0 + a1 + a2 + a3;
-        }
-        for (; k < cpw; ++k) w += lane_sum(e0 + 128 * k);
+    for (int cb = warp; cb < nch; cb += kDU * kSW) {
+        uint64_t w[kDU];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
-        if (lane == 0) ctot[ch] = w;
+        for (int u = 0; u < kDU; ++u) w[u] = 0;
+        for (int k = 0; k < cpw; ++k) {
+            float4 q[kDU];
+#pragma unroll
+            for (int u = 0; u < kDU; ++u) {
+                const int e = (cb + u * kSW) * csz + 128 * k + 4 * lane;
+                q[u] = e < nvec ? load4(v, e, vec) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
+#pragma unroll
+            for (int u = 0; u < kDU; ++u) {
+                const int e = (cb + u * kSW) * csz + 128 * k + 4 * lane;
+                w[u] += kmass(q[u].x, e) + kmass(q[u].y, e + 1) + kmass(q[u].z, e + 2) + kmass(q[u].w, e + 3);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int u = 0; u < kDU; ++u) w[u] += __shfl_xor_sync(0xffffffffu, w[u], o);
+        if (lane == 0)
+#pragma unroll
+            for (int u = 0; u < kDU; ++u)
+                if (cb + u * kSW < nch) ctot[cb + u * kSW] = w[u];
     }
     __syncthreads();
     // exclusive scan of the chunk sums, four consecutive chunks per thread
@@ -492,7 +505,7 @@ __device__ void draw_pass(Ctx& c, const View& v, const Keep& kp, bool vec, float
         if (j < c.rank) pre += sm->gath[j][0];
     }
     cluster_arrive();  // all remote reads of this CTA are done
-    const uint64_t u53 = philox_word0(seed, offset) >> 11;
+    const uint64_t u53 = sm->u53;
     const uint64_t X = static_cast<uint64_t>((static_cast<unsigned __int128>(u53) * Sp) >> 53);  // floor(u*Sp) < Sp
     if (!(pre <= X && X < pre + tot)) return;  // the draw lies in another CTA
     const uint64_t Xr = X - pre;
@@ -545,10 +558,10 @@ __device__ void draw_pass(Ctx& c, const View& v, const Keep& kp, bool vec, float
 
 // ------------------------------------------------------------------ rank-0 finish on a gathered list
 // The list holds n distinct candidate sort keys, a superset of the top-kk set.
-// Small lists (n <= 128): one warp, four candidates per lane in registers.
-// Ranks by comparison with every candidate; masses are scattered to their rank
-// (top-p prefix) and then to their id order among the kept tokens (draw), each
-// followed by a warp scan; only __syncwarp, no block barriers.
+// Small lists (n <= 128): four candidates per lane of warp 0.  Ranks by
+// comparison with every candidate (the comparisons shared out over the CTA's
+// warps); masses are scattered to their rank (top-p prefix) and then to their
+// id order among the kept tokens (draw), each followed by a warp scan.
 constexpr int kSmallList = 128;
 
 // Exclusive scan of buf[0..128) (4 consecutive entries per lane) in place; returns the total.
@@ -578,79 +591,109 @@ __device__ __forceinline__ uint64_t warp_scan128(unsigned long long* buf) {
 }
 
 __device__ void solo_finish_small(SampSmem* sm, int n, int kk, float pp, uint64_t mth, float zmax, float c2,
-                                  uint64_t seed, uint64_t offset, int32_t* tok_out) {
-    if (threadIdx.x >= 32) return;
-    const int lane = threadIdx.x;
+                                  int32_t* tok_out) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned long long* a = sm->list;
-    unsigned long long* buf = sm->hist;                                      // [128] scratch masses / prefixes
-    unsigned int* kf = reinterpret_cast<unsigned int*>(sm->hist + 128);      // [128] kept flags
-    unsigned int* ids = kf + 128;                                            // [128] token ids
+    unsigned long long* buf = sm->hist;                                  // [128] scratch masses / prefixes
+    unsigned int* kf = reinterpret_cast<unsigned int*>(sm->hist + 128);  // [128] kept flags
+    unsigned int* ids = kf + 128;                                        // [128] token ids
+    unsigned int* rk = ids + 128;                                        // [128] ranks in (z desc, id asc)
+    unsigned int* idr = rk + 128;                                        // [128] ranks among kept ids
+    // the two all-pairs counts are split by j over the CTA's warps (warp w
+    // takes j in [w n / 16, (w + 1) n / 16)) and summed with shared atomics;
+    // the rest runs on warp 0.  Candidate i = lane + 32 q.
+    const int j0 = warp * n / kSW, j1 = (warp + 1) * n / kSW;
+    if (tid < 128) {
+        rk[tid] = 0u;
+        idr[tid] = 0u;
+    }
     unsigned long long key[4];
-    unsigned int rank[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
     for (int q = 0; q < 4; ++q) key[q] = lane + 32 * q < n ? a[lane + 32 * q] : 0ull;
-    for (int j = 0; j < n; ++j) {
-        const unsigned long long kj = a[j];
+    __syncthreads();
+    {
+        unsigned int r[4] = {0u, 0u, 0u, 0u};
+#pragma unroll 4
+        for (int j = j0; j < j1; ++j) {
+            const unsigned long long kj = a[j];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) rank[q] += kj > key[q] ? 1u : 0u;
-    }
-    uint64_t W[4];
-    bool in_k[4], kept[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const bool valid = lane + 32 * q < n;
-        W[q] = valid ? mass(key_float(static_cast<uint32_t>(key[q] >> 32)), zmax, c2) : 0ull;
-        in_k[q] = valid && rank[q] < static_cast<unsigned int>(kk);
-        kept[q] = in_k[q];
-    }
-    // top-p on the top-k set in rank order
-#pragma unroll
-    for (int q = 0; q < 4; ++q) buf[4 * lane + q] = 0ull;
-    __syncwarp();
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-        if (in_k[q]) buf[rank[q]] = W[q];
-    __syncwarp();
-    const uint64_t sk = warp_scan128(buf);
-    if (pp < 1.f) {
-        const uint64_t target = ceil_mul_p(pp, sk);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) kept[q] = in_k[q] && buf[rank[q]] < target;  // prefix before it < target
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) kept[q] = kept[q] && W[q] >= mth;  // min-p, after top-p
-    __syncwarp();
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int i = lane + 32 * q;
-        if (i < n) {
-            kf[i] = kept[q] ? 1u : 0u;
-            ids[i] = static_cast<unsigned int>(sort_key_id(key[q]));
+            for (int q = 0; q < 4; ++q) r[q] += kj > key[q] ? 1u : 0u;
         }
-        buf[4 * lane + q] = 0ull;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (r[q]) atomicAdd(&rk[lane + 32 * q], r[q]);
     }
-    __syncwarp();
+    __syncthreads();
+    uint64_t W[4];
+    bool kept[4];
+    if (warp == 0) {
+        unsigned int rank[4];
+        bool in_k[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const bool valid = lane + 32 * q < n;
+            rank[q] = rk[lane + 32 * q];
+            W[q] = valid ? mass(key_float(static_cast<uint32_t>(key[q] >> 32)), zmax, c2) : 0ull;
+            in_k[q] = valid && rank[q] < static_cast<unsigned int>(kk);
+            kept[q] = in_k[q];
+        }
+        // top-p on the top-k set in rank order
+#pragma unroll
+        for (int q = 0; q < 4; ++q) buf[4 * lane + q] = 0ull;
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (in_k[q]) buf[rank[q]] = W[q];
+        __syncwarp();
+        const uint64_t sk = warp_scan128(buf);
+        if (pp < 1.f) {
+            const uint64_t target = ceil_mul_p(pp, sk);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) kept[q] = in_k[q] && buf[rank[q]] < target;  // prefix before it < target
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) kept[q] = kept[q] && W[q] >= mth;  // min-p, after top-p
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int i = lane + 32 * q;
+            if (i < n) {
+                kf[i] = kept[q] ? 1u : 0u;
+                ids[i] = static_cast<unsigned int>(sort_key_id(key[q]));
+            }
+            buf[4 * lane + q] = 0ull;
+        }
+    }
+    __syncthreads();
     // draw: kept tokens in id order
-    unsigned int idr[4] = {0u, 0u, 0u, 0u};
     unsigned int myid[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) myid[q] = static_cast<unsigned int>(sort_key_id(key[q]));
-    for (int j = 0; j < n; ++j) {
-        const unsigned int fj = kf[j], idj = ids[j];
+    {
+        unsigned int r[4] = {0u, 0u, 0u, 0u};
+#pragma unroll 4
+        for (int j = j0; j < j1; ++j) {
+            const unsigned int fj = kf[j], idj = ids[j];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) idr[q] += (fj && idj < myid[q]) ? 1u : 0u;
+            for (int q = 0; q < 4; ++q) r[q] += (fj && idj < myid[q]) ? 1u : 0u;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (r[q] && lane + 32 * q < n) atomicAdd(&idr[lane + 32 * q], r[q]);
     }
+    __syncthreads();
+    if (warp != 0) return;
 #pragma unroll
     for (int q = 0; q < 4; ++q)
-        if (kept[q]) buf[idr[q]] = W[q];
+        if (kept[q]) buf[idr[lane + 32 * q]] = W[q];
     __syncwarp();
     const uint64_t Sp = warp_scan128(buf);
-    const uint64_t u53 = philox_word0(seed, offset) >> 11;
+    const uint64_t u53 = sm->u53;
     const uint64_t X = static_cast<uint64_t>((static_cast<unsigned __int128>(u53) * Sp) >> 53);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         if (kept[q] && W[q] > 0) {
-            const uint64_t before = buf[idr[q]];
+            const uint64_t before = buf[idr[lane + 32 * q]];
             if (before <= X && X < before + W[q]) *tok_out = static_cast<int>(myid[q]);
         }
     }
@@ -659,9 +702,9 @@ __device__ void solo_finish_small(SampSmem* sm, int n, int kk, float pp, uint64_
 // Larger lists: bitonic sort by (z desc, id asc), keep the first kk, apply
 // top-p exactly, re-sort the kept tokens by id and draw.
 __device__ void solo_finish(SampSmem* sm, int n, int kk, float pp, uint64_t mth, float zmax, float c2,
-                            uint64_t seed, uint64_t offset, int32_t* tok_out) {
+                            int32_t* tok_out) {
     if (n <= kSmallList) {
-        solo_finish_small(sm, n, kk, pp, mth, zmax, c2, seed, offset, tok_out);
+        solo_finish_small(sm, n, kk, pp, mth, zmax, c2, tok_out);
         return;
     }
     const int tid = threadIdx.x;
@@ -715,7 +758,7 @@ __device__ void solo_finish(SampSmem* sm, int n, int kk, float pp, uint64_t mth,
     for (int j = b0; j < b1; ++j) w += a[j] & wmask;
     uint64_t Sp;
     const uint64_t ex = block_excl_scan_u64(w, sm->wsum, Sp);
-    const uint64_t u53 = philox_word0(seed, offset) >> 11;
+    const uint64_t u53 = sm->u53;
     const uint64_t X = static_cast<uint64_t>((static_cast<unsigned __int128>(u53) * Sp) >> 53);
     if (ex <= X && X < ex + w) {
         uint64_t cum = ex;
@@ -731,7 +774,7 @@ __device__ void solo_finish(SampSmem* sm, int n, int kk, float pp, uint64_t mth,
 
 // ------------------------------------------------------------------ exact fallback (whole cluster)
 __device__ void fallback_select_and_draw(Ctx& c, const View& v, Keep& kp, bool vec, int kk, float pp, float zmax,
-                                         float c2, uint64_t seed, uint64_t offset, int32_t* tok_out) {
+                                         float c2, int32_t* tok_out) {
     if (kk > 0) {
         kp.k_on = true;
         uint64_t target = static_cast<uint64_t>(kk), above = 0, binw = 0;
@@ -759,7 +802,7 @@ __device__ void fallback_select_and_draw(Ctx& c, const View& v, Keep& kp, bool v
         kp.zp = key_float(kp.taup);
         kp.idp = tie_select(c, v, kp, true, kp.taup, need);
     }
-    draw_pass(c, v, kp, vec, zmax, c2, seed, offset, tok_out);
+    draw_pass(c, v, kp, vec, zmax, c2, tok_out);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -819,6 +862,9 @@ __global__ void __launch_bounds__(kST, 2)
         sm->gcount = 0u;
         sm->lcount = 0u;
     }
+    // the draw's uniform depends on the row's seed and offset alone: computed
+    // here, off the critical path of the finish
+    if (tid == kST - 1) sm->u53 = philox_word0(seed, offset) >> 11;
     if (smem_slice) {
         const bool aligned = ((reinterpret_cast<uintptr_t>(grow) & 15u) == 0);
         const int nbulk = aligned ? (n & ~3) : 0;
@@ -1010,6 +1056,82 @@ __global__ void __launch_bounds__(kST, 2)
             kb.scale = (range > 0.f && sc < INFINITY) ? sc : 0.f;
         }
         const float zfloor = bounded ? kbound : -INFINITY;
+        if (!vec && bounded && kk_in <= kRegTopk) {
+            // Slice in global memory and a small k: the histogram is taken over
+            // the first pass's thread maxima (distinct logits, held in
+            // registers), so the slice is not read a second time.  Bin bk is
+            // where the maxima >= kbound first number k: the k-th largest
+            // maximum lies in bins 0..bk, hence so does every top-k member (each
+            // is >= it).  A member is its thread's maximum or belongs to a thread
+            // whose maximum is larger, so only the threads whose maximum is in
+            // bins 0..bk read their logits again and push those in bins 0..bk.
+            for (int i = tid; i < kb.nb; i += kST) cnt[i] = 0u;
+            if (tid == 0) {
+                sm->bc[0] = kb.nb - 1;
+                sm->bc[1] = 0;
+            }
+            __syncthreads();
+            if (tmax >= zfloor) atomicAdd(&cnt[kb(tmax)], 1u);
+            cluster.sync();
+            uint32_t g[4] = {0u, 0u, 0u, 0u};
+            if (tid * 4 < kb.nb) sum_remote_u4(cluster, cnt, c.nc, g);
+            const uint64_t tsum = static_cast<uint64_t>(g[0]) + g[1] + g[2] + g[3];
+            uint64_t counted;
+            const uint64_t ex = block_excl_scan_u64(tsum, sm->wsum, counted);
+            kk = kk_in;
+            if (ex < static_cast<uint64_t>(kk) && ex + tsum >= static_cast<uint64_t>(kk)) {
+                uint64_t cc = ex;
+                for (int q = 0; q < 4; ++q) {
+                    cc += g[q];
+                    if (cc >= static_cast<uint64_t>(kk)) {
+                        sm->bc[0] = static_cast<unsigned long long>(tid * 4 + q);
+                        sm->bc[1] = cc;
+                        break;
+                    }
+                }
+            }
+            __syncthreads();
+            const int bk = static_cast<int>(sm->bc[0]);
+            const bool reached = sm->bc[1] >= static_cast<unsigned long long>(kk);  // same in every CTA
+            if (reached) {
+                // the qualifying threads' slots 4 (t + kST m) are spread over the
+                // whole CTA, one 16-byte load per thread, so the rescans cost one
+                // round trip to L2 instead of one per qualifying lane of a warp
+                int* qlist = reinterpret_cast<int*>(sm->hist + kLocBase);
+                if (tmax >= zfloor && kb(tmax) <= bk) qlist[atomicAdd(&sm->lcount, 1u)] = tid;
+                __syncthreads();
+                const int nq = static_cast<int>(sm->lcount);
+                const int spt = (nvec + 4 * kST - 1) / (4 * kST);  // slots per thread
+                for (int i0 = tid - lane; i0 < nq * spt; i0 += kST) {  // warp-uniform trip count
+                    const int i = i0 + lane;
+                    int el = 0;
+                    float4 q = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                    if (i < nq * spt) {
+                        const int qi = i / spt;
+                        el = 4 * (qlist[qi] + kST * (i - qi * spt));
+                        if (el < nvec) q = load4(v, el, false);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float z = f4at(q, j);
+                        const bool pred = z > -INFINITY && z >= zfloor && kb(z) <= bk;
+                        gather_push(pred, pred ? sort_key(z, lo + el + j) : 0ull, gcount0, list0);
+                    }
+                }
+            }
+            cluster.sync();  // candidates complete in rank 0; its bins are no longer read
+            const unsigned int ng = *gcount0;
+            cluster_arrive();  // rank 0 stays until every CTA has read its count
+            if (reached && ng <= static_cast<unsigned int>(kListCap)) {
+                if (c.rank == 0) solo_finish(sm, static_cast<int>(ng), kk, pp, kp.mth, zmax, c2, tok_out);
+                cluster_wait();
+                return;
+            }
+            cluster_wait();
+            fallback_select_and_draw(c, v, kp, vec, kk, pp, zmax, c2, tok_out);
+            cluster_wait();
+            return;
+        }
         for (int i = tid; i < kb.nb; i += kST) cnt[i] = 0u;
         if (tid == 0) {
             sm->bc[0] = kb.nb - 1;
@@ -1081,11 +1203,11 @@ __global__ void __launch_bounds__(kST, 2)
                 }
                 cluster.sync();  // candidates complete in rank 0; no remote access follows
                 if (c.rank != 0) return;
-                solo_finish(sm, static_cast<int>(total), kk, pp, kp.mth, zmax, c2, seed, offset, tok_out);
+                solo_finish(sm, static_cast<int>(total), kk, pp, kp.mth, zmax, c2, tok_out);
                 return;
             }
             cluster.sync();  // remote histogram reads are done before the fallback reuses it
-            fallback_select_and_draw(c, v, kp, vec, kk, pp, zmax, c2, seed, offset, tok_out);
+            fallback_select_and_draw(c, v, kp, vec, kk, pp, zmax, c2, tok_out);
             cluster_wait();
             return;
         }
@@ -1299,18 +1421,18 @@ __global__ void __launch_bounds__(kST, 2)
                 kp.taup = static_cast<uint32_t>(sm->bc[5]);
                 kp.zp = key_float(kp.taup);
                 kp.idp = static_cast<int>(static_cast<uint32_t>(sm->bc[6]));
-                draw_pass(c, v, kp, vec, zmax, c2, seed, offset, tok_out);
+                draw_pass(c, v, kp, vec, zmax, c2, tok_out);
                 cluster_wait();
                 return;
             }
         }
-        fallback_select_and_draw(c, v, kp, vec, 0, pp, zmax, c2, seed, offset, tok_out);
+        fallback_select_and_draw(c, v, kp, vec, 0, pp, zmax, c2, tok_out);
         cluster_wait();
         return;
     }
 
     // ---------------- no filter: draw over every finite logit
-    draw_pass(c, v, kp, vec, zmax, c2, seed, offset, tok_out);
+    draw_pass(c, v, kp, vec, zmax, c2, tok_out);
     cluster_wait();
 }
 
