@@ -114,6 +114,8 @@ def _load():
             lib.oracle_spec_verify_row.restype = i32
             lib.oracle_sample_row_ex.argtypes = [P, i32, f32, i32, f32, f32, u64, u64, P, P, P, P, P]
             lib.oracle_sample_row_ex.restype = i32
+            lib.oracle_sample_row_typical.argtypes = [P, i32, f32, f32, u64, u64, P, P, P, P, P, P, P]
+            lib.oracle_sample_row_typical.restype = i32
             lib.oracle_process_logits.argtypes = [P, i32, i32, P, P, P, P, P, P, P]
             lib.oracle_process_logits.restype = i32
             lib.oracle_kv_append_chunk.argtypes = [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32]
@@ -304,6 +306,26 @@ def sample_row(z, temperature: float, top_k: int, top_p: float, seed: int, offse
                                    ctypes.byref(nk), _ptr(probs) if want_probs else None)
     res = dict(token=int(tok.value), status=int(st), draw_margin=float(dm.value),
                cut_margin=float(cm.value), n_kept=int(nk.value))
+    if want_probs:
+        res["probs"] = probs
+    return res
+
+
+def sample_row_typical(z, temperature: float, typical_p: float, seed: int, offset: int, want_probs: bool = False):
+    """One row of typical sampling. Returns dict(token, status, draw_margin,
+    cut_margin, center_margin, entropy, n_kept[, probs])."""
+    z = np.ascontiguousarray(z, dtype=np.float32)
+    V = z.shape[0]
+    tok = ctypes.c_int32(0)
+    dm, cm, ctm, ent = ctypes.c_double(0), ctypes.c_double(0), ctypes.c_double(0), ctypes.c_double(0)
+    nk = ctypes.c_int32(0)
+    probs = np.zeros(V, dtype=np.float64) if want_probs else None
+    st = _load().oracle_sample_row_typical(_ptr(z), V, float(temperature), float(typical_p),
+                                        int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), ctypes.byref(tok),
+                                        ctypes.byref(dm), ctypes.byref(cm), ctypes.byref(ctm), ctypes.byref(ent),
+                                        ctypes.byref(nk), _ptr(probs) if want_probs else None)
+    res = dict(token=int(tok.value), status=int(st), draw_margin=float(dm.value), cut_margin=float(cm.value),
+               center_margin=float(ctm.value), entropy=float(ent.value), n_kept=int(nk.value))
     if want_probs:
         res["probs"] = probs
     return res

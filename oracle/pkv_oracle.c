@@ -486,6 +486,146 @@ int oracle_sample_row(const float* z, int V, float temperature, int top_k, float
                                 cut_margin, n_kept, probs);
 }
 
+/* Typical sampling ("LLM inference serving tutorial" 3.1, other samplers;
+ * Meister et al., "Locally Typical Sampling"), for one row:
+ *   p_i = exp((z_i - z_max)/T) / S over the finite logits (T > 0);
+ *   H(p) = -sum_i p_i ln p_i;  d_i = |-ln p_i - H(p)|;
+ *   the kept set is the smallest prefix of the tokens sorted by d ascending
+ *   whose cumulative probability reaches typical_p (boundary token kept),
+ *   renormalised; the draw walks it in token-id order with the request's
+ *   Philox uniform, as in oracle_sample_row_ex.
+ * With u_i = (z_i - z_max) log2(e) / T and ubar = sum_i p_i u_i one has
+ * -ln p_i - H = ln 2 (ubar - u_i), so the order by d is the order by
+ * |u_i - ubar|.  That order is a decision taken in floating point; it is taken
+ * in the kernel's precision so that both sides make the same one: ubar rounded
+ * to a multiple of 2^-8, then in float32, each operation rounded on its own,
+ * c2 = min(log2(e) / T, 1e30), u_i = (z_i - z_max) * c2 and
+ * dk_i = |u_i - ubar|; ties in dk go to the larger u_i (the more probable
+ * token), then to the smaller id.  The cumulative sums use the float64 p_i.
+ * T == 0 is the greedy branch; typical_p >= 1 keeps every finite logit.
+ * Errors: as oracle_sample_row_ex, and typical_p <= 0 or NaN -> OR_INVALID_ARG.
+ * Diagnostics: entropy = H(p) in nats; center_margin = distance (log2 units)
+ * from ubar to the nearest midpoint of the 2^-8 grid (where the rounding of
+ * ubar could go either way); cut_margin and draw_margin as in the top-p
+ * sampler; probs (optional) = the final renormalised distribution. */
+typedef struct {
+    float dk, u;
+    int32_t id;
+    double p;
+} typ_t;
+
+static int cmp_typ(const void* a, const void* b) {
+    const typ_t* x = (const typ_t*)a;
+    const typ_t* y = (const typ_t*)b;
+    if (x->dk < y->dk) return -1;
+    if (x->dk > y->dk) return 1;
+    if (x->u > y->u) return -1;
+    if (x->u < y->u) return 1;
+    return (x->id < y->id) ? -1 : (x->id > y->id ? 1 : 0);
+}
+
+int oracle_sample_row_typical(const float* z, int V, float temperature, float typical_p, uint64_t seed,
+                              uint64_t offset, int32_t* token, double* draw_margin, double* cut_margin,
+                              double* center_margin, double* entropy, int32_t* n_kept, double* probs) {
+    *center_margin = 1.0;
+    *entropy = 0.0;
+    if (temperature == 0.0f || typical_p >= 1.0f) /* greedy, or no truncation (NaN p goes on) */
+        return oracle_sample_row_ex(z, V, temperature, 0, 1.0f, 0.0f, seed, offset, token, draw_margin,
+                                    cut_margin, n_kept, probs);
+    *token = -1;
+    *draw_margin = 0.0;
+    *cut_margin = 1.0;
+    *n_kept = 0;
+    if (probs) for (int i = 0; i < V; ++i) probs[i] = 0.0;
+    int n = 0;
+    float zmaxf = -INFINITY;
+    for (int i = 0; i < V; ++i) {
+        if (isnan(z[i]) || (isinf(z[i]) && z[i] > 0)) return OR_NONFINITE;
+        if (isfinite(z[i])) {
+            ++n;
+            if (z[i] > zmaxf) zmaxf = z[i];
+        }
+    }
+    if (n == 0) return OR_NONFINITE;
+    if (!(temperature >= 0.0f)) return OR_INVALID_ARG;
+    if (!(typical_p > 0.0f)) return OR_INVALID_ARG; /* <= 0 or NaN */
+
+    /* the distribution, its entropy and the literal d_i */
+    const double T = (double)temperature, zmax = (double)zmaxf, L2E = 1.4426950408889634;
+    typ_t* t = (typ_t*)malloc(sizeof(typ_t) * (size_t)n);
+    double S = 0.0;
+    int k = 0;
+    for (int i = 0; i < V; ++i)
+        if (isfinite(z[i])) {
+            t[k].id = i;
+            t[k].p = exp(((double)z[i] - zmax) / T);
+            S += t[k].p;
+            ++k;
+        }
+    double H = 0.0, ubar = 0.0;
+    for (int j = 0; j < n; ++j) {
+        t[j].p /= S;
+        if (t[j].p > 0.0) H -= t[j].p * log(t[j].p);
+        ubar += t[j].p * (((double)z[t[j].id] - zmax) / T * L2E);
+    }
+    *entropy = H;
+    /* ubar in log2 units relative to the maximum, rounded to the 2^-8 grid */
+    const double g = ubar * 256.0;
+    *center_margin = fabs(fabs(g - floor(g)) - 0.5) / 256.0;
+    const float ub = (float)(rint(g) / 256.0);
+    float c2 = 1.4426950408889634f / temperature;
+    if (c2 > 1.0e30f) c2 = 1.0e30f;
+    for (int j = 0; j < n; ++j) {
+        const float a = z[t[j].id] - zmaxf;
+        const float u = a * c2;
+        const float d = u - ub;
+        t[j].u = u;
+        t[j].dk = fabsf(d);
+    }
+    qsort(t, (size_t)n, sizeof(typ_t), cmp_typ);
+
+    /* smallest prefix reaching typical_p */
+    const double tp = (double)typical_p;
+    double cum = 0.0, prev = 0.0;
+    int m = n;
+    for (int j = 0; j < n; ++j) {
+        prev = cum;
+        cum += t[j].p;
+        if (cum >= tp) { m = j + 1; break; }
+    }
+    {
+        double d1 = fabs(cum - tp), d0 = fabs(prev - tp);
+        *cut_margin = d1 < d0 ? d1 : d0;
+    }
+
+    /* renormalise; draw in token-id order */
+    double Sp = 0.0;
+    for (int j = 0; j < m; ++j) Sp += t[j].p;
+    double* pi = (double*)calloc((size_t)V, sizeof(double));
+    unsigned char* kept = (unsigned char*)calloc((size_t)V, 1);
+    for (int j = 0; j < m; ++j) { pi[t[j].id] = t[j].p / Sp; kept[t[j].id] = 1; }
+    const double u = oracle_uniform(seed, offset);
+    double c = 0.0, cprev = 0.0;
+    int tok = -1, last = -1;
+    for (int i = 0; i < V; ++i) {
+        if (!kept[i]) continue;
+        last = i;
+        cprev = c;
+        c += pi[i];
+        if (c > u) { tok = i; break; }
+    }
+    if (tok < 0) { tok = last; *draw_margin = 0.0; }
+    else {
+        double a = u - cprev, bnd = c - u;
+        *draw_margin = a < bnd ? a : bnd;
+    }
+    *token = tok;
+    *n_kept = m;
+    if (probs) for (int i = 0; i < V; ++i) probs[i] = pi[i];
+    free(t); free(pi); free(kept);
+    return OR_OK;
+}
+
 /* Logits processors before the sampler ("LLM inference serving tutorial" 3.1
  * pipeline: hard constraints, then penalties, then temperature and filters;
  * 3.2 penalty definitions; 3.3 constraint masks), in place on logits [B, V]:
