@@ -253,6 +253,31 @@ pkv_status pkv_sample_tokens_ex(int32_t* tokens, const float* logits, int B, int
                                 const uint64_t* offsets, int32_t* dev_status, void* stream);
 
 /*
+ * Typical sampling ("LLM inference serving tutorial" 3.1, other samplers;
+ * Meister et al., locally typical sampling): for row b with T = temperature[b]
+ * > 0 and tau = typical_p[b] < 1, p = softmax(z / T) over the finite logits,
+ * H(p) = -sum p_i ln p_i, and the kept set is the smallest prefix of the tokens
+ * in ascending d_i = |-ln p_i - H(p)| whose probability reaches tau (boundary
+ * token kept), renormalised and drawn in token-id order with the same Philox
+ * uniform as pkv_sample_tokens (key (seeds[b], 0), counter (offsets[b], 0, 0,
+ * 0)).  Since -ln p_i - H = ln 2 (ubar - u_i) with u_i = (z_i - zmax) log2(e) / T
+ * and ubar the p-weighted mean of u, the order is taken as |u_i - ubar| in
+ * float32 (u_i = (z_i - zmax) * min(log2(e) / T, 1e30), each operation rounded
+ * on its own) with ubar rounded to a multiple of 2^-8; ties go to the larger
+ * u_i, then to the smaller id.  T == 0 is greedy (lowest id among equal
+ * maxima); tau >= 1 keeps every finite logit.  tokens: device int32 [B];
+ * logits: device float32 [B, V] row-major (-inf = banned); temperature,
+ * typical_p: device float32 [B]; seeds, offsets: device uint64 [B].  Errors
+ * (token -1 for the row, status recorded): NaN / +inf / no finite logit ->
+ * PKV_ERR_NONFINITE; T < 0 or NaN, or T > 0 with tau <= 0 or NaN ->
+ * PKV_ERR_INVALID_ARG.  Host: B < 0, V < 1 or V > 2^23, NULL pointers ->
+ * PKV_ERR_INVALID_ARG.  One CTA per row; no workspace, nothing allocated.
+ */
+pkv_status pkv_sample_tokens_typical(int32_t* tokens, const float* logits, int B, int V, const float* temperature,
+                                     const float* typical_p, const uint64_t* seeds, const uint64_t* offsets,
+                                     int32_t* dev_status, void* stream);
+
+/*
  * Logits processors, in place on logits float32 [B, V], in the order of the
  * "LLM inference serving tutorial" 3.1 pipeline (before temperature and the
  * filters of pkv_sample_tokens):

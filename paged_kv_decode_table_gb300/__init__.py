@@ -86,6 +86,8 @@ def load_library():
         lib.pkv_paged_prefill_attention.restype = i32
         lib.pkv_sample_tokens_ex.argtypes = [P, P, i32, i32, P, P, P, P, P, P, P, P]
         lib.pkv_sample_tokens_ex.restype = i32
+        lib.pkv_sample_tokens_typical.argtypes = [P, P, i32, i32, P, P, P, P, P, P]
+        lib.pkv_sample_tokens_typical.restype = i32
         lib.pkv_apply_logits_processors.argtypes = [P, i32, i32, P, P, P, P, P, P, P, P, P]
         lib.pkv_apply_logits_processors.restype = i32
         lib.pkv_spec_verify_workspace_bytes.argtypes = [i32, i32]
@@ -274,6 +276,31 @@ def sample_tokens(logits, temperature, top_k, top_p, seeds, offsets, tokens=None
                                             _ptr(top_k), _ptr(top_p), _ptr(seeds), _ptr(offsets),
                                             None, 0, _ptr(status), _stream(dev))
     _raise("pkv_sample_tokens", code)
+    return tokens
+
+
+def sample_tokens_typical(logits, temperature, typical_p, seeds, offsets, tokens=None, status=None):
+    """Typical sampling: one token per row of logits [B, V] (float32); returns
+    tokens [B] int32.  typical_p is float32 [B]; seeds / offsets as in
+    sample_tokens."""
+    B, V = logits.shape
+    dev = logits.device
+    _check_cuda("logits", logits, torch.float32)
+    _check_cuda("temperature", temperature, torch.float32, (B,), dev)
+    _check_cuda("typical_p", typical_p, torch.float32, (B,), dev)
+    if seeds.dtype not in (torch.int64, torch.uint64) or offsets.dtype not in (torch.int64, torch.uint64):
+        raise TypeError("seeds and offsets must be 64-bit integer tensors")
+    _check_cuda("seeds", seeds, shape=(B,), device=dev)
+    _check_cuda("offsets", offsets, shape=(B,), device=dev)
+    if tokens is None:
+        tokens = torch.empty(B, dtype=torch.int32, device=dev)
+    _check_cuda("tokens", tokens, torch.int32, (B,), dev)
+    if status is not None:
+        _check_cuda("status", status, torch.int32, (1,), dev)
+    code = load_library().pkv_sample_tokens_typical(_ptr(tokens), _ptr(logits), B, V, _ptr(temperature),
+                                                    _ptr(typical_p), _ptr(seeds), _ptr(offsets), _ptr(status),
+                                                    _stream(dev))
+    _raise("pkv_sample_tokens_typical", code)
     return tokens
 
 

@@ -20,6 +20,9 @@ int device_sm_count();
 cudaError_t launch_sampler(int32_t* tokens, const float* logits, int B, int V, const float* temperature,
                            const int32_t* top_k, const float* top_p, const float* min_p, const uint64_t* seeds,
                            const uint64_t* offsets, int32_t* status, cudaStream_t stream);
+cudaError_t launch_typical_sampler(int32_t* tokens, const float* logits, int B, int V, const float* temperature,
+                                   const float* typical_p, const uint64_t* seeds, const uint64_t* offsets,
+                                   int32_t* status, cudaStream_t stream);
 cudaError_t launch_logits_processors(float* logits, int B, int V, const uint32_t* mask, const int32_t* row_ptr,
                                      const int32_t* tokens, const int32_t* counts, const float* rep,
                                      const float* freq, const float* pres, int32_t* status, cudaStream_t stream);
@@ -198,6 +201,16 @@ pkv_status pkv_sample_tokens_ex(int32_t* tokens, const float* logits, int B, int
     if (!tokens || !logits || !temperature || !top_k || !top_p || !seeds || !offsets) return PKV_ERR_INVALID_ARG;
     return cuda_status(pkv::launch_sampler(tokens, logits, B, V, temperature, top_k, top_p, min_p, seeds, offsets,
                                            dev_status, static_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_sample_tokens_typical(int32_t* tokens, const float* logits, int B, int V, const float* temperature,
+                                     const float* typical_p, const uint64_t* seeds, const uint64_t* offsets,
+                                     int32_t* dev_status, void* stream) {
+    if (B < 0 || V < 1 || V > (1 << 23)) return PKV_ERR_INVALID_ARG;
+    if (B == 0) return PKV_OK;
+    if (!tokens || !logits || !temperature || !typical_p || !seeds || !offsets) return PKV_ERR_INVALID_ARG;
+    return cuda_status(pkv::launch_typical_sampler(tokens, logits, B, V, temperature, typical_p, seeds, offsets,
+                                                   dev_status, static_cast<cudaStream_t>(stream)));
 }
 
 pkv_status pkv_apply_logits_processors(float* logits, int B, int V, const uint32_t* allow_mask,

@@ -1,0 +1,605 @@
+// typical_sampler.cu -- typical sampling, one CTA per row.
+//
+// "LLM inference serving tutorial" section 3.1 (other samplers: typical
+// sampling; Meister et al., locally typical sampling): over the temperature
+// distribution p of the finite logits, tokens are taken in ascending
+// d_i = |-ln p_i - H(p)| until their probability first reaches typical_p
+// (boundary token kept); the kept set is renormalised and drawn in token-id
+// order with the request's Philox uniform, as in the sampler.
+//
+// With u_i = (z_i - zmax) log2(e) / T and ubar = sum_i p_i u_i one has
+// -ln p_i - H = ln 2 (ubar - u_i): the order by d is the order by |u_i - ubar|,
+// so the kept set is an interval of logits around the p-weighted mean.  The
+// order is a decision taken in floating point and is fixed in float32: ubar is
+// rounded to a multiple of 2^-8, u_i = (z_i - zmax) * c2 and
+// dk_i = |u_i - ubar| are each rounded on their own (no fused multiply-add),
+// ties in dk go to the larger u_i, then to the smaller id.  Masses are the
+// sampler's 2^-40 fixed-point weights floor(2^u * 2^40), so the cut and the
+// draw are exact integer arithmetic.
+//
+// Passes over the row (the first from HBM, the rest from L2): maximum and
+// finiteness; the mass sum S and the weighted sum of u (for ubar); a
+// three-digit radix select (11/11/10 bits of dk, mass histograms) for the
+// cut's dk; when several u share that dk, the same select over u; the rank of
+// the cut among equal (dk, u) in id order; the draw (chunk sums of the kept
+// masses, a scan, one chunk walked).
+#include <math.h>
+
+#include "pkv_common.cuh"
+#include "sampling_math.cuh"
+
+namespace pkv {
+
+constexpr int kTyT = 1024;          // threads per CTA (one row)
+constexpr int kTyW = kTyT / 32;     // warps
+constexpr int kTyBins = 2048;       // radix digits (11 bits), or draw chunks
+
+struct TySmem {
+    unsigned long long hist[kTyBins];  // mass histogram, sorted window keys, or chunk sums / prefixes
+    unsigned int cnt[kTyBins];         // count histogram, or the window's token ids
+    unsigned int nwin;
+    unsigned long long wsum[kTyW];
+    double dsum[kTyW];
+    float fv[kTyW];
+    unsigned long long bc[4];
+    unsigned long long u53;  // the row's uniform, top 53 bits of Philox word 0
+};
+
+// ------------------------------------------------------------------ CTA reductions
+// Every thread returns the CTA-wide result.  Each starts with a barrier, so
+// back-to-back calls do not race on the per-warp slots.
+__device__ __forceinline__ uint64_t ty_warp_sum(uint64_t v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ uint64_t ty_sum_u64(uint64_t v, TySmem* sm) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    v = ty_warp_sum(v);
+    __syncthreads();
+    if (lane == 0) sm->wsum[warp] = v;
+    __syncthreads();
+    return ty_warp_sum(sm->wsum[lane]);
+}
+__device__ double ty_sum_f64(double v, TySmem* sm) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    __syncthreads();
+    if (lane == 0) sm->dsum[warp] = v;
+    __syncthreads();
+    double t = sm->dsum[lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    return t;
+}
+template <bool kMax>
+__device__ float ty_ext_f(float v, TySmem* sm) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float y = __shfl_xor_sync(0xffffffffu, v, o);
+        v = kMax ? fmaxf(v, y) : fminf(v, y);
+    }
+    __syncthreads();
+    if (lane == 0) sm->fv[warp] = v;
+    __syncthreads();
+    float t = sm->fv[lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float y = __shfl_xor_sync(0xffffffffu, t, o);
+        t = kMax ? fmaxf(t, y) : fminf(t, y);
+    }
+    return t;
+}
+// Exclusive prefix of v over the threads in index order; total = the sum.
+__device__ uint64_t ty_excl_scan(uint64_t v, TySmem* sm, uint64_t& total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint64_t inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+    }
+    __syncthreads();
+    if (lane == 31) sm->wsum[warp] = inc;
+    __syncthreads();
+    const uint64_t w = sm->wsum[lane];
+    uint64_t wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t y = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += y;
+    }
+    total = __shfl_sync(0xffffffffu, wi, 31);
+    const uint64_t before = __shfl_sync(0xffffffffu, wi - w, warp);
+    return before + inc - v;
+}
+
+// Strided sweep over the row, f(i, x) for every element: thread t takes the
+// 4-element slots 4 (t + kTyT m), kU of them loaded before any is processed
+// (16-byte loads when the row is 16-byte aligned), so that each thread keeps
+// kU loads in flight.
+constexpr int kTyU = 4;
+template <typename F>
+__device__ __forceinline__ void ty_sweep(const float* __restrict__ z, int n, F&& f) {
+    const bool a16 = (reinterpret_cast<uintptr_t>(z) & 15u) == 0;
+    for (int e0 = 4 * static_cast<int>(threadIdx.x); e0 < n; e0 += 4 * kTyT * kTyU) {
+        float4 q[kTyU];
+#pragma unroll
+        for (int u = 0; u < kTyU; ++u) {
+            const int e = e0 + 4 * kTyT * u;
+            if (a16 && e + 4 <= n) {
+                q[u] = __ldg(reinterpret_cast<const float4*>(z + e));
+            } else {
+                q[u].x = e < n ? z[e] : -INFINITY;
+                q[u].y = e + 1 < n ? z[e + 1] : -INFINITY;
+                q[u].z = e + 2 < n ? z[e + 2] : -INFINITY;
+                q[u].w = e + 3 < n ? z[e + 3] : -INFINITY;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kTyU; ++u) {
+            const int e = e0 + 4 * kTyT * u;
+            if (e < n) f(e, q[u].x);
+            if (e + 1 < n) f(e + 1, q[u].y);
+            if (e + 2 < n) f(e + 2, q[u].z);
+            if (e + 3 < n) f(e + 3, q[u].w);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ radix select
+// Among the row's elements that keyf accepts (keyf(x, i, key, m) -> in scope,
+// with its 32-bit key and mass) and whose key matches `prefix` in the top
+// `pbits` bits: the digit d of key bits [shift, shift + nbits) at which the
+// cumulative mass in ascending key order, starting from `above`, first
+// reaches `target`.  `above` is advanced past the smaller digits.
+template <typename KeyF>
+__device__ uint32_t ty_radix(const float* __restrict__ z, int n, TySmem* sm, KeyF keyf, uint32_t prefix, int pbits,
+                             int shift, int nbits, uint64_t target, uint64_t& above) {
+    const int tid = threadIdx.x;
+    const int nb = 1 << nbits;
+    for (int i = tid; i < nb; i += kTyT) sm->hist[i] = 0ull;
+    if (tid == 0) {
+        sm->bc[0] = static_cast<unsigned long long>(nb - 1);
+        sm->bc[1] = above;
+    }
+    __syncthreads();
+    // a thread's run of equal digits is added once (the leading digits of a
+    // row cluster in a few bins, where shared atomics would serialise)
+    uint32_t cd = 0u;
+    uint64_t cs = 0;
+    ty_sweep(z, n, [&](int i, float x) {
+        uint32_t key;
+        uint64_t m;
+        if (!keyf(x, i, key, m)) return;
+        if (pbits && (key >> (32 - pbits)) != prefix) return;
+        const uint32_t d = (key >> shift) & static_cast<uint32_t>(nb - 1);
+        if (d != cd) {
+            if (cs) atomicAdd(&sm->hist[cd], static_cast<unsigned long long>(cs));
+            cd = d;
+            cs = 0;
+        }
+        cs += m;
+    });
+    if (cs) atomicAdd(&sm->hist[cd], static_cast<unsigned long long>(cs));
+    __syncthreads();
+    const int b0 = 2 * tid;  // two digits per thread, ascending
+    const uint64_t h0 = b0 < nb ? sm->hist[b0] : 0ull, h1 = b0 + 1 < nb ? sm->hist[b0 + 1] : 0ull;
+    uint64_t tot;
+    const uint64_t c0 = above + ty_excl_scan(h0 + h1, sm, tot);
+    if (c0 < target && c0 + h0 + h1 >= target) {
+        if (c0 + h0 >= target) {
+            sm->bc[0] = static_cast<unsigned long long>(b0);
+            sm->bc[1] = c0;
+        } else {
+            sm->bc[0] = static_cast<unsigned long long>(b0 + 1);
+            sm->bc[1] = c0 + h0;
+        }
+    }
+    __syncthreads();
+    const uint32_t d = static_cast<uint32_t>(sm->bc[0]);
+    above = sm->bc[1];
+    __syncthreads();  // bc and hist are reused by the next call
+    return d;
+}
+
+// ------------------------------------------------------------------ ordered find
+// First element i (ascending) at which the running sum of valf(z[i], i) exceeds
+// X = xf(total).  The row is cut into chunks of 128 * cpw consecutive elements
+// (at most kTyBins chunks); warp w sums chunks w, w + 32, ... with coalesced
+// loads, the chunk sums are scanned, and warp 0 walks the one chunk holding X.
+// Returns -1 when X >= total (nothing to find).
+template <typename ValF, typename XF>
+__device__ int ty_ordered_find(const float* __restrict__ z, int n, TySmem* sm, ValF valf, XF xf) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nvec = (n + 3) & ~3;
+    const int cpw = max(1, (nvec + 128 * kTyBins - 1) / (128 * kTyBins));
+    const int csz = 128 * cpw;
+    const int nch = (nvec + csz - 1) / csz;
+    const bool a16 = (reinterpret_cast<uintptr_t>(z) & 15u) == 0;
+    auto load4 = [&](int e) -> float4 {  // the lane's 4 elements starting at e (-inf past n)
+        if (a16 && e + 4 <= n) return __ldg(reinterpret_cast<const float4*>(z + e));
+        float4 q;
+        q.x = e < n ? z[e] : -INFINITY;
+        q.y = e + 1 < n ? z[e + 1] : -INFINITY;
+        q.z = e + 2 < n ? z[e + 2] : -INFINITY;
+        q.w = e + 3 < n ? z[e + 3] : -INFINITY;
+        return q;
+    };
+    auto val4 = [&](const float4& q, int e) -> uint64_t {
+        return (e < n ? valf(q.x, e) : 0ull) + (e + 1 < n ? valf(q.y, e + 1) : 0ull) +
+               (e + 2 < n ? valf(q.z, e + 2) : 0ull) + (e + 3 < n ? valf(q.w, e + 3) : 0ull);
+    };
+    // warp w sums chunks w, w + 32, w + 64, w + 96 together (four loads in flight)
+    for (int cb = warp; cb < nch; cb += 4 * kTyW) {
+        uint64_t w[4] = {0ull, 0ull, 0ull, 0ull};
+        for (int k = 0; k < cpw; ++k) {
+            float4 q[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) q[u] = load4((cb + u * kTyW) * csz + 128 * k + 4 * lane);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) w[u] += val4(q[u], (cb + u * kTyW) * csz + 128 * k + 4 * lane);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const uint64_t t = ty_warp_sum(w[u]);
+            if (lane == 0 && cb + u * kTyW < nch) sm->hist[cb + u * kTyW] = t;
+        }
+    }
+    __syncthreads();
+    const int c0 = 2 * tid;
+    const uint64_t a0 = c0 < nch ? sm->hist[c0] : 0ull, a1 = c0 + 1 < nch ? sm->hist[c0 + 1] : 0ull;
+    uint64_t tot;
+    const uint64_t ex = ty_excl_scan(a0 + a1, sm, tot);
+    if (c0 < nch) sm->hist[c0] = ex;
+    if (c0 + 1 < nch) sm->hist[c0 + 1] = ex + a0;
+    const uint64_t X = xf(tot);
+    if (tid == 0) {
+        sm->bc[2] = ~0ull;  // chunk holding X
+        sm->bc[3] = ~0ull;  // the element found
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int ch = c0 + q;
+        if (ch < nch) {
+            const uint64_t lo = sm->hist[ch], hi = ch + 1 < nch ? sm->hist[ch + 1] : tot;
+            if (lo <= X && X < hi) sm->bc[2] = static_cast<unsigned long long>(ch);
+        }
+    }
+    __syncthreads();
+    const unsigned long long cs = sm->bc[2];
+    if (warp == 0 && cs != ~0ull) {
+        uint64_t base = sm->hist[cs];
+        for (int k = 0; k < cpw; ++k) {
+            const int e = static_cast<int>(cs) * csz + 128 * k + 4 * lane;
+            const float4 q = load4(e);
+            const uint64_t m[4] = {e < n ? valf(q.x, e) : 0ull, e + 1 < n ? valf(q.y, e + 1) : 0ull,
+                                   e + 2 < n ? valf(q.z, e + 2) : 0ull, e + 3 < n ? valf(q.w, e + 3) : 0ull};
+            const uint64_t mine = m[0] + m[1] + m[2] + m[3];
+            uint64_t inc = mine;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint64_t y = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += y;
+            }
+            const uint64_t before = base + inc - mine;
+            if (before <= X && X < before + mine) {
+                uint64_t cum = before;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    cum += m[j];
+                    if (cum > X) {
+                        sm->bc[3] = static_cast<unsigned long long>(e + j);
+                        break;
+                    }
+                }
+            }
+            base += __shfl_sync(0xffffffffu, inc, 31);
+            if (base > X) break;  // warp-uniform
+        }
+    }
+    __syncthreads();
+    const unsigned long long f = sm->bc[3];
+    __syncthreads();  // bc and hist are reused by the next call
+    return f == ~0ull ? -1 : static_cast<int>(f);
+}
+
+// ------------------------------------------------------------------ kernel
+__global__ void __launch_bounds__(kTyT, 1)
+    typical_sampler_kernel(int32_t* __restrict__ tokens, const float* __restrict__ logits, int V,
+                           const float* __restrict__ temperature, const float* __restrict__ typical_p,
+                           const uint64_t* __restrict__ seeds, const uint64_t* __restrict__ offsets,
+                           int32_t* status) {
+    __shared__ TySmem smem;
+    TySmem* sm = &smem;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int tid = threadIdx.x, row = blockIdx.x;
+    const float* z = logits + static_cast<size_t>(row) * V;
+    const float T = temperature[row], tp = typical_p[row];
+    if (tid == kTyT - 1) sm->u53 = philox_word0(seeds[row], offsets[row]) >> 11;
+
+    // ---- maximum and finiteness
+    float mx = -INFINITY, mn = INFINITY;
+    unsigned int bad = 0u;
+    ty_sweep(z, V, [&](int, float x) {
+        mx = fmaxf(mx, x);
+        mn = fminf(mn, x > -INFINITY ? x : INFINITY);
+        bad |= (x < INFINITY) ? 0u : 1u;  // NaN or +inf
+    });
+    mx = ty_ext_f<true>(mx, sm);
+    mn = ty_ext_f<false>(mn, sm);
+    bad = static_cast<unsigned int>(ty_sum_u64(bad, sm));
+    int err = 0;
+    if (bad || !(mx > -INFINITY)) err = PKV_ERR_NONFINITE;
+    else if (!(T >= 0.f)) err = PKV_ERR_INVALID_ARG;
+    else if (T != 0.f && !(tp > 0.f)) err = PKV_ERR_INVALID_ARG;  // typical_p <= 0 or NaN
+    if (err) {
+        if (tid == 0) {
+            tokens[row] = -1;
+            report(status, err);
+        }
+        return;
+    }
+    if (T == 0.f) {  // greedy: the lowest id holding the maximum
+        float first = INFINITY;
+        for (int i = tid; i < V; i += kTyT)
+            if (z[i] == mx) {
+                first = static_cast<float>(i);  // ids < 2^23 are exact in float
+                break;
+            }
+        first = ty_ext_f<false>(first, sm);
+        if (tid == 0) tokens[row] = static_cast<int32_t>(first);
+        return;
+    }
+    const float c2 = fminf(1.4426950408889634f / T, 1.0e30f);  // log2(e) / T, kept finite
+    auto uof = [&](float x) { return __fmul_rn(__fsub_rn(x, mx), c2); };
+    auto draw_x = [&](uint64_t tot) {  // floor(u * tot) < tot
+        return static_cast<uint64_t>((static_cast<unsigned __int128>(sm->u53) * tot) >> 53);
+    };
+    if (!(tp < 1.f)) {  // no truncation: every finite logit
+        const int tok = ty_ordered_find(
+            z, V, sm, [&](float x, int) -> uint64_t { return x > -INFINITY ? fx40(hw_exp2(uof(x))) : 0ull; },
+            draw_x);
+        if (tid == 0) tokens[row] = tok;
+        return;
+    }
+
+    // ---- S and the p-weighted mean of u, rounded to the 2^-8 grid
+    uint64_t s = 0;
+    float wu = 0.f;
+    ty_sweep(z, V, [&](int, float x) {
+        if (!(x > -INFINITY)) return;
+        const float u = uof(x);
+        const float w = hw_exp2(u);
+        s += fx40(w);
+        if (w > 0.f) wu = fmaf(w, u, wu);
+    });
+    const uint64_t S = ty_sum_u64(s, sm);
+    const double WU = ty_sum_f64(static_cast<double>(wu), sm);
+    const double ubar = WU / (static_cast<double>(S) * 0x1p-40);
+    const float ub = static_cast<float>(rint(ubar * 256.0) / 256.0);
+    auto dkey = [&](float u) { return __float_as_uint(fabsf(__fsub_rn(u, ub))); };  // monotone in dk >= 0
+    const uint64_t target = ceil_mul_p(tp, S);  // >= 1, <= S
+
+    // ---- 2048 bins linear in dk over [0, dkmax] (bin 0: closest to the mean):
+    // mass and count per bin; the bin where the cumulative mass in ascending
+    // dk first reaches the target holds the cut
+    const float umin = uof(mn);
+    const float dkmax = fmaxf(fabsf(__fsub_rn(umin, ub)), fabsf(ub));
+    const float sc = static_cast<float>(kTyBins) / dkmax;
+    const float scale = (dkmax > 0.f && sc < INFINITY) ? sc : 0.f;  // 0: one bin
+    auto dbin = [&](uint32_t dk) {  // monotone non-decreasing in dk; inf * 0 (NaN) -> the last bin
+        const float t = __uint_as_float(dk) * scale;
+        return t < static_cast<float>(kTyBins - 1) ? static_cast<int>(t) : kTyBins - 1;
+    };
+    float* hf = reinterpret_cast<float*>(sm->hist);  // approximate bin masses (weights 2^u)
+    for (int i = tid; i < kTyBins; i += kTyT) hf[i] = 0.f;
+    if (tid == 0) sm->nwin = 0u;
+    __syncthreads();
+    {
+        int cb = 0;  // a thread's run of equal bins is added once
+        float cw = 0.f;
+        ty_sweep(z, V, [&](int, float x) {
+            if (!(x > -INFINITY)) return;
+            const float u = uof(x);
+            const int bq = dbin(dkey(u));
+            if (bq != cb) {
+                if (cw > 0.f) atomicAdd(&hf[cb], cw);
+                cb = bq;
+                cw = 0.f;
+            }
+            cw += hw_exp2(u);
+        });
+        if (cw > 0.f) atomicAdd(&hf[cb], cw);
+    }
+    __syncthreads();
+    // The float sums locate the cut only approximately: the window of bins
+    // [blo, bhi] covers cumulative masses within S / 2^13 of the target on
+    // either side; the gather pass checks it with exact masses.
+    {
+        const uint64_t del = (S >> 13) ? (S >> 13) : 1ull;
+        const uint64_t tlo = target > del ? target - del : 1ull, thi = target + del;
+        const int b0 = 2 * tid;
+        const uint64_t h0 = __float2ull_rn(hf[b0] * 0x1p40f), h1 = __float2ull_rn(hf[b0 + 1] * 0x1p40f);
+        if (tid == 0) {
+            sm->bc[0] = 0ull;
+            sm->bc[1] = kTyBins - 1;
+        }
+        uint64_t tot;
+        const uint64_t c0 = ty_excl_scan(h0 + h1, sm, tot);  // (begins with a barrier)
+        if (c0 < tlo && c0 + h0 + h1 >= tlo) sm->bc[0] = static_cast<unsigned long long>(c0 + h0 >= tlo ? b0 : b0 + 1);
+        if (c0 < thi && c0 + h0 + h1 >= thi) sm->bc[1] = static_cast<unsigned long long>(c0 + h0 >= thi ? b0 : b0 + 1);
+    }
+    __syncthreads();
+    const int blo = static_cast<int>(sm->bc[0]), bhi = max(blo, static_cast<int>(sm->bc[1]));
+    __syncthreads();
+
+    // ---- the window's logits into shared memory (and the exact mass above
+    // it), sorted by (dk, larger u first, id): key (dk bits << 32 | ~okey(u))
+    // ascending, then id
+    unsigned long long* key = sm->hist;
+    unsigned int* ids = sm->cnt;
+    uint64_t at = 0;
+    ty_sweep(z, V, [&](int i, float x) {
+        if (!(x > -INFINITY)) return;
+        const float u = uof(x);
+        const uint32_t dk = dkey(u);
+        const int bq = dbin(dk);
+        if (bq < blo) {
+            at += fx40(hw_exp2(u));
+        } else if (bq <= bhi) {
+            const unsigned int slot = atomicAdd(&sm->nwin, 1u);
+            if (slot < static_cast<unsigned int>(kTyBins)) {
+                key[slot] = (static_cast<unsigned long long>(dk) << 32) | static_cast<uint32_t>(~okey(u));
+                ids[slot] = static_cast<unsigned int>(i);
+            }
+        }
+    });
+    uint64_t above = ty_sum_u64(at, sm);  // exact mass of the bins before the window
+    const unsigned int nw = sm->nwin;
+
+    uint32_t dstar = 0u;
+    float ustar = 0.f;
+    int idstar = -1;
+    bool found = false;
+    if (nw >= 1 && nw <= static_cast<unsigned int>(kTyBins) && above < target) {
+        int np2 = 1;
+        while (np2 < static_cast<int>(nw)) np2 <<= 1;
+        for (int i = static_cast<int>(nw) + tid; i < np2; i += kTyT) {
+            key[i] = ~0ull;
+            ids[i] = ~0u;
+        }
+        __syncthreads();
+        for (int k = 2; k <= np2; k <<= 1)
+            for (int j = k >> 1; j > 0; j >>= 1) {
+                for (int i = tid; i < np2; i += kTyT) {
+                    const int l = i ^ j;
+                    if (l > i) {
+                        const bool up = (i & k) == 0;
+                        const unsigned long long ki = key[i], kl = key[l];
+                        const bool gt = ki > kl || (ki == kl && ids[i] > ids[l]);
+                        if (gt == up) {
+                            key[i] = kl;
+                            key[l] = ki;
+                            const unsigned int t = ids[i];
+                            ids[i] = ids[l];
+                            ids[l] = t;
+                        }
+                    }
+                }
+                __syncthreads();
+            }
+        // cumulative mass in sorted order: thread t takes entries [2t, 2t + 2)
+        auto wmass = [&](int j) -> uint64_t {
+            return j < static_cast<int>(nw) ? fx40(hw_exp2(key_float(~static_cast<uint32_t>(key[j])))) : 0ull;
+        };
+        const int j0 = 2 * tid;
+        const uint64_t w0 = wmass(j0), w1 = wmass(j0 + 1);
+        if (tid == 0) sm->bc[2] = ~0ull;
+        uint64_t wt;
+        const uint64_t c0 = above + ty_excl_scan(w0 + w1, sm, wt);  // (begins with a barrier)
+        if (c0 < target && c0 + w0 + w1 >= target) sm->bc[2] = static_cast<unsigned long long>(c0 + w0 >= target ? j0 : j0 + 1);
+        __syncthreads();
+        if (sm->bc[2] != ~0ull) {  // the cut lies in the window
+            const int jc = static_cast<int>(sm->bc[2]);
+            dstar = static_cast<uint32_t>(key[jc] >> 32);
+            ustar = key_float(~static_cast<uint32_t>(key[jc]));
+            idstar = static_cast<int>(ids[jc]);
+            found = true;
+        }
+        __syncthreads();  // hist / cnt are reused below
+    }
+    if (!found) {
+        // ---- the window missed or overflowed: radix select over the dk bits
+        // of every finite logit, then over u, then the rank in id order
+        above = 0;
+        auto kd = [&](float x, int, uint32_t& k, uint64_t& m) -> bool {
+            if (!(x > -INFINITY)) return false;
+            const float u = uof(x);
+            k = dkey(u);
+            m = fx40(hw_exp2(u));
+            return true;
+        };
+        const uint32_t d0 = ty_radix(z, V, sm, kd, 0u, 0, 21, 11, target, above);
+        const uint32_t d1 = ty_radix(z, V, sm, kd, d0, 11, 10, 11, target, above);
+        const uint32_t d2 = ty_radix(z, V, sm, kd, (d0 << 11) | d1, 22, 0, 10, target, above);
+        dstar = (d0 << 21) | (d1 << 10) | d2;
+        float gmin = INFINITY, gmax = -INFINITY;
+        ty_sweep(z, V, [&](int, float x) {
+            if (!(x > -INFINITY)) return;
+            const float u = uof(x);
+            if (dkey(u) == dstar) {
+                gmin = fminf(gmin, u);
+                gmax = fmaxf(gmax, u);
+            }
+        });
+        gmin = ty_ext_f<false>(gmin, sm);
+        gmax = ty_ext_f<true>(gmax, sm);
+        ustar = gmax;
+        if (!(gmin == gmax)) {
+            auto ku = [&](float x, int, uint32_t& k, uint64_t& m) -> bool {
+                if (!(x > -INFINITY)) return false;
+                const float u = uof(x);
+                if (dkey(u) != dstar) return false;
+                k = ~okey(u);  // ascending key = descending u
+                m = fx40(hw_exp2(u));
+                return true;
+            };
+            const uint32_t e0 = ty_radix(z, V, sm, ku, 0u, 0, 21, 11, target, above);
+            const uint32_t e1 = ty_radix(z, V, sm, ku, e0, 11, 10, 11, target, above);
+            const uint32_t e2 = ty_radix(z, V, sm, ku, (e0 << 11) | e1, 22, 0, 10, target, above);
+            ustar = key_float(~((e0 << 21) | (e1 << 10) | e2));
+        }
+        // the cut among equal (dk, u) (equal masses): the r-th in id order
+        const uint64_t mstar = fx40(hw_exp2(ustar));
+        const uint64_t need = target - above;
+        const uint64_t r = mstar ? (need + mstar - 1) / mstar : 1ull;
+        const float us = ustar;
+        const uint32_t ds = dstar;
+        idstar = ty_ordered_find(
+            z, V, sm,
+            [&](float x, int) -> uint64_t {
+                if (!(x > -INFINITY)) return 0ull;
+                const float u = uof(x);
+                return (dkey(u) == ds && u == us) ? 1ull : 0ull;
+            },
+            [&](uint64_t) { return r - 1; });
+    }
+
+    // ---- the draw over the kept set in id order
+    const int tok = ty_ordered_find(
+        z, V, sm,
+        [&](float x, int i) -> uint64_t {
+            if (!(x > -INFINITY)) return 0ull;
+            const float u = uof(x);
+            const uint32_t dk = dkey(u);
+            const bool keep = dk < dstar || (dk == dstar && (u > ustar || (u == ustar && i <= idstar)));
+            return keep ? fx40(hw_exp2(u)) : 0ull;
+        },
+        draw_x);
+    if (tid == 0) tokens[row] = tok;
+}
+
+cudaError_t launch_typical_sampler(int32_t* tokens, const float* logits, int B, int V, const float* temperature,
+                                   const float* typical_p, const uint64_t* seeds, const uint64_t* offsets,
+                                   int32_t* status, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(B), 1, 1);
+    cfg.blockDim = dim3(kTyT, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t err = cudaLaunchKernelEx(&cfg, typical_sampler_kernel, tokens, logits, V, temperature, typical_p,
+                                         seeds, offsets, status);
+    if (err != cudaSuccess) return err;
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -75,6 +75,9 @@ def test_argument_errors_return_before_launch(lib):
     assert lib.pkv_sample_tokens(None, None, 4, 0, None, None, None, None, None, None, 0, None, None) == 1
     assert lib.pkv_sample_tokens(None, None, 4, 1 << 24, None, None, None, None, None, None, 0, None, None) == 1
     assert lib.pkv_sample_tokens(None, None, 0, 100, None, None, None, None, None, None, 0, None, None) == 0
+    assert lib.pkv_sample_tokens_typical(None, None, 4, 100, None, None, None, None, None, None) == 1
+    assert lib.pkv_sample_tokens_typical(None, None, 4, 1 << 24, None, None, None, None, None, None) == 1
+    assert lib.pkv_sample_tokens_typical(None, None, 0, 100, None, None, None, None, None, None) == 0
 
 
 def test_library_has_no_oracle_dependency():
