@@ -481,9 +481,11 @@ def _time_calls(fn, n: int, flush=None):
 def run_extras(args):
     """One JSON line per extra measurement (not part of the default bench line):
     attention calls on the batch-64, long-context and fragmented workloads, the
-    sampler alone on its three workloads (L2 flushed between calls), speculative
-    verification, block copies, and attention over forked sequences that share
-    prefix blocks."""
+    sampler alone on its three workloads (L2 flushed between calls), the sampler
+    variants (min-p, typical sampling, logits processors), speculative
+    verification, chunked prefill, block copies, and attention over forked
+    sequences that share prefix blocks."""
+    import numpy as np
     import paged_kv_decode_table_gb300 as pkv
     from paged_kv_decode_table_gb300 import build as pkv_build
     pkv_build.build()
@@ -527,6 +529,46 @@ def run_extras(args):
               "frac_of_measured": by / (t["median_us"] * 1e-6) / 1e9 / peak})
         del si
         torch.cuda.empty_cache()
+
+    # sampler variants on the batch-64 logits: min-p after top-p, typical sampling,
+    # and the logits processors (constraint masks on every row, 200 penalised
+    # tokens per row)
+    w = W.workload(2)
+    si = W.make_sampler_inputs(w, dev)
+    tok = torch.empty(w.batch, dtype=torch.int32, device=dev)
+    by = 4 * w.batch * w.vocab
+    mp = torch.full((w.batch,), 0.05, dtype=torch.float32, device=dev)
+    t = _time_calls(lambda: pkv.sample_tokens(si["logits"], si["temperature"], si["top_k"], si["top_p"], si["seeds"],
+                                              si["offsets"], tokens=tok, min_p=mp), 50, flush=flush)
+    emit({"extra": "sample_tokens_min_p", "workload": f"{w.batch}x{w.vocab} T0.7 k50 p0.9 min_p0.05", **t,
+          "tokens_per_s": w.batch / (t["median_us"] * 1e-6), "logits_GB/s": by / (t["median_us"] * 1e-6) / 1e9,
+          "frac_of_measured": by / (t["median_us"] * 1e-6) / 1e9 / peak})
+    for tpv in (0.9, 0.2):
+        tpt = torch.full((w.batch,), tpv, dtype=torch.float32, device=dev)
+        t = _time_calls(lambda: pkv.sample_tokens_typical(si["logits"], si["temperature"], tpt, si["seeds"],
+                                                          si["offsets"], tokens=tok), 20, flush=flush)
+        emit({"extra": "sample_tokens_typical", "workload": f"{w.batch}x{w.vocab} T0.7 typical_p {tpv}", **t,
+              "tokens_per_s": w.batch / (t["median_us"] * 1e-6), "logits_GB/s": by / (t["median_us"] * 1e-6) / 1e9,
+              "frac_of_measured": by / (t["median_us"] * 1e-6) / 1e9 / peak})
+    rng = np.random.default_rng(3)
+    words = (w.vocab + 31) // 32
+    mask = torch.from_numpy(rng.integers(0, 2**32, (w.batch, words), dtype=np.uint64).astype(np.uint32).view(np.int32)).to(dev)
+    npen = 200
+    toks = torch.from_numpy(np.concatenate([rng.choice(w.vocab, npen, replace=False) for _ in range(w.batch)]).astype(np.int32)).to(dev)
+    cnts = torch.from_numpy(rng.integers(1, 6, w.batch * npen).astype(np.int32)).to(dev)
+    rp = torch.arange(0, w.batch * npen + 1, npen, dtype=torch.int32, device=dev)
+    rep = torch.full((w.batch,), 1.2, dtype=torch.float32, device=dev)
+    frq = torch.full((w.batch,), 0.3, dtype=torch.float32, device=dev)
+    prs = torch.full((w.batch,), 0.2, dtype=torch.float32, device=dev)
+    lg = si["logits"].clone()
+    t = _time_calls(lambda: pkv.apply_logits_processors(lg, allow_mask=mask, row_ptr=rp, tokens=toks, counts=cnts,
+                                                        repetition=rep, frequency=frq, presence=prs), 50, flush=flush)
+    pby = w.batch * words * 4 + w.batch * w.vocab // 2 * 4 + w.batch * npen * 16   # mask, ~half the row banned, lists
+    emit({"extra": "apply_logits_processors", "workload": f"{w.batch}x{w.vocab}, random masks, {npen} penalised "
+          f"tokens per row", "bytes": pby, **t, "GB/s": pby / (t["median_us"] * 1e-6) / 1e9,
+          "frac_of_measured": pby / (t["median_us"] * 1e-6) / 1e9 / peak})
+    del si, lg, mask
+    torch.cuda.empty_cache()
 
     # speculative verification: 64 requests, 4 drafts each, 128256-token vocabulary
     B, gamma, V = 64, 4, 128256
