@@ -13,12 +13,15 @@
 //
 // Attention (bf16, D = 128, block_size a multiple of 16): one CTA per (tile of
 // 16 chunk tokens of one sequence, KV head h), one warp per query head of the
-// group.  A warp holds its 16 query rows as mma.sync A fragments (tokens on M);
-// the CTA streams head h's K and V in 32-key steps through a four-step
-// cp.async ring in shared memory (128-byte-swizzled rows; rows past the tile's
-// last position are zero-filled) shared by the G warps; S = Q K^T and O += P V
-// by m16n8k16 bf16 MMAs with fp32 accumulation, causal mask and online softmax
-// in the log2 domain.  Each K/V sub-tile is used by 16 tokens x G heads.
+// group.  A warp keeps its 16 query rows (tokens on M) in its own
+// 128-byte-swizzled shared-memory tile and reads them as mma.sync A fragments
+// with ldmatrix; the CTA streams head h's K and V in 32-key steps through a
+// two-slot cp.async ring in shared memory (one step in flight while the other
+// is used; rows past the tile's last position are zero-filled) shared by the G
+// warps; S = Q K^T and O += P V by m16n8k16 bf16 MMAs with fp32 accumulation,
+// causal mask and online softmax in the log2 domain.  Each K/V sub-tile is used
+// by 16 tokens x G heads.  Up to 4 heads per group: 128-thread CTAs, four per
+// SM; up to 8: 256 threads, two per SM (128 registers a thread either way).
 #include <math.h>
 
 #include "pkv_common.cuh"
