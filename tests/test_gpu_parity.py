@@ -161,6 +161,43 @@ def test_attention_deterministic_and_scale_override():
     assert np.all(np.abs(got - ref) <= 2e-2 + 2e-2 * np.abs(ref))
 
 
+def test_attention_workspace_contents_and_graph_replay():
+    """The workspace's contents are ignored on entry: the result must not
+    depend on what it held before (random bytes, or what a previous call left),
+    and replays of one captured launch must match the eager call bit for bit."""
+    w = W.workload(2, batch=24)
+    inp = W.make_decode_inputs(w, "cuda", with_logits=False)
+    args = (inp["q"], inp["k_cache"], inp["v_cache"], inp["block_tables"], inp["seq_lens"])
+    nbytes = pkv.decode_workspace_bytes(w.batch, w.n_q_heads, w.head_dim)
+    ws0 = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    ref = pkv.paged_decode_attention(*args, workspace=ws0).clone()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+    wsr = torch.randint(0, 256, (nbytes,), generator=g, dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(ref)
+    for _ in range(3):
+        pkv.paged_decode_attention(*args, out=out, workspace=wsr)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
+    st = pkv.new_status()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        pkv.paged_decode_attention(*args, out=out, workspace=wsr, status=st)   # warm-up on the side stream
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            pkv.paged_decode_attention(*args, out=out, workspace=wsr, status=st)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(4):
+        out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
+    assert pkv.check_status(st) == 0
+    rows = np.random.default_rng(1).choice(w.batch * w.n_q_heads, 200, replace=False)
+    compare_attention(ref, inp, "bf16", rows=np.sort(rows))
+
+
 def test_decode_step_append_then_attend():
     """The token appended this step is attended to (seq_lens counts it)."""
     w = W.workload(2, batch=7, len_lo=1, len_hi=500)
