@@ -809,18 +809,42 @@ static EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
-static bool encode_pool_map(CUtensorMap* map, const void* pool, int NB, int Hkv, int BS) {
+// Tensor map over a pool [NB, Hkv, BS, 128] bf16 seen as rows of 128 elements,
+// boxes of 64 elements x box_rows rows, 128-byte swizzle.
+bool encode_pool_box(CUtensorMap* map, const void* pool, int NB, int Hkv, int BS, int box_rows) {
     EncodeTiledFn enc = get_encode_fn();
-    if (!enc) return false;
+    if (!enc || box_rows < 1 || box_rows > 256) return false;
     const cuuint64_t rows = static_cast<cuuint64_t>(NB) * Hkv * BS;
     cuuint64_t gdim[2] = {static_cast<cuuint64_t>(kDim), rows};
     cuuint64_t gstride[1] = {static_cast<cuuint64_t>(kDim) * 2};
-    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(Hkv * BS)};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1, 1};
     CUresult res = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), gdim, gstride, box, estr,
                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return res == CUDA_SUCCESS;
+}
+
+// The same pool seen in three dimensions (64 elements, rows, the two 64-element
+// halves of a row), boxes of 64 x box_rows x 2: both halves of box_rows rows
+// in one copy, landing as [half][row][64] (two 128-byte-swizzled atoms).
+bool encode_pool_box_halves(CUtensorMap* map, const void* pool, int NB, int Hkv, int BS, int box_rows) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc || box_rows < 1 || box_rows > 256) return false;
+    const cuuint64_t rows = static_cast<cuuint64_t>(NB) * Hkv * BS;
+    cuuint64_t gdim[3] = {64, rows, 2};
+    cuuint64_t gstride[2] = {static_cast<cuuint64_t>(kDim) * 2, 128};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult res = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), gdim, gstride, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return res == CUDA_SUCCESS;
+}
+
+// The attention stage: all Hkv * BS rows of one block in one box.
+static bool encode_pool_map(CUtensorMap* map, const void* pool, int NB, int Hkv, int BS) {
+    return encode_pool_box(map, pool, NB, Hkv, BS, Hkv * BS);
 }
 
 int device_sm_count() {

@@ -20,6 +20,12 @@ int device_sm_count();
 cudaError_t launch_sampler(int32_t* tokens, const float* logits, int B, int V, const float* temperature,
                            const int32_t* top_k, const float* top_p, const float* min_p, const uint64_t* seeds,
                            const uint64_t* offsets, int32_t* status, cudaStream_t stream);
+bool prefill_tc_supported(int Hq, int Hkv, int D, int BS, const void* q, const void* out, const void* k,
+                          const void* v);
+cudaError_t launch_prefill_tc(void* out, const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
+                              const int32_t* q_start, int B, int T_new, int Hq, int Hkv, int BS, int NB, float scale,
+                              int32_t* status, cudaStream_t stream);
 cudaError_t launch_typical_sampler(int32_t* tokens, const float* logits, int B, int V, const float* temperature,
                                    const float* typical_p, const uint64_t* seeds, const uint64_t* offsets,
                                    int32_t* status, cudaStream_t stream);
@@ -143,6 +149,10 @@ pkv_status pkv_paged_prefill_attention(void* out, const void* q, const void* k_c
         (reinterpret_cast<uintptr_t>(out) & 3u))
         return PKV_ERR_UNSUPPORTED;
     if (scale <= 0.f) scale = 1.0f / sqrtf(static_cast<float>(D));
+    if (pkv::prefill_tc_supported(Hq, Hkv, D, block_size, q, out, k_cache, v_cache))
+        return cuda_status(pkv::launch_prefill_tc(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                                  seq_lens, q_start, B, T_new, Hq, Hkv, block_size, num_blocks,
+                                                  scale, dev_status, static_cast<cudaStream_t>(stream)));
     return cuda_status(pkv::launch_prefill_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                                      seq_lens, q_start, B, T_new, Hq, Hkv, block_size, num_blocks,
                                                      scale, dev_status, static_cast<cudaStream_t>(stream)));

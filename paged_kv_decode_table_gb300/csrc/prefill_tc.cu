@@ -1,0 +1,519 @@
+// prefill_tc.cu -- chunked-prefill attention on the fifth-generation tensor
+// cores: tcgen05 MMAs with accumulators in tensor memory (TMEM), operands
+// staged in shared memory by TMA.  Same results as prefill_attn_kernel (the
+// chunk's causal GQA attention over the paged cache; "Suy luan & Toi uu hoa
+// (Inference)" 2.1 and 4.1, the lab's prefill step, "LLM inference serving
+// tutorial" 5.4) for bf16, D = 128, G = Hq / Hkv in {1, 2, 4, 8}, block_size a
+// multiple of 16 and 16-byte aligned q / out / pools.
+//
+//  * One CTA per (128 query rows, KV head h).  Row r is (chunk token r / G,
+//    query head h G + r % G): 128 / G consecutive tokens of one sequence times
+//    the G heads that share K/V head h, so each K/V tile serves all of them.
+//  * K and V of head h stream in 64-key tiles through a four-stage ring.  The
+//    paged layout allows TMA boxes of one block's 16 keys at most: K comes in
+//    boxes of 16 keys x 64 dimensions into two 64-row, 128-byte-swizzled atoms
+//    (so that S is one N = 64 MMA per k-step); V in boxes of 16 keys x both
+//    halves (4 KB, a 3-D view of the pool), one per 16-key group (each PV
+//    k-step reads one group).  12 lanes of the producer warp issue a tile's
+//    boxes together; the block ids come from a window of the block table kept
+//    in shared memory.  Each CTA walks its key tiles starting at a different
+//    tile, so that the CTAs sharing a sequence do not read the same blocks at
+//    the same time.
+//  * One MMA lane issues S = Q K^T (M 128, N 64, K 128; Q and K K-major) into
+//    one of two TMEM buffers and O += P V (M 128, N 128, K 64; P K-major from
+//    shared memory, V MN-major, i.e. as stored, one 16-key group per k-step)
+//    into a TMEM accumulator, and
+//    signals completion through mbarriers (tcgen05.commit).  S of tile j + 1
+//    runs while the softmax works on tile j.
+//  * Four softmax warps: thread r owns row r (TMEM lane r).  It reads its 64
+//    scores (tcgen05.ld), applies the causal mask and the scale in the log2
+//    domain, and exponentiates against a reference maximum that is raised only
+//    when the row maximum exceeds it by more than 8, in which case the row of
+//    O in TMEM and the running sum are rescaled first; P (bf16, values at most
+//    2^8) goes to shared memory for the PV MMA, and the sum accumulates the
+//    fp32 values.  Rows past the chunk are computed on zero queries and
+//    not stored.  The V rows of keys at or past the sequence length (which may
+//    hold anything, NaN included) are cleared before the last PV MMA.
+//  * Epilogue: O / sum from TMEM to the bf16 output rows.
+// Every mbarrier wait is bounded; a CTA that gives up records PKV_ERR_TIMEOUT,
+// waits (bounded) for its own TMA copies, and still frees its TMEM.
+#include <cuda.h>
+#include <math.h>
+
+#include "pkv_common.cuh"
+
+namespace pkv {
+
+bool encode_pool_box(CUtensorMap* map, const void* pool, int NB, int Hkv, int BS, int box_rows);
+bool encode_pool_box_halves(CUtensorMap* map, const void* pool, int NB, int Hkv, int BS, int box_rows);
+
+constexpr int kTcDim = 128;
+constexpr int kTcRows = 128;                 // query rows per CTA (TMEM lanes)
+constexpr int kTcKeys = 64;                  // keys per tile
+constexpr int kTcStages = 4;                 // K/V ring depth
+constexpr int kTcQBytes = kTcRows * kTcDim * 2;           // 32 KB: two 64-column atoms of 128 rows
+constexpr int kTcPBytes = kTcRows * kTcKeys * 2;          // 16 KB: one atom of 128 rows
+constexpr int kTcKBytes = kTcKeys * kTcDim * 2;           // 16 KB per operand tile
+constexpr int kTcGroupBytes = 16 * kTcDim * 2;            // 4 KB: 16 keys x 128 dimensions
+constexpr int kTcStageBytes = 2 * kTcKBytes;              // K then V
+constexpr int kTcWin = 512;                  // block-table entries kept in shared memory
+constexpr int kTcThreads = 6 * 32;           // 4 softmax warps, producer warp, MMA warp
+constexpr int kTcTmemCols = 256;             // S buffers at columns 0 and 64, O at 128
+
+struct TcSmem {  // follows the 1024-aligned operand area
+    uint64_t kv_full[kTcStages], kv_empty[kTcStages];
+    uint64_t s_full[2], s_free[2];
+    uint64_t p_full, o_done;
+    uint32_t tmem_base;
+    int b, tile, bad;
+    int tbl[kTcWin];
+};
+constexpr size_t kTcOperandBytes = kTcQBytes + kTcPBytes + kTcStages * static_cast<size_t>(kTcStageBytes);
+constexpr size_t kTcSmemBytes = 1024 + kTcOperandBytes + sizeof(TcSmem);
+
+// ------------------------------------------------------------------ tcgen05 helpers
+// Shared-memory matrix descriptor, 128-byte swizzle: start address, leading
+// byte offset (K-major: unused; MN-major: the stride between 64-element atoms
+// along M / N), stride byte offset (the stride between groups of 8 rows), the
+// descriptor version of this architecture.
+__device__ __forceinline__ uint64_t tc_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Instruction descriptor of kind::f16: bf16 A and B, fp32 accumulator, M x N,
+// B K-major or MN-major (A always K-major here).
+__host__ __device__ constexpr uint32_t tc_idesc(int M, int N, bool b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+// Arrive on bar once every tcgen05 operation this thread issued so far is complete.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// 32 consecutive columns of this thread's TMEM lane (warp w reads lanes 32 (w % 4) ..).
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+        "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
+        "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// Byte offset of (row, 16-byte chunk) in a tile of 128-byte rows with the
+// 128-byte swizzle (the chunk index XOR the row's low three bits).
+__device__ __forceinline__ uint32_t sw128(int row, int chunk) {
+    return static_cast<uint32_t>(row) * 128u + (static_cast<uint32_t>(chunk ^ (row & 7)) << 4);
+}
+__device__ __forceinline__ float tc_ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                      const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ out,
+                      const int32_t* __restrict__ block_tables, int max_blocks, const int32_t* __restrict__ seq_lens,
+                      const int32_t* __restrict__ q_start, int B, int Hq, int Hkv, int BS, int NB, float scale_log2,
+                      int32_t* status) {
+    extern __shared__ uint8_t tc_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sQ = base;
+    uint8_t* sP = base + kTcQBytes;
+    uint8_t* sKV = sP + kTcPBytes;
+    TcSmem* sm = reinterpret_cast<TcSmem*>(base + kTcOperandBytes);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = Hq / Hkv, h = blockIdx.y;
+    const int TQ = kTcRows / G;  // chunk tokens per CTA
+
+    // ---- prologue, independent of the inputs
+    if (tid == 0) {
+        for (int s = 0; s < kTcStages; ++s) {
+            mbar_init(&sm->kv_full[s], 1);
+            mbar_init(&sm->kv_empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm->s_full[i], 1);
+            mbar_init(&sm->s_free[i], kTcRows);
+        }
+        mbar_init(&sm->p_full, kTcRows);
+        mbar_init(&sm->o_done, 1);
+        fence_mbar_init();
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+        sm->b = -1;
+        sm->tile = 0;
+        sm->bad = 0;
+    }
+    if (warp == 5) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&sm->tmem_base)),
+                     "r"(kTcTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the chunk's K/V are in the cache
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    __syncthreads();
+    if (warp == 0) {  // this CTA's tile: tiles of TQ chunk tokens, sequence after sequence
+        int acc = 0;
+        for (int b0 = 0; b0 < B; b0 += 32) {
+            const int bb = b0 + lane;
+            const int n = bb < B ? q_start[bb + 1] - q_start[bb] : 0;
+            const int tiles = n > 0 ? (n + TQ - 1) / TQ : 0;
+            int inc = tiles;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += y;
+            }
+            const int ex = acc + inc - tiles;
+            const int x = static_cast<int>(blockIdx.x);
+            if (tiles > 0 && ex <= x && x < ex + tiles) {
+                sm->b = bb;
+                sm->tile = x - ex;
+            }
+            acc += __shfl_sync(0xffffffffu, inc, 31);
+            if (acc > x) break;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm->tmem_base;
+    const int b = sm->b, tile = sm->tile;
+    bool active = b >= 0;  // a spare CTA of the upper-bound grid has no tile
+    int n = 0, L = 0, t0 = 0, nt = 0, p0 = 0;
+    if (active) {
+        n = q_start[b + 1] - q_start[b];
+        L = seq_lens[b];
+        t0 = q_start[b] + TQ * tile;
+        nt = min(TQ, n - TQ * tile);
+        p0 = L - n + TQ * tile;  // position of the tile's first token
+    }
+    const bool bad_len = active && (L < n || static_cast<long long>(L) > static_cast<long long>(max_blocks) * BS);
+    // this thread's row (softmax warps): token tl of the tile, query head qh
+    const int r = tid, tl = r / G, qh = h * G + (r - tl * G);
+    const bool row_valid = active && tid < kTcRows && tl < nt;
+    if (bad_len) {
+        if (tid == 0) report(status, PKV_ERR_DEVICE_BOUNDS);
+        if (row_valid) {
+            uint4* o = reinterpret_cast<uint4*>(out + (static_cast<size_t>(t0 + tl) * Hq + qh) * kTcDim);
+            for (int c = 0; c < 16; ++c) o[c] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        active = false;
+    }
+    const int plast = p0 + nt - 1;                    // the tile's last position (keys 0 .. plast are read)
+    const int ntiles = active ? plast / kTcKeys + 1 : 0;
+    // iteration j handles key tile (j + rot) mod ntiles (any order gives the same softmax)
+    const int rot = ntiles > 0 ? static_cast<int>((blockIdx.x * 13u + blockIdx.y * 7u) % static_cast<unsigned>(ntiles)) : 0;
+    const int nblk_used = active ? plast / BS + 1 : 0;
+    const int pos = row_valid ? p0 + tl : plast;      // the row's position (rows past the chunk: the last)
+
+    // ---- the query tile: row r into two 128-byte-swizzled atoms (rows past the chunk: zeros)
+    if (active && tid < kTcRows) {
+        const uint4* src = reinterpret_cast<const uint4*>(q + (static_cast<size_t>(t0 + (row_valid ? tl : 0)) * Hq + qh) * kTcDim);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            const uint4 v = row_valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(sQ + (c >> 3) * (kTcQBytes / 2) + sw128(r, c & 7)) = v;
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    bool fail = false;
+    if (warp == 4 && active) {
+        // ------------------------------------------------ producer warp
+        const int32_t* trow = block_tables + static_cast<size_t>(b) * max_blocks;
+        int win0 = -kTcWin;
+        for (int j = 0; j < ntiles && !fail; ++j) {
+            const int s = j % kTcStages;
+            const int kt = j + rot < ntiles ? j + rot : j + rot - ntiles;
+            const int kb0 = (kt * kTcKeys) / BS, kb1 = min(nblk_used - 1, (kt * kTcKeys + kTcKeys - 1) / BS);
+            if (kb0 < win0 || kb1 >= win0 + kTcWin) {  // move the block-table window (whole warp)
+                __syncwarp();
+                win0 = kb0;
+                for (int i = lane; i < kTcWin; i += 32) sm->tbl[i] = win0 + i < nblk_used ? trow[win0 + i] : 0;
+                __syncwarp();
+            }
+            // lane 0 waits for the stage and arms its transaction count; then 12
+            // lanes issue the tile's boxes at once
+            int y = 0;
+            if (lane == 0) {
+                if (!mbar_wait(&sm->kv_empty[s], ((j / kTcStages) & 1) ^ 1)) {
+                    report(status, PKV_ERR_TIMEOUT);
+                    fail = true;
+                }
+            }
+            fail = __shfl_sync(0xffffffffu, fail, 0);
+            if (fail) break;
+            if (lane < kTcKeys / 16) {  // the rows of 16-key box `lane` (a bad block id is flagged
+                                        // before the arrive below, which orders it ahead of the epilogue)
+                const int key0 = kt * kTcKeys + 16 * lane;
+                const int kb = key0 / BS;
+                int blk = 0, slot = 0;
+                if (kb < nblk_used) {  // later keys: any valid rows (masked; their V rows are cleared)
+                    blk = sm->tbl[kb - win0];
+                    slot = key0 - kb * BS;
+                    if (blk < 0 || blk >= NB) {
+                        sm->bad = 1;
+                        report(status, PKV_ERR_DEVICE_BOUNDS);
+                        blk = 0;
+                    }
+                }
+                y = (blk * Hkv + h) * BS + slot;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(&sm->kv_full[s], kTcStageBytes);
+            __syncwarp();
+            {
+                // lanes 0-7: K, group lane >> 1, half lane & 1 (2 KB each, into the two
+                // 64-row atoms); lanes 8-11: V, group lane - 8, both halves (4 KB)
+                const int grp = lane < 8 ? lane >> 1 : lane - 8;
+                const int yb = __shfl_sync(0xffffffffu, y, grp & 3);
+                uint8_t* st = sKV + static_cast<size_t>(s) * kTcStageBytes;
+                if (lane < 8)
+                    tma_load_2d(st + (lane & 1) * (kTcKBytes / 2) + 2048 * grp, &tmK, 64 * (lane & 1), yb,
+                                &sm->kv_full[s]);
+                else if (lane < 12)
+                    tma_load_3d(st + kTcKBytes + kTcGroupBytes * grp, &tmV, 0, yb, 0, &sm->kv_full[s]);
+            }
+        }
+        // no copy of this CTA may still be in flight when it exits
+        if (lane == 0)
+            for (int j = max(0, ntiles - kTcStages); j < ntiles; ++j)
+                mbar_wait(&sm->kv_full[j % kTcStages], (j / kTcStages) & 1);
+    } else if (warp == 5 && active) {
+        // ------------------------------------------------ MMA warp (lane 0 issues)
+        if (lane == 0) {
+            const uint32_t tS0 = tmem, tO = tmem + 128;
+            constexpr uint32_t idS = tc_idesc(kTcRows, kTcKeys, false), idO = tc_idesc(kTcRows, kTcDim, true);
+            const uint32_t qa = smem_u32(sQ), pa = smem_u32(sP), kva = smem_u32(sKV);
+            auto issue_pv = [&](int jj) -> bool {  // O += P_jj V_jj
+                if (!mbar_wait(&sm->p_full, jj & 1)) return false;
+                tc_fence_after();
+                const uint32_t vb = kva + (jj % kTcStages) * kTcStageBytes + kTcKBytes;
+#pragma unroll
+                for (int kk = 0; kk < kTcKeys / 16; ++kk)
+                    tc_mma(tO, tc_desc(pa + 32 * kk, 16, 1024), tc_desc(vb + kTcGroupBytes * kk, kTcGroupBytes / 2, 1024),
+                           idO, (jj > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(&sm->o_done);
+                tc_commit(&sm->kv_empty[jj % kTcStages]);
+                return true;
+            };
+            for (int j = 0; j < ntiles && !fail; ++j) {
+                const int s = j % kTcStages;
+                if (!mbar_wait(&sm->kv_full[s], (j / kTcStages) & 1) ||
+                    (j >= 2 && !mbar_wait(&sm->s_free[j & 1], ((j >> 1) - 1) & 1))) {
+                    fail = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t kb = kva + s * kTcStageBytes;
+#pragma unroll
+                for (int kk = 0; kk < kTcDim / 16; ++kk)
+                    tc_mma(tS0 + 64 * (j & 1), tc_desc(qa + (kk >> 2) * (kTcQBytes / 2) + 32 * (kk & 3), 16, 1024),
+                           tc_desc(kb + (kk >> 2) * (kTcKBytes / 2) + 32 * (kk & 3), 16, 1024), idS,
+                           kk > 0 ? 1u : 0u);
+                tc_commit(&sm->s_full[j & 1]);
+                if (j >= 1 && !issue_pv(j - 1)) fail = true;
+            }
+            if (!fail && ntiles > 0 && !issue_pv(ntiles - 1)) fail = true;
+            if (fail) report(status, PKV_ERR_TIMEOUT);
+        }
+        __syncwarp();
+    } else if (warp < 4 && active) {
+        // ------------------------------------------------ softmax warps: thread r owns row r
+        const uint32_t lrow = static_cast<uint32_t>(warp * 32) << 16;  // this warp's TMEM lanes
+        float m_ref = -INFINITY, lsum = 0.f;
+        for (int j = 0; j < ntiles; ++j) {
+            const int buf = j & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&sm->s_full[buf], (j >> 1) & 1))) {  // tcgen05.ld needs the whole warp
+                fail = true;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sr[2][32];
+            tc_ld32(tmem + lrow + 64 * buf, sr[0]);
+            tc_ld32(tmem + lrow + 64 * buf + 32, sr[1]);
+            tc_fence_before();
+            mbar_arrive(&sm->s_free[buf]);  // the buffer may take S of tile j + 2
+            const int kt = j + rot < ntiles ? j + rot : j + rot - ntiles;
+            const int kbase = kt * kTcKeys;
+            // maximum of the raw scores (the scale is positive), eight chains;
+            // the causal mask only on tiles that reach past the tile's first position
+            float mxs[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mxs[k] = -INFINITY;
+            if (kbase + kTcKeys - 1 > p0) {
+#pragma unroll
+                for (int c = 0; c < kTcKeys; ++c) {
+                    const float v = kbase + c <= pos ? __uint_as_float(sr[c >> 5][c & 31]) : -INFINITY;
+                    sr[c >> 5][c & 31] = __float_as_uint(v);
+                    mxs[c & 7] = fmaxf(mxs[c & 7], v);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < kTcKeys; ++c) mxs[c & 7] = fmaxf(mxs[c & 7], __uint_as_float(sr[c >> 5][c & 31]));
+            }
+            const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
+                                   fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7]))) *
+                             scale_log2;
+            // the reference maximum moves only when the row maximum passes it by more than 8
+            const float m_new = mx > m_ref + 8.f ? mx : m_ref;
+            const bool resc = m_new != m_ref;
+            const float a = resc ? tc_ex2(m_ref - m_new) : 1.f;
+            m_ref = m_new;
+            const float nmu = m_ref == -INFINITY ? 0.f : -m_ref;
+            // P = 2^(s scale - m_ref) (masked scores give 0), the sum in eight chains
+            uint32_t pk[kTcKeys / 2];
+            float ls[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+#pragma unroll
+            for (int c = 0; c < kTcKeys / 2; ++c) {
+                const float e0 = tc_ex2(fmaf(__uint_as_float(sr[(2 * c) >> 5][(2 * c) & 31]), scale_log2, nmu));
+                const float e1 = tc_ex2(fmaf(__uint_as_float(sr[(2 * c + 1) >> 5][(2 * c + 1) & 31]), scale_log2, nmu));
+                pk[c] = pack_bf16x2(e0, e1);
+                ls[c & 7] += e0 + e1;
+            }
+            lsum = lsum * a + (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
+            // PV of tile j - 1 must be complete before O is rescaled or P is overwritten
+            if (j > 0) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&sm->o_done, (j - 1) & 1))) {
+                    fail = true;
+                    break;
+                }
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+                    for (int cc = 0; cc < kTcDim / 32; ++cc) {
+                        uint32_t o[32];
+                        tc_ld32(tmem + lrow + 128 + 32 * cc, o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
+                        tc_st32(tmem + lrow + 128 + 32 * cc, o);
+                    }
+                }
+            }
+            if (kt == ntiles - 1) {  // the V rows of keys at or past L may hold anything: clear them
+                const int rlo = max(0, min(kTcKeys, L - kbase));
+                uint8_t* vb = sKV + static_cast<size_t>(j % kTcStages) * kTcStageBytes + kTcKBytes;
+                for (int idx = tid; idx < (kTcKeys - rlo) * 16; idx += kTcRows) {
+                    const int rr = rlo + (idx >> 4), half = (idx >> 3) & 1, ch = idx & 7;
+                    *reinterpret_cast<uint4*>(vb + kTcGroupBytes * (rr >> 4) + half * (kTcGroupBytes / 2) +
+                                              (rr & 15) * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            // P row r (64 bf16 = 8 chunks of 16 bytes) into the K-major P tile
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+                *reinterpret_cast<uint4*>(sP + sw128(r, ch)) =
+                    make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&sm->p_full);
+        }
+        // ---- epilogue: O / sum of the last PV
+        if (!fail && ntiles > 0 && !__all_sync(0xffffffffu, mbar_wait(&sm->o_done, (ntiles - 1) & 1))) fail = true;
+        if (fail) {
+            if (lane == 0) report(status, PKV_ERR_TIMEOUT);
+        } else {
+            tc_fence_after();
+            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+            const bool store = row_valid && !sm->bad;
+            uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(t0 + (row_valid ? tl : 0)) * Hq + qh) * kTcDim);
+#pragma unroll 1
+            for (int cc = 0; cc < kTcDim / 32; ++cc) {
+                uint32_t o[32];
+                tc_ld32(tmem + lrow + 128 + 32 * cc, o);
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+                if (row_valid) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        dst[4 * cc + k] = store ? make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3])
+                                                : make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+        }
+    }
+    // ---- every role is done with TMEM
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcTmemCols)
+                     : "memory");
+    }
+}
+
+bool prefill_tc_supported(int Hq, int Hkv, int D, int BS, const void* q, const void* out, const void* k,
+                          const void* v) {
+    const int G = Hkv > 0 ? Hq / Hkv : 0;
+    auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    return D == kTcDim && BS % 16 == 0 && (G == 1 || G == 2 || G == 4 || G == 8) && a16(q) && a16(out) && a16(k) &&
+           a16(v);
+}
+
+cudaError_t launch_prefill_tc(void* out, const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
+                              const int32_t* q_start, int B, int T_new, int Hq, int Hkv, int BS, int NB, float scale,
+                              int32_t* status, cudaStream_t stream) {
+    const int G = Hq / Hkv, TQ = kTcRows / G;
+    const long long tiles = static_cast<long long>(T_new) / TQ + B;
+    if (tiles > 0x7fffffffLL || Hkv > 65535) return cudaErrorInvalidConfiguration;
+    CUtensorMap tmK, tmV;
+    if (!encode_pool_box(&tmK, k_cache, NB, Hkv, BS, 16) || !encode_pool_box_halves(&tmV, v_cache, NB, Hkv, BS, 16))
+        return cudaErrorInvalidValue;
+    cudaError_t err = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(kTcSmemBytes));
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(Hkv), 1);
+    cfg.blockDim = dim3(kTcThreads, 1, 1);
+    cfg.dynamicSmemBytes = kTcSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const float scale_log2 = scale * 1.4426950408889634f;
+    err = cudaLaunchKernelEx(&cfg, prefill_tc_kernel, tmK, tmV, static_cast<const __nv_bfloat16*>(q),
+                             static_cast<__nv_bfloat16*>(out), block_tables, max_blocks, seq_lens, q_start, B, Hq, Hkv,
+                             BS, NB, scale_log2, status);
+    if (err != cudaSuccess) return err;
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -87,6 +87,8 @@ def _check(inp, rows=None):
     ([1, 16, 37, 0, 100], 300, 32, 8, 16),
     ([5, 33], 2000, 64, 8, 16),     # 8 query heads per KV head
     ([17, 64, 3], 500, 8, 8, 32),   # one query head per KV head, 32-token blocks
+    ([40, 7, 130], 700, 16, 8, 16),  # two query heads per KV head
+    ([33, 90], 900, 24, 8, 16),      # three per KV head: the mma.sync kernel (no 128-row tile)
 ])
 def test_prefill_matches_oracle(chunks, prefix_hi, Hq, Hkv, BS):
     inp = _inputs(sum(chunks) + prefix_hi, chunks, prefix_hi, Hq=Hq, Hkv=Hkv, BS=BS)
