@@ -672,6 +672,52 @@ def run_extras(args):
     return 0
 
 
+def run_prefill_case(args):
+    """The small chunked-prefill case the prefill profile is captured on: 4
+    sequences with a 512-token chunk each after a 1024..4096-token prefix, 32
+    query / 8 KV heads, D 128, block 16, bf16; `--warmup` untimed calls, then
+    `--steps` timed ones (CUDA events on the stream)."""
+    import paged_kv_decode_table_gb300 as pkv
+    from paged_kv_decode_table_gb300 import build as pkv_build
+    pkv_build.build()
+    pkv.load_library()
+    dev = torch.device("cuda", 0)
+    Bp, chunk, Hq, Hkv, D, BS = 4, 512, 32, 8, 128, 16
+    gen = torch.Generator().manual_seed(5)
+    prefix = torch.randint(1024, 4097, (Bp,), generator=gen)
+    L = (prefix + chunk).to(torch.int32)
+    nb = (L + BS - 1) // BS
+    NB = int(nb.sum())
+    perm = torch.randperm(NB, generator=gen).to(torch.int32)
+    bt = torch.full((Bp, int(nb.max())), -1, dtype=torch.int32)
+    o = 0
+    for b in range(Bp):
+        bt[b, :nb[b]] = perm[o:o + int(nb[b])]
+        o += int(nb[b])
+    g = torch.Generator(device=dev)
+    g.manual_seed(6)
+    K = torch.randn((NB, Hkv, BS, D), generator=g, device=dev).to(torch.bfloat16)
+    V = torch.randn((NB, Hkv, BS, D), generator=g, device=dev).to(torch.bfloat16)
+    q = torch.randn((Bp * chunk, Hq, D), generator=g, device=dev).to(torch.bfloat16)
+    qs = torch.arange(0, Bp * chunk + 1, chunk, dtype=torch.int32, device=dev)
+    bt, L = bt.to(dev), L.to(dev)
+    out = torch.empty_like(q)
+    st = pkv.new_status()
+    for _ in range(args.warmup):
+        pkv.paged_prefill_attention(q, K, V, bt, L, qs, out=out, status=st)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        pkv.paged_prefill_attention(q, K, V, bt, L, qs, out=out, status=st)
+    e1.record()
+    torch.cuda.synchronize()
+    assert pkv.check_status(st) == 0
+    print(json.dumps({"case": "prefill 4 x 512-token chunks", "calls": args.steps,
+                      "us_per_call": e0.elapsed_time(e1) / max(1, args.steps) * 1000}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -681,7 +727,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--extras", action="store_true",
                     help="print extra measurement lines (other workloads, sampler alone, block copies)")
+    ap.add_argument("--prefill-case", action="store_true",
+                    help="time the small chunked-prefill case of the prefill profile (--warmup, --steps calls)")
     args = ap.parse_args()
+    if args.prefill_case:
+        return run_prefill_case(args)
     if args.impl == "reference":
         return run_reference(args)
     if args.extras:
