@@ -56,19 +56,20 @@ constexpr int kTcPBytes = kTcRows * kTcKeys * 2;          // 16 KB: one atom of 
 constexpr int kTcKBytes = kTcKeys * kTcDim * 2;           // 16 KB per operand tile
 constexpr int kTcGroupBytes = 16 * kTcDim * 2;            // 4 KB: 16 keys x 128 dimensions
 constexpr int kTcStageBytes = 2 * kTcKBytes;              // K then V
-constexpr int kTcWin = 512;                  // block-table entries kept in shared memory
-constexpr int kTcThreads = 6 * 32;           // 4 softmax warps, producer warp, MMA warp
+constexpr int kTcWin = 2048;                 // block-table entries kept in shared memory
+constexpr int kTcThreads = 8 * 32;           // 4 softmax warps, producer warp 4, MMA warp 5, producer warps 6-7
 constexpr int kTcTmemCols = 256;             // S buffers at columns 0 and 64, O at 128
 
 struct TcSmem {  // follows the 1024-aligned operand area
     uint64_t kv_full[kTcStages], kv_empty[kTcStages];
     uint64_t s_full[2], s_free[2];
-    uint64_t p_full, o_done;
+    uint64_t p_full[2], o_done[2];  // per P buffer
     uint32_t tmem_base;
     int b, tile, bad;
+    int rows[kTcStages][4];  // pool rows of the tile's four 16-key boxes, per stage
     int tbl[kTcWin];
 };
-constexpr size_t kTcOperandBytes = kTcQBytes + kTcPBytes + kTcStages * static_cast<size_t>(kTcStageBytes);
+constexpr size_t kTcOperandBytes = kTcQBytes + 2 * kTcPBytes + kTcStages * static_cast<size_t>(kTcStageBytes);
 constexpr size_t kTcSmemBytes = 1024 + kTcOperandBytes + sizeof(TcSmem);
 
 // ------------------------------------------------------------------ tcgen05 helpers
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = base;
     uint8_t* sP = base + kTcQBytes;
-    uint8_t* sKV = sP + kTcPBytes;
+    uint8_t* sKV = sP + 2 * kTcPBytes;  // P is double-buffered
     TcSmem* sm = reinterpret_cast<TcSmem*>(base + kTcOperandBytes);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = Hq / Hkv, h = blockIdx.y;
@@ -160,8 +161,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&sm->s_full[i], 1);
             mbar_init(&sm->s_free[i], kTcRows);
         }
-        mbar_init(&sm->p_full, kTcRows);
-        mbar_init(&sm->o_done, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm->p_full[i], kTcRows);
+            mbar_init(&sm->o_done[i], 1);
+        }
         fence_mbar_init();
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
@@ -249,62 +252,71 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
 
     bool fail = false;
-    if (warp == 4 && active) {
-        // ------------------------------------------------ producer warp
+    if ((warp == 4 || warp >= 6) && active) {
+        // ------------------------------------------------ producer warps 4, 6, 7
+        // Warp 4 waits for the stage, reads the tile's four block rows, arms the
+        // stage's transaction count and meets warps 6 and 7 at a named
+        // barrier; then each issues four boxes (warp 4: K groups 0-1, warp 6: K
+        // groups 2-3, warp 7: V).  Copies issued from one warp serialise, so
+        // three warps load a tile about three times faster.
+        const int pw = warp == 4 ? 0 : warp - 5;
         const int32_t* trow = block_tables + static_cast<size_t>(b) * max_blocks;
         int win0 = -kTcWin;
         for (int j = 0; j < ntiles && !fail; ++j) {
             const int s = j % kTcStages;
             const int kt = j + rot < ntiles ? j + rot : j + rot - ntiles;
-            const int kb0 = (kt * kTcKeys) / BS, kb1 = min(nblk_used - 1, (kt * kTcKeys + kTcKeys - 1) / BS);
-            if (kb0 < win0 || kb1 >= win0 + kTcWin) {  // move the block-table window (whole warp)
-                __syncwarp();
-                win0 = kb0;
-                for (int i = lane; i < kTcWin; i += 32) sm->tbl[i] = win0 + i < nblk_used ? trow[win0 + i] : 0;
-                __syncwarp();
-            }
-            // lane 0 waits for the stage and arms its transaction count; then 12
-            // lanes issue the tile's boxes at once
-            int y = 0;
-            if (lane == 0) {
-                if (!mbar_wait(&sm->kv_empty[s], ((j / kTcStages) & 1) ^ 1)) {
+            if (pw == 0) {
+                const int kb0 = (kt * kTcKeys) / BS, kb1 = min(nblk_used - 1, (kt * kTcKeys + kTcKeys - 1) / BS);
+                if (kb0 < win0 || kb1 >= win0 + kTcWin) {  // move the block-table window (warp 4 alone reads it)
+                    __syncwarp();
+                    win0 = kb0;
+                    for (int i = lane; i < kTcWin; i += 32) sm->tbl[i] = win0 + i < nblk_used ? trow[win0 + i] : 0;
+                    __syncwarp();
+                }
+                if (lane == 0 && !mbar_wait(&sm->kv_empty[s], ((j / kTcStages) & 1) ^ 1)) {
                     report(status, PKV_ERR_TIMEOUT);
                     fail = true;
                 }
-            }
-            fail = __shfl_sync(0xffffffffu, fail, 0);
-            if (fail) break;
-            if (lane < kTcKeys / 16) {  // the rows of 16-key box `lane` (a bad block id is flagged
-                                        // before the arrive below, which orders it ahead of the epilogue)
-                const int key0 = kt * kTcKeys + 16 * lane;
-                const int kb = key0 / BS;
-                int blk = 0, slot = 0;
-                if (kb < nblk_used) {  // later keys: any valid rows (masked; their V rows are cleared)
-                    blk = sm->tbl[kb - win0];
-                    slot = key0 - kb * BS;
-                    if (blk < 0 || blk >= NB) {
-                        sm->bad = 1;
-                        report(status, PKV_ERR_DEVICE_BOUNDS);
-                        blk = 0;
+                fail = __shfl_sync(0xffffffffu, fail, 0);
+                if (!fail && lane < kTcKeys / 16) {  // the rows of 16-key box `lane` (a bad block id is
+                                                      // flagged before the arrive below)
+                    const int key0 = kt * kTcKeys + 16 * lane;
+                    const int kb = key0 / BS;
+                    int blk = 0, slot = 0;
+                    if (kb < nblk_used) {  // later keys: any valid rows (masked; their V rows are cleared)
+                        blk = sm->tbl[kb - win0];
+                        slot = key0 - kb * BS;
+                        if (blk < 0 || blk >= NB) {
+                            sm->bad = 1;
+                            report(status, PKV_ERR_DEVICE_BOUNDS);
+                            blk = 0;
+                        }
                     }
+                    sm->rows[s][lane] = (blk * Hkv + h) * BS + slot;
                 }
-                y = (blk * Hkv + h) * BS + slot;
+                __syncwarp();
+                if (!fail && lane == 0) mbar_arrive_expect_tx(&sm->kv_full[s], kTcStageBytes);
+                if (lane == 0) sm->rows[s][0] |= fail ? static_cast<int>(0x80000000u) : 0;  // tell the others
+                __syncwarp();
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive_expect_tx(&sm->kv_full[s], kTcStageBytes);
-            __syncwarp();
-            {
-                // lanes 0-7: K, group lane >> 1, half lane & 1 (2 KB each, into the two
-                // 64-row atoms); lanes 8-11: V, group lane - 8, both halves (4 KB)
-                const int grp = lane < 8 ? lane >> 1 : lane - 8;
-                const int yb = __shfl_sync(0xffffffffu, y, grp & 3);
+            asm volatile("bar.sync 1, 96;" ::: "memory");  // the rows are published (warps 4, 6, 7)
+            const int r0 = sm->rows[s][0];
+            if (r0 < 0) {  // warp 4 gave up
+                fail = true;
+                break;
+            }
+            if (lane < 4) {
                 uint8_t* st = sKV + static_cast<size_t>(s) * kTcStageBytes;
-                if (lane < 8)
-                    tma_load_2d(st + (lane & 1) * (kTcKBytes / 2) + 2048 * grp, &tmK, 64 * (lane & 1), yb,
+                if (pw < 2) {  // K: group 2 pw + lane / 2, half lane & 1 (2 KB into the two 64-row atoms)
+                    const int grp = 2 * pw + (lane >> 1);
+                    tma_load_2d(st + (lane & 1) * (kTcKBytes / 2) + 2048 * grp, &tmK, 64 * (lane & 1),
+                                sm->rows[s][grp], &sm->kv_full[s]);
+                } else {  // V: group lane, both halves (4 KB)
+                    tma_load_3d(st + kTcKBytes + kTcGroupBytes * lane, &tmV, 0, sm->rows[s][lane], 0,
                                 &sm->kv_full[s]);
-                else if (lane < 12)
-                    tma_load_3d(st + kTcKBytes + kTcGroupBytes * grp, &tmV, 0, yb, 0, &sm->kv_full[s]);
+                }
             }
+            __syncwarp();
         }
         // no copy of this CTA may still be in flight when it exits
         if (lane == 0)
@@ -316,15 +328,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t tS0 = tmem, tO = tmem + 128;
             constexpr uint32_t idS = tc_idesc(kTcRows, kTcKeys, false), idO = tc_idesc(kTcRows, kTcDim, true);
             const uint32_t qa = smem_u32(sQ), pa = smem_u32(sP), kva = smem_u32(sKV);
-            auto issue_pv = [&](int jj) -> bool {  // O += P_jj V_jj
-                if (!mbar_wait(&sm->p_full, jj & 1)) return false;
+            auto issue_pv = [&](int jj) -> bool {  // O += P_jj V_jj (P buffer jj & 1)
+                if (!mbar_wait(&sm->p_full[jj & 1], (jj >> 1) & 1)) return false;
                 tc_fence_after();
                 const uint32_t vb = kva + (jj % kTcStages) * kTcStageBytes + kTcKBytes;
+                const uint32_t pb = pa + (jj & 1) * kTcPBytes;
 #pragma unroll
                 for (int kk = 0; kk < kTcKeys / 16; ++kk)
-                    tc_mma(tO, tc_desc(pa + 32 * kk, 16, 1024), tc_desc(vb + kTcGroupBytes * kk, kTcGroupBytes / 2, 1024),
+                    tc_mma(tO, tc_desc(pb + 32 * kk, 16, 1024), tc_desc(vb + kTcGroupBytes * kk, kTcGroupBytes / 2, 1024),
                            idO, (jj > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(&sm->o_done);
+                tc_commit(&sm->o_done[jj & 1]);
                 tc_commit(&sm->kv_empty[jj % kTcStages]);
                 return true;
             };
@@ -405,14 +418,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 ls[c & 7] += e0 + e1;
             }
             lsum = lsum * a + (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
-            // PV of tile j - 1 must be complete before O is rescaled or P is overwritten
-            if (j > 0) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&sm->o_done, (j - 1) & 1))) {
+            // O is rescaled only once the PV of tile j - 1 is complete; P_j goes to
+            // buffer j & 1 once the PV of tile j - 2 has read it
+            if (j > 0 && __any_sync(0xffffffffu, resc)) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&sm->o_done[(j - 1) & 1], ((j - 1) >> 1) & 1))) {
                     fail = true;
                     break;
                 }
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, resc)) {
+                {
 #pragma unroll 1
                     for (int cc = 0; cc < kTcDim / 32; ++cc) {
                         uint32_t o[32];
@@ -432,17 +446,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                               (rr & 15) * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
+            if (j >= 2) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&sm->o_done[j & 1], ((j - 2) >> 1) & 1))) {
+                    fail = true;
+                    break;
+                }
+                tc_fence_after();
+            }
             // P row r (64 bf16 = 8 chunks of 16 bytes) into the K-major P tile
+            uint8_t* pbuf = sP + (j & 1) * kTcPBytes;
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch)
-                *reinterpret_cast<uint4*>(sP + sw128(r, ch)) =
+                *reinterpret_cast<uint4*>(pbuf + sw128(r, ch)) =
                     make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(&sm->p_full);
+            mbar_arrive(&sm->p_full[j & 1]);
         }
         // ---- epilogue: O / sum of the last PV
-        if (!fail && ntiles > 0 && !__all_sync(0xffffffffu, mbar_wait(&sm->o_done, (ntiles - 1) & 1))) fail = true;
+        if (!fail && ntiles > 0 &&
+            !__all_sync(0xffffffffu, mbar_wait(&sm->o_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1)))
+            fail = true;
         if (fail) {
             if (lane == 0) report(status, PKV_ERR_TIMEOUT);
         } else {
