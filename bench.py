@@ -673,16 +673,17 @@ def run_extras(args):
 
 
 def run_prefill_case(args):
-    """The small chunked-prefill case the prefill profile is captured on: 4
-    sequences with a 512-token chunk each after a 1024..4096-token prefix, 32
-    query / 8 KV heads, D 128, block 16, bf16; `--warmup` untimed calls, then
-    `--steps` timed ones (CUDA events on the stream)."""
+    """The chunked-prefill case the prefill profile is captured on:
+    `--prefill-seqs` sequences (default 4) with a 512-token chunk each after a
+    1024..4096-token prefix, 32 query / 8 KV heads, D 128, block 16, bf16;
+    `--warmup` untimed calls, then `--steps` timed ones (CUDA events on the
+    stream)."""
     import paged_kv_decode_table_gb300 as pkv
     from paged_kv_decode_table_gb300 import build as pkv_build
     pkv_build.build()
     pkv.load_library()
     dev = torch.device("cuda", 0)
-    Bp, chunk, Hq, Hkv, D, BS = 4, 512, 32, 8, 128, 16
+    Bp, chunk, Hq, Hkv, D, BS = args.prefill_seqs, 512, 32, 8, 128, 16
     gen = torch.Generator().manual_seed(5)
     prefix = torch.randint(1024, 4097, (Bp,), generator=gen)
     L = (prefix + chunk).to(torch.int32)
@@ -713,7 +714,7 @@ def run_prefill_case(args):
     e1.record()
     torch.cuda.synchronize()
     assert pkv.check_status(st) == 0
-    print(json.dumps({"case": "prefill 4 x 512-token chunks", "calls": args.steps,
+    print(json.dumps({"case": f"prefill {Bp} x 512-token chunks", "calls": args.steps,
                       "us_per_call": e0.elapsed_time(e1) / max(1, args.steps) * 1000}))
     return 0
 
@@ -729,6 +730,7 @@ def main():
                     help="print extra measurement lines (other workloads, sampler alone, block copies)")
     ap.add_argument("--prefill-case", action="store_true",
                     help="time the small chunked-prefill case of the prefill profile (--warmup, --steps calls)")
+    ap.add_argument("--prefill-seqs", type=int, default=4, help="sequences of the --prefill-case workload")
     args = ap.parse_args()
     if args.prefill_case:
         return run_prefill_case(args)

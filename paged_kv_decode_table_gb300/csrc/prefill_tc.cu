@@ -44,33 +44,34 @@
 
 namespace pkv {
 
-bool encode_pool_box(CUtensorMap* map, const void* pool, int NB, int Hkv, int BS, int box_rows);
 bool encode_pool_box_halves(CUtensorMap* map, const void* pool, int NB, int Hkv, int BS, int box_rows);
 
 constexpr int kTcDim = 128;
-constexpr int kTcRows = 128;                 // query rows per CTA (TMEM lanes)
+constexpr int kTcRows = 128;                 // query rows per query tile (TMEM lanes)
+constexpr int kTcQT = 2;                     // query tiles per CTA, sharing every K/V tile
 constexpr int kTcKeys = 64;                  // keys per tile
-constexpr int kTcStages = 4;                 // K/V ring depth
-constexpr int kTcQBytes = kTcRows * kTcDim * 2;           // 32 KB: two 64-column atoms of 128 rows
-constexpr int kTcPBytes = kTcRows * kTcKeys * 2;          // 16 KB: one atom of 128 rows
+constexpr int kTcStages = 6;                 // K/V ring depth
 constexpr int kTcKBytes = kTcKeys * kTcDim * 2;           // 16 KB per operand tile
 constexpr int kTcGroupBytes = 16 * kTcDim * 2;            // 4 KB: 16 keys x 128 dimensions
 constexpr int kTcStageBytes = 2 * kTcKBytes;              // K then V
 constexpr int kTcWin = 2048;                 // block-table entries kept in shared memory
-constexpr int kTcThreads = 8 * 32;           // 4 softmax warps, producer warp 4, MMA warp 5, producer warps 6-7
-constexpr int kTcTmemCols = 256;             // S buffers at columns 0 and 64, O at 128
+// warps 0-7: softmax (warp w: query tile w / 4, TMEM lanes 32 (w % 4) ..); warp 8:
+// producer (block rows); warp 9: S MMAs; warp 10: PV MMAs; warps 11-12: producers
+constexpr int kTcWarpProd = 8, kTcWarpS = 9, kTcWarpPV = 10;
+constexpr int kTcThreads = 13 * 32;
+constexpr int kTcTmemCols = 512;             // query tile t: Q at 256 t, S (then P) at 256 t + 64, O at 256 t + 128
 
 struct TcSmem {  // follows the 1024-aligned operand area
     uint64_t kv_full[kTcStages], kv_empty[kTcStages];
-    uint64_t s_full[2], s_free[2];
-    uint64_t p_full[2], o_done[2];  // per P buffer
+    uint64_t s_full[kTcQT], p_full[kTcQT], o_done[kTcQT];
     uint32_t tmem_base;
     int b, tile, bad;
     int rows[kTcStages][4];  // pool rows of the tile's four 16-key boxes, per stage
     int tbl[kTcWin];
 };
-constexpr size_t kTcOperandBytes = kTcQBytes + 2 * kTcPBytes + kTcStages * static_cast<size_t>(kTcStageBytes);
+constexpr size_t kTcOperandBytes = kTcStages * static_cast<size_t>(kTcStageBytes);
 constexpr size_t kTcSmemBytes = 1024 + kTcOperandBytes + sizeof(TcSmem);
+static_assert(kTcSmemBytes <= 227 * 1024, "shared memory of one CTA");
 
 // ------------------------------------------------------------------ tcgen05 helpers
 // Shared-memory matrix descriptor, 128-byte swizzle: start address, leading
@@ -92,6 +93,14 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, 
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+// The same with A (M x 16 bf16, row m in TMEM lane m, two elements per column) in tensor memory.
+__device__ __forceinline__ void tc_mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
 // Arrive on bar once every tcgen05 operation this thread issued so far is complete.
@@ -129,10 +138,45 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32])
 __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
     return static_cast<uint32_t>(row) * 128u + (static_cast<uint32_t>(chunk ^ (row & 7)) << 4);
 }
+// 4-D tiled copy (the K boxes); x, y, z, w are the box's start coordinates.
+__device__ __forceinline__ void tma_load_4d(void* smem_dst, const void* tmap, int x, int y, int z, int w,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+        "[%6];" ::"r"(smem_u32(smem_dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+        : "memory");
+}
 __device__ __forceinline__ float tc_ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+__device__ __forceinline__ int warp_sum_i(int x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+__device__ __forceinline__ int warp_max_i(int x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = max(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+// Chunk tiles of one sequence (n chunk tokens, length L after the chunk, TC
+// tokens per tile) that read more than v key tiles.  Full tile c reads up to
+// position L - n + TC (c + 1) - 1, the last tile up to L - 1; the count grows
+// with c.  L below n (an invalid length, reported by the CTA that owns the
+// tile) is taken as n, so that the order is defined for any input.
+__device__ __forceinline__ int tc_tiles_longer(int n, int L, int TC, int v) {
+    if (n <= 0) return 0;
+    const int tiles = (n + TC - 1) / TC;
+    const long long Lc = max(L, n), P = Lc - n;
+    int cnt = (Lc - 1) / kTcKeys + 1 > v ? 1 : 0;
+    const long long x = static_cast<long long>(kTcKeys) * v - P + 1;  // full tile c qualifies iff TC (c + 1) >= x
+    const long long cmin = x <= 0 ? 0 : (x + TC - 1) / TC - 1;
+    cnt += static_cast<int>(max(0LL, static_cast<long long>(tiles - 1) - cmin));
+    return cnt;
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -143,13 +187,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                       int32_t* status) {
     extern __shared__ uint8_t tc_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sQ = base;
-    uint8_t* sP = base + kTcQBytes;
-    uint8_t* sKV = sP + 2 * kTcPBytes;  // P is double-buffered
+    uint8_t* sKV = base;
     TcSmem* sm = reinterpret_cast<TcSmem*>(base + kTcOperandBytes);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int G = Hq / Hkv, h = blockIdx.y;
-    const int TQ = kTcRows / G;  // chunk tokens per CTA
+    const int G = Hq / Hkv, h = static_cast<int>(blockIdx.x) % Hkv;
+    const int TQ = kTcRows / G;    // chunk tokens per query tile
+    const int TC = kTcQT * TQ;     // chunk tokens per CTA
 
     // ---- prologue, independent of the inputs
     if (tid == 0) {
@@ -157,13 +200,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&sm->kv_full[s], 1);
             mbar_init(&sm->kv_empty[s], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&sm->s_full[i], 1);
-            mbar_init(&sm->s_free[i], kTcRows);
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&sm->p_full[i], kTcRows);
-            mbar_init(&sm->o_done[i], 1);
+        for (int t = 0; t < kTcQT; ++t) {
+            mbar_init(&sm->s_full[t], 1);
+            mbar_init(&sm->p_full[t], kTcRows);
+            mbar_init(&sm->o_done[t], 1);
         }
         fence_mbar_init();
         prefetch_tmap(&tmK);
@@ -172,7 +212,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         sm->tile = 0;
         sm->bad = 0;
     }
-    if (warp == 5) {
+    if (warp == kTcWarpS) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(&sm->tmem_base)),
                      "r"(kTcTmemCols)
@@ -182,26 +222,63 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the chunk's K/V are in the cache
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __syncthreads();
-    if (warp == 0) {  // this CTA's tile: tiles of TQ chunk tokens, sequence after sequence
-        int acc = 0;
+    if (warp == 0) {
+        // This CTA's chunk tile: the one of rank k when the chunk tiles of all
+        // sequences are ordered by their number of key tiles, longest first (ties:
+        // sequence order, then tile order), so that the longest start in the first
+        // wave.  v = the rank's key-tile count, found by bisection on the counts.
+        const int k = static_cast<int>(blockIdx.x) / Hkv;
+        int total = 0, vmax = 0;
         for (int b0 = 0; b0 < B; b0 += 32) {
             const int bb = b0 + lane;
-            const int n = bb < B ? q_start[bb + 1] - q_start[bb] : 0;
-            const int tiles = n > 0 ? (n + TQ - 1) / TQ : 0;
-            int inc = tiles;
+            if (bb < B) {
+                const int n = q_start[bb + 1] - q_start[bb];
+                if (n > 0) {
+                    total += (n + TC - 1) / TC;
+                    vmax = max(vmax, (max(seq_lens[bb], n) - 1) / kTcKeys + 1);
+                }
+            }
+        }
+        total = warp_sum_i(total);
+        vmax = warp_max_i(vmax);
+        if (k < total) {
+            auto longer = [&](int v) {  // chunk tiles (all sequences) with more than v key tiles
+                int c = 0;
+                for (int bb = lane; bb < B; bb += 32) c += tc_tiles_longer(q_start[bb + 1] - q_start[bb], seq_lens[bb], TC, v);
+                return warp_sum_i(c);
+            };
+            int lo = 1, hi = vmax;  // the smallest v with longer(v) <= k
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (longer(mid) <= k) hi = mid;
+                else lo = mid + 1;
+            }
+            const int v = lo;
+            int idx = k - longer(v);  // among the tiles with exactly v key tiles, in sequence order
+            for (int b0 = 0; b0 < B; b0 += 32) {
+                const int bb = b0 + lane;
+                int e = 0, first = 0;
+                if (bb < B) {
+                    const int n = q_start[bb + 1] - q_start[bb], L = seq_lens[bb];
+                    const int ge = tc_tiles_longer(n, L, TC, v - 1);
+                    e = ge - tc_tiles_longer(n, L, TC, v);
+                    first = (n > 0 ? (n + TC - 1) / TC : 0) - ge;  // the counts grow along the chunk
+                }
+                int inc = e;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, inc, o);
-                if (lane >= o) inc += y;
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, inc, o);
+                    if (lane >= o) inc += y;
+                }
+                const int ex = inc - e;
+                if (e > 0 && ex <= idx && idx < inc) {
+                    sm->b = bb;
+                    sm->tile = first + (idx - ex);
+                }
+                const int tot = __shfl_sync(0xffffffffu, inc, 31);
+                if (idx < tot) break;
+                idx -= tot;
             }
-            const int ex = acc + inc - tiles;
-            const int x = static_cast<int>(blockIdx.x);
-            if (tiles > 0 && ex <= x && x < ex + tiles) {
-                sm->b = bb;
-                sm->tile = x - ex;
-            }
-            acc += __shfl_sync(0xffffffffu, inc, 31);
-            if (acc > x) break;
         }
     }
     tc_fence_before();
@@ -214,14 +291,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (active) {
         n = q_start[b + 1] - q_start[b];
         L = seq_lens[b];
-        t0 = q_start[b] + TQ * tile;
-        nt = min(TQ, n - TQ * tile);
-        p0 = L - n + TQ * tile;  // position of the tile's first token
+        t0 = q_start[b] + TC * tile;
+        nt = min(TC, n - TC * tile);
+        p0 = L - n + TC * tile;  // position of the CTA's first token
     }
     const bool bad_len = active && (L < n || static_cast<long long>(L) > static_cast<long long>(max_blocks) * BS);
-    // this thread's row (softmax warps): token tl of the tile, query head qh
-    const int r = tid, tl = r / G, qh = h * G + (r - tl * G);
-    const bool row_valid = active && tid < kTcRows && tl < nt;
+    // this thread's row (softmax warps): query tile qt, row r = token tl of the CTA, query head qh
+    const bool softmax_warp = warp < 4 * kTcQT;
+    const int qt = warp >> 2, r = tid & (kTcRows - 1);
+    const int tl = qt * TQ + r / G, qh = h * G + r % G;
+    const bool row_valid = active && softmax_warp && tl < nt;
     if (bad_len) {
         if (tid == 0) report(status, PKV_ERR_DEVICE_BOUNDS);
         if (row_valid) {
@@ -230,36 +309,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         active = false;
     }
-    const int plast = p0 + nt - 1;                    // the tile's last position (keys 0 .. plast are read)
+    const int plast = p0 + nt - 1;                    // the CTA's last position (keys 0 .. plast are read)
     const int ntiles = active ? plast / kTcKeys + 1 : 0;
     // iteration j handles key tile (j + rot) mod ntiles (any order gives the same softmax)
-    const int rot = ntiles > 0 ? static_cast<int>((blockIdx.x * 13u + blockIdx.y * 7u) % static_cast<unsigned>(ntiles)) : 0;
+    const int rot = ntiles > 0 ? static_cast<int>((blockIdx.x * 13u) % static_cast<unsigned>(ntiles)) : 0;
     const int nblk_used = active ? plast / BS + 1 : 0;
     const int pos = row_valid ? p0 + tl : plast;      // the row's position (rows past the chunk: the last)
 
-    // ---- the query tile: row r into two 128-byte-swizzled atoms (rows past the chunk: zeros)
-    if (active && tid < kTcRows) {
+    // ---- the query tiles: row r of tile qt into TMEM lane r, columns 256 qt .. + 63 (two
+    // bf16 per column; rows past the chunk: zeros), the A operand of S = Q K^T
+    if (active && softmax_warp) {
         const uint4* src = reinterpret_cast<const uint4*>(q + (static_cast<size_t>(t0 + (row_valid ? tl : 0)) * Hq + qh) * kTcDim);
+        const uint32_t lrow = static_cast<uint32_t>((warp & 3) * 32) << 16;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            const uint4 v = row_valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(sQ + (c >> 3) * (kTcQBytes / 2) + sw128(r, c & 7)) = v;
+        for (int hv = 0; hv < 2; ++hv) {
+            uint32_t w[32];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint4 v = row_valid ? __ldg(src + 8 * hv + c) : make_uint4(0u, 0u, 0u, 0u);
+                w[4 * c] = v.x;
+                w[4 * c + 1] = v.y;
+                w[4 * c + 2] = v.z;
+                w[4 * c + 3] = v.w;
+            }
+            tc_st32(tmem + 256 * qt + lrow + 32 * hv, w);
         }
     }
-    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
     bool fail = false;
-    if ((warp == 4 || warp >= 6) && active) {
-        // ------------------------------------------------ producer warps 4, 6, 7
-        // Warp 4 waits for the stage, reads the tile's four block rows, arms the
-        // stage's transaction count and meets warps 6 and 7 at a named
-        // barrier; then each issues four boxes (warp 4: K groups 0-1, warp 6: K
-        // groups 2-3, warp 7: V).  Copies issued from one warp serialise, so
-        // three warps load a tile about three times faster.
-        const int pw = warp == 4 ? 0 : warp - 5;
+    if ((warp == kTcWarpProd || warp > kTcWarpPV) && active) {
+        // ------------------------------------------------ producer warps 8, 11, 12
+        // Warp 8 waits for the stage, reads the tile's four block rows, arms the
+        // stage's transaction count and meets warps 11 and 12 at a named
+        // barrier; then the three warps issue the tile's eight 4 KB boxes (box i:
+        // K of 16-key group i for i < 4, V of group i - 4 otherwise; warp pw takes
+        // i = pw, pw + 3, pw + 6).
+        const int pw = warp == kTcWarpProd ? 0 : warp - kTcWarpPV;
         const int32_t* trow = block_tables + static_cast<size_t>(b) * max_blocks;
         int win0 = -kTcWin;
         for (int j = 0; j < ntiles && !fail; ++j) {
@@ -267,7 +355,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int kt = j + rot < ntiles ? j + rot : j + rot - ntiles;
             if (pw == 0) {
                 const int kb0 = (kt * kTcKeys) / BS, kb1 = min(nblk_used - 1, (kt * kTcKeys + kTcKeys - 1) / BS);
-                if (kb0 < win0 || kb1 >= win0 + kTcWin) {  // move the block-table window (warp 4 alone reads it)
+                if (kb0 < win0 || kb1 >= win0 + kTcWin) {  // move the block-table window (warp 8 alone reads it)
                     __syncwarp();
                     win0 = kb0;
                     for (int i = lane; i < kTcWin; i += 32) sm->tbl[i] = win0 + i < nblk_used ? trow[win0 + i] : 0;
@@ -299,22 +387,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (lane == 0) sm->rows[s][0] |= fail ? static_cast<int>(0x80000000u) : 0;  // tell the others
                 __syncwarp();
             }
-            asm volatile("bar.sync 1, 96;" ::: "memory");  // the rows are published (warps 4, 6, 7)
+            asm volatile("bar.sync 1, 96;" ::: "memory");  // the rows are published (warps 8, 11, 12)
             const int r0 = sm->rows[s][0];
-            if (r0 < 0) {  // warp 4 gave up
+            if (r0 < 0) {  // warp 8 gave up
                 fail = true;
                 break;
             }
-            if (lane < 4) {
+            const int bi = pw + 3 * lane;
+            if (lane < 3 && bi < 8) {
                 uint8_t* st = sKV + static_cast<size_t>(s) * kTcStageBytes;
-                if (pw < 2) {  // K: group 2 pw + lane / 2, half lane & 1 (2 KB into the two 64-row atoms)
-                    const int grp = 2 * pw + (lane >> 1);
-                    tma_load_2d(st + (lane & 1) * (kTcKBytes / 2) + 2048 * grp, &tmK, 64 * (lane & 1),
-                                sm->rows[s][grp], &sm->kv_full[s]);
-                } else {  // V: group lane, both halves (4 KB)
-                    tma_load_3d(st + kTcKBytes + kTcGroupBytes * lane, &tmV, 0, sm->rows[s][lane], 0,
+                if (bi < 4)  // K of group bi: [8-row half][64-dimension half][8 rows][128 B]
+                    tma_load_4d(st + kTcGroupBytes * bi, &tmK, 0, 0, 0, sm->rows[s][bi] >> 3, &sm->kv_full[s]);
+                else  // V of group bi - 4: [64-dimension half][16 rows][128 B]
+                    tma_load_3d(st + kTcKBytes + kTcGroupBytes * (bi - 4), &tmV, 0, sm->rows[s][bi - 4], 0,
                                 &sm->kv_full[s]);
-                }
             }
             __syncwarp();
         }
@@ -322,70 +408,90 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0)
             for (int j = max(0, ntiles - kTcStages); j < ntiles; ++j)
                 mbar_wait(&sm->kv_full[j % kTcStages], (j / kTcStages) & 1);
-    } else if (warp == 5 && active) {
-        // ------------------------------------------------ MMA warp (lane 0 issues)
+    } else if (warp == kTcWarpS && active) {
+        // ------------------------------------------------ S = Q K^T for both query tiles (lane 0 issues)
+        // Q (A) from tensor memory, K (B) from the stage.  S_j of query tile t
+        // overwrites P_{j-1}, so it waits for the PV of tile j - 1.
         if (lane == 0) {
-            const uint32_t tS0 = tmem, tO = tmem + 128;
-            constexpr uint32_t idS = tc_idesc(kTcRows, kTcKeys, false), idO = tc_idesc(kTcRows, kTcDim, true);
-            const uint32_t qa = smem_u32(sQ), pa = smem_u32(sP), kva = smem_u32(sKV);
-            auto issue_pv = [&](int jj) -> bool {  // O += P_jj V_jj (P buffer jj & 1)
-                if (!mbar_wait(&sm->p_full[jj & 1], (jj >> 1) & 1)) return false;
-                tc_fence_after();
-                const uint32_t vb = kva + (jj % kTcStages) * kTcStageBytes + kTcKBytes;
-                const uint32_t pb = pa + (jj & 1) * kTcPBytes;
-#pragma unroll
-                for (int kk = 0; kk < kTcKeys / 16; ++kk)
-                    tc_mma(tO, tc_desc(pb + 32 * kk, 16, 1024), tc_desc(vb + kTcGroupBytes * kk, kTcGroupBytes / 2, 1024),
-                           idO, (jj > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(&sm->o_done[jj & 1]);
-                tc_commit(&sm->kv_empty[jj % kTcStages]);
-                return true;
-            };
+            constexpr uint32_t idS = tc_idesc(kTcRows, kTcKeys, false);
+            const uint32_t kva = smem_u32(sKV);
             for (int j = 0; j < ntiles && !fail; ++j) {
                 const int s = j % kTcStages;
-                if (!mbar_wait(&sm->kv_full[s], (j / kTcStages) & 1) ||
-                    (j >= 2 && !mbar_wait(&sm->s_free[j & 1], ((j >> 1) - 1) & 1))) {
+                if (!mbar_wait(&sm->kv_full[s], (j / kTcStages) & 1)) {
                     fail = true;
                     break;
                 }
-                tc_fence_after();
                 const uint32_t kb = kva + s * kTcStageBytes;
+                for (int t = 0; t < kTcQT; ++t) {
+                    if (j >= 1 && !mbar_wait(&sm->o_done[t], (j - 1) & 1)) {
+                        fail = true;
+                        break;
+                    }
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kTcDim / 16; ++kk)
-                    tc_mma(tS0 + 64 * (j & 1), tc_desc(qa + (kk >> 2) * (kTcQBytes / 2) + 32 * (kk & 3), 16, 1024),
-                           tc_desc(kb + (kk >> 2) * (kTcKBytes / 2) + 32 * (kk & 3), 16, 1024), idS,
-                           kk > 0 ? 1u : 0u);
-                tc_commit(&sm->s_full[j & 1]);
-                if (j >= 1 && !issue_pv(j - 1)) fail = true;
+                    for (int kk = 0; kk < kTcDim / 16; ++kk)
+                        tc_mma_ta(tmem + 256 * t + 64, tmem + 256 * t + 8 * kk,
+                                  tc_desc(kb + (kk >> 2) * 1024 + 32 * (kk & 3), 16, 2048), idS, kk > 0 ? 1u : 0u);
+                    tc_commit(&sm->s_full[t]);
+                }
             }
-            if (!fail && ntiles > 0 && !issue_pv(ntiles - 1)) fail = true;
             if (fail) report(status, PKV_ERR_TIMEOUT);
         }
         __syncwarp();
-    } else if (warp < 4 && active) {
-        // ------------------------------------------------ softmax warps: thread r owns row r
-        const uint32_t lrow = static_cast<uint32_t>(warp * 32) << 16;  // this warp's TMEM lanes
+    } else if (warp == kTcWarpPV && active) {
+        // ------------------------------------------------ O += P V for both query tiles (lane 0 issues)
+        // P of query tile t (bf16, over the first 32 columns of the S it was
+        // computed from) is the A operand, read from tensor memory.  Both P tiles
+        // of key tile j were written after the softmax read S_j, so once their PV
+        // MMAs are complete nothing reads the stage any more.
+        if (lane == 0) {
+            constexpr uint32_t idO = tc_idesc(kTcRows, kTcDim, true);
+            const uint32_t kva = smem_u32(sKV);
+            for (int j = 0; j < ntiles && !fail; ++j) {
+                const int s = j % kTcStages;
+                const uint32_t vb = kva + s * kTcStageBytes + kTcKBytes;
+                for (int t = 0; t < kTcQT; ++t) {  // query tile 0 first: its softmax warps clear V rows past L
+                    if (!mbar_wait(&sm->p_full[t], j & 1)) {
+                        fail = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t tp = tmem + 256 * t + 64;
+#pragma unroll
+                    for (int kk = 0; kk < kTcKeys / 16; ++kk)
+                        tc_mma_ta(tmem + 256 * t + 128, tp + 8 * kk,
+                                  tc_desc(vb + kTcGroupBytes * kk, kTcGroupBytes / 2, 1024), idO,
+                                  (j > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(&sm->o_done[t]);
+                }
+                if (!fail) tc_commit(&sm->kv_empty[s]);
+            }
+            if (fail) report(status, PKV_ERR_TIMEOUT);
+        }
+        __syncwarp();
+    } else if (softmax_warp && active) {
+        // ------------------------------------------------ softmax warps: thread r of query tile qt owns row r
+        const uint32_t lrow = static_cast<uint32_t>((warp & 3) * 32) << 16;  // this warp's TMEM lanes
+        const uint32_t tq = tmem + 256 * qt;
+        const int p0t = p0 + qt * TQ;  // the query tile's first position
         float m_ref = -INFINITY, lsum = 0.f;
         for (int j = 0; j < ntiles; ++j) {
-            const int buf = j & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&sm->s_full[buf], (j >> 1) & 1))) {  // tcgen05.ld needs the whole warp
+            if (!__all_sync(0xffffffffu, mbar_wait(&sm->s_full[qt], j & 1))) {  // tcgen05.ld needs the whole warp
                 fail = true;
                 break;
             }
             tc_fence_after();
             uint32_t sr[2][32];
-            tc_ld32(tmem + lrow + 64 * buf, sr[0]);
-            tc_ld32(tmem + lrow + 64 * buf + 32, sr[1]);
-            tc_fence_before();
-            mbar_arrive(&sm->s_free[buf]);  // the buffer may take S of tile j + 2
+            tc_ld32(tq + lrow + 64, sr[0]);
+            tc_ld32(tq + lrow + 96, sr[1]);
             const int kt = j + rot < ntiles ? j + rot : j + rot - ntiles;
             const int kbase = kt * kTcKeys;
             // maximum of the raw scores (the scale is positive), eight chains;
-            // the causal mask only on tiles that reach past the tile's first position
+            // the causal mask only on tiles that reach past the query tile's first position
             float mxs[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) mxs[k] = -INFINITY;
-            if (kbase + kTcKeys - 1 > p0) {
+            if (kbase + kTcKeys - 1 > p0t) {
 #pragma unroll
                 for (int c = 0; c < kTcKeys; ++c) {
                     const float v = kbase + c <= pos ? __uint_as_float(sr[c >> 5][c & 31]) : -INFINITY;
@@ -418,54 +524,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 ls[c & 7] += e0 + e1;
             }
             lsum = lsum * a + (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
-            // O is rescaled only once the PV of tile j - 1 is complete; P_j goes to
-            // buffer j & 1 once the PV of tile j - 2 has read it
+            // S_j was issued after the PV of tile j - 1 had completed: O may be rescaled
             if (j > 0 && __any_sync(0xffffffffu, resc)) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&sm->o_done[(j - 1) & 1], ((j - 1) >> 1) & 1))) {
-                    fail = true;
-                    break;
-                }
-                tc_fence_after();
-                {
 #pragma unroll 1
-                    for (int cc = 0; cc < kTcDim / 32; ++cc) {
-                        uint32_t o[32];
-                        tc_ld32(tmem + lrow + 128 + 32 * cc, o);
+                for (int cc = 0; cc < kTcDim / 32; ++cc) {
+                    uint32_t o[32];
+                    tc_ld32(tq + lrow + 128 + 32 * cc, o);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
-                        tc_st32(tmem + lrow + 128 + 32 * cc, o);
-                    }
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
+                    tc_st32(tq + lrow + 128 + 32 * cc, o);
                 }
             }
-            if (kt == ntiles - 1) {  // the V rows of keys at or past L may hold anything: clear them
+            if (qt == 0 && kt == ntiles - 1) {  // the V rows of keys at or past L may hold anything: clear them
                 const int rlo = max(0, min(kTcKeys, L - kbase));
                 uint8_t* vb = sKV + static_cast<size_t>(j % kTcStages) * kTcStageBytes + kTcKBytes;
-                for (int idx = tid; idx < (kTcKeys - rlo) * 16; idx += kTcRows) {
+                for (int idx = r; idx < (kTcKeys - rlo) * 16; idx += kTcRows) {
                     const int rr = rlo + (idx >> 4), half = (idx >> 3) & 1, ch = idx & 7;
                     *reinterpret_cast<uint4*>(vb + kTcGroupBytes * (rr >> 4) + half * (kTcGroupBytes / 2) +
                                               (rr & 15) * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
-            if (j >= 2) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&sm->o_done[j & 1], ((j - 2) >> 1) & 1))) {
-                    fail = true;
-                    break;
-                }
-                tc_fence_after();
-            }
-            // P row r (64 bf16 = 8 chunks of 16 bytes) into the K-major P tile
-            uint8_t* pbuf = sP + (j & 1) * kTcPBytes;
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-                *reinterpret_cast<uint4*>(pbuf + sw128(r, ch)) =
-                    make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-            fence_proxy_async_smem();
+            // P row r (64 bf16, two per column) over the first 32 columns of S
+            tc_st32(tq + lrow + 64, pk);
+            if (qt == 0 && kt == ntiles - 1) fence_proxy_async_smem();  // the cleared V rows
             tc_fence_before();
-            mbar_arrive(&sm->p_full[j & 1]);
+            mbar_arrive(&sm->p_full[qt]);
         }
         // ---- epilogue: O / sum of the last PV
         if (!fail && ntiles > 0 &&
-            !__all_sync(0xffffffffu, mbar_wait(&sm->o_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1)))
+            !__all_sync(0xffffffffu, mbar_wait(&sm->o_done[qt], (ntiles - 1) & 1)))
             fail = true;
         if (fail) {
             if (lane == 0) report(status, PKV_ERR_TIMEOUT);
@@ -477,7 +564,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll 1
             for (int cc = 0; cc < kTcDim / 32; ++cc) {
                 uint32_t o[32];
-                tc_ld32(tmem + lrow + 128 + 32 * cc, o);
+                tc_ld32(tq + lrow + 128 + 32 * cc, o);
                 uint32_t w[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
@@ -494,11 +581,43 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ---- every role is done with TMEM
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kTcWarpS) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcTmemCols)
                      : "memory");
     }
+}
+
+// The K pool [NB, Hkv, BS, 128] bf16 in four dimensions: (64 elements, 8 rows,
+// the two 64-element halves of a row, groups of 8 rows), with boxes of
+// 64 x 8 x 2 x 2.  One box holds 16 consecutive rows and lands as
+// [8-row group][half][8 rows][128 B]: for either half, successive 8-row groups
+// sit 2048 bytes apart, so a 64-key tile of four boxes is one K-major,
+// 128-byte-swizzled operand per half with a 2048-byte group stride.
+static bool encode_pool_k16(CUtensorMap* map, const void* pool, int NB, int Hkv, int BS) {
+    typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+    static EncodeFn enc = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult qres;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qres) ==
+                cudaSuccess &&
+            qres == cudaDriverEntryPointSuccess)
+            enc = reinterpret_cast<EncodeFn>(p);
+        tried = true;
+    }
+    const cuuint64_t rows = static_cast<cuuint64_t>(NB) * Hkv * BS;
+    if (!enc || rows % 8 != 0) return false;
+    cuuint64_t gdim[4] = {64, 8, 2, rows / 8};
+    cuuint64_t gstride[3] = {kTcDim * 2, 128, 8 * kTcDim * 2};
+    cuuint32_t box[4] = {64, 8, 2, 2};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(pool), gdim, gstride, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool prefill_tc_supported(int Hq, int Hkv, int D, int BS, const void* q, const void* out, const void* k,
@@ -513,17 +632,17 @@ cudaError_t launch_prefill_tc(void* out, const void* q, const void* k_cache, con
                               const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
                               const int32_t* q_start, int B, int T_new, int Hq, int Hkv, int BS, int NB, float scale,
                               int32_t* status, cudaStream_t stream) {
-    const int G = Hq / Hkv, TQ = kTcRows / G;
-    const long long tiles = static_cast<long long>(T_new) / TQ + B;
-    if (tiles > 0x7fffffffLL || Hkv > 65535) return cudaErrorInvalidConfiguration;
+    const int G = Hq / Hkv, TC = kTcQT * (kTcRows / G);
+    const long long tiles = static_cast<long long>(T_new) / TC + B;
+    if (tiles * Hkv > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     CUtensorMap tmK, tmV;
-    if (!encode_pool_box(&tmK, k_cache, NB, Hkv, BS, 16) || !encode_pool_box_halves(&tmV, v_cache, NB, Hkv, BS, 16))
+    if (!encode_pool_k16(&tmK, k_cache, NB, Hkv, BS) || !encode_pool_box_halves(&tmV, v_cache, NB, Hkv, BS, 16))
         return cudaErrorInvalidValue;
     cudaError_t err = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(kTcSmemBytes));
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(Hkv), 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(tiles * Hkv), 1, 1);  // KV head innermost
     cfg.blockDim = dim3(kTcThreads, 1, 1);
     cfg.dynamicSmemBytes = kTcSmemBytes;
     cfg.stream = stream;
