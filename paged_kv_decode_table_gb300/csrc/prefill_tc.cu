@@ -6,34 +6,40 @@
 // tutorial" 5.4) for bf16, D = 128, G = Hq / Hkv in {1, 2, 4, 8}, block_size a
 // multiple of 16 and 16-byte aligned q / out / pools.
 //
-//  * One CTA per (128 query rows, KV head h).  Row r is (chunk token r / G,
-//    query head h G + r % G): 128 / G consecutive tokens of one sequence times
-//    the G heads that share K/V head h, so each K/V tile serves all of them.
-//  * K and V of head h stream in 64-key tiles through a four-stage ring.  The
-//    paged layout allows TMA boxes of one block's 16 keys at most: K comes in
-//    boxes of 16 keys x 64 dimensions into two 64-row, 128-byte-swizzled atoms
-//    (so that S is one N = 64 MMA per k-step); V in boxes of 16 keys x both
-//    halves (4 KB, a 3-D view of the pool), one per 16-key group (each PV
-//    k-step reads one group).  12 lanes of the producer warp issue a tile's
-//    boxes together; the block ids come from a window of the block table kept
-//    in shared memory.  Each CTA walks its key tiles starting at a different
-//    tile, so that the CTAs sharing a sequence do not read the same blocks at
-//    the same time.
-//  * One MMA lane issues S = Q K^T (M 128, N 64, K 128; Q and K K-major) into
-//    one of two TMEM buffers and O += P V (M 128, N 128, K 64; P K-major from
-//    shared memory, V MN-major, i.e. as stored, one 16-key group per k-step)
-//    into a TMEM accumulator, and
-//    signals completion through mbarriers (tcgen05.commit).  S of tile j + 1
-//    runs while the softmax works on tile j.
-//  * Four softmax warps: thread r owns row r (TMEM lane r).  It reads its 64
-//    scores (tcgen05.ld), applies the causal mask and the scale in the log2
-//    domain, and exponentiates against a reference maximum that is raised only
-//    when the row maximum exceeds it by more than 8, in which case the row of
-//    O in TMEM and the running sum are rescaled first; P (bf16, values at most
-//    2^8) goes to shared memory for the PV MMA, and the sum accumulates the
-//    fp32 values.  Rows past the chunk are computed on zero queries and
-//    not stored.  The V rows of keys at or past the sequence length (which may
-//    hold anything, NaN included) are cleared before the last PV MMA.
+//  * One CTA per (two query tiles of 128 rows, KV head h).  Row r of query
+//    tile t is (chunk token t TQ + r / G, query head h G + r % G), TQ = 128 / G:
+//    2 TQ consecutive tokens of one sequence times the G heads that share K/V
+//    head h, so each K/V tile serves 256 rows.  The CTAs take the chunk tiles
+//    longest first (by the number of key tiles they read; the KV head is the
+//    innermost grid index), so that the longest start in the first wave.
+//  * K and V of head h stream in 64-key tiles through a six-stage ring.  The
+//    paged layout allows TMA boxes of one block's 16 keys at most.  K comes in
+//    one 4 KB box per 16 keys through a 4-D view of the pool that lands the
+//    two 64-dimension halves interleaved at 1 KB, so that for either half the
+//    8-row groups of the tile sit 2 KB apart (one N = 64 MMA per k-step); V in
+//    one 4 KB box per 16 keys (a 3-D view, both halves, one box per PV k-step).
+//    Three producer warps issue a tile's eight boxes together; the block ids
+//    come from a window of the block table kept in shared memory.  Each CTA
+//    walks its key tiles starting at a different tile, so that the CTAs
+//    sharing a sequence do not read the same blocks at the same time.
+//  * Tensor memory, per query tile t (256 columns): Q (bf16, two per column)
+//    at 256 t, S at 256 t + 64, O at 256 t + 128.  One warp issues
+//    S = Q K^T (M 128, N 64, K 128; A = Q from tensor memory, B = K from the
+//    stage), another O += P V (M 128, N 128, K 64; A = P from tensor memory,
+//    B = V as stored, MN-major, one 16-key group per k-step).  P (bf16)
+//    overwrites the first 32 columns of the S it came from, so S of tile j + 1
+//    waits for the PV of tile j; the two query tiles interleave on the tensor
+//    pipe.  Completion is signalled through mbarriers (tcgen05.commit).
+//  * Eight softmax warps, four per query tile: thread r owns row r (TMEM lane
+//    r).  It reads its 64 scores (tcgen05.ld), applies the causal mask and the
+//    scale in the log2 domain, and exponentiates against a reference maximum
+//    that is raised only when the row maximum exceeds it by more than 8, in
+//    which case the row of O in TMEM and the running sum are rescaled first;
+//    P (bf16, values at most 2^8) goes back to tensor memory for the PV MMA,
+//    and the sum accumulates the fp32 values.  Rows past the chunk are
+//    computed on zero queries and not stored.  The V rows of keys at or past
+//    the sequence length (which may hold anything, NaN included) are cleared
+//    before the last PV MMAs.
 //  * Epilogue: O / sum from TMEM to the bf16 output rows.
 // Every mbarrier wait is bounded; a CTA that gives up records PKV_ERR_TIMEOUT,
 // waits (bounded) for its own TMA copies, and still frees its TMEM.
