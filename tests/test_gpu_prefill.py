@@ -89,9 +89,18 @@ def _check(inp, rows=None):
     ([17, 64, 3], 500, 8, 8, 32),   # one query head per KV head, 32-token blocks
     ([40, 7, 130], 700, 16, 8, 16),  # two query heads per KV head
     ([33, 90], 900, 24, 8, 16),      # three per KV head: the mma.sync kernel (no 128-row tile)
+    ([300, 129, 5], 600, 8, 8, 16),  # one per KV head, chunks filling both 128-token query tiles, ragged
 ])
 def test_prefill_matches_oracle(chunks, prefix_hi, Hq, Hkv, BS):
     inp = _inputs(sum(chunks) + prefix_hi, chunks, prefix_hi, Hq=Hq, Hkv=Hkv, BS=BS)
+    _check(inp)
+
+
+def test_prefill_many_sequences():
+    # 45 sequences: the CTAs' longest-first assignment walks the sequences 32 at a time
+    rng = np.random.default_rng(17)
+    chunks = [int(c) for c in rng.integers(0, 41, 45)]
+    inp = _inputs(23, chunks, 700)
     _check(inp)
 
 
