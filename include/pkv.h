@@ -273,7 +273,8 @@ pkv_status pkv_sample_tokens_ex(int32_t* tokens, const float* logits, int B, int
  * (token -1 for the row, status recorded): NaN / +inf / no finite logit ->
  * PKV_ERR_NONFINITE; T < 0 or NaN, or T > 0 with tau <= 0 or NaN ->
  * PKV_ERR_INVALID_ARG.  Host: B < 0, V < 1 or V > 2^23, NULL pointers ->
- * PKV_ERR_INVALID_ARG.  One CTA per row; no workspace, nothing allocated.
+ * PKV_ERR_INVALID_ARG.  One thread-block cluster of 1-8 CTAs per row (as many
+ * as fill the device with one CTA per SM); no workspace, nothing allocated.
  */
 pkv_status pkv_sample_tokens_typical(int32_t* tokens, const float* logits, int B, int V, const float* temperature,
                                      const float* typical_p, const uint64_t* seeds, const uint64_t* offsets,

@@ -1,4 +1,4 @@
-// typical_sampler.cu -- typical sampling, one CTA per row.
+// typical_sampler.cu -- typical sampling, one thread-block cluster per row.
 //
 // "LLM inference serving tutorial" section 3.1 (other samplers: typical
 // sampling; Meister et al., locally typical sampling): over the temperature
@@ -17,20 +17,30 @@
 // sampler's 2^-40 fixed-point weights floor(2^u * 2^40), so the cut and the
 // draw are exact integer arithmetic.
 //
-// Passes over the row (the first from HBM, the rest from L2): maximum and
-// finiteness; the mass sum S and the weighted sum of u (for ubar); a
-// three-digit radix select (11/11/10 bits of dk, mass histograms) for the
-// cut's dk; when several u share that dk, the same select over u; the rank of
-// the cut among equal (dk, u) in id order; the draw (chunk sums of the kept
-// masses, a scan, one chunk walked).
+// A row is spread over a cluster of 1-8 CTAs (as many as fill the GPU with
+// one CTA per SM), each sweeping one slice; per-CTA partials are combined in
+// rank order through distributed shared memory, so every CTA holds the same
+// results.  Passes over the slices (the first from HBM, the rest from L2):
+// maximum and finiteness; the mass sum S and the weighted sum of u (for
+// ubar); 2048 float bins linear in dk, summed over the cluster, which locate
+// the cut approximately; the logits of a window of bins around it pushed into
+// rank 0 (with the exact mass above the window), where they are sorted and
+// the cut found exactly; the draw (chunk sums of the kept masses, a scan over
+// the cluster, one chunk walked by the CTA holding the draw).  When the
+// window misses or overflows, rank 0 alone takes an exact radix select over
+// the whole row (11/11/10 bits of dk, then of u, then the rank in id order)
+// and draws.
+#include <cooperative_groups.h>
 #include <math.h>
 
 #include "pkv_common.cuh"
 #include "sampling_math.cuh"
 
+namespace cg = cooperative_groups;
+
 namespace pkv {
 
-constexpr int kTyT = 1024;          // threads per CTA (one row)
+constexpr int kTyT = 1024;          // threads per CTA
 constexpr int kTyW = kTyT / 32;     // warps
 constexpr int kTyBins = 2048;       // radix digits (11 bits), or draw chunks
 
@@ -43,6 +53,15 @@ struct TySmem {
     float fv[kTyW];
     unsigned long long bc[4];
     unsigned long long u53;  // the row's uniform, top 53 bits of Philox word 0
+    // cluster exchange: one CTA's partial of a cluster-wide reduction, in two
+    // alternating slots (a slot is rewritten only after the barrier of the
+    // next exchange, which every reader of it has passed)
+    struct {
+        unsigned long long u;
+        double d;
+        float f[2];
+    } xch[2];
+    unsigned long long res[4];  // rank 0: the cut (found, dk, u bits, id) for the cluster
 };
 
 // ------------------------------------------------------------------ CTA reductions
@@ -308,24 +327,60 @@ __device__ int ty_ordered_find(const float* __restrict__ z, int n, TySmem* sm, V
 }
 
 // ------------------------------------------------------------------ kernel
+// One cluster of nc CTAs per row; CTA `rank` sweeps the slice [lo, lo + n) of
+// the row.  Reductions combine the CTAs' partials in rank order, so every CTA
+// holds the same, deterministic results.
 __global__ void __launch_bounds__(kTyT, 1)
-    typical_sampler_kernel(int32_t* __restrict__ tokens, const float* __restrict__ logits, int V,
+    typical_sampler_kernel(int32_t* __restrict__ tokens, const float* __restrict__ logits, int V, int slice,
                            const float* __restrict__ temperature, const float* __restrict__ typical_p,
                            const uint64_t* __restrict__ seeds, const uint64_t* __restrict__ offsets,
                            int32_t* status) {
     __shared__ TySmem smem;
     TySmem* sm = &smem;
+    cg::cluster_group cl = cg::this_cluster();
+    const int nc = static_cast<int>(cl.num_blocks()), rank = static_cast<int>(cl.block_rank());
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int tid = threadIdx.x, row = blockIdx.x;
+    const int tid = threadIdx.x, row = blockIdx.x / nc;
     const float* z = logits + static_cast<size_t>(row) * V;
+    const int lo = min(V, rank * slice), n = min(V, lo + slice) - lo;
+    const float* zs = z + lo;  // this CTA's slice
     const float T = temperature[row], tp = typical_p[row];
     if (tid == kTyT - 1) sm->u53 = philox_word0(seeds[row], offsets[row]) >> 11;
+    if (rank == 0 && tid == 0) tokens[row] = -1;  // overwritten (after a cluster barrier) by the draw
+
+    // cluster exchange: thread 0 publishes the CTA's partial, the barrier makes
+    // it visible, every thread then reads the nc partials with rd(r)
+    int xk = 0;
+    auto publish = [&](unsigned long long u, double d, float f0, float f1) {
+        if (tid == 0) {
+            sm->xch[xk & 1].u = u;
+            sm->xch[xk & 1].d = d;
+            sm->xch[xk & 1].f[0] = f0;
+            sm->xch[xk & 1].f[1] = f1;
+        }
+        cl.sync();
+    };
+    auto rd = [&](int r) { return cl.map_shared_rank(&sm->xch[xk & 1], r); };
+    // X (a position in the cluster's total of per-CTA totals `tot`, from Xof of
+    // that total) relative to this CTA, or ~0 when it lies in another CTA
+    auto cluster_x = [&](uint64_t tot, auto Xof) -> uint64_t {
+        publish(tot, 0.0, 0.f, 0.f);
+        uint64_t excl = 0, grand = 0;
+        for (int r = 0; r < nc; ++r) {
+            const uint64_t t = rd(r)->u;
+            excl += r < rank ? t : 0ull;
+            grand += t;
+        }
+        ++xk;
+        const uint64_t X = Xof(grand);
+        return (X >= excl && X - excl < tot) ? X - excl : ~0ull;
+    };
 
     // ---- maximum and finiteness
     float mx = -INFINITY, mn = INFINITY;
     unsigned int bad = 0u;
-    ty_sweep(z, V, [&](int, float x) {
+    ty_sweep(zs, n, [&](int, float x) {
         mx = fmaxf(mx, x);
         mn = fminf(mn, x > -INFINITY ? x : INFINITY);
         bad |= (x < INFINITY) ? 0u : 1u;  // NaN or +inf
@@ -333,26 +388,38 @@ __global__ void __launch_bounds__(kTyT, 1)
     mx = ty_ext_f<true>(mx, sm);
     mn = ty_ext_f<false>(mn, sm);
     bad = static_cast<unsigned int>(ty_sum_u64(bad, sm));
+    publish(bad, 0.0, mx, mn);
+    bad = 0u;
+    mx = -INFINITY;
+    mn = INFINITY;
+    for (int r = 0; r < nc; ++r) {
+        bad |= static_cast<unsigned int>(rd(r)->u);
+        mx = fmaxf(mx, rd(r)->f[0]);
+        mn = fminf(mn, rd(r)->f[1]);
+    }
+    ++xk;
     int err = 0;
     if (bad || !(mx > -INFINITY)) err = PKV_ERR_NONFINITE;
     else if (!(T >= 0.f)) err = PKV_ERR_INVALID_ARG;
     else if (T != 0.f && !(tp > 0.f)) err = PKV_ERR_INVALID_ARG;  // typical_p <= 0 or NaN
     if (err) {
-        if (tid == 0) {
-            tokens[row] = -1;
-            report(status, err);
-        }
+        if (rank == 0 && tid == 0) report(status, err);
+        cl.sync();  // no CTA leaves while a peer may still read its slot
         return;
     }
     if (T == 0.f) {  // greedy: the lowest id holding the maximum
         float first = INFINITY;
-        for (int i = tid; i < V; i += kTyT)
-            if (z[i] == mx) {
-                first = static_cast<float>(i);  // ids < 2^23 are exact in float
+        for (int i = tid; i < n; i += kTyT)
+            if (zs[i] == mx) {
+                first = static_cast<float>(lo + i);  // ids < 2^24 are exact in float
                 break;
             }
         first = ty_ext_f<false>(first, sm);
-        if (tid == 0) tokens[row] = static_cast<int32_t>(first);
+        publish(0ull, 0.0, first, 0.f);
+        for (int r = 0; r < nc; ++r) first = fminf(first, rd(r)->f[0]);
+        ++xk;
+        if (rank == 0 && tid == 0) tokens[row] = static_cast<int32_t>(first);
+        cl.sync();
         return;
     }
     const float c2 = fminf(1.4426950408889634f / T, 1.0e30f);  // log2(e) / T, kept finite
@@ -361,33 +428,43 @@ __global__ void __launch_bounds__(kTyT, 1)
         return static_cast<uint64_t>((static_cast<unsigned __int128>(sm->u53) * tot) >> 53);
     };
     if (!(tp < 1.f)) {  // no truncation: every finite logit
-        const int tok = ty_ordered_find(
-            z, V, sm, [&](float x, int) -> uint64_t { return x > -INFINITY ? fx40(hw_exp2(uof(x))) : 0ull; },
-            draw_x);
-        if (tid == 0) tokens[row] = tok;
+        const int f = ty_ordered_find(
+            zs, n, sm, [&](float x, int) -> uint64_t { return x > -INFINITY ? fx40(hw_exp2(uof(x))) : 0ull; },
+            [&](uint64_t tot) { return cluster_x(tot, draw_x); });
+        if (f >= 0 && tid == 0) tokens[row] = lo + f;
+        cl.sync();
         return;
     }
 
     // ---- S and the p-weighted mean of u, rounded to the 2^-8 grid
     uint64_t s = 0;
     float wu = 0.f;
-    ty_sweep(z, V, [&](int, float x) {
+    ty_sweep(zs, n, [&](int, float x) {
         if (!(x > -INFINITY)) return;
         const float u = uof(x);
         const float w = hw_exp2(u);
         s += fx40(w);
         if (w > 0.f) wu = fmaf(w, u, wu);
     });
-    const uint64_t S = ty_sum_u64(s, sm);
-    const double WU = ty_sum_f64(static_cast<double>(wu), sm);
+    const uint64_t Sc = ty_sum_u64(s, sm);
+    const double WUc = ty_sum_f64(static_cast<double>(wu), sm);
+    publish(Sc, WUc, 0.f, 0.f);
+    uint64_t S = 0;
+    double WU = 0.0;
+    for (int r = 0; r < nc; ++r) {
+        S += rd(r)->u;
+        WU += rd(r)->d;
+    }
+    ++xk;
     const double ubar = WU / (static_cast<double>(S) * 0x1p-40);
     const float ub = static_cast<float>(rint(ubar * 256.0) / 256.0);
     auto dkey = [&](float u) { return __float_as_uint(fabsf(__fsub_rn(u, ub))); };  // monotone in dk >= 0
     const uint64_t target = ceil_mul_p(tp, S);  // >= 1, <= S
 
     // ---- 2048 bins linear in dk over [0, dkmax] (bin 0: closest to the mean):
-    // mass and count per bin; the bin where the cumulative mass in ascending
-    // dk first reaches the target holds the cut
+    // the mass per bin (float, summed over the cluster in rank order); the bin
+    // where the cumulative mass in ascending dk first reaches the target holds
+    // the cut
     const float umin = uof(mn);
     const float dkmax = fmaxf(fabsf(__fsub_rn(umin, ub)), fabsf(ub));
     const float sc = static_cast<float>(kTyBins) / dkmax;
@@ -403,7 +480,7 @@ __global__ void __launch_bounds__(kTyT, 1)
     {
         int cb = 0;  // a thread's run of equal bins is added once
         float cw = 0.f;
-        ty_sweep(z, V, [&](int, float x) {
+        ty_sweep(zs, n, [&](int, float x) {
             if (!(x > -INFINITY)) return;
             const float u = uof(x);
             const int bq = dbin(dkey(u));
@@ -416,15 +493,21 @@ __global__ void __launch_bounds__(kTyT, 1)
         });
         if (cw > 0.f) atomicAdd(&hf[cb], cw);
     }
-    __syncthreads();
+    cl.sync();  // every CTA's bins are complete (and rank 0's window count is zero)
     // The float sums locate the cut only approximately: the window of bins
     // [blo, bhi] covers cumulative masses within S / 2^13 of the target on
     // either side; the gather pass checks it with exact masses.
     {
+        const int b0 = 2 * tid;
+        float f0 = 0.f, f1 = 0.f;
+        for (int r = 0; r < nc; ++r) {
+            const float* hr = cl.map_shared_rank(hf, r);
+            f0 += hr[b0];
+            f1 += hr[b0 + 1];
+        }
         const uint64_t del = (S >> 13) ? (S >> 13) : 1ull;
         const uint64_t tlo = target > del ? target - del : 1ull, thi = target + del;
-        const int b0 = 2 * tid;
-        const uint64_t h0 = __float2ull_rn(hf[b0] * 0x1p40f), h1 = __float2ull_rn(hf[b0 + 1] * 0x1p40f);
+        const uint64_t h0 = __float2ull_rn(f0 * 0x1p40f), h1 = __float2ull_rn(f1 * 0x1p40f);
         if (tid == 0) {
             sm->bc[0] = 0ull;
             sm->bc[1] = kTyBins - 1;
@@ -436,15 +519,18 @@ __global__ void __launch_bounds__(kTyT, 1)
     }
     __syncthreads();
     const int blo = static_cast<int>(sm->bc[0]), bhi = max(blo, static_cast<int>(sm->bc[1]));
-    __syncthreads();
+    cl.sync();  // no CTA reads another's bins any more; rank 0's bins become the window list
 
-    // ---- the window's logits into shared memory (and the exact mass above
-    // it), sorted by (dk, larger u first, id): key (dk bits << 32 | ~okey(u))
-    // ascending, then id
+    // ---- the window's logits into rank 0's shared memory (and the exact mass
+    // above it), to be sorted by (dk, larger u first, id): key
+    // (dk bits << 32 | ~okey(u)) ascending, then id
     unsigned long long* key = sm->hist;
     unsigned int* ids = sm->cnt;
+    unsigned long long* key0 = cl.map_shared_rank(sm->hist, 0);
+    unsigned int* ids0 = cl.map_shared_rank(sm->cnt, 0);
+    unsigned int* nwin0 = cl.map_shared_rank(&sm->nwin, 0);
     uint64_t at = 0;
-    ty_sweep(z, V, [&](int i, float x) {
+    ty_sweep(zs, n, [&](int i, float x) {
         if (!(x > -INFINITY)) return;
         const float u = uof(x);
         const uint32_t dk = dkey(u);
@@ -452,70 +538,92 @@ __global__ void __launch_bounds__(kTyT, 1)
         if (bq < blo) {
             at += fx40(hw_exp2(u));
         } else if (bq <= bhi) {
-            const unsigned int slot = atomicAdd(&sm->nwin, 1u);
+            const unsigned int slot = atomicAdd(nwin0, 1u);
             if (slot < static_cast<unsigned int>(kTyBins)) {
-                key[slot] = (static_cast<unsigned long long>(dk) << 32) | static_cast<uint32_t>(~okey(u));
-                ids[slot] = static_cast<unsigned int>(i);
+                key0[slot] = (static_cast<unsigned long long>(dk) << 32) | static_cast<uint32_t>(~okey(u));
+                ids0[slot] = static_cast<unsigned int>(lo + i);
             }
         }
     });
-    uint64_t above = ty_sum_u64(at, sm);  // exact mass of the bins before the window
-    const unsigned int nw = sm->nwin;
+    const uint64_t atc = ty_sum_u64(at, sm);
+    publish(atc, 0.0, 0.f, 0.f);  // its barrier also completes the pushes into rank 0
+    uint64_t above = 0;
+    for (int r = 0; r < nc; ++r) above += rd(r)->u;  // exact mass of the bins before the window
+    ++xk;
 
+    // ---- rank 0 sorts the window and finds the cut; the cluster reads the result
     uint32_t dstar = 0u;
     float ustar = 0.f;
     int idstar = -1;
     bool found = false;
-    if (nw >= 1 && nw <= static_cast<unsigned int>(kTyBins) && above < target) {
-        int np2 = 1;
-        while (np2 < static_cast<int>(nw)) np2 <<= 1;
-        for (int i = static_cast<int>(nw) + tid; i < np2; i += kTyT) {
-            key[i] = ~0ull;
-            ids[i] = ~0u;
-        }
-        __syncthreads();
-        for (int k = 2; k <= np2; k <<= 1)
-            for (int j = k >> 1; j > 0; j >>= 1) {
-                for (int i = tid; i < np2; i += kTyT) {
-                    const int l = i ^ j;
-                    if (l > i) {
-                        const bool up = (i & k) == 0;
-                        const unsigned long long ki = key[i], kl = key[l];
-                        const bool gt = ki > kl || (ki == kl && ids[i] > ids[l]);
-                        if (gt == up) {
-                            key[i] = kl;
-                            key[l] = ki;
-                            const unsigned int t = ids[i];
-                            ids[i] = ids[l];
-                            ids[l] = t;
+    if (rank == 0) {
+        const unsigned int nw = sm->nwin;
+        if (nw >= 1 && nw <= static_cast<unsigned int>(kTyBins) && above < target) {
+            int np2 = 1;
+            while (np2 < static_cast<int>(nw)) np2 <<= 1;
+            for (int i = static_cast<int>(nw) + tid; i < np2; i += kTyT) {
+                key[i] = ~0ull;
+                ids[i] = ~0u;
+            }
+            __syncthreads();
+            for (int k = 2; k <= np2; k <<= 1)
+                for (int j = k >> 1; j > 0; j >>= 1) {
+                    for (int i = tid; i < np2; i += kTyT) {
+                        const int l = i ^ j;
+                        if (l > i) {
+                            const bool up = (i & k) == 0;
+                            const unsigned long long ki = key[i], kl = key[l];
+                            const bool gt = ki > kl || (ki == kl && ids[i] > ids[l]);
+                            if (gt == up) {
+                                key[i] = kl;
+                                key[l] = ki;
+                                const unsigned int t = ids[i];
+                                ids[i] = ids[l];
+                                ids[l] = t;
+                            }
                         }
                     }
+                    __syncthreads();
                 }
-                __syncthreads();
+            // cumulative mass in sorted order: thread t takes entries [2t, 2t + 2)
+            auto wmass = [&](int j) -> uint64_t {
+                return j < static_cast<int>(nw) ? fx40(hw_exp2(key_float(~static_cast<uint32_t>(key[j])))) : 0ull;
+            };
+            const int j0 = 2 * tid;
+            const uint64_t w0 = wmass(j0), w1 = wmass(j0 + 1);
+            if (tid == 0) sm->bc[2] = ~0ull;
+            uint64_t wt;
+            const uint64_t c0 = above + ty_excl_scan(w0 + w1, sm, wt);  // (begins with a barrier)
+            if (c0 < target && c0 + w0 + w1 >= target) sm->bc[2] = static_cast<unsigned long long>(c0 + w0 >= target ? j0 : j0 + 1);
+            __syncthreads();
+            if (sm->bc[2] != ~0ull) {  // the cut lies in the window
+                const int jc = static_cast<int>(sm->bc[2]);
+                dstar = static_cast<uint32_t>(key[jc] >> 32);
+                ustar = key_float(~static_cast<uint32_t>(key[jc]));
+                idstar = static_cast<int>(ids[jc]);
+                found = true;
             }
-        // cumulative mass in sorted order: thread t takes entries [2t, 2t + 2)
-        auto wmass = [&](int j) -> uint64_t {
-            return j < static_cast<int>(nw) ? fx40(hw_exp2(key_float(~static_cast<uint32_t>(key[j])))) : 0ull;
-        };
-        const int j0 = 2 * tid;
-        const uint64_t w0 = wmass(j0), w1 = wmass(j0 + 1);
-        if (tid == 0) sm->bc[2] = ~0ull;
-        uint64_t wt;
-        const uint64_t c0 = above + ty_excl_scan(w0 + w1, sm, wt);  // (begins with a barrier)
-        if (c0 < target && c0 + w0 + w1 >= target) sm->bc[2] = static_cast<unsigned long long>(c0 + w0 >= target ? j0 : j0 + 1);
-        __syncthreads();
-        if (sm->bc[2] != ~0ull) {  // the cut lies in the window
-            const int jc = static_cast<int>(sm->bc[2]);
-            dstar = static_cast<uint32_t>(key[jc] >> 32);
-            ustar = key_float(~static_cast<uint32_t>(key[jc]));
-            idstar = static_cast<int>(ids[jc]);
-            found = true;
+            __syncthreads();  // hist / cnt are reused below
         }
-        __syncthreads();  // hist / cnt are reused below
+        if (tid == 0) {
+            sm->res[0] = found ? 1ull : 0ull;
+            sm->res[1] = dstar;
+            sm->res[2] = __float_as_uint(ustar);
+            sm->res[3] = static_cast<uint32_t>(idstar);
+        }
     }
-    if (!found) {
-        // ---- the window missed or overflowed: radix select over the dk bits
-        // of every finite logit, then over u, then the rank in id order
+    cl.sync();
+    {
+        const unsigned long long* r0 = cl.map_shared_rank(sm->res, 0);
+        found = r0[0] != 0ull;
+        dstar = static_cast<uint32_t>(r0[1]);
+        ustar = __uint_as_float(static_cast<uint32_t>(r0[2]));
+        idstar = static_cast<int>(static_cast<uint32_t>(r0[3]));
+    }
+    if (!found && rank == 0) {
+        // ---- the window missed or overflowed: rank 0 alone, over the whole row:
+        // radix select over the dk bits of every finite logit, then over u, then
+        // the rank in id order
         above = 0;
         auto kd = [&](float x, int, uint32_t& k, uint64_t& m) -> bool {
             if (!(x > -INFINITY)) return false;
@@ -570,34 +678,62 @@ __global__ void __launch_bounds__(kTyT, 1)
             [&](uint64_t) { return r - 1; });
     }
 
+
     // ---- the draw over the kept set in id order
-    const int tok = ty_ordered_find(
-        z, V, sm,
-        [&](float x, int i) -> uint64_t {
-            if (!(x > -INFINITY)) return 0ull;
-            const float u = uof(x);
-            const uint32_t dk = dkey(u);
-            const bool keep = dk < dstar || (dk == dstar && (u > ustar || (u == ustar && i <= idstar)));
-            return keep ? fx40(hw_exp2(u)) : 0ull;
-        },
-        draw_x);
-    if (tid == 0) tokens[row] = tok;
+    auto kept = [&](float x, int i) -> uint64_t {  // i: the id
+        if (!(x > -INFINITY)) return 0ull;
+        const float u = uof(x);
+        const uint32_t dk = dkey(u);
+        const bool keep = dk < dstar || (dk == dstar && (u > ustar || (u == ustar && i <= idstar)));
+        return keep ? fx40(hw_exp2(u)) : 0ull;
+    };
+    if (!found) {
+        if (rank == 0) {
+            const int tok = ty_ordered_find(z, V, sm, kept, draw_x);
+            if (tid == 0) tokens[row] = tok;
+        }
+        cl.sync();
+        return;
+    }
+    const int f = ty_ordered_find(
+        zs, n, sm, [&](float x, int i) { return kept(x, lo + i); },
+        [&](uint64_t tot) { return cluster_x(tot, draw_x); });
+    if (f >= 0 && tid == 0) tokens[row] = lo + f;
+    cl.sync();  // no CTA leaves while a peer may still read its slot
+}
+
+int device_sm_count();
+
+// CTAs per row: as many as fill the GPU with one CTA per SM (1, 2, 4 or 8),
+// keeping slices of at least 2048 logits.
+static int typical_cluster_size(int B, int V) {
+    const int sms = device_sm_count();
+    int nc = 1;
+    while (nc < 8 && static_cast<long long>(B) * nc * 2 <= sms && V / (nc * 2) >= 2048) nc *= 2;
+    return nc;
 }
 
 cudaError_t launch_typical_sampler(int32_t* tokens, const float* logits, int B, int V, const float* temperature,
                                    const float* typical_p, const uint64_t* seeds, const uint64_t* offsets,
                                    int32_t* status, cudaStream_t stream) {
+    const int nc = typical_cluster_size(B, V);
+    int slice = (V + nc - 1) / nc;
+    slice = (slice + 3) & ~3;  // slices start on 16-byte boundaries of a 16-byte aligned row
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(B), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(B) * nc, 1, 1);
     cfg.blockDim = dim3(kTyT, 1, 1);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = nc;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t err = cudaLaunchKernelEx(&cfg, typical_sampler_kernel, tokens, logits, V, temperature, typical_p,
-                                         seeds, offsets, status);
+    cfg.numAttrs = 2;
+    cudaError_t err = cudaLaunchKernelEx(&cfg, typical_sampler_kernel, tokens, logits, V, slice, temperature,
+                                         typical_p, seeds, offsets, status);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
