@@ -717,6 +717,36 @@ def run_extras(args):
     return 0
 
 
+def run_typical_case(args):
+    """The typical-sampling case the typical sampler profile is captured on: the
+    sampler rows of the batch-64 GQA workload (64 x 128256 logits, T 0.7) with
+    typical_p 0.9; `--warmup` untimed calls, then `--steps` timed ones (CUDA
+    events on the stream, logits resident in L2 after the first call)."""
+    import paged_kv_decode_table_gb300 as pkv
+    from paged_kv_decode_table_gb300 import build as pkv_build
+    pkv_build.build()
+    pkv.load_library()
+    dev = torch.device("cuda", 0)
+    w = W.workload(2)
+    si = W.make_sampler_inputs(w, dev)
+    tok = torch.empty(w.batch, dtype=torch.int32, device=dev)
+    tpt = torch.full((w.batch,), 0.9, dtype=torch.float32, device=dev)
+    st = pkv.new_status()
+    for _ in range(args.warmup):
+        pkv.sample_tokens_typical(si["logits"], si["temperature"], tpt, si["seeds"], si["offsets"], tokens=tok, status=st)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        pkv.sample_tokens_typical(si["logits"], si["temperature"], tpt, si["seeds"], si["offsets"], tokens=tok, status=st)
+    e1.record()
+    torch.cuda.synchronize()
+    assert pkv.check_status(st) == 0
+    print(json.dumps({"case": f"typical sampling {w.batch} x {w.vocab}, T 0.7, typical_p 0.9", "calls": args.steps,
+                      "us_per_call": e0.elapsed_time(e1) / max(1, args.steps) * 1000}))
+    return 0
+
+
 def run_prefill_case(args):
     """The chunked-prefill case the prefill profile is captured on:
     `--prefill-seqs` sequences (default 4) with a 512-token chunk each after a
@@ -776,9 +806,13 @@ def main():
     ap.add_argument("--prefill-case", action="store_true",
                     help="time the small chunked-prefill case of the prefill profile (--warmup, --steps calls)")
     ap.add_argument("--prefill-seqs", type=int, default=4, help="sequences of the --prefill-case workload")
+    ap.add_argument("--typical-case", action="store_true",
+                    help="time the typical-sampling case of the typical sampler profile (--warmup, --steps calls)")
     args = ap.parse_args()
     if args.prefill_case:
         return run_prefill_case(args)
+    if args.typical_case:
+        return run_typical_case(args)
     if args.impl == "reference":
         return run_reference(args)
     if args.extras:
