@@ -153,6 +153,27 @@ __device__ __forceinline__ void tma_load_4d(void* smem_dst, const void* tmap, in
         "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
         : "memory");
 }
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float tc_max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+// (x0, x1) = (a0 b + c, a1 b + c) and (s0, s1) += (a0, a1) as paired fp32 operations
+__device__ __forceinline__ void tc_fma2(float& x0, float& x1, float a0, float a1, float b, float c) {
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\tmov.b64 rc, {%5, %5};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(x0), "=f"(x1)
+        : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+__device__ __forceinline__ void tc_add2(float& s0, float& s1, float a0, float a1) {
+    asm("{\n\t.reg .b64 ra, rs;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rs, {%0, %1};\n\t"
+        "add.rn.f32x2 rs, rs, ra;\n\tmov.b64 {%0, %1}, rs;\n\t}"
+        : "+f"(s0), "+f"(s1)
+        : "f"(a0), "f"(a1));
+}
 __device__ __forceinline__ float tc_ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -494,42 +515,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int kbase = kt * kTcKeys;
             // maximum of the raw scores (the scale is positive), eight chains;
             // the causal mask only on tiles that reach past the query tile's first position
-            float mxs[8];
+            // (three-input maxima: two scores per instruction, four chains)
+            float mxs[4];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) mxs[k] = -INFINITY;
+            for (int k = 0; k < 4; ++k) mxs[k] = -INFINITY;
             if (kbase + kTcKeys - 1 > p0t) {
 #pragma unroll
                 for (int c = 0; c < kTcKeys; ++c) {
                     const float v = kbase + c <= pos ? __uint_as_float(sr[c >> 5][c & 31]) : -INFINITY;
                     sr[c >> 5][c & 31] = __float_as_uint(v);
-                    mxs[c & 7] = fmaxf(mxs[c & 7], v);
                 }
-            } else {
-#pragma unroll
-                for (int c = 0; c < kTcKeys; ++c) mxs[c & 7] = fmaxf(mxs[c & 7], __uint_as_float(sr[c >> 5][c & 31]));
             }
-            const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
-                                   fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7]))) *
-                             scale_log2;
+#pragma unroll
+            for (int c = 0; c < kTcKeys; c += 2)
+                mxs[(c >> 1) & 3] = tc_max3(mxs[(c >> 1) & 3], __uint_as_float(sr[c >> 5][c & 31]),
+                                            __uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]));
+            const float mx = fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])) * scale_log2;
             // the reference maximum moves only when the row maximum passes it by more than 8
             const float m_new = mx > m_ref + 8.f ? mx : m_ref;
             const bool resc = m_new != m_ref;
             const float a = resc ? tc_ex2(m_ref - m_new) : 1.f;
             m_ref = m_new;
             const float nmu = m_ref == -INFINITY ? 0.f : -m_ref;
-            // P = 2^(s scale - m_ref) (masked scores give 0), the sum in eight chains
+            // P = 2^(s scale - m_ref) (masked scores give 0), the sum in four chains of
+            // pairs (the scale, the offset and the sum as paired fp32 operations)
             uint32_t pk[kTcKeys / 2];
-            float ls[8];
+            float ls[4][2];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+            for (int k = 0; k < 4; ++k) ls[k][0] = ls[k][1] = 0.f;
 #pragma unroll
             for (int c = 0; c < kTcKeys / 2; ++c) {
-                const float e0 = tc_ex2(fmaf(__uint_as_float(sr[(2 * c) >> 5][(2 * c) & 31]), scale_log2, nmu));
-                const float e1 = tc_ex2(fmaf(__uint_as_float(sr[(2 * c + 1) >> 5][(2 * c + 1) & 31]), scale_log2, nmu));
+                float t0, t1;
+                tc_fma2(t0, t1, __uint_as_float(sr[(2 * c) >> 5][(2 * c) & 31]),
+                        __uint_as_float(sr[(2 * c + 1) >> 5][(2 * c + 1) & 31]), scale_log2, nmu);
+                const float e0 = tc_ex2(t0), e1 = tc_ex2(t1);
                 pk[c] = pack_bf16x2(e0, e1);
-                ls[c & 7] += e0 + e1;
+                tc_add2(ls[c & 3][0], ls[c & 3][1], e0, e1);
             }
-            lsum = lsum * a + (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
+            lsum = lsum * a + (((ls[0][0] + ls[0][1]) + (ls[1][0] + ls[1][1])) +
+                               ((ls[2][0] + ls[2][1]) + (ls[3][0] + ls[3][1])));
             // S_j was issued after the PV of tile j - 1 had completed: O may be rescaled
             if (j > 0 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
