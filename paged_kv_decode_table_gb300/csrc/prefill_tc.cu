@@ -12,7 +12,7 @@
 //    head h, so each K/V tile serves 256 rows.  The CTAs take the chunk tiles
 //    longest first (by the number of key tiles they read; the KV head is the
 //    innermost grid index), so that the longest start in the first wave.
-//  * K and V of head h stream in 64-key tiles through a six-stage ring.  The
+//  * K and V of head h stream in 64-key tiles through a five-stage ring.  The
 //    paged layout allows TMA boxes of one block's 16 keys at most.  K comes in
 //    one 4 KB box per 16 keys through a 4-D view of the pool that lands the
 //    two 64-dimension halves interleaved at 1 KB, so that for either half the
@@ -25,18 +25,20 @@
 //  * Tensor memory, per query tile t (256 columns): Q (bf16, two per column)
 //    at 256 t, S at 256 t + 64, O at 256 t + 128.  One warp issues
 //    S = Q K^T (M 128, N 64, K 128; A = Q from tensor memory, B = K from the
-//    stage), another O += P V (M 128, N 128, K 64; A = P from tensor memory,
-//    B = V as stored, MN-major, one 16-key group per k-step).  P (bf16)
-//    overwrites the first 32 columns of the S it came from, so S of tile j + 1
-//    waits for the PV of tile j; the two query tiles interleave on the tensor
-//    pipe.  Completion is signalled through mbarriers (tcgen05.commit).
+//    stage), another O += P V (M 128, N 128, K 64; A = P from a K-major,
+//    128-byte-swizzled shared tile per query tile, B = V as stored, MN-major,
+//    one 16-key group per k-step).  The softmax releases S as soon as it has
+//    read it, so S of tile j + 1 runs during the softmax of tile j; P of tile
+//    j + 1 is written once the PV of tile j is complete.  The two query tiles
+//    interleave on the tensor pipe.  Completion is signalled through
+//    mbarriers (tcgen05.commit).
 //  * Eight softmax warps, four per query tile: thread r owns row r (TMEM lane
 //    r).  It reads its 64 scores (tcgen05.ld), applies the causal mask and the
 //    scale in the log2 domain, and exponentiates against a reference maximum
 //    that is raised only when the row maximum exceeds it by more than 8, in
 //    which case the row of O in TMEM and the running sum are rescaled first;
-//    P (bf16, values at most 2^8) goes back to tensor memory for the PV MMA,
-//    and the sum accumulates the fp32 values.  Rows past the chunk are
+//    P (bf16, values at most 2^8) goes to shared memory for the PV MMA, and
+//    the sum accumulates the fp32 values.  Rows past the chunk are
 //    computed on zero queries and not stored.  The V rows of keys at or past
 //    the sequence length (which may hold anything, NaN included) are cleared
 //    before the last PV MMAs.
@@ -56,7 +58,8 @@ constexpr int kTcDim = 128;
 constexpr int kTcRows = 128;                 // query rows per query tile (TMEM lanes)
 constexpr int kTcQT = 2;                     // query tiles per CTA, sharing every K/V tile
 constexpr int kTcKeys = 64;                  // keys per tile
-constexpr int kTcStages = 6;                 // K/V ring depth
+constexpr int kTcStages = 5;                 // K/V ring depth
+constexpr int kTcPBytes = kTcRows * kTcKeys * 2;          // 16 KB: P of one query tile, one atom of 128 rows
 constexpr int kTcKBytes = kTcKeys * kTcDim * 2;           // 16 KB per operand tile
 constexpr int kTcGroupBytes = 16 * kTcDim * 2;            // 4 KB: 16 keys x 128 dimensions
 constexpr int kTcStageBytes = 2 * kTcKBytes;              // K then V
@@ -69,13 +72,13 @@ constexpr int kTcTmemCols = 512;             // query tile t: Q at 256 t, S (the
 
 struct TcSmem {  // follows the 1024-aligned operand area
     uint64_t kv_full[kTcStages], kv_empty[kTcStages];
-    uint64_t s_full[kTcQT], p_full[kTcQT], o_done[kTcQT];
+    uint64_t s_full[kTcQT], s_free[kTcQT], p_full[kTcQT], o_done[kTcQT];
     uint32_t tmem_base;
     int b, tile, bad;
     int rows[kTcStages][4];  // pool rows of the tile's four 16-key boxes, per stage
     int tbl[kTcWin];
 };
-constexpr size_t kTcOperandBytes = kTcStages * static_cast<size_t>(kTcStageBytes);
+constexpr size_t kTcOperandBytes = kTcQT * static_cast<size_t>(kTcPBytes) + kTcStages * static_cast<size_t>(kTcStageBytes);
 constexpr size_t kTcSmemBytes = 1024 + kTcOperandBytes + sizeof(TcSmem);
 static_assert(kTcSmemBytes <= 227 * 1024, "shared memory of one CTA");
 
@@ -214,7 +217,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                       int32_t* status) {
     extern __shared__ uint8_t tc_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sKV = base;
+    uint8_t* sP = base;                          // P of query tile t at t kTcPBytes
+    uint8_t* sKV = base + kTcQT * kTcPBytes;
     TcSmem* sm = reinterpret_cast<TcSmem*>(base + kTcOperandBytes);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = Hq / Hkv, h = static_cast<int>(blockIdx.x) % Hkv;
@@ -229,6 +233,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         for (int t = 0; t < kTcQT; ++t) {
             mbar_init(&sm->s_full[t], 1);
+            mbar_init(&sm->s_free[t], kTcRows);
             mbar_init(&sm->p_full[t], kTcRows);
             mbar_init(&sm->o_done[t], 1);
         }
@@ -438,7 +443,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else if (warp == kTcWarpS && active) {
         // ------------------------------------------------ S = Q K^T for both query tiles (lane 0 issues)
         // Q (A) from tensor memory, K (B) from the stage.  S_j of query tile t
-        // overwrites P_{j-1}, so it waits for the PV of tile j - 1.
+        // overwrites S_{j-1} once the softmax has read it, so it runs while the
+        // softmax works on tile j - 1.
         if (lane == 0) {
             constexpr uint32_t idS = tc_idesc(kTcRows, kTcKeys, false);
             const uint32_t kva = smem_u32(sKV);
@@ -450,7 +456,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 const uint32_t kb = kva + s * kTcStageBytes;
                 for (int t = 0; t < kTcQT; ++t) {
-                    if (j >= 1 && !mbar_wait(&sm->o_done[t], (j - 1) & 1)) {
+                    if (j >= 1 && !mbar_wait(&sm->s_free[t], (j - 1) & 1)) {
                         fail = true;
                         break;
                     }
@@ -467,13 +473,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
     } else if (warp == kTcWarpPV && active) {
         // ------------------------------------------------ O += P V for both query tiles (lane 0 issues)
-        // P of query tile t (bf16, over the first 32 columns of the S it was
-        // computed from) is the A operand, read from tensor memory.  Both P tiles
-        // of key tile j were written after the softmax read S_j, so once their PV
-        // MMAs are complete nothing reads the stage any more.
+        // P of query tile t (bf16, a K-major 128-byte-swizzled shared tile) is
+        // the A operand.  Both P tiles of key tile j were written after the
+        // softmax read S_j, so once their PV MMAs are complete nothing reads the
+        // stage any more.
         if (lane == 0) {
             constexpr uint32_t idO = tc_idesc(kTcRows, kTcDim, true);
-            const uint32_t kva = smem_u32(sKV);
+            const uint32_t pa = smem_u32(sP), kva = smem_u32(sKV);
             for (int j = 0; j < ntiles && !fail; ++j) {
                 const int s = j % kTcStages;
                 const uint32_t vb = kva + s * kTcStageBytes + kTcKBytes;
@@ -483,12 +489,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t tp = tmem + 256 * t + 64;
+                    const uint32_t pb = pa + t * kTcPBytes;
 #pragma unroll
                     for (int kk = 0; kk < kTcKeys / 16; ++kk)
-                        tc_mma_ta(tmem + 256 * t + 128, tp + 8 * kk,
-                                  tc_desc(vb + kTcGroupBytes * kk, kTcGroupBytes / 2, 1024), idO,
-                                  (j > 0 || kk > 0) ? 1u : 0u);
+                        tc_mma(tmem + 256 * t + 128, tc_desc(pb + 32 * kk, 16, 1024),
+                               tc_desc(vb + kTcGroupBytes * kk, kTcGroupBytes / 2, 1024), idO,
+                               (j > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(&sm->o_done[t]);
                 }
                 if (!fail) tc_commit(&sm->kv_empty[s]);
@@ -511,6 +517,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             uint32_t sr[2][32];
             tc_ld32(tq + lrow + 64, sr[0]);
             tc_ld32(tq + lrow + 96, sr[1]);
+            tc_fence_before();
+            mbar_arrive(&sm->s_free[qt]);  // S may take the next tile
             const int kt = j + rot < ntiles ? j + rot : j + rot - ntiles;
             const int kbase = kt * kTcKeys;
             // maximum of the raw scores (the scale is positive), eight chains;
@@ -554,7 +562,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             lsum = lsum * a + (((ls[0][0] + ls[0][1]) + (ls[1][0] + ls[1][1])) +
                                ((ls[2][0] + ls[2][1]) + (ls[3][0] + ls[3][1])));
-            // S_j was issued after the PV of tile j - 1 had completed: O may be rescaled
+            // the PV of tile j - 1 is complete: O may be rescaled and the P tile rewritten
+            if (j > 0) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&sm->o_done[qt], (j - 1) & 1))) {
+                    fail = true;
+                    break;
+                }
+                tc_fence_after();
+            }
             if (j > 0 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
                 for (int cc = 0; cc < kTcDim / 32; ++cc) {
@@ -574,9 +589,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                               (rr & 15) * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
-            // P row r (64 bf16, two per column) over the first 32 columns of S
-            tc_st32(tq + lrow + 64, pk);
-            if (qt == 0 && kt == ntiles - 1) fence_proxy_async_smem();  // the cleared V rows
+            // P row r (64 bf16 = 8 chunks of 16 bytes) into the K-major P tile of query tile qt
+            uint8_t* pbuf = sP + qt * kTcPBytes;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+                *reinterpret_cast<uint4*>(pbuf + sw128(r, ch)) =
+                    make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+            fence_proxy_async_smem();  // P and the cleared V rows, for the PV MMA
             tc_fence_before();
             mbar_arrive(&sm->p_full[qt]);
         }
