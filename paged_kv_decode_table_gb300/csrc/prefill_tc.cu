@@ -18,10 +18,11 @@
 //    two 64-dimension halves interleaved at 1 KB, so that for either half the
 //    8-row groups of the tile sit 2 KB apart (one N = 64 MMA per k-step); V in
 //    one 4 KB box per 16 keys (a 3-D view, both halves, one box per PV k-step).
-//    Three producer warps issue a tile's eight boxes together; the block ids
-//    come from a window of the block table kept in shared memory.  Each CTA
-//    walks its key tiles starting at a different tile, so that the CTAs
-//    sharing a sequence do not read the same blocks at the same time.
+//    Three producer warps issue a tile's eight boxes, each on its own (its
+//    own window of the block table in shared memory, its own arrival on the
+//    stage's barrier).  Each CTA walks its key tiles starting at a different
+//    tile, so that the CTAs sharing a sequence do not read the same blocks at
+//    the same time.
 //  * Tensor memory, per query tile t (256 columns): Q (bf16, two per column)
 //    at 256 t, S at 256 t + 64, O at 256 t + 128.  One warp issues
 //    S = Q K^T (M 128, N 64, K 128; A = Q from tensor memory, B = K from the
@@ -63,7 +64,8 @@ constexpr int kTcPBytes = kTcRows * kTcKeys * 2;          // 16 KB: P of one que
 constexpr int kTcKBytes = kTcKeys * kTcDim * 2;           // 16 KB per operand tile
 constexpr int kTcGroupBytes = 16 * kTcDim * 2;            // 4 KB: 16 keys x 128 dimensions
 constexpr int kTcStageBytes = 2 * kTcKBytes;              // K then V
-constexpr int kTcWin = 2048;                 // block-table entries kept in shared memory
+constexpr int kTcProd = 3;                   // producer warps
+constexpr int kTcWin = 640;                  // block-table entries kept in shared memory, per producer warp
 // warps 0-7: softmax (warp w: query tile w / 4, TMEM lanes 32 (w % 4) ..); warp 8:
 // producer (block rows); warp 9: S MMAs; warp 10: PV MMAs; warps 11-12: producers
 constexpr int kTcWarpProd = 8, kTcWarpS = 9, kTcWarpPV = 10;
@@ -75,8 +77,7 @@ struct TcSmem {  // follows the 1024-aligned operand area
     uint64_t s_full[kTcQT], s_free[kTcQT], p_full[kTcQT], o_done[kTcQT];
     uint32_t tmem_base;
     int b, tile, bad;
-    int rows[kTcStages][4];  // pool rows of the tile's four 16-key boxes, per stage
-    int tbl[kTcWin];
+    int tbl[kTcProd][kTcWin];
 };
 constexpr size_t kTcOperandBytes = kTcQT * static_cast<size_t>(kTcPBytes) + kTcStages * static_cast<size_t>(kTcStageBytes);
 constexpr size_t kTcSmemBytes = 1024 + kTcOperandBytes + sizeof(TcSmem);
@@ -228,7 +229,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ---- prologue, independent of the inputs
     if (tid == 0) {
         for (int s = 0; s < kTcStages; ++s) {
-            mbar_init(&sm->kv_full[s], 1);
+            mbar_init(&sm->kv_full[s], kTcProd);  // one arrival (with its bytes) per producer warp
             mbar_init(&sm->kv_empty[s], 1);
         }
         for (int t = 0; t < kTcQT; ++t) {
@@ -374,65 +375,58 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     bool fail = false;
     if ((warp == kTcWarpProd || warp > kTcWarpPV) && active) {
         // ------------------------------------------------ producer warps 8, 11, 12
-        // Warp 8 waits for the stage, reads the tile's four block rows, arms the
-        // stage's transaction count and meets warps 11 and 12 at a named
-        // barrier; then the three warps issue the tile's eight 4 KB boxes (box i:
-        // K of 16-key group i for i < 4, V of group i - 4 otherwise; warp pw takes
-        // i = pw, pw + 3, pw + 6).
+        // The three warps work independently: warp pw issues boxes i = pw, pw + 3,
+        // pw + 6 of every tile (box i: K of 16-key group i for i < 4, V of group
+        // i - 4 otherwise), with block ids from its own window of the block table;
+        // it waits for the stage itself and arms the stage's transaction count
+        // with its own bytes (the stage's full barrier expects one arrival per
+        // producer warp), so one warp's bookkeeping overlaps the others' copies.
         const int pw = warp == kTcWarpProd ? 0 : warp - kTcWarpPV;
+        const int nbox = pw < 2 ? 3 : 2;  // boxes of this warp per tile
+        int* tbl = sm->tbl[pw];
         const int32_t* trow = block_tables + static_cast<size_t>(b) * max_blocks;
         int win0 = -kTcWin;
         for (int j = 0; j < ntiles && !fail; ++j) {
             const int s = j % kTcStages;
             const int kt = j + rot < ntiles ? j + rot : j + rot - ntiles;
-            if (pw == 0) {
-                const int kb0 = (kt * kTcKeys) / BS, kb1 = min(nblk_used - 1, (kt * kTcKeys + kTcKeys - 1) / BS);
-                if (kb0 < win0 || kb1 >= win0 + kTcWin) {  // move the block-table window (warp 8 alone reads it)
-                    __syncwarp();
-                    win0 = kb0;
-                    for (int i = lane; i < kTcWin; i += 32) sm->tbl[i] = win0 + i < nblk_used ? trow[win0 + i] : 0;
-                    __syncwarp();
-                }
-                if (lane == 0 && !mbar_wait(&sm->kv_empty[s], ((j / kTcStages) & 1) ^ 1)) {
-                    report(status, PKV_ERR_TIMEOUT);
-                    fail = true;
-                }
-                fail = __shfl_sync(0xffffffffu, fail, 0);
-                if (!fail && lane < kTcKeys / 16) {  // the rows of 16-key box `lane` (a bad block id is
-                                                      // flagged before the arrive below)
-                    const int key0 = kt * kTcKeys + 16 * lane;
-                    const int kb = key0 / BS;
-                    int blk = 0, slot = 0;
-                    if (kb < nblk_used) {  // later keys: any valid rows (masked; their V rows are cleared)
-                        blk = sm->tbl[kb - win0];
-                        slot = key0 - kb * BS;
-                        if (blk < 0 || blk >= NB) {
-                            sm->bad = 1;
-                            report(status, PKV_ERR_DEVICE_BOUNDS);
-                            blk = 0;
-                        }
-                    }
-                    sm->rows[s][lane] = (blk * Hkv + h) * BS + slot;
-                }
+            const int kb0 = (kt * kTcKeys) / BS, kb1 = min(nblk_used - 1, (kt * kTcKeys + kTcKeys - 1) / BS);
+            if (kb0 < win0 || kb1 >= win0 + kTcWin) {  // move this warp's window of the block table
                 __syncwarp();
-                if (!fail && lane == 0) mbar_arrive_expect_tx(&sm->kv_full[s], kTcStageBytes);
-                if (lane == 0) sm->rows[s][0] |= fail ? static_cast<int>(0x80000000u) : 0;  // tell the others
+                win0 = kb0;
+                for (int i = lane; i < kTcWin; i += 32) tbl[i] = win0 + i < nblk_used ? trow[win0 + i] : 0;
                 __syncwarp();
             }
-            asm volatile("bar.sync 1, 96;" ::: "memory");  // the rows are published (warps 8, 11, 12)
-            const int r0 = sm->rows[s][0];
-            if (r0 < 0) {  // warp 8 gave up
+            if (lane == 0 && !mbar_wait(&sm->kv_empty[s], ((j / kTcStages) & 1) ^ 1)) {
+                report(status, PKV_ERR_TIMEOUT);
                 fail = true;
-                break;
             }
+            fail = __shfl_sync(0xffffffffu, fail, 0);
+            if (fail) break;
             const int bi = pw + 3 * lane;
-            if (lane < 3 && bi < 8) {
+            int row = 0;
+            if (lane < nbox) {  // the pool row of box bi's first key
+                const int key0 = kt * kTcKeys + 16 * (bi & 3);
+                const int kb = key0 / BS;
+                int blk = 0, slot = 0;
+                if (kb < nblk_used) {  // later keys: any valid rows (masked; their V rows are cleared)
+                    blk = tbl[kb - win0];
+                    slot = key0 - kb * BS;
+                    if (blk < 0 || blk >= NB) {
+                        sm->bad = 1;
+                        report(status, PKV_ERR_DEVICE_BOUNDS);
+                        blk = 0;
+                    }
+                }
+                row = (blk * Hkv + h) * BS + slot;
+            }
+            if (lane == 0) mbar_arrive_expect_tx(&sm->kv_full[s], nbox * kTcGroupBytes);
+            __syncwarp();  // the arrival precedes this warp's copies
+            if (lane < nbox) {
                 uint8_t* st = sKV + static_cast<size_t>(s) * kTcStageBytes;
                 if (bi < 4)  // K of group bi: [8-row half][64-dimension half][8 rows][128 B]
-                    tma_load_4d(st + kTcGroupBytes * bi, &tmK, 0, 0, 0, sm->rows[s][bi] >> 3, &sm->kv_full[s]);
+                    tma_load_4d(st + kTcGroupBytes * bi, &tmK, 0, 0, 0, row >> 3, &sm->kv_full[s]);
                 else  // V of group bi - 4: [64-dimension half][16 rows][128 B]
-                    tma_load_3d(st + kTcKBytes + kTcGroupBytes * (bi - 4), &tmV, 0, sm->rows[s][bi - 4], 0,
-                                &sm->kv_full[s]);
+                    tma_load_3d(st + kTcKBytes + kTcGroupBytes * (bi - 4), &tmV, 0, row, 0, &sm->kv_full[s]);
             }
             __syncwarp();
         }
