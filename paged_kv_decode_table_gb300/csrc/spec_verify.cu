@@ -21,13 +21,17 @@
 //
 // Two kernels: row statistics (max, lowest argmax, mass sum in one pass over
 // the row, the sum kept relative to a running maximum) with one CTA per logits
-// row; then one CTA per request for the tests (one thread per draft
-// position) and the final draw (chunked inverse CDF over the vocabulary).
+// row; then one thread-block cluster per request (1-8 CTAs) for the tests (one
+// thread per draft position, in every CTA) and the final draw (chunked inverse
+// CDF over the vocabulary, spread over the CTAs' slices).
+#include <cooperative_groups.h>
 #include <limits.h>
 #include <math.h>
 
 #include "pkv_common.cuh"
 #include "sampling_math.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace pkv {
 
@@ -169,14 +173,19 @@ __global__ void __launch_bounds__(kVT)
     }
 }
 
-// ------------------------------------------------------------------ CTA inverse-CDF draw
-// First element e (ascending) of [0, n) whose running mass exceeds
-// floor(u * total), masses given four at a time by m4(e, out[4]).  Chunks of
-// 128 * cpw elements: warp w sums chunks w, w + 16, ... (lane l takes elements
-// 4l..4l+3 of each 128), the chunk sums are scanned in shared memory, and warp
-// 0 walks the chunk that holds the draw.  Returns -1 when the total is 0.
-template <typename M4>
-__device__ int cta_draw(int n, M4 m4, uint64_t u53, unsigned long long* ctot, unsigned long long* red, int* sel) {
+// ------------------------------------------------------------------ inverse-CDF draw over a slice
+// This CTA's part of a draw over the slices of a cluster: the first element e
+// (ascending) of its slice [0, n) at which the running mass, counted from the
+// masses of the earlier slices, exceeds the draw position.  Masses come four
+// at a time from m4(e, out[4]).  Chunks of 128 * cpw elements: warp w sums
+// chunks w, w + 16, ... (lane l takes elements 4l..4l+3 of each 128), the chunk
+// sums are scanned in shared memory; xf(total, X) turns this slice's total into
+// the draw position relative to the slice (~0 when it lies in another slice)
+// and returns false when the cluster's total is 0; then warp 0 walks the chunk
+// that holds the draw.  Returns the element, -1 when the draw lies in another
+// slice, -2 when the cluster's total is 0.
+template <typename M4, typename XF>
+__device__ int cta_draw(int n, M4 m4, XF xf, unsigned long long* ctot, unsigned long long* red, int* sel) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nv = (n + 3) & ~3;
     const int cpw = max(1, (nv + 128 * kDrawChunks - 1) / (128 * kDrawChunks));
@@ -227,8 +236,8 @@ __device__ int cta_draw(int n, M4 m4, uint64_t u53, unsigned long long* ctot, un
         run += t4[q];
     }
     __syncthreads();
-    if (total == 0) return -1;
-    const uint64_t X = static_cast<uint64_t>((static_cast<unsigned __int128>(u53) * total) >> 53);
+    uint64_t X = ~0ull;
+    if (!xf(total, X)) return -2;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const int ch = 4 * tid + q;
@@ -276,19 +285,28 @@ __device__ int cta_draw(int n, M4 m4, uint64_t u53, unsigned long long* ctot, un
 }
 
 // ------------------------------------------------------------------ verification
+// One cluster of nc CTAs per request: every CTA takes the (cheap) tests; the
+// final draw is spread over the vocabulary slices [rank * slice, ...) of the
+// cluster, the slices' totals exchanged through distributed shared memory,
+// and the CTA whose slice holds the draw writes the token.  Rank 0 writes the
+// other outputs.
 __global__ void __launch_bounds__(kVT)
     spec_verify_kernel(int32_t* __restrict__ tokens_out, int32_t* __restrict__ n_accepted,
                        int32_t* __restrict__ seq_lens_out, const float* __restrict__ target,
                        const float* __restrict__ draft, const int32_t* __restrict__ draft_tokens,
-                       const int32_t* __restrict__ seq_lens, int gamma, int V, const float* __restrict__ temperature,
-                       const uint64_t* __restrict__ seeds, const uint64_t* __restrict__ offsets,
-                       const RowStat* __restrict__ stats, int32_t* status) {
+                       const int32_t* __restrict__ seq_lens, int gamma, int V, int slice,
+                       const float* __restrict__ temperature, const uint64_t* __restrict__ seeds,
+                       const uint64_t* __restrict__ offsets, const RowStat* __restrict__ stats, int32_t* status) {
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the row statistics are complete
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ unsigned long long ctot[kDrawChunks];
     __shared__ unsigned long long red[kVW];
+    __shared__ unsigned long long xslot[2];  // this slice's total, alternating per draw
     __shared__ int sel, nrej, err;
-    const int b = blockIdx.x, tid = threadIdx.x;
+    cg::cluster_group cl = cg::this_cluster();
+    const int nc = static_cast<int>(cl.num_blocks()), rank = static_cast<int>(cl.block_rank());
+    const int b = blockIdx.x / nc, tid = threadIdx.x;
+    const int lo = min(V, rank * slice), ns = min(V, lo + slice) - lo;  // this CTA's slice of the vocabulary
     const int rows = 2 * gamma + 1;
     const RowStat* st = stats + static_cast<size_t>(b) * rows;
     const float T = temperature[b];
@@ -310,12 +328,14 @@ __global__ void __launch_bounds__(kVT)
         nrej = gamma;
     }
     __syncthreads();
-    if (err) {
-        for (int i = tid; i <= gamma; i += kVT) tok[i] = -1;
-        if (tid == 0) {
-            n_accepted[b] = 0;
-            seq_lens_out[b] = L;
-            report(status, err);
+    if (err) {  // the same in every CTA of the cluster, before any exchange
+        if (rank == 0) {
+            for (int i = tid; i <= gamma; i += kVT) tok[i] = -1;
+            if (tid == 0) {
+                n_accepted[b] = 0;
+                seq_lens_out[b] = L;
+                report(status, err);
+            }
         }
         return;
     }
@@ -341,10 +361,17 @@ __global__ void __launch_bounds__(kVT)
     }
     __syncthreads();
     const int n = nrej;
-    int final_tok;
-    if (T == 0.f) {
-        final_tok = st[n].argmax;
-    } else {
+    // rank 0 writes every output but the drawn token (before the draw's cluster
+    // barrier, so that the CTA holding the draw writes that one after it)
+    if (rank == 0) {
+        for (int i = tid; i <= gamma; i += kVT)
+            tok[i] = i < n ? draft_tokens[static_cast<size_t>(b) * gamma + i] : (i == n && T == 0.f ? st[n].argmax : -1);
+        if (tid == 0) {
+            n_accepted[b] = n;
+            seq_lens_out[b] = L - gamma + n;
+        }
+    }
+    if (T != 0.f) {
         const uint64_t u53 = philox_word0(seed, offset, 0) >> 11;
         const float* zt = target + (static_cast<size_t>(b) * (gamma + 1) + n) * V;
         const bool alt = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(zt) & 15u) == 0);
@@ -356,7 +383,23 @@ __global__ void __launch_bounds__(kVT)
             m[2] = mass(q.z, mt, c2);
             m[3] = mass(q.w, mt, c2);
         };
-        final_tok = -1;
+        int xk = 0;
+        auto xf = [&](uint64_t tot, uint64_t& X) -> bool {  // the draw position relative to this slice
+            if (tid == 0) xslot[xk & 1] = tot;
+            cl.sync();
+            uint64_t excl = 0, grand = 0;
+            for (int r = 0; r < nc; ++r) {
+                const uint64_t t = *cl.map_shared_rank(&xslot[xk & 1], r);
+                excl += r < rank ? t : 0ull;
+                grand += t;
+            }
+            ++xk;
+            if (grand == 0) return false;
+            const uint64_t Xg = static_cast<uint64_t>((static_cast<unsigned __int128>(u53) * grand) >> 53);
+            X = (Xg >= excl && Xg - excl < tot) ? Xg - excl : ~0ull;
+            return true;
+        };
+        int f = -2;
         if (n < gamma) {
             // residual max(0, p - q) in 2^-40 fixed point of probability
             const float* zd = draft + (static_cast<size_t>(b) * gamma + n) * V;
@@ -374,21 +417,20 @@ __global__ void __launch_bounds__(kVT)
                     m[j] = fx40(fminf(fmaxf(r, 0.f), 1.f));
                 }
             };
-            final_tok = cta_draw(V, resid_mass, u53, ctot, red, &sel);
+            f = cta_draw(ns, [&](int e, uint64_t* m) { resid_mass(lo + e, m); }, xf, ctot, red, &sel);
         }
-        if (final_tok < 0) final_tok = cta_draw(V, target_mass, u53, ctot, red, &sel);
-    }
-    for (int i = tid; i <= gamma; i += kVT)
-        tok[i] = i < n ? draft_tokens[static_cast<size_t>(b) * gamma + i] : (i == n ? final_tok : -1);
-    if (tid == 0) {
-        n_accepted[b] = n;
-        seq_lens_out[b] = L - gamma + n;
+        if (f == -2)  // no residual mass (or every draft kept): draw from p
+            f = cta_draw(ns, [&](int e, uint64_t* m) { target_mass(lo + e, m); }, xf, ctot, red, &sel);
+        if (f >= 0 && tid == 0) tok[n] = lo + f;
+        cl.sync();  // no CTA leaves while a peer may still read its slot
     }
 }
 
 size_t spec_verify_workspace_bytes(int B, int gamma) {
     return static_cast<size_t>(B) * (2 * static_cast<size_t>(gamma) + 1) * sizeof(RowStat);
 }
+
+int device_sm_count();
 
 cudaError_t launch_spec_verify(int32_t* tokens_out, int32_t* n_accepted, int32_t* seq_lens_out, const float* target,
                                const float* draft, const int32_t* draft_tokens, const int32_t* seq_lens, int B,
@@ -406,9 +448,24 @@ cudaError_t launch_spec_verify(int32_t* tokens_out, int32_t* n_accepted, int32_t
     cfg.numAttrs = 1;
     cudaError_t err = cudaLaunchKernelEx(&cfg, spec_stats_kernel, target, draft, gamma, V, temperature, stats);
     if (err != cudaSuccess) return err;
-    cfg.gridDim = dim3(static_cast<unsigned>(B), 1, 1);
+    // CTAs per request: as many as fit two 512-thread CTAs per SM (1, 2, 4 or 8),
+    // slices of at least 4096 logits
+    const int sms = device_sm_count();
+    int nc = 1;
+    while (nc < 8 && static_cast<long long>(B) * nc * 2 <= 2LL * sms && V / (nc * 2) >= 4096) nc *= 2;
+    int slice = (V + nc - 1) / nc;
+    slice = (slice + 3) & ~3;  // slices start on 16-byte boundaries of a 16-byte aligned row
+    cudaLaunchAttribute attr2[2];
+    attr2[0] = attr[0];
+    attr2[1].id = cudaLaunchAttributeClusterDimension;
+    attr2[1].val.clusterDim.x = nc;
+    attr2[1].val.clusterDim.y = 1;
+    attr2[1].val.clusterDim.z = 1;
+    cfg.attrs = attr2;
+    cfg.numAttrs = 2;
+    cfg.gridDim = dim3(static_cast<unsigned>(B) * nc, 1, 1);
     err = cudaLaunchKernelEx(&cfg, spec_verify_kernel, tokens_out, n_accepted, seq_lens_out, target, draft,
-                             draft_tokens, seq_lens, gamma, V, temperature, seeds, offsets,
+                             draft_tokens, seq_lens, gamma, V, slice, temperature, seeds, offsets,
                              static_cast<const RowStat*>(stats), status);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
