@@ -229,12 +229,12 @@ pkv_status pkv_kv_append_chunk(const void* k_new, const void* v_new, void* k_cac
  * The chunk's own K/V must already be in the cache (pkv_kv_append_chunk first).
  * scale <= 0 selects 1/sqrt(D).  bf16 only, D = 128, block_size a multiple of
  * 16, Hq / Hkv <= 8, 16-byte aligned pools and 4-byte aligned q / out (else
- * PKV_ERR_UNSUPPORTED).  fp32 accumulation.  With Hq / Hkv in {1, 2, 4, 8} and
- * 16-byte aligned q / out: one CTA per (two tiles of 128 rows of chunk tokens x
- * query heads, KV head), the longest key ranges first, with tcgen05 MMAs and
- * TMEM accumulators; otherwise one CTA per (16 chunk tokens, KV head) with
- * mma.sync.  A sequence with an invalid
- * length or block id gets zero output and PKV_ERR_DEVICE_BOUNDS.
+ * PKV_ERR_UNSUPPORTED).  fp32 accumulation.  With 16-byte aligned q / out:
+ * one CTA per (two tiles of up to 128 rows of chunk tokens x query heads, KV
+ * head), the longest key ranges first, with tcgen05 MMAs and TMEM
+ * accumulators; otherwise one CTA per (16 chunk tokens, KV head) with
+ * mma.sync.  A sequence with an invalid length or block id gets zero output
+ * and PKV_ERR_DEVICE_BOUNDS.
  */
 pkv_status pkv_paged_prefill_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
                                        const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,

@@ -190,11 +190,22 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
 
     // this warp's query tile (16 tokens x 128 dims of head qh) in shared memory,
     // 128-byte-swizzled like the K tiles; rows past the chunk are zero
+    // (q rows sit 256-byte multiples after q, so q's own alignment decides
+    // between 16-byte loads and four 4-byte ones)
     uint8_t* qtile = ring + kPRingBytes + warp * 4096;
+    const bool q16 = (reinterpret_cast<uintptr_t>(q) & 15u) == 0;
     for (int c = lane; c < 256; c += 32) {
         const int row = c >> 4, ch = c & 15;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (row < nt) v = __ldg(reinterpret_cast<const uint4*>(q + (static_cast<size_t>(t0 + row) * Hq + qh) * kPDim) + ch);
+        if (row < nt) {
+            const __nv_bfloat16* src = q + (static_cast<size_t>(t0 + row) * Hq + qh) * kPDim + 8 * ch;
+            if (q16) {
+                v = __ldg(reinterpret_cast<const uint4*>(src));
+            } else {
+                const uint32_t* s4 = reinterpret_cast<const uint32_t*>(src);
+                v = make_uint4(__ldg(s4), __ldg(s4 + 1), __ldg(s4 + 2), __ldg(s4 + 3));
+            }
+        }
         *reinterpret_cast<uint4*>(qtile + (ch >> 3) * kPBox + row * 128 + (((ch & 7) ^ (row & 7)) << 4)) = v;
     }
     __syncwarp();

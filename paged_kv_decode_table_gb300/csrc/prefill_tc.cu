@@ -3,13 +3,15 @@
 // staged in shared memory by TMA.  Same results as prefill_attn_kernel (the
 // chunk's causal GQA attention over the paged cache; "Suy luan & Toi uu hoa
 // (Inference)" 2.1 and 4.1, the lab's prefill step, "LLM inference serving
-// tutorial" 5.4) for bf16, D = 128, G = Hq / Hkv in {1, 2, 4, 8}, block_size a
+// tutorial" 5.4) for bf16, D = 128, G = Hq / Hkv from 1 to 8, block_size a
 // multiple of 16 and 16-byte aligned q / out / pools.
 //
 //  * One CTA per (two query tiles of 128 rows, KV head h).  Row r of query
-//    tile t is (chunk token t TQ + r / G, query head h G + r % G), TQ = 128 / G:
-//    2 TQ consecutive tokens of one sequence times the G heads that share K/V
-//    head h, so each K/V tile serves 256 rows.  The CTAs take the chunk tiles
+//    tile t is (chunk token t TQ + r / G, query head h G + r % G), TQ =
+//    floor(128 / G): 2 TQ consecutive tokens of one sequence times the G heads
+//    that share K/V head h, so each K/V tile serves up to 256 rows (rows TQ G
+//    .. 127 of a tile, when G does not divide 128, are padding: computed on
+//    zero queries and not stored).  The CTAs take the chunk tiles
 //    longest first (by the number of key tiles they read; the KV head is the
 //    innermost grid index), so that the longest start in the first wave.
 //  * K and V of head h stream in 64-key tiles through a five-stage ring.  The
@@ -223,7 +225,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     TcSmem* sm = reinterpret_cast<TcSmem*>(base + kTcOperandBytes);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = Hq / Hkv, h = static_cast<int>(blockIdx.x) % Hkv;
-    const int TQ = kTcRows / G;    // chunk tokens per query tile
+    const int TQ = kTcRows / G;    // chunk tokens per query tile (rows TQ G .. 127 are padding)
     const int TC = kTcQT * TQ;     // chunk tokens per CTA
 
     // ---- prologue, independent of the inputs
@@ -333,7 +335,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const bool softmax_warp = warp < 4 * kTcQT;
     const int qt = warp >> 2, r = tid & (kTcRows - 1);
     const int tl = qt * TQ + r / G, qh = h * G + r % G;
-    const bool row_valid = active && softmax_warp && tl < nt;
+    const bool row_valid = active && softmax_warp && r < TQ * G && tl < nt;  // rows TQ G .. 127: padding
     if (bad_len) {
         if (tid == 0) report(status, PKV_ERR_DEVICE_BOUNDS);
         if (row_valid) {
@@ -667,7 +669,7 @@ bool prefill_tc_supported(int Hq, int Hkv, int D, int BS, const void* q, const v
                           const void* v) {
     const int G = Hkv > 0 ? Hq / Hkv : 0;
     auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-    return D == kTcDim && BS % 16 == 0 && (G == 1 || G == 2 || G == 4 || G == 8) && a16(q) && a16(out) && a16(k) &&
+    return D == kTcDim && BS % 16 == 0 && G >= 1 && G <= 8 && Hq == G * Hkv && a16(q) && a16(out) && a16(k) &&
            a16(v);
 }
 

@@ -88,11 +88,26 @@ def _check(inp, rows=None):
     ([5, 33], 2000, 64, 8, 16),     # 8 query heads per KV head
     ([17, 64, 3], 500, 8, 8, 32),   # one query head per KV head, 32-token blocks
     ([40, 7, 130], 700, 16, 8, 16),  # two query heads per KV head
-    ([33, 90], 900, 24, 8, 16),      # three per KV head: the mma.sync kernel (no 128-row tile)
+    ([33, 90], 900, 24, 8, 16),      # three per KV head: 42 tokens x 3 heads per 128-row tile, 2 padding rows
+    ([50, 20], 400, 56, 8, 16),      # seven per KV head: 18 tokens x 7 heads, 2 padding rows
     ([300, 129, 5], 600, 8, 8, 16),  # one per KV head, chunks filling both 128-token query tiles, ragged
 ])
 def test_prefill_matches_oracle(chunks, prefix_hi, Hq, Hkv, BS):
     inp = _inputs(sum(chunks) + prefix_hi, chunks, prefix_hi, Hq=Hq, Hkv=Hkv, BS=BS)
+    _check(inp)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(24, 8), (32, 8)])
+def test_prefill_unaligned_query_takes_the_mma_sync_kernel(Hq, Hkv):
+    # q 8 bytes past a 16-byte boundary: the tensor-core kernel needs 16-byte
+    # aligned rows, so the mma.sync kernel serves the call
+    inp = _inputs(31, [40, 7, 130], 700, Hq=Hq, Hkv=Hkv)
+    q = inp["q"]
+    buf = torch.empty(q.numel() + 4, dtype=q.dtype, device=q.device)
+    qu = buf[4:].view(q.shape)
+    qu.copy_(q)
+    assert qu.data_ptr() % 16 == 8
+    inp["q"] = qu
     _check(inp)
 
 
