@@ -14,7 +14,8 @@
 // p_i = softmax(z_target[i] / T) and q_i = softmax(z_draft[i] / T) over finite
 // logits, represented as in the sampler: fixed-point masses floor(w * 2^40) of
 // w = 2^((z - zmax) log2(e) / T).  The row sums for the tests come from one
-// pass (relative error ~1e-7); the final draw sums its own masses exactly.  Uniform
+// pass (a compensated fp32 sum of the weights, relative error ~1e-7); the
+// final draw sums its own fixed-point masses exactly.  Uniform
 // number j of a request is Philox4x64-10 word 0 at counter (offset, j, 0, 0)
 // under key (seed, 0), top 53 bits: j = i + 1 for the test at draft position i,
 // j = 0 for the final draw, which walks token ids in ascending order.
@@ -44,7 +45,7 @@ struct RowStat {   // 32 bytes per logits row
     int argmax;    // lowest id holding zmax (-1: no finite logit)
     int bad;       // NaN or +inf present
     int pad;
-    unsigned long long S;  // ~ sum of floor(2^40 * 2^((z - zmax) c2)) (T > 0), relative error ~1e-7
+    unsigned long long S;  // ~ 2^40 * sum of 2^((z - zmax) c2) (T > 0), relative error ~1e-7
     unsigned long long pad2;
 };
 
@@ -89,15 +90,16 @@ __global__ void __launch_bounds__(kVT)
     const float T = temperature[b];
     const bool sum = T > 0.f;
     const float c2 = sum ? fminf(1.4426950408889634f / T, 1.0e30f) : 0.f;
-    // one pass: running maximum (lowest id among equals) and the fixed-point
-    // mass sum relative to it.  The thread takes its logits in batches of 32;
-    // a batch's maximum is found first, the sum so far is rescaled to it if it
-    // is larger (at most once per batch), then the batch's masses are added.
+    // one pass: running maximum (lowest id among equals) and the sum of the
+    // weights 2^((z - m) c2) relative to it, compensated (Kahan) in fp32.  The
+    // thread takes its logits in batches of 32; a batch's maximum is found
+    // first, the sum so far is rescaled to it if it is larger (at most once per
+    // batch), then the batch's weights are added.
     constexpr int kU = 8;  // float4 slots per batch
     float m = -INFINITY;
     int id = INT_MAX;
     int bad = 0;
-    uint64_t acc = 0;
+    float ks = 0.f, kc = 0.f;  // the sum and its running compensation
     for (int e0 = 4 * tid; e0 < V; e0 += 4 * kVT * kU) {
         float4 q[kU];
 #pragma unroll
@@ -117,15 +119,26 @@ __global__ void __launch_bounds__(kVT)
             }
         }
         if (bm > m) {  // earlier batches hold lower ids, so an equal maximum keeps id
-            if (sum && acc)
-                acc = static_cast<uint64_t>(static_cast<double>(acc) * static_cast<double>(hw_exp2((m - bm) * c2)));
+            if (sum && ks != 0.f) {
+                const float sc = hw_exp2((m - bm) * c2);
+                ks *= sc;
+                kc *= sc;
+            }
             m = bm;
             id = bid;
         }
         if (sum && m > -INFINITY) {
 #pragma unroll
-            for (int u = 0; u < kU; ++u)
-                acc += mass(q[u].x, m, c2) + mass(q[u].y, m, c2) + mass(q[u].z, m, c2) + mass(q[u].w, m, c2);
+            for (int u = 0; u < kU; ++u) {
+                const float zz[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float y = weight(zz[j], m, c2) - kc;
+                    const float t = ks + y;
+                    kc = (t - ks) - y;
+                    ks = t;
+                }
+            }
         }
     }
     const float mt = m;  // this thread's maximum, the reference of acc
@@ -157,8 +170,11 @@ __global__ void __launch_bounds__(kVT)
     }
     uint64_t S = 0;
     if (!bad && m > -INFINITY && sum) {
-        // each thread's sum moved to the row maximum (relative error ~1e-7)
-        const double part = acc ? static_cast<double>(acc) * static_cast<double>(hw_exp2((mt - m) * c2)) : 0.0;
+        // each thread's sum moved to the row maximum, in units of 2^-40 (relative
+        // error ~1e-7)
+        const double part = ks != 0.f ? (static_cast<double>(ks) - static_cast<double>(kc)) *
+                                            static_cast<double>(hw_exp2((mt - m) * c2)) * 1099511627776.0
+                                      : 0.0;
         S = static_cast<uint64_t>(block_sum_f64(part, dred) + 0.5);
     }
     if (tid == 0) {
