@@ -68,11 +68,11 @@ constexpr int kTcGroupBytes = 16 * kTcDim * 2;            // 4 KB: 16 keys x 128
 constexpr int kTcStageBytes = 2 * kTcKBytes;              // K then V
 constexpr int kTcProd = 3;                   // producer warps
 constexpr int kTcWin = 640;                  // block-table entries kept in shared memory, per producer warp
-// warps 0-7: softmax (warp w: query tile w / 4, TMEM lanes 32 (w % 4) ..); warp 8:
-// producer (block rows); warp 9: S MMAs; warp 10: PV MMAs; warps 11-12: producers
+// warps 0-7: softmax (warp w: query tile w / 4, TMEM lanes 32 (w % 4) ..); warps 8,
+// 11 and 12: producers; warp 9: S MMAs (and the TMEM allocation); warp 10: PV MMAs
 constexpr int kTcWarpProd = 8, kTcWarpS = 9, kTcWarpPV = 10;
 constexpr int kTcThreads = 13 * 32;
-constexpr int kTcTmemCols = 512;             // query tile t: Q at 256 t, S (then P) at 256 t + 64, O at 256 t + 128
+constexpr int kTcTmemCols = 512;             // query tile t: Q at 256 t, S at 256 t + 64, O at 256 t + 128
 
 struct TcSmem {  // follows the 1024-aligned operand area
     uint64_t kv_full[kTcStages], kv_empty[kTcStages];
