@@ -216,7 +216,8 @@ def test_decode_step_append_then_attend():
 
 # ----------------------------------------------------------------- sampler
 @pytest.mark.parametrize("num,batch,vocab", [(1, None, None), (2, 16, None), (4, 64, None), (5, 64, 20000),
-                                             (5, 32, None), (2, 8, 300001), (5, 24, 1001)])
+                                             (5, 32, None), (2, 8, 300001), (5, 24, 1001),
+                                             (5, 6, 1 << 23)])  # the largest vocabulary the entry point takes
 def test_sampler_parity(num, batch, vocab):
     w = W.workload(num)
     s = W.make_sampler_inputs(w, "cuda", batch=batch, vocab=vocab)

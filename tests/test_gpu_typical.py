@@ -59,7 +59,8 @@ def _compare(z, T, tp, seeds, offs, max_exempt=None):
     return exempt
 
 
-@pytest.mark.parametrize("B,V,seed", [(64, 128256, 1), (32, 32000, 2), (16, 152064, 3), (40, 4099, 4), (8, 300001, 5)])
+@pytest.mark.parametrize("B,V,seed", [(64, 128256, 1), (32, 32000, 2), (16, 152064, 3), (40, 4099, 4), (8, 300001, 5),
+                                      (2, 1 << 23, 6)])  # the largest vocabulary the entry point takes
 def test_typical_matches_oracle(B, V, seed):
     rng = np.random.default_rng(seed)
     z = np.empty((B, V), np.float32)
