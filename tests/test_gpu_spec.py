@@ -97,6 +97,16 @@ def test_spec_verify_full_vocabulary():
     assert exempt <= 2 and accepted > 0
 
 
+def test_spec_verify_largest_vocabulary():
+    # the largest vocabulary the entry point takes (2^23); three requests, so
+    # only parity is checked (not that both outcomes occur)
+    inp = _inputs(3, 2, 1 << 23, seed=5)
+    tok, nacc, slo = _run(inp)
+    torch.cuda.synchronize()
+    exempt, _ = _compare(inp, tok, nacc, slo)
+    assert exempt <= 1
+
+
 def test_spec_verify_errors():
     B, gamma, V = 6, 2, 300
     inp = _inputs(B, gamma, V, seed=5, temps=(1.0,))
