@@ -126,6 +126,15 @@ def test_prefill_long_chunks_sampled_rows():
     _check(inp, rows=rows)
 
 
+def test_prefill_long_context_chunk():
+    # a 4096-token chunk after a 12000-token prefix: key ranges past the
+    # producers' 640-block table window, 64 chunk tiles of one sequence
+    inp = _inputs(13, [4096, 3], 12000)
+    rng = np.random.default_rng(5)
+    rows = np.sort(rng.choice(inp["T"] * inp["Hq"], 400, replace=False))
+    _check(inp, rows=rows)
+
+
 def test_prefill_bad_length():
     inp = _inputs(4, [8, 8], 50)
     L = inp["L"].clone()
