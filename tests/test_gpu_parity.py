@@ -76,6 +76,8 @@ CASES = [
     (2, dict(batch=4, n_q_heads=8, n_kv_heads=8, len_lo=100, len_hi=500), "MHA G=1 (fast kernel)"),
     (2, dict(batch=4, block_size=32, n_kv_heads=4, n_q_heads=16, len_lo=33, len_hi=700), "block_size 32 (fast kernel)"),
     (2, dict(batch=4, dtype="f32", len_lo=1, len_hi=300), "f32 D=128 (generic kernel)"),
+    (3, dict(batch=1, len_lo=262144, len_hi=262144), "one 256K-token sequence split over every SM (fast kernel)"),
+    (2, dict(batch=2048, len_lo=1, len_hi=48), "2048 short sequences, many per range (fast kernel)"),
 ]
 
 
