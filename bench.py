@@ -717,6 +717,48 @@ def run_extras(args):
     return 0
 
 
+def run_spec_case(args):
+    """The speculative-verification case its profile is captured on (the
+    extras workload: 64 requests, 4 drafts each, 128256-token vocabulary,
+    T 0.8); `--warmup` untimed calls, then `--steps` timed ones, L2 flushed
+    before every call (CUDA events on the stream around each call)."""
+    import paged_kv_decode_table_gb300 as pkv
+    from paged_kv_decode_table_gb300 import build as pkv_build
+    pkv_build.build()
+    pkv.load_library()
+    dev = torch.device("cuda", 0)
+    B, gamma, V = 64, 4, 128256
+    g = torch.Generator(device=dev)
+    g.manual_seed(2024)
+    tgt = torch.randn((B, gamma + 1, V), generator=g, device=dev) * 2.0
+    drf = (tgt[:, :gamma] + 0.5 * torch.randn((B, gamma, V), generator=g, device=dev)).contiguous()
+    x = torch.topk(drf, 4, dim=2).indices[..., 1].to(torch.int32).contiguous()
+    seq = torch.full((B,), 2048, dtype=torch.int32, device=dev)
+    temp = torch.full((B,), 0.8, dtype=torch.float32, device=dev)
+    sd = torch.arange(B, dtype=torch.int64, device=dev)
+    off = torch.zeros(B, dtype=torch.int64, device=dev)
+    wsv = torch.empty(pkv.spec_verify_workspace_bytes(B, gamma), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    st = pkv.new_status()
+    for _ in range(args.warmup):
+        flush.zero_()
+        pkv.spec_verify(tgt, drf, x, seq, temp, sd, off, workspace=wsv, status=st)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        pkv.spec_verify(tgt, drf, x, seq, temp, sd, off, workspace=wsv, status=st)
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) * 1000)
+    assert pkv.check_status(st) == 0
+    print(json.dumps({"case": f"speculative verification {B} requests x {gamma} drafts, V {V}", "calls": args.steps,
+                      "median_us": statistics.median(times) if times else None}))
+    return 0
+
+
 def run_typical_case(args):
     """The typical-sampling case the typical sampler profile is captured on: the
     sampler rows of the batch-64 GQA workload (64 x 128256 logits, T 0.7) with
@@ -806,6 +848,8 @@ def main():
     ap.add_argument("--prefill-case", action="store_true",
                     help="time the small chunked-prefill case of the prefill profile (--warmup, --steps calls)")
     ap.add_argument("--prefill-seqs", type=int, default=4, help="sequences of the --prefill-case workload")
+    ap.add_argument("--spec-case", action="store_true",
+                    help="time the speculative-verification case of its profile (--warmup, --steps calls)")
     ap.add_argument("--typical-case", action="store_true",
                     help="time the typical-sampling case of the typical sampler profile (--warmup, --steps calls)")
     args = ap.parse_args()
@@ -813,6 +857,8 @@ def main():
         return run_prefill_case(args)
     if args.typical_case:
         return run_typical_case(args)
+    if args.spec_case:
+        return run_spec_case(args)
     if args.impl == "reference":
         return run_reference(args)
     if args.extras:
