@@ -1,7 +1,8 @@
 """Benchmark of one batched paged-KV decode step on GB300.
 
-A step = kv_append (new K/V token per sequence) -> paged_decode_attention
-(split-KV main kernel, combine) -> sample_tokens, over one batch of the
+A step = paged_decode_attention_append (the new K/V token of each sequence
+written into its block by the split-KV main kernel just before it loads that
+block, then the combine kernel) -> sample_tokens, over one batch of the
 Llama-style GQA workload: batch 64, 32 query / 8 KV heads, head_dim 128,
 block_size 16, lengths uniform in [512, 4096], shuffled block tables, bf16 KV,
 logits over a 128256-token vocabulary (T = 0.7, top_k = 50, top_p = 0.9).
@@ -9,7 +10,7 @@ logits over a 128256-token vocabulary (T = 0.7, top_k = 50, top_p = 0.9).
 Printed (one JSON line, rank 0):
   value          algorithmic HBM bytes of the whole step / device step time (GB/s)
   sampled_tokens_per_s   batch / device step time
-  roofline       paged_decode_attention's achieved GB/s (CUDA events around each
+  roofline       paged_decode_attention_append's achieved GB/s (CUDA events around each
                  call in a second timed run of up to 500 steps) against the
                  measured copy peak
   e2e            the same metric with host buffers: every step one pinned H2D copy
@@ -189,7 +190,7 @@ def _config(w, inp, extra=None):
         "total_tokens": int(sl.to(torch.int64).sum()), "num_blocks": inp["num_blocks"], "vocab": w.vocab,
         "sampler": {"temperature": w.temperature, "top_k": w.top_k, "top_p": w.top_p},
         "kv_dtype": "bf16", "logits_dtype": "f32",
-        "step": "kv_append -> paged_decode_attention (split-KV main, combine) -> sample_tokens",
+        "step": "paged_decode_attention_append (split-KV main with the KV append, combine) -> sample_tokens",
     }
     if extra:
         cfg.update(extra)
@@ -317,8 +318,8 @@ def run_gpu(args):
     k_cache, v_cache = inp["k_cache"], inp["v_cache"]
 
     def step(q, k_new, v_new, bt, sl, logits, temp, tk, tp, seeds, offs):
-        pkv.kv_append(k_new, v_new, k_cache, v_cache, bt, sl, status=status)
-        pkv.paged_decode_attention(q, k_cache, v_cache, bt, sl, out=out, workspace=ws, status=status)
+        pkv.paged_decode_attention_append(q, k_new, v_new, k_cache, v_cache, bt, sl, out=out, workspace=ws,
+                                          status=status)
         pkv.sample_tokens(logits, temp, tk, tp, seeds, offs, tokens=tokens, status=status)
 
     dev_args = (inp["q"], inp["k_new"], inp["v_new"], inp["block_tables"], inp["seq_lens"], inp["logits"],
@@ -333,7 +334,7 @@ def run_gpu(args):
     # Timed region 1 (the headline): K whole steps back to back, events only at
     # its ends, so that the kernels of a step chain as they would in a server.
     # Timed region 2 (the roofline): K2 more steps with events around every
-    # paged_decode_attention call, giving that call's average device duration.
+    # paged_decode_attention_append call, giving that call's average device duration.
     k2 = min(args.steps, 500)
     a0 = [torch.cuda.Event(enable_timing=True) for _ in range(k2)]
     a1 = [torch.cuda.Event(enable_timing=True) for _ in range(k2)]
@@ -347,11 +348,10 @@ def run_gpu(args):
         step(*dev_args)
     t1.record(stream)
     for i in range(k2):
-        pkv.kv_append(inp["k_new"], inp["v_new"], k_cache, v_cache, inp["block_tables"], inp["seq_lens"],
-                      status=status)
         a0[i].record(stream)
-        pkv.paged_decode_attention(inp["q"], k_cache, v_cache, inp["block_tables"], inp["seq_lens"], out=out,
-                                   workspace=ws, status=status)
+        pkv.paged_decode_attention_append(inp["q"], inp["k_new"], inp["v_new"], k_cache, v_cache,
+                                          inp["block_tables"], inp["seq_lens"], out=out, workspace=ws,
+                                          status=status)
         a1[i].record(stream)
         pkv.sample_tokens(inp["logits"], inp["temperature"], inp["top_k"], inp["top_p"], inp["seeds"],
                           inp["offsets"], tokens=tokens, status=status)
@@ -463,10 +463,11 @@ def run_gpu(args):
     total_bytes = _sum_over_ranks(float(bytes_step["total"]), world, dev)
     value = total_bytes / (ms * 1e-3) / 1e9
     peak, peak_kind = _peaks()
-    attn_gbs = bytes_step["attention"] / (attn_ms * 1e-3) / 1e9
+    attn_bytes = bytes_step["attention"] + bytes_step["append"]
+    attn_gbs = attn_bytes / (attn_ms * 1e-3) / 1e9
     traffic = _traffic_per_launch()
     fast = True  # bf16, D=128, BS=16, Hkv=8: TMA/mma path -> main and combine kernels
-    launches = args.steps * (1 + (2 if fast else 1) + 1)  # append + attention + sampler
+    launches = args.steps * ((2 if fast else 2 + 1) + 1)  # attention with the append (+ combine) + sampler
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -478,11 +479,12 @@ def run_gpu(args):
         "sampled_tokens_per_s": B * world / (ms * 1e-3),
         "pct_of_8TBps": value / 8000.0 * 100.0,
         "pct_of_measured_peak": value / peak * 100.0,
-        "roofline": {"kernel": "paged_decode_attention (split-KV main + combine kernels), per call",
+        "roofline": {"kernel": "paged_decode_attention_append (split-KV main with the KV append + combine "
+                               "kernels), per call",
                      "bound": "hbm", "achieved": attn_gbs, "peak": peak, "unit": "GB/s",
                      "frac": attn_gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "traffic": traffic, "algorithmic_bytes_per_call": bytes_step["attention"],
+                     "traffic": traffic, "algorithmic_bytes_per_call": attn_bytes,
                      "ms_per_call": attn_ms},
         "e2e": {"value": total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": B * 4,

@@ -117,8 +117,8 @@ size_t pkv_decode_workspace_bytes(int B, int Hq, int D, int num_sms);
  * 1 <= D <= 256; the fast path (bf16, D = 128, block_size a multiple of 16,
  * 1 <= Hkv <= 8, Hq/Hkv <= 16, Hkv * block_size <= 256 with at least two
  * 512*Hkv*block_size-byte stages fitting in shared memory, 16-byte aligned q,
- * out and pools) uses TMA and tensor-core MMA in three kernels chained by
- * programmatic dependent launch; other shapes use a generic CUDA-core kernel.  Sequences with a length outside [0, max_blocks_per_seq*block_size]
+ * out and pools) uses TMA and tensor-core MMA in two kernels (split-KV, then the
+ * combine) chained by programmatic dependent launch; other shapes use a generic CUDA-core kernel.  Sequences with a length outside [0, max_blocks_per_seq*block_size]
  * or a block id outside [0, num_blocks) get zero output and
  * PKV_ERR_DEVICE_BOUNDS.  The KV slots past L in a sequence's last block are
  * never used (their contents may be anything, NaN included).
@@ -129,6 +129,29 @@ pkv_status pkv_paged_decode_attention(void* out, const void* q, const void* k_ca
                                       int Hq, int Hkv, int D, int block_size, int num_blocks,
                                       float scale, pkv_dtype dtype, void* workspace,
                                       size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * KV append and decode attention in one call: the same result (caches, out,
+ * dev_status) as pkv_kv_append(k_new, v_new, k_cache, v_cache, ...) followed by
+ * pkv_paged_decode_attention(out, q, k_cache, v_cache, ...) on the same stream,
+ * with the arguments of both.  On the fast path (as for
+ * pkv_paged_decode_attention, plus 16-byte aligned k_new and v_new) the
+ * attention kernel writes each sequence's new token into its last block just
+ * before loading that block, which saves the separate append launch and its
+ * pass over the batch; elsewhere the two kernels run back to back.
+ * Precondition (which copy-on-write guarantees): the block that receives a
+ * sequence's new token is not read by another sequence of the same batch.
+ * Lengths outside [1, max_blocks_per_seq*block_size] record
+ * PKV_ERR_DEVICE_BOUNDS, as the append does.  k_cache and v_cache are written.
+ */
+pkv_status pkv_paged_decode_attention_append(void* out, const void* q, const void* k_new,
+                                             const void* v_new, void* k_cache, void* v_cache,
+                                             const int32_t* block_tables, int max_blocks_per_seq,
+                                             const int32_t* seq_lens, int B, int Hq, int Hkv, int D,
+                                             int block_size, int num_blocks, float scale,
+                                             pkv_dtype dtype, void* workspace,
+                                             size_t workspace_bytes, int32_t* dev_status,
+                                             void* stream);
 
 /*
  * pkv_paged_decode_attention without a caller-supplied workspace.  The pages

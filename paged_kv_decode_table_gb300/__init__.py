@@ -27,6 +27,7 @@ import threading
 import torch
 
 __all__ = ["PkvError", "load_library", "library_path", "kv_append", "paged_decode_attention",
+           "paged_decode_attention_append",
            "decode_workspace_bytes", "sample_tokens", "sample_workspace_bytes", "status_string",
            "new_status", "check_status", "STATUS", "copy_blocks", "BlockPool", "spec_verify",
            "spec_verify_workspace_bytes", "apply_logits_processors", "kv_append_chunk",
@@ -74,6 +75,9 @@ def load_library():
         lib.pkv_paged_decode_attention.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, f32,
                                                    i32, P, sz, P, P]
         lib.pkv_paged_decode_attention.restype = i32
+        lib.pkv_paged_decode_attention_append.argtypes = [P, P, P, P, P, P, P, i32, P, i32, i32, i32, i32, i32,
+                                                          i32, f32, i32, P, sz, P, P]
+        lib.pkv_paged_decode_attention_append.restype = i32
         lib.pkv_sample_workspace_bytes.argtypes = [i32, i32]
         lib.pkv_sample_workspace_bytes.restype = sz
         lib.pkv_sample_tokens.argtypes = [P, P, i32, i32, P, P, P, P, P, P, sz, P, P]
@@ -238,6 +242,44 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, seq_lens, out=None
                                           _ptr(workspace), workspace.numel() * workspace.element_size(),
                                           _ptr(status), _stream(dev))
     _raise("pkv_paged_decode_attention", code)
+    return out
+
+
+def paged_decode_attention_append(q, k_new, v_new, k_cache, v_cache, block_tables, seq_lens, out=None,
+                                  scale: float = 0.0, workspace=None, status=None):
+    """kv_append(k_new, v_new, ...) then paged_decode_attention(q, ...) in one call; returns out."""
+    B, Hq, D = q.shape
+    NB, Hkv, BS, D2 = k_cache.shape
+    dev = q.device
+    if D2 != D:
+        raise ValueError("head_dim of q and the cache differ")
+    _check_cuda("q", q)
+    _check_cuda("k_cache", k_cache, q.dtype, device=dev)
+    _check_cuda("v_cache", v_cache, q.dtype, k_cache.shape, dev)
+    _check_cuda("k_new", k_new, q.dtype, (B, Hkv, D), dev)
+    _check_cuda("v_new", v_new, q.dtype, (B, Hkv, D), dev)
+    _check_cuda("block_tables", block_tables, torch.int32, device=dev)
+    _check_cuda("seq_lens", seq_lens, torch.int32, (B,), dev)
+    if block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise ValueError("block_tables must be [B, max_blocks_per_seq]")
+    if out is None:
+        out = torch.empty_like(q)
+    _check_cuda("out", out, q.dtype, q.shape, dev)
+    lib = load_library()
+    need = int(lib.pkv_decode_workspace_bytes(B, Hq, D, 0))
+    if workspace is None:
+        with torch.cuda.device(dev):
+            workspace = _workspace(dev, need)
+    _check_cuda("workspace", workspace, device=dev)
+    if status is not None:
+        _check_cuda("status", status, torch.int32, (1,), dev)
+    code = lib.pkv_paged_decode_attention_append(_ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                                                 _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+                                                 _ptr(seq_lens), B, Hq, Hkv, D, BS, NB, float(scale),
+                                                 _dtype_code(q), _ptr(workspace),
+                                                 workspace.numel() * workspace.element_size(), _ptr(status),
+                                                 _stream(dev))
+    _raise("pkv_paged_decode_attention_append", code)
     return out
 
 

@@ -100,6 +100,12 @@ __device__ __forceinline__ int cta_excl_scan(int v, int* red, int& total) {
 }
 
 // ------------------------------------------------------------------ fast kernel
+// Orders this thread's earlier generic-proxy global writes before its later
+// async-proxy (TMA) accesses of global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 constexpr int kMaxStages = 8;
 constexpr int kDim = 128;
 
@@ -128,7 +134,8 @@ __global__ void __launch_bounds__((kFastMaxKvHeads + 1) * 32, 1)
                             const int32_t* __restrict__ block_tables, int max_blocks, int B, int Hq, int Hkv,
                             int BS, int NB, float scale_log2, int nst, const int32_t* __restrict__ seq_lens,
                             SeqInfo* __restrict__ info, float* __restrict__ part_ml, float* __restrict__ part_o,
-                            int32_t* status) {
+                            int32_t* status, const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                            uint4* kpool, uint4* vpool) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int R = Hkv * BS;
@@ -172,6 +179,15 @@ __global__ void __launch_bounds__((kFastMaxKvHeads + 1) * 32, 1)
     const int n_first = static_cast<int>(threadIdx.x) < B ? seq_blocks(seq_lens, threadIdx.x, max_blocks, BS) : 0;
     int tsum = n_first;
     for (int b = threadIdx.x + nthr; b < B; b += nthr) tsum += seq_blocks(seq_lens, b, max_blocks, BS);
+    if (k_new != nullptr && blockIdx.x == 0) {
+        // with the append fused in, a length the append cannot place is an
+        // error even where attention alone accepts it (L = 0)
+        for (int b = threadIdx.x; b < B; b += nthr) {
+            const int L = seq_lens[b];
+            if (L < 1 || static_cast<long long>(L) > static_cast<long long>(max_blocks) * BS)
+                report(status, PKV_ERR_DEVICE_BOUNDS);
+        }
+    }
     int total;
     cta_excl_scan(tsum, sch, total);
     const int W = total > 0 ? (total + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x) : 1;
@@ -196,8 +212,11 @@ __global__ void __launch_bounds__((kFastMaxKvHeads + 1) * 32, 1)
     }
 
     if (warp == CW) {
-        // ------------------------------------------------ producer (one lane)
-        if (lane != 0) return;
+        // ------------------------------------------------ producer warp
+        // Lane 0 waits on the ring and issues the copies.  With the append
+        // fused in, the whole warp first writes a sequence's new token (every
+        // KV head) into its last block, just before that block is loaded: the
+        // one CTA that reads the block is the one that writes it.
         // walk the sequences from the one holding block `start`; empty and
         // invalid sequences have no blocks and are stepped over
         int b = sch[33], cs = sch[34];
@@ -211,58 +230,81 @@ __global__ void __launch_bounds__((kFastMaxKvHeads + 1) * 32, 1)
                 cL = seq_lens[b];
             }
             const int j = i - cs;
-            const bool first = (j == 0) || (i == start);
-            const bool last = (j == cn - 1) || (i == end - 1);
-            const bool whole = (cs >= start) && (cs + cn <= end);
-            const bool head = cs < start;  // began in an earlier range (set on every stage of the piece)
-            if (j == 0) {
-                SeqInfo si;  // the combine kernel's view of this sequence
-                si.s = cs;
-                si.n = cn;
-                si.W = W;
-                si.pad = 0;
-                info[b] = si;
-            }
-            const int stage = it % nst;
-            const uint32_t round = static_cast<uint32_t>(it / nst);
-            if (!mbar_wait(&empty[stage], (round & 1u) ^ 1u)) {
-                report(status, PKV_ERR_TIMEOUT);
-                return;
-            }
-            if (first) {
-                const int qs = piece & 1;
-                const uint32_t qr = static_cast<uint32_t>(piece >> 1);
-                if (!mbar_wait(&qempty[qs], (qr & 1u) ^ 1u)) {
-                    report(status, PKV_ERR_TIMEOUT);
-                    return;
-                }
-                mbar_arrive_expect_tx(&qfull[qs], q_bytes);
-                tma_load_1d(qring + static_cast<size_t>(qs) * q_bytes, q + static_cast<size_t>(b) * Hq * kDim,
-                            q_bytes, &qfull[qs]);
-                ++piece;
-            }
             const int blk = block_tables[static_cast<size_t>(b) * max_blocks + j];
             const bool valid = blk >= 0 && blk < NB;
-            StageMeta mt;
-            mt.b = b;
-            mt.j = j;
-            mt.ntok = min(BS, cL - j * BS);
-            mt.flags = (valid ? kValid : 0) | (first ? kFirst : 0) | (last ? kLast : 0) | (whole ? kWhole : 0) |
-                       (head ? kHead : 0);
-            meta[stage] = mt;
-            uint64_t* fb = &full[stage];
-            if (valid) {
-                mbar_arrive_expect_tx(fb, stage_bytes);
-                uint8_t* st = stages + static_cast<size_t>(stage) * stage_bytes;
-                const int y = blk * R;
-                tma_load_2d(st, &tmK, 0, y, fb);
-                tma_load_2d(st + box_bytes, &tmK, 64, y, fb);
-                tma_load_2d(st + 2 * box_bytes, &tmV, 0, y, fb);
-                tma_load_2d(st + 3 * box_bytes, &tmV, 64, y, fb);
-            } else {
-                report(status, PKV_ERR_DEVICE_BOUNDS);
-                mbar_arrive(fb);
+            if (k_new != nullptr && valid && j == cn - 1) {  // warp-uniform
+                // the new token sits at position cL - 1, in this block
+                constexpr int kRowVecs = kDim * 2 / 16;
+                const int slot = cL - 1 - j * BS;
+                for (int e = lane; e < Hkv * kRowVecs; e += 32) {
+                    const int hh = e / kRowVecs, c = e - hh * kRowVecs;
+                    const size_t src = static_cast<size_t>(b * Hkv + hh) * kRowVecs + c;
+                    const size_t dst = ((static_cast<size_t>(blk) * Hkv + hh) * BS + slot) * kRowVecs + c;
+                    kpool[dst] = __ldg(k_new + src);
+                    vpool[dst] = __ldg(v_new + src);
+                }
+                // the rows are written through the generic proxy and read
+                // back by this warp's TMA (the async proxy)
+                fence_proxy_async_global();
+                __syncwarp();
             }
+            int ok = 1;
+            if (lane == 0) {
+                const bool first = (j == 0) || (i == start);
+                const bool last = (j == cn - 1) || (i == end - 1);
+                const bool whole = (cs >= start) && (cs + cn <= end);
+                const bool head = cs < start;  // began in an earlier range (set on every stage of the piece)
+                if (j == 0) {
+                    SeqInfo si;  // the combine kernel's view of this sequence
+                    si.s = cs;
+                    si.n = cn;
+                    si.W = W;
+                    si.pad = 0;
+                    info[b] = si;
+                }
+                const int stage = it % nst;
+                const uint32_t round = static_cast<uint32_t>(it / nst);
+                if (!mbar_wait(&empty[stage], (round & 1u) ^ 1u)) {
+                    report(status, PKV_ERR_TIMEOUT);
+                    ok = 0;
+                }
+                if (ok && first) {
+                    const int qs = piece & 1;
+                    const uint32_t qr = static_cast<uint32_t>(piece >> 1);
+                    if (!mbar_wait(&qempty[qs], (qr & 1u) ^ 1u)) {
+                        report(status, PKV_ERR_TIMEOUT);
+                        ok = 0;
+                    } else {
+                        mbar_arrive_expect_tx(&qfull[qs], q_bytes);
+                        tma_load_1d(qring + static_cast<size_t>(qs) * q_bytes,
+                                    q + static_cast<size_t>(b) * Hq * kDim, q_bytes, &qfull[qs]);
+                        ++piece;
+                    }
+                }
+                if (ok) {
+                    StageMeta mt;
+                    mt.b = b;
+                    mt.j = j;
+                    mt.ntok = min(BS, cL - j * BS);
+                    mt.flags = (valid ? kValid : 0) | (first ? kFirst : 0) | (last ? kLast : 0) |
+                               (whole ? kWhole : 0) | (head ? kHead : 0);
+                    meta[stage] = mt;
+                    uint64_t* fb = &full[stage];
+                    if (valid) {
+                        mbar_arrive_expect_tx(fb, stage_bytes);
+                        uint8_t* st = stages + static_cast<size_t>(stage) * stage_bytes;
+                        const int y = blk * R;
+                        tma_load_2d(st, &tmK, 0, y, fb);
+                        tma_load_2d(st + box_bytes, &tmK, 64, y, fb);
+                        tma_load_2d(st + 2 * box_bytes, &tmV, 0, y, fb);
+                        tma_load_2d(st + 3 * box_bytes, &tmV, 64, y, fb);
+                    } else {
+                        report(status, PKV_ERR_DEVICE_BOUNDS);
+                        mbar_arrive(fb);
+                    }
+                }
+            }
+            if (!__shfl_sync(0xffffffffu, ok, 0)) return;  // a wait ran out: the whole warp leaves
         }
         return;
     }
@@ -889,16 +931,32 @@ static FastPlan plan_fast(int Hq, int Hkv, int D, int BS, pkv_dtype dt, const vo
     return fp;
 }
 
+cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                             const int32_t* block_tables, int max_blocks, const int32_t* seq_lens, int B, int Hkv,
+                             int D, int BS, int NB, pkv_dtype dtype, int32_t* status, cudaStream_t stream);
+
+// k_new / v_new non-null: append each sequence's new token first (same result
+// as launch_kv_append followed by attention).  The fast kernel does the append
+// itself; every other case launches the append kernel before attention.
 cudaError_t launch_decode_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
                                     const int32_t* block_tables, int max_blocks, const int32_t* seq_lens, int B,
                                     int Hq, int Hkv, int D, int BS, int NB, float scale, pkv_dtype dtype,
                                     void* workspace, int P, int32_t* status, cudaStream_t stream,
-                                    bool* used_fast) {
+                                    bool* used_fast, const void* k_new, const void* v_new) {
     if (scale <= 0.f) scale = 1.0f / sqrtf(static_cast<float>(D));
     const FastPlan fp = plan_fast(Hq, Hkv, D, BS, dtype, k_cache, v_cache, q, out);
     CUtensorMap tmK, tmV;
     bool fast = fp.ok && encode_pool_map(&tmK, k_cache, NB, Hkv, BS) && encode_pool_map(&tmV, v_cache, NB, Hkv, BS);
     if (used_fast) *used_fast = fast;
+    const bool append = k_new != nullptr;
+    const bool fused = fast && append && (reinterpret_cast<uintptr_t>(k_new) & 15u) == 0 &&
+                       (reinterpret_cast<uintptr_t>(v_new) & 15u) == 0;
+    if (append && !fused) {
+        cudaError_t e = launch_kv_append(k_new, v_new, const_cast<void*>(k_cache), const_cast<void*>(v_cache),
+                                         block_tables, max_blocks, seq_lens, B, Hkv, D, BS, NB, dtype, status,
+                                         stream);
+        if (e != cudaSuccess) return e;
+    }
     if (!fast) {
         const unsigned grid = static_cast<unsigned>(B) * Hq;
         if (dtype == PKV_F32)
@@ -936,7 +994,11 @@ cudaError_t launch_decode_attention(void* out, const void* q, const void* k_cach
     cfg.numAttrs = 1;
     err = cudaLaunchKernelEx(&cfg, kern, tmK, tmV, static_cast<const __nv_bfloat16*>(q),
                              static_cast<__nv_bfloat16*>(out), block_tables, max_blocks, B, Hq, Hkv, BS, NB,
-                             scale_log2, fp.nst, seq_lens, info, part_ml, part_o, status);
+                             scale_log2, fp.nst, seq_lens, info, part_ml, part_o, status,
+                             static_cast<const uint4*>(fused ? k_new : nullptr),
+                             static_cast<const uint4*>(fused ? v_new : nullptr),
+                             static_cast<uint4*>(const_cast<void*>(k_cache)),
+                             static_cast<uint4*>(const_cast<void*>(v_cache)));
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t ccfg = {};
     ccfg.blockDim = dim3(kCombThreads, 1, 1);
@@ -1021,6 +1083,6 @@ extern "C" pkv_status pkv_paged_decode_attention_noalloc(void* out, const void* 
     if (ws == nullptr) return PKV_ERR_CUDA;
     err = pkv::launch_decode_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, B, Hq,
                                        Hkv, D, block_size, num_blocks, scale, dtype, ws, P, dev_status,
-                                       static_cast<cudaStream_t>(stream), nullptr);
+                                       static_cast<cudaStream_t>(stream), nullptr, nullptr, nullptr);
     return err == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

@@ -14,7 +14,8 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_cache
 cudaError_t launch_decode_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
                                     const int32_t* block_tables, int max_blocks, const int32_t* seq_lens, int B,
                                     int Hq, int Hkv, int D, int BS, int NB, float scale, pkv_dtype dtype,
-                                    void* workspace, int P, int32_t* status, cudaStream_t stream, bool* used_fast);
+                                    void* workspace, int P, int32_t* status, cudaStream_t stream, bool* used_fast,
+                                    const void* k_new, const void* v_new);
 size_t decode_workspace_bytes(int B, int Hq, int D, int P);
 int device_sm_count();
 cudaError_t launch_sampler(int32_t* tokens, const float* logits, int B, int V, const float* temperature,
@@ -182,7 +183,29 @@ pkv_status pkv_paged_decode_attention(void* out, const void* q, const void* k_ca
     return cuda_status(pkv::launch_decode_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                                     seq_lens, B, Hq, Hkv, D, block_size, num_blocks, scale, dtype,
                                                     workspace, P, dev_status, static_cast<cudaStream_t>(stream),
-                                                    nullptr));
+                                                    nullptr, nullptr, nullptr));
+}
+
+pkv_status pkv_paged_decode_attention_append(void* out, const void* q, const void* k_new, const void* v_new,
+                                             void* k_cache, void* v_cache, const int32_t* block_tables,
+                                             int max_blocks_per_seq, const int32_t* seq_lens, int B, int Hq, int Hkv,
+                                             int D, int block_size, int num_blocks, float scale, pkv_dtype dtype,
+                                             void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                             void* stream) {
+    if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || D < 1 || D > 256 || block_size < 1 || num_blocks < 1 ||
+        max_blocks_per_seq < 1 || !dtype_ok(dtype))
+        return PKV_ERR_INVALID_ARG;
+    if (B == 0) return PKV_OK;
+    if (!out || !q || !k_new || !v_new || !k_cache || !v_cache || !block_tables || !seq_lens || !workspace)
+        return PKV_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return PKV_ERR_INVALID_ARG;
+    const int P = pkv::device_sm_count();
+    if (P <= 0) return PKV_ERR_CUDA;
+    if (workspace_bytes < pkv::decode_workspace_bytes(B, Hq, D, P)) return PKV_ERR_INVALID_ARG;
+    return cuda_status(pkv::launch_decode_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                                    seq_lens, B, Hq, Hkv, D, block_size, num_blocks, scale, dtype,
+                                                    workspace, P, dev_status, static_cast<cudaStream_t>(stream),
+                                                    nullptr, k_new, v_new));
 }
 
 size_t pkv_sample_workspace_bytes(int B, int V) {

@@ -72,6 +72,13 @@ def test_argument_errors_return_before_launch(lib):
                                           None, 0, None, None) == 1   # D too large
     assert lib.pkv_paged_decode_attention(None, None, None, None, None, 1, None, 0, 4, 2, 4, 4, 1, 0.0, 0,
                                           None, 0, None, None) == 0   # empty batch
+    A = lib.pkv_paged_decode_attention_append
+    assert A(None, None, None, None, None, None, None, 1, None, 2, 3, 2, 4, 4, 1, 0.0, 0,
+             None, 0, None, None) == 1   # Hq % Hkv != 0
+    assert A(None, None, None, None, None, None, None, 1, None, 0, 4, 2, 4, 4, 1, 0.0, 0,
+             None, 0, None, None) == 0   # empty batch
+    assert A(P(16), P(16), None, P(16), P(16), P(16), P(16), 1, P(16), 2, 4, 2, 4, 4, 1, 0.0, 0,
+             P(16), 1 << 30, None, None) == 1   # k_new missing
     assert lib.pkv_sample_tokens(None, None, 4, 0, None, None, None, None, None, None, 0, None, None) == 1
     assert lib.pkv_sample_tokens(None, None, 4, 1 << 24, None, None, None, None, None, None, 0, None, None) == 1
     assert lib.pkv_sample_tokens(None, None, 0, 100, None, None, None, None, None, None, 0, None, None) == 0
