@@ -6,6 +6,8 @@
  *                               physical block through the block table;
  *   pkv_paged_decode_attention  GQA decode attention for one query token per
  *                               sequence over all cached K/V (split-KV inside);
+ *                               pkv_paged_decode_attention_append does the
+ *                               append and the attention in one call;
  *   pkv_sample_tokens           temperature -> top-k -> renormalise -> top-p ->
  *                               renormalise -> seeded per-request draw.
  * Shared prefixes: a host-side reference-counted block pool (pkv_block_pool_*,
