@@ -546,13 +546,15 @@ __global__ void __launch_bounds__(kCombThreads)
     combine_warp_kernel(const SeqInfo* __restrict__ info, const int32_t* __restrict__ seq_lens, int max_blocks,
                         int BS, const float* __restrict__ part_ml, const float* __restrict__ part_o,
                         T* __restrict__ out, int B, int Hq, int32_t* status) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");  // the main kernel's partials are visible
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const long long u = static_cast<long long>(blockIdx.x) * kCombWarps + (threadIdx.x >> 5);
     if (u >= static_cast<long long>(B) * Hq) return;
     const int b = static_cast<int>(u / Hq), qh = static_cast<int>(u - static_cast<long long>(b) * Hq);
+    // the lengths predate the main kernel (which launched this one only after
+    // its own wait on its predecessors), so they are read before the wait
     const int L = seq_lens[b];
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the main kernel's partials are visible
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const bool valid = L >= 0 && static_cast<long long>(L) <= static_cast<long long>(max_blocks) * BS;
     if (!valid && qh == 0 && lane == 0) report(status, PKV_ERR_DEVICE_BOUNDS);
     const int n = valid ? (L + BS - 1) / BS : 0;
@@ -634,11 +636,11 @@ __global__ void __launch_bounds__(kCombThreads)
     __shared__ float wsh[kCombMaxPieces];
     __shared__ float4 accsh[kCombWarps][32];
     __shared__ float red[2][kCombWarps];
-    asm volatile("griddepcontrol.wait;" ::: "memory");  // the main kernel's partials are visible
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = blockIdx.x / Hq, qh = blockIdx.x - (blockIdx.x / Hq) * Hq;
-    const int L = seq_lens[b];
+    const int L = seq_lens[b];  // predates the main kernel: read before the wait
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the main kernel's partials are visible
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const bool valid = L >= 0 && static_cast<long long>(L) <= static_cast<long long>(max_blocks) * BS;
     if (!valid && qh == 0 && tid == 0) report(status, PKV_ERR_DEVICE_BOUNDS);
     const int n = valid ? (L + BS - 1) / BS : 0;
