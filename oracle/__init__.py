@@ -313,7 +313,7 @@ def sample_row(z, temperature: float, top_k: int, top_p: float, seed: int, offse
 
 def sample_row_typical(z, temperature: float, typical_p: float, seed: int, offset: int, want_probs: bool = False):
     """One row of typical sampling. Returns dict(token, status, draw_margin,
-    cut_margin, center_margin, entropy, n_kept[, probs])."""
+    cut_margin, order_margin, entropy, n_kept[, probs])."""
     z = np.ascontiguousarray(z, dtype=np.float32)
     V = z.shape[0]
     tok = ctypes.c_int32(0)
@@ -325,7 +325,7 @@ def sample_row_typical(z, temperature: float, typical_p: float, seed: int, offse
                                         ctypes.byref(dm), ctypes.byref(cm), ctypes.byref(ctm), ctypes.byref(ent),
                                         ctypes.byref(nk), _ptr(probs) if want_probs else None)
     res = dict(token=int(tok.value), status=int(st), draw_margin=float(dm.value), cut_margin=float(cm.value),
-               center_margin=float(ctm.value), entropy=float(ent.value), n_kept=int(nk.value))
+               order_margin=float(ctm.value), entropy=float(ent.value), n_kept=int(nk.value))
     if want_probs:
         res["probs"] = probs
     return res

@@ -487,47 +487,48 @@ int oracle_sample_row(const float* z, int V, float temperature, int top_k, float
 }
 
 /* Typical sampling ("LLM inference serving tutorial" 3.1, other samplers;
- * Meister et al., "Locally Typical Sampling"), for one row:
- *   p_i = exp((z_i - z_max)/T) / S over the finite logits (T > 0);
- *   H(p) = -sum_i p_i ln p_i;  d_i = |-ln p_i - H(p)|;
- *   the kept set is the smallest prefix of the tokens sorted by d ascending
- *   whose cumulative probability reaches typical_p (boundary token kept),
- *   renormalised; the draw walks it in token-id order with the request's
- *   Philox uniform, as in oracle_sample_row_ex.
- * With u_i = (z_i - z_max) log2(e) / T and ubar = sum_i p_i u_i one has
- * -ln p_i - H = ln 2 (ubar - u_i), so the order by d is the order by
- * |u_i - ubar|.  That order is a decision taken in floating point; it is taken
- * in the kernel's precision so that both sides make the same one: ubar rounded
- * to a multiple of 2^-8, then in float32, each operation rounded on its own,
- * c2 = min(log2(e) / T, 1e30), u_i = (z_i - z_max) * c2 and
- * dk_i = |u_i - ubar|; ties in dk go to the larger u_i (the more probable
- * token), then to the smaller id.  The cumulative sums use the float64 p_i.
+ * appendix A [D01]; Meister et al., "Locally Typical Sampling"), for one row,
+ * literally in float64:
+ *   a_i = (z_i - z_max) / T and p_i = exp(a_i) / S over the finite logits,
+ *     S = sum_i exp(a_i) (T > 0);
+ *   ln p_i = a_i - ln S (the logarithm of that same p_i, taken without the
+ *     exp round trip so that it stays finite where exp(a_i) underflows);
+ *   H(p) = -sum_i p_i ln p_i (a term with p_i = 0 contributes 0);
+ *   d_i = |-ln p_i - H(p)|;
+ *   the tokens in ascending d; equal d_i go to the larger logit (the more
+ *   probable token) first, then to the smaller id;
+ *   the kept set is the smallest prefix of that order whose cumulative
+ *   probability reaches typical_p (boundary token kept), renormalised; the
+ *   draw walks it in token-id order with the request's Philox uniform, as in
+ *   oracle_sample_row_ex.
  * T == 0 is the greedy branch; typical_p >= 1 keeps every finite logit.
  * Errors: as oracle_sample_row_ex, and typical_p <= 0 or NaN -> OR_INVALID_ARG.
- * Diagnostics: entropy = H(p) in nats; center_margin = distance (log2 units)
- * from ubar to the nearest midpoint of the 2^-8 grid (where the rounding of
- * ubar could go either way); cut_margin and draw_margin as in the top-p
- * sampler; probs (optional) = the final renormalised distribution. */
+ * Diagnostics: entropy = H(p) in nats; order_margin = the gap in d (nats)
+ * between the boundary token and its nearest neighbours in the order whose
+ * logit differs from its own, below and above (1 when there is none): where
+ * it is tiny, rounding in another implementation could exchange the two and
+ * move the cut; cut_margin and draw_margin as in the top-p sampler; probs
+ * (optional) = the final renormalised distribution. */
 typedef struct {
-    float dk, u;
+    double d, p;
+    float z;
     int32_t id;
-    double p;
 } typ_t;
 
 static int cmp_typ(const void* a, const void* b) {
     const typ_t* x = (const typ_t*)a;
     const typ_t* y = (const typ_t*)b;
-    if (x->dk < y->dk) return -1;
-    if (x->dk > y->dk) return 1;
-    if (x->u > y->u) return -1;
-    if (x->u < y->u) return 1;
+    if (x->d < y->d) return -1;
+    if (x->d > y->d) return 1;
+    if (x->z > y->z) return -1;
+    if (x->z < y->z) return 1;
     return (x->id < y->id) ? -1 : (x->id > y->id ? 1 : 0);
 }
 
 int oracle_sample_row_typical(const float* z, int V, float temperature, float typical_p, uint64_t seed,
                               uint64_t offset, int32_t* token, double* draw_margin, double* cut_margin,
-                              double* center_margin, double* entropy, int32_t* n_kept, double* probs) {
-    *center_margin = 1.0;
+                              double* order_margin, double* entropy, int32_t* n_kept, double* probs) {
+    *order_margin = 1.0;
     *entropy = 0.0;
     if (temperature == 0.0f || typical_p >= 1.0f) /* greedy, or no truncation (NaN p goes on) */
         return oracle_sample_row_ex(z, V, temperature, 0, 1.0f, 0.0f, seed, offset, token, draw_margin,
@@ -550,38 +551,30 @@ int oracle_sample_row_typical(const float* z, int V, float temperature, float ty
     if (!(temperature >= 0.0f)) return OR_INVALID_ARG;
     if (!(typical_p > 0.0f)) return OR_INVALID_ARG; /* <= 0 or NaN */
 
-    /* the distribution, its entropy and the literal d_i */
-    const double T = (double)temperature, zmax = (double)zmaxf, L2E = 1.4426950408889634;
+    /* the distribution p, ln p, the entropy H and d */
+    const double T = (double)temperature, zmax = (double)zmaxf;
     typ_t* t = (typ_t*)malloc(sizeof(typ_t) * (size_t)n);
+    double* a = (double*)malloc(sizeof(double) * (size_t)n);
     double S = 0.0;
     int k = 0;
     for (int i = 0; i < V; ++i)
         if (isfinite(z[i])) {
             t[k].id = i;
-            t[k].p = exp(((double)z[i] - zmax) / T);
+            t[k].z = z[i];
+            a[k] = ((double)z[i] - zmax) / T;
+            t[k].p = exp(a[k]);
             S += t[k].p;
             ++k;
         }
-    double H = 0.0, ubar = 0.0;
+    const double lnS = log(S);
+    double H = 0.0;
     for (int j = 0; j < n; ++j) {
         t[j].p /= S;
-        if (t[j].p > 0.0) H -= t[j].p * log(t[j].p);
-        ubar += t[j].p * (((double)z[t[j].id] - zmax) / T * L2E);
+        if (t[j].p > 0.0) H -= t[j].p * (a[j] - lnS);
     }
     *entropy = H;
-    /* ubar in log2 units relative to the maximum, rounded to the 2^-8 grid */
-    const double g = ubar * 256.0;
-    *center_margin = fabs(fabs(g - floor(g)) - 0.5) / 256.0;
-    const float ub = (float)(rint(g) / 256.0);
-    float c2 = 1.4426950408889634f / temperature;
-    if (c2 > 1.0e30f) c2 = 1.0e30f;
-    for (int j = 0; j < n; ++j) {
-        const float a = z[t[j].id] - zmaxf;
-        const float u = a * c2;
-        const float d = u - ub;
-        t[j].u = u;
-        t[j].dk = fabsf(d);
-    }
+    for (int j = 0; j < n; ++j) t[j].d = fabs(-(a[j] - lnS) - H);
+    free(a);
     qsort(t, (size_t)n, sizeof(typ_t), cmp_typ);
 
     /* smallest prefix reaching typical_p */
@@ -596,6 +589,21 @@ int oracle_sample_row_typical(const float* z, int V, float temperature, float ty
     {
         double d1 = fabs(cum - tp), d0 = fabs(prev - tp);
         *cut_margin = d1 < d0 ? d1 : d0;
+    }
+    {   /* gaps in d around the boundary token c = m - 1 */
+        const int c = m - 1;
+        double gap = 1.0;
+        for (int j = c - 1; j >= 0; --j)
+            if (t[j].z != t[c].z) {
+                if (t[c].d - t[j].d < gap) gap = t[c].d - t[j].d;
+                break;
+            }
+        for (int j = c + 1; j < n; ++j)
+            if (t[j].z != t[c].z) {
+                if (t[j].d - t[c].d < gap) gap = t[j].d - t[c].d;
+                break;
+            }
+        *order_margin = gap;
     }
 
     /* renormalise; draw in token-id order */

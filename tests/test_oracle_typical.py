@@ -6,8 +6,10 @@ ascending d whose cumulative probability reaches typical_p, renormalise.  Pinned
 to the page's worked example ([D01], tests/golden/typical_sampling_d01.txt),
 closed forms (uniform rows: H = ln n, every d = 0, so the first ceil(tau n) ids
 are kept), the interval property of the kept set, shift invariance, the
-typical_p >= 1 and T = 0 reductions to the pinned sampler, the literal
-float64 definition on well-separated rows, and a chi-square test of the draws.
+typical_p >= 1 and T = 0 reductions to the pinned sampler, the definition
+written out independently with numpy (small rows, and 40 rows of 128256
+logits), a constructed row whose kept set changes if the centre is rounded,
+and a chi-square test of the draws.
 """
 import math
 
@@ -83,13 +85,12 @@ def test_kept_set_is_an_interval_around_the_mean(seed):
     ubar = float((p * u).sum())
     dist = np.abs(u - ubar)
     # every dropped token is at least as far from the mean as every kept one
-    # (up to the 2^-8 rounding of the centre and float32 rounding)
-    assert dist[~kept].min() >= dist[kept].max() - 2 * 2.0**-9 - 1e-5
+    assert dist[~kept].min() >= dist[kept].max() - 1e-9
     # the kept mass reaches typical_p, and dropping one of the farthest kept
-    # tokens (those within the rounding band of the boundary) would not
+    # tokens would not
     assert p[kept].sum() >= np.float32(tp) - 1e-12
-    band = np.nonzero(kept & (dist >= dist[kept].max() - 2.0**-8 - 1e-5))[0]
-    assert any(p[kept].sum() - p[j] < np.float32(tp) + 1e-9 for j in band)
+    band = np.nonzero(kept & (dist >= dist[kept].max() - 1e-9))[0]
+    assert any(p[kept].sum() - p[j] < np.float32(tp) + 1e-12 for j in band)
     # the entropy the oracle reports is the page's H
     assert abs(r["entropy"] - float(-(p[p > 0] * np.log(p[p > 0])).sum())) < 1e-9
 
@@ -115,35 +116,108 @@ def test_reductions_to_the_pinned_sampler():
         assert g["token"] == int(np.argmax(z))
 
 
-def test_literal_definition_on_separated_rows():
-    """Where no two tokens are close in d and the centre is far from a
-    rounding midpoint, the float32 order equals the literal float64 order."""
+def _literal_kept(z, T, tp):
+    """The section 3.1 definition written out with numpy in float64: p, H,
+    d = |-ln p - H|, ascending d (equal d: larger logit, then smaller id),
+    the smallest prefix reaching typical_p.  Returns (kept ids, gap in d at
+    the boundary to the nearest neighbours with a different logit)."""
+    fin = np.isfinite(z)
+    ids = np.nonzero(fin)[0]
+    a = (z[ids].astype(np.float64) - z[ids].max()) / T
+    lnp = a - math.log(np.exp(a).sum())
+    p = np.exp(lnp)
+    H = float(-(p * lnp).sum())
+    d = np.abs(-lnp - H)
+    order = np.lexsort((ids, -z[ids].astype(np.float64), d))
+    cum = np.cumsum(p[order])
+    m = int(np.searchsorted(cum, np.float32(tp), side="left")) + 1
+    m = min(m, ids.size)
+    c = m - 1
+    zc, dc, gap = z[ids[order[c]]], d[order[c]], np.inf
+    for j in range(c - 1, -1, -1):
+        if z[ids[order[j]]] != zc:
+            gap = min(gap, dc - d[order[j]])
+            break
+    for j in range(c + 1, ids.size):
+        if z[ids[order[j]]] != zc:
+            gap = min(gap, d[order[j]] - dc)
+            break
+    return set(ids[order[:m]].tolist()), gap
+
+
+def test_literal_definition_on_small_rows():
+    """Rows of 4..8 tokens, every threshold: the oracle's kept set is the
+    definition's, written out independently above."""
     checked = 0
-    for seed in range(200):
+    for seed in range(60):
         rng = np.random.default_rng(200 + seed)
         V = int(rng.integers(4, 9))
         z = (rng.standard_normal(V) * 1.5).astype(np.float32)
-        T = 1.0
-        p = np.exp((z.astype(np.float64) - z.max()) / T)
-        p /= p.sum()
-        H = float(-(p * np.log(p)).sum())
-        d = np.abs(-np.log(p) - H)
-        if np.diff(np.sort(d)).min() < 1e-3 or oracle.sample_row_typical(z, T, 0.5, 1, 0)["center_margin"] < 1e-4:
-            continue
-        order = sorted(range(V), key=lambda i: (d[i], -p[i], i))
+        T = float(np.float32(rng.uniform(0.5, 1.5)))
         for tp in (0.1, 0.3, 0.5, 0.7, 0.9):
-            cum, keep = 0.0, set()
-            for i in order:
-                keep.add(i)
-                cum += p[i]
-                if cum >= np.float32(tp):
-                    break
+            keep, gap = _literal_kept(z, T, tp)
+            if gap < 1e-12:
+                continue
             r = oracle.sample_row_typical(z, T, tp, 1, 0, want_probs=True)
             assert _support(r) == keep, (seed, tp)
-        checked += 1
-        if checked == 12:
-            break
-    assert checked == 12
+            checked += 1
+    assert checked >= 250
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_literal_definition_on_vocabulary_rows(seed):
+    """Rows of 128256 logits ~ N(0, 1) or N(0, 2^2), T in [0.5, 1.5],
+    typical_p in {0.2, 0.5, 0.9, 0.95}: the kept set and the boundary gap are
+    the definition's; the token is the draw over that set in id order."""
+    rng = np.random.default_rng(7000 + seed)
+    V = 128256
+    z = (rng.standard_normal(V) * (1.0 if seed % 2 else 2.0)).astype(np.float32)
+    T = float(np.float32(rng.uniform(0.5, 1.5)))
+    tp = float(np.float32([0.2, 0.5, 0.9, 0.95][seed % 4]))
+    keep, gap = _literal_kept(z, T, tp)
+    r = oracle.sample_row_typical(z, T, tp, seed, 3, want_probs=True)
+    assert r["status"] == oracle.OK
+    if gap > 1e-12:
+        assert _support(r) == keep
+        assert abs(r["order_margin"] - gap) <= 1e-12
+    k = np.array(sorted(_support(r)))
+    pk = np.exp((z[k].astype(np.float64) - z.max()) / T)
+    cdf = np.cumsum(pk / pk.sum())
+    u = oracle.uniform(seed, 3)
+    assert r["token"] == int(k[min(np.searchsorted(cdf, u, side="right"), k.size - 1)])
+
+
+def test_centre_is_not_rounded():
+    """A row whose p-weighted mean sits 0.45 of a 2^-8 step (log2 units) above
+    a multiple of 2^-8: 1024 logits at 0 and 3070 at -c (T = 1) put the mean
+    of a = z - z_max at abar = -c w / (1024 + w), w = 3070 e^-c; two probes sit
+    at abar + 2e-4 and abar - 7e-4.  Every other token is far from abar, so in
+    the definition's order the first probe comes first (d = 2e-4 against
+    7e-4, each moved by about 1e-7 by the probes' own weight), and a
+    typical_p below its probability keeps it alone.  A centre rounded to the
+    2^-8 grid (down by 0.45 * 2^-8 * ln 2 = 1.2e-3 nats) would put the second
+    probe first instead."""
+    c = float(np.float32(0.8069599866867065))
+    w = 3070 * math.exp(-c)
+    abar = -c * w / (1024 + w)
+    frac = (abar / math.log(2) * 256) % 1.0
+    assert 0.40 < frac < 0.50                       # the rounding goes down by ~0.45 step
+    zi, zj = np.float32(abar + 2e-4), np.float32(abar - 7e-4)
+    z = np.concatenate([np.zeros(1024, np.float32), np.full(3070, -c, np.float32), [zi, zj]]).astype(np.float32)
+    perm = np.random.default_rng(0).permutation(z.size)
+    zz = z[perm]
+    i_id, j_id = int(np.nonzero(perm == 4094)[0][0]), int(np.nonzero(perm == 4095)[0][0])
+    # on the grid the second probe would be nearer the centre
+    grid = math.floor(abar / math.log(2) * 256) / 256 * math.log(2)
+    assert abs(float(zj) - grid) < abs(float(zi) - grid)
+    for seed in range(4):
+        r = oracle.sample_row_typical(zz, 1.0, 1e-4, seed, 0, want_probs=True)
+        assert r["status"] == oracle.OK
+        assert _support(r) == {i_id} and r["token"] == i_id
+        assert abs(r["order_margin"] - 5e-4) < 1e-5
+    # a threshold above the first probe's probability takes the second one next
+    r = oracle.sample_row_typical(zz, 1.0, 5e-4, 0, 0, want_probs=True)
+    assert _support(r) == {i_id, j_id}
 
 
 def test_draws_follow_the_kept_distribution():
