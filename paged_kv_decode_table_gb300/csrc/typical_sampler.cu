@@ -45,8 +45,9 @@ constexpr int kTyW = kTyT / 32;     // warps
 constexpr int kTyBins = 2048;       // radix digits (11 bits), or draw chunks
 
 struct TySmem {
-    unsigned long long hist[kTyBins];  // mass histogram, sorted window keys, or chunk sums / prefixes
-    unsigned int cnt[kTyBins];         // count histogram, or the window's token ids
+    unsigned long long hist[kTyBins];  // mass histogram, the window's D keys, or chunk sums / prefixes
+    unsigned int cnt[kTyBins];         // the window's token ids
+    unsigned int zk[kTyBins];          // the window's logit keys ~okey(z) (ascending: larger logit first)
     unsigned int nwin;
     unsigned long long wsum[kTyW];
     double dsum[kTyW];
@@ -57,12 +58,22 @@ struct TySmem {
     // alternating slots (a slot is rewritten only after the barrier of the
     // next exchange, which every reader of it has passed)
     struct {
-        unsigned long long u;
-        double d;
+        unsigned long long u[2];
+        double d[2];
         float f[2];
     } xch[2];
-    unsigned long long res[4];  // rank 0: the cut (found, dk, u bits, id) for the cluster
+    unsigned long long res[4];  // rank 0: the cut (found, D bits, logit key, id) for the cluster
 };
+
+// Compensated (Kahan) float summation: the sum so far is s - c, c carrying the
+// rounding error of each addition (explicit round-to-nearest operations, so
+// that no contraction or reassociation undoes it).
+__device__ __forceinline__ void kahan_add(float& s, float& c, float v) {
+    const float y = __fsub_rn(v, c);
+    const float t = __fadd_rn(s, y);
+    c = __fsub_rn(__fsub_rn(t, s), y);
+    s = t;
+}
 
 // ------------------------------------------------------------------ CTA reductions
 // Every thread returns the CTA-wide result.  Each starts with a barrier, so
@@ -352,10 +363,12 @@ __global__ void __launch_bounds__(kTyT, 1)
     // cluster exchange: thread 0 publishes the CTA's partial, the barrier makes
     // it visible, every thread then reads the nc partials with rd(r)
     int xk = 0;
-    auto publish = [&](unsigned long long u, double d, float f0, float f1) {
+    auto publish = [&](unsigned long long u0, unsigned long long u1, double d0, double d1, float f0, float f1) {
         if (tid == 0) {
-            sm->xch[xk & 1].u = u;
-            sm->xch[xk & 1].d = d;
+            sm->xch[xk & 1].u[0] = u0;
+            sm->xch[xk & 1].u[1] = u1;
+            sm->xch[xk & 1].d[0] = d0;
+            sm->xch[xk & 1].d[1] = d1;
             sm->xch[xk & 1].f[0] = f0;
             sm->xch[xk & 1].f[1] = f1;
         }
@@ -365,10 +378,10 @@ __global__ void __launch_bounds__(kTyT, 1)
     // X (a position in the cluster's total of per-CTA totals `tot`, from Xof of
     // that total) relative to this CTA, or ~0 when it lies in another CTA
     auto cluster_x = [&](uint64_t tot, auto Xof) -> uint64_t {
-        publish(tot, 0.0, 0.f, 0.f);
+        publish(tot, 0ull, 0.0, 0.0, 0.f, 0.f);
         uint64_t excl = 0, grand = 0;
         for (int r = 0; r < nc; ++r) {
-            const uint64_t t = rd(r)->u;
+            const uint64_t t = rd(r)->u[0];
             excl += r < rank ? t : 0ull;
             grand += t;
         }
@@ -388,12 +401,12 @@ __global__ void __launch_bounds__(kTyT, 1)
     mx = ty_ext_f<true>(mx, sm);
     mn = ty_ext_f<false>(mn, sm);
     bad = static_cast<unsigned int>(ty_sum_u64(bad, sm));
-    publish(bad, 0.0, mx, mn);
+    publish(bad, 0ull, 0.0, 0.0, mx, mn);
     bad = 0u;
     mx = -INFINITY;
     mn = INFINITY;
     for (int r = 0; r < nc; ++r) {
-        bad |= static_cast<unsigned int>(rd(r)->u);
+        bad |= static_cast<unsigned int>(rd(r)->u[0]);
         mx = fmaxf(mx, rd(r)->f[0]);
         mn = fminf(mn, rd(r)->f[1]);
     }
@@ -415,7 +428,7 @@ __global__ void __launch_bounds__(kTyT, 1)
                 break;
             }
         first = ty_ext_f<false>(first, sm);
-        publish(0ull, 0.0, first, 0.f);
+        publish(0ull, 0ull, 0.0, 0.0, first, 0.f);
         for (int r = 0; r < nc; ++r) first = fminf(first, rd(r)->f[0]);
         ++xk;
         if (rank == 0 && tid == 0) tokens[row] = static_cast<int32_t>(first);
@@ -424,56 +437,88 @@ __global__ void __launch_bounds__(kTyT, 1)
     }
     const float c2 = fminf(1.4426950408889634f / T, 1.0e30f);  // log2(e) / T, kept finite
     auto uof = [&](float x) { return __fmul_rn(__fsub_rn(x, mx), c2); };
+    // the fixed-point mass of a logit, as the sampler's (cut and draw)
+    auto massof = [&](float x) { return fx40(hw_exp2(uof(x))); };
+    // u with the scale log2(e) / T carried in two floats (chi + clo), for the
+    // centre and the order; exact_only when that scale is beyond 1e30 (then
+    // every order decision is taken on D in double)
+    const double mxd = static_cast<double>(mx);
+    const double c2d = 1.4426950408889634 / static_cast<double>(T);
+    const bool exact_only = !(c2d <= 1.0e30);
+    const float chi = exact_only ? 1.0e30f : static_cast<float>(c2d);
+    const float clo = exact_only ? 0.f : static_cast<float>(c2d - static_cast<double>(chi));
+    auto ucof = [&](float x) {
+        const float dz = __fsub_rn(x, mx);
+        return __fmaf_rn(dz, chi, __fmul_rn(dz, clo));
+    };
     auto draw_x = [&](uint64_t tot) {  // floor(u * tot) < tot
         return static_cast<uint64_t>((static_cast<unsigned __int128>(sm->u53) * tot) >> 53);
     };
     if (!(tp < 1.f)) {  // no truncation: every finite logit
         const int f = ty_ordered_find(
-            zs, n, sm, [&](float x, int) -> uint64_t { return x > -INFINITY ? fx40(hw_exp2(uof(x))) : 0ull; },
+            zs, n, sm, [&](float x, int) -> uint64_t { return x > -INFINITY ? massof(x) : 0ull; },
             [&](uint64_t tot) { return cluster_x(tot, draw_x); });
         if (f >= 0 && tid == 0) tokens[row] = lo + f;
         cl.sync();
         return;
     }
 
-    // ---- S and the p-weighted mean of u, rounded to the 2^-8 grid
+    // ---- S (exact fixed-point masses) and the p-weighted mean of u.  The
+    // centre ubar = sum w u / sum w takes u from the compensated scale ucof and
+    // Kahan sums per thread, double across threads and CTAs (error ~1e-7 in
+    // log2 units on vocabulary rows; a plain float scale would bias it by the
+    // rounding of log2(e) / T times the spread of u).
     uint64_t s = 0;
-    float wu = 0.f;
+    float ws = 0.f, wc = 0.f, us = 0.f, uc = 0.f;
     ty_sweep(zs, n, [&](int, float x) {
         if (!(x > -INFINITY)) return;
-        const float u = uof(x);
+        s += massof(x);
+        const float u = ucof(x);
         const float w = hw_exp2(u);
-        s += fx40(w);
-        if (w > 0.f) wu = fmaf(w, u, wu);
+        if (w > 0.f) {
+            kahan_add(ws, wc, w);
+            kahan_add(us, uc, __fmul_rn(w, u));
+        }
     });
     const uint64_t Sc = ty_sum_u64(s, sm);
-    const double WUc = ty_sum_f64(static_cast<double>(wu), sm);
-    publish(Sc, WUc, 0.f, 0.f);
+    const double Wc = ty_sum_f64(static_cast<double>(ws) - static_cast<double>(wc), sm);
+    const double WUc = ty_sum_f64(static_cast<double>(us) - static_cast<double>(uc), sm);
+    publish(Sc, 0ull, Wc, WUc, 0.f, 0.f);
     uint64_t S = 0;
-    double WU = 0.0;
+    double W = 0.0, WU = 0.0;
     for (int r = 0; r < nc; ++r) {
-        S += rd(r)->u;
-        WU += rd(r)->d;
+        S += rd(r)->u[0];
+        W += rd(r)->d[0];
+        WU += rd(r)->d[1];
     }
     ++xk;
-    const double ubar = WU / (static_cast<double>(S) * 0x1p-40);
-    const float ub = static_cast<float>(rint(ubar * 256.0) / 256.0);
-    auto dkey = [&](float u) { return __float_as_uint(fabsf(__fsub_rn(u, ub))); };  // monotone in dk >= 0
+    const double ubar = WU / W;  // W >= 1: the maximum weighs 1
+    const float ubf = static_cast<float>(ubar);
+    // The order key: D = |u - ubar| in double (log2 units; d = D ln 2), with a
+    // float estimate dk = |ucof(x) - ubf| within errf(u) of it (4x the error
+    // bound of the float operations), so that only logits whose dk lies within
+    // errf of a threshold need D.
+    auto dex = [&](float x) -> double {
+        return fabs(__dsub_rn(__dmul_rn(__dsub_rn(static_cast<double>(x), mxd), c2d), ubar));
+    };
+    auto dkf = [&](float u) { return fabsf(__fsub_rn(u, ubf)); };
+    auto errf = [&](float u) {
+        return exact_only ? INFINITY : __fmaf_rn(__fadd_rn(fabsf(u), fabsf(ubf)), 0x1p-19f, 0x1p-126f);
+    };
     const uint64_t target = ceil_mul_p(tp, S);  // >= 1, <= S
 
     // ---- 2048 bins linear in dk over [0, dkmax] (bin 0: closest to the mean):
-    // the mass per bin (float, summed over the cluster in rank order); the bin
-    // where the cumulative mass in ascending dk first reaches the target holds
-    // the cut
-    const float umin = uof(mn);
-    const float dkmax = fmaxf(fabsf(__fsub_rn(umin, ub)), fabsf(ub));
+    // the weight per bin (float, summed over the cluster in rank order); the
+    // bin where the cumulative weight in ascending dk first reaches the target
+    // holds the cut, approximately
+    const float dkmax = fmaxf(dkf(ucof(mn)), fabsf(ubf));
     const float sc = static_cast<float>(kTyBins) / dkmax;
     const float scale = (dkmax > 0.f && sc < INFINITY) ? sc : 0.f;  // 0: one bin
-    auto dbin = [&](uint32_t dk) {  // monotone non-decreasing in dk; inf * 0 (NaN) -> the last bin
-        const float t = __uint_as_float(dk) * scale;
+    auto dbin = [&](float dk) {  // monotone non-decreasing in dk; inf * 0 (NaN) -> the last bin
+        const float t = dk * scale;
         return t < static_cast<float>(kTyBins - 1) ? static_cast<int>(t) : kTyBins - 1;
     };
-    float* hf = reinterpret_cast<float*>(sm->hist);  // approximate bin masses (weights 2^u)
+    float* hf = reinterpret_cast<float*>(sm->hist);  // approximate bin weights 2^u
     for (int i = tid; i < kTyBins; i += kTyT) hf[i] = 0.f;
     if (tid == 0) sm->nwin = 0u;
     __syncthreads();
@@ -482,8 +527,8 @@ __global__ void __launch_bounds__(kTyT, 1)
         float cw = 0.f;
         ty_sweep(zs, n, [&](int, float x) {
             if (!(x > -INFINITY)) return;
-            const float u = uof(x);
-            const int bq = dbin(dkey(u));
+            const float u = ucof(x);
+            const int bq = dbin(dkf(u));
             if (bq != cb) {
                 if (cw > 0.f) atomicAdd(&hf[cb], cw);
                 cb = bq;
@@ -521,48 +566,73 @@ __global__ void __launch_bounds__(kTyT, 1)
     const int blo = static_cast<int>(sm->bc[0]), bhi = max(blo, static_cast<int>(sm->bc[1]));
     cl.sync();  // no CTA reads another's bins any more; rank 0's bins become the window list
 
-    // ---- the window's logits into rank 0's shared memory (and the exact mass
-    // above it), to be sorted by (dk, larger u first, id): key
-    // (dk bits << 32 | ~okey(u)) ascending, then id
+    // ---- the window: logits with Ed <= D < Fd (the bins' edges, in double);
+    // membership is decided on D itself wherever dk is within errf of an edge
+    const bool one_bin = !(scale > 0.f);
+    const double Ed = (one_bin || blo == 0) ? 0.0 : static_cast<double>(blo) / static_cast<double>(scale);
+    const double Fd = (one_bin || bhi >= kTyBins - 1) ? static_cast<double>(INFINITY)
+                                                      : static_cast<double>(bhi + 1) / static_cast<double>(scale);
+    // 0: before [lo, hi) in the order, 1: inside, 2: after
+    auto where = [&](float x, double lod, double hid) -> int {
+        const float u = ucof(x);
+        const float dk = dkf(u), e = errf(u);
+        const float lof = static_cast<float>(lod), hif = static_cast<float>(hid);
+        if (dk < lof - e) return 0;
+        if (dk > lof + e && dk < hif - e) return 1;
+        if (dk > hif + e) return 2;
+        const double D = dex(x);
+        return D < lod ? 0 : (D < hid ? 1 : 2);
+    };
+
+    // ---- the window's logits into rank 0's shared memory, keyed (D bits,
+    // logit key, id) ascending; the exact masses before and inside the window
     unsigned long long* key = sm->hist;
     unsigned int* ids = sm->cnt;
+    unsigned int* zkw = sm->zk;
     unsigned long long* key0 = cl.map_shared_rank(sm->hist, 0);
     unsigned int* ids0 = cl.map_shared_rank(sm->cnt, 0);
+    unsigned int* zk0 = cl.map_shared_rank(sm->zk, 0);
     unsigned int* nwin0 = cl.map_shared_rank(&sm->nwin, 0);
-    uint64_t at = 0;
+    uint64_t at = 0, in = 0;
     ty_sweep(zs, n, [&](int i, float x) {
         if (!(x > -INFINITY)) return;
-        const float u = uof(x);
-        const uint32_t dk = dkey(u);
-        const int bq = dbin(dk);
-        if (bq < blo) {
-            at += fx40(hw_exp2(u));
-        } else if (bq <= bhi) {
+        const int w = where(x, Ed, Fd);
+        if (w == 0) {
+            at += massof(x);
+        } else if (w == 1) {
+            in += massof(x);
             const unsigned int slot = atomicAdd(nwin0, 1u);
             if (slot < static_cast<unsigned int>(kTyBins)) {
-                key0[slot] = (static_cast<unsigned long long>(dk) << 32) | static_cast<uint32_t>(~okey(u));
+                key0[slot] = static_cast<unsigned long long>(__double_as_longlong(dex(x)));
+                zk0[slot] = ~okey(x);
                 ids0[slot] = static_cast<unsigned int>(lo + i);
             }
         }
     });
     const uint64_t atc = ty_sum_u64(at, sm);
-    publish(atc, 0.0, 0.f, 0.f);  // its barrier also completes the pushes into rank 0
-    uint64_t above = 0;
-    for (int r = 0; r < nc; ++r) above += rd(r)->u;  // exact mass of the bins before the window
+    const uint64_t inc = ty_sum_u64(in, sm);
+    publish(atc, inc, 0.0, 0.0, 0.f, 0.f);  // its barrier also completes the pushes into rank 0
+    uint64_t above = 0, inwin = 0;
+    for (int r = 0; r < nc; ++r) {
+        above += rd(r)->u[0];  // exact mass before the window
+        inwin += rd(r)->u[1];  // exact mass of the window
+    }
     ++xk;
+    const bool cut_in_window = above < target && target <= above + inwin;
 
     // ---- rank 0 sorts the window and finds the cut; the cluster reads the result
-    uint32_t dstar = 0u;
-    float ustar = 0.f;
+    unsigned long long dstar = 0ull;
+    uint32_t zstar = 0u;
     int idstar = -1;
     bool found = false;
     if (rank == 0) {
         const unsigned int nw = sm->nwin;
-        if (nw >= 1 && nw <= static_cast<unsigned int>(kTyBins) && above < target) {
+        if (cut_in_window && nw <= static_cast<unsigned int>(kTyBins)) {
             int np2 = 1;
             while (np2 < static_cast<int>(nw)) np2 <<= 1;
             for (int i = static_cast<int>(nw) + tid; i < np2; i += kTyT) {
                 key[i] = ~0ull;
+                zkw[i] = ~0u;
                 ids[i] = ~0u;
             }
             __syncthreads();
@@ -573,10 +643,13 @@ __global__ void __launch_bounds__(kTyT, 1)
                         if (l > i) {
                             const bool up = (i & k) == 0;
                             const unsigned long long ki = key[i], kl = key[l];
-                            const bool gt = ki > kl || (ki == kl && ids[i] > ids[l]);
+                            const unsigned int zi = zkw[i], zl = zkw[l];
+                            const bool gt = ki > kl || (ki == kl && (zi > zl || (zi == zl && ids[i] > ids[l])));
                             if (gt == up) {
                                 key[i] = kl;
                                 key[l] = ki;
+                                zkw[i] = zl;
+                                zkw[l] = zi;
                                 const unsigned int t = ids[i];
                                 ids[i] = ids[l];
                                 ids[l] = t;
@@ -587,7 +660,7 @@ __global__ void __launch_bounds__(kTyT, 1)
                 }
             // cumulative mass in sorted order: thread t takes entries [2t, 2t + 2)
             auto wmass = [&](int j) -> uint64_t {
-                return j < static_cast<int>(nw) ? fx40(hw_exp2(key_float(~static_cast<uint32_t>(key[j])))) : 0ull;
+                return j < static_cast<int>(nw) ? massof(key_float(~zkw[j])) : 0ull;
             };
             const int j0 = 2 * tid;
             const uint64_t w0 = wmass(j0), w1 = wmass(j0 + 1);
@@ -596,19 +669,19 @@ __global__ void __launch_bounds__(kTyT, 1)
             const uint64_t c0 = above + ty_excl_scan(w0 + w1, sm, wt);  // (begins with a barrier)
             if (c0 < target && c0 + w0 + w1 >= target) sm->bc[2] = static_cast<unsigned long long>(c0 + w0 >= target ? j0 : j0 + 1);
             __syncthreads();
-            if (sm->bc[2] != ~0ull) {  // the cut lies in the window
+            if (sm->bc[2] != ~0ull) {  // always, since the cut lies in the window
                 const int jc = static_cast<int>(sm->bc[2]);
-                dstar = static_cast<uint32_t>(key[jc] >> 32);
-                ustar = key_float(~static_cast<uint32_t>(key[jc]));
+                dstar = key[jc];
+                zstar = zkw[jc];
                 idstar = static_cast<int>(ids[jc]);
                 found = true;
             }
-            __syncthreads();  // hist / cnt are reused below
+            __syncthreads();  // hist / cnt / zk are reused below
         }
         if (tid == 0) {
             sm->res[0] = found ? 1ull : 0ull;
             sm->res[1] = dstar;
-            sm->res[2] = __float_as_uint(ustar);
+            sm->res[2] = zstar;
             sm->res[3] = static_cast<uint32_t>(idstar);
         }
     }
@@ -616,76 +689,93 @@ __global__ void __launch_bounds__(kTyT, 1)
     {
         const unsigned long long* r0 = cl.map_shared_rank(sm->res, 0);
         found = r0[0] != 0ull;
-        dstar = static_cast<uint32_t>(r0[1]);
-        ustar = __uint_as_float(static_cast<uint32_t>(r0[2]));
+        dstar = r0[1];
+        zstar = static_cast<uint32_t>(r0[2]);
         idstar = static_cast<int>(static_cast<uint32_t>(r0[3]));
     }
     if (!found && rank == 0) {
-        // ---- the window missed or overflowed: rank 0 alone, over the whole row:
-        // radix select over the dk bits of every finite logit, then over u, then
-        // the rank in id order
-        above = 0;
-        auto kd = [&](float x, int, uint32_t& k, uint64_t& m) -> bool {
-            if (!(x > -INFINITY)) return false;
-            const float u = uof(x);
-            k = dkey(u);
-            m = fx40(hw_exp2(u));
+        // ---- the window overflowed (more than 2048 logits) or missed the cut:
+        // rank 0 alone, over the whole row, takes an exact radix select over
+        // the window's logits (the whole row when it missed): the 64 bits of D,
+        // then the logit key, then the rank in id order
+        const bool whole = !cut_in_window;
+        const double lod = whole ? 0.0 : Ed, hid = whole ? static_cast<double>(INFINITY) : Fd;
+        above = whole ? 0ull : above;
+        auto inw = [&](float x) { return x > -INFINITY && (whole || where(x, lod, hid) == 1); };
+        auto kh = [&](float x, int, uint32_t& k, uint64_t& m) -> bool {
+            if (!inw(x)) return false;
+            k = static_cast<uint32_t>(static_cast<unsigned long long>(__double_as_longlong(dex(x))) >> 32);
+            m = massof(x);
             return true;
         };
-        const uint32_t d0 = ty_radix(z, V, sm, kd, 0u, 0, 21, 11, target, above);
-        const uint32_t d1 = ty_radix(z, V, sm, kd, d0, 11, 10, 11, target, above);
-        const uint32_t d2 = ty_radix(z, V, sm, kd, (d0 << 11) | d1, 22, 0, 10, target, above);
-        dstar = (d0 << 21) | (d1 << 10) | d2;
+        const uint32_t a0 = ty_radix(z, V, sm, kh, 0u, 0, 21, 11, target, above);
+        const uint32_t a1 = ty_radix(z, V, sm, kh, a0, 11, 10, 11, target, above);
+        const uint32_t a2 = ty_radix(z, V, sm, kh, (a0 << 11) | a1, 22, 0, 10, target, above);
+        const uint32_t dhi = (a0 << 21) | (a1 << 10) | a2;
+        auto kl = [&](float x, int, uint32_t& k, uint64_t& m) -> bool {
+            if (!inw(x)) return false;
+            const unsigned long long db = static_cast<unsigned long long>(__double_as_longlong(dex(x)));
+            if (static_cast<uint32_t>(db >> 32) != dhi) return false;
+            k = static_cast<uint32_t>(db);
+            m = massof(x);
+            return true;
+        };
+        const uint32_t b0 = ty_radix(z, V, sm, kl, 0u, 0, 21, 11, target, above);
+        const uint32_t b1 = ty_radix(z, V, sm, kl, b0, 11, 10, 11, target, above);
+        const uint32_t b2 = ty_radix(z, V, sm, kl, (b0 << 11) | b1, 22, 0, 10, target, above);
+        dstar = (static_cast<unsigned long long>(dhi) << 32) | ((b0 << 21) | (b1 << 10) | b2);
+        const double ds = __longlong_as_double(static_cast<long long>(dstar));
+        // among equal D: the larger logit first (ascending ~okey)
         float gmin = INFINITY, gmax = -INFINITY;
         ty_sweep(z, V, [&](int, float x) {
-            if (!(x > -INFINITY)) return;
-            const float u = uof(x);
-            if (dkey(u) == dstar) {
-                gmin = fminf(gmin, u);
-                gmax = fmaxf(gmax, u);
-            }
+            if (!inw(x) || dex(x) != ds) return;
+            gmin = fminf(gmin, x);
+            gmax = fmaxf(gmax, x);
         });
         gmin = ty_ext_f<false>(gmin, sm);
         gmax = ty_ext_f<true>(gmax, sm);
-        ustar = gmax;
+        zstar = ~okey(gmax);
         if (!(gmin == gmax)) {
-            auto ku = [&](float x, int, uint32_t& k, uint64_t& m) -> bool {
-                if (!(x > -INFINITY)) return false;
-                const float u = uof(x);
-                if (dkey(u) != dstar) return false;
-                k = ~okey(u);  // ascending key = descending u
-                m = fx40(hw_exp2(u));
+            auto kz = [&](float x, int, uint32_t& k, uint64_t& m) -> bool {
+                if (!inw(x) || dex(x) != ds) return false;
+                k = ~okey(x);
+                m = massof(x);
                 return true;
             };
-            const uint32_t e0 = ty_radix(z, V, sm, ku, 0u, 0, 21, 11, target, above);
-            const uint32_t e1 = ty_radix(z, V, sm, ku, e0, 11, 10, 11, target, above);
-            const uint32_t e2 = ty_radix(z, V, sm, ku, (e0 << 11) | e1, 22, 0, 10, target, above);
-            ustar = key_float(~((e0 << 21) | (e1 << 10) | e2));
+            const uint32_t e0 = ty_radix(z, V, sm, kz, 0u, 0, 21, 11, target, above);
+            const uint32_t e1 = ty_radix(z, V, sm, kz, e0, 11, 10, 11, target, above);
+            const uint32_t e2 = ty_radix(z, V, sm, kz, (e0 << 11) | e1, 22, 0, 10, target, above);
+            zstar = (e0 << 21) | (e1 << 10) | e2;
         }
-        // the cut among equal (dk, u) (equal masses): the r-th in id order
-        const uint64_t mstar = fx40(hw_exp2(ustar));
+        // the cut among equal (D, logit) (equal masses): the r-th in id order
+        const uint64_t mstar = massof(key_float(~zstar));
         const uint64_t need = target - above;
         const uint64_t r = mstar ? (need + mstar - 1) / mstar : 1ull;
-        const float us = ustar;
-        const uint32_t ds = dstar;
+        const uint32_t zs_ = zstar;
         idstar = ty_ordered_find(
             z, V, sm,
-            [&](float x, int) -> uint64_t {
-                if (!(x > -INFINITY)) return 0ull;
-                const float u = uof(x);
-                return (dkey(u) == ds && u == us) ? 1ull : 0ull;
-            },
+            [&](float x, int) -> uint64_t { return (inw(x) && dex(x) == ds && ~okey(x) == zs_) ? 1ull : 0ull; },
             [&](uint64_t) { return r - 1; });
     }
 
-
-    // ---- the draw over the kept set in id order
+    // ---- the draw over the kept set in id order: (D, logit key, id) up to the cut's
+    const double ds = __longlong_as_double(static_cast<long long>(dstar));
+    const float dsf = static_cast<float>(ds);
     auto kept = [&](float x, int i) -> uint64_t {  // i: the id
         if (!(x > -INFINITY)) return 0ull;
-        const float u = uof(x);
-        const uint32_t dk = dkey(u);
-        const bool keep = dk < dstar || (dk == dstar && (u > ustar || (u == ustar && i <= idstar)));
-        return keep ? fx40(hw_exp2(u)) : 0ull;
+        const float u = ucof(x);
+        const float dk = dkf(u), e = errf(u);
+        bool keep;
+        if (dk < dsf - e) {
+            keep = true;
+        } else if (dk > dsf + e) {
+            keep = false;
+        } else {
+            const double D = dex(x);
+            const uint32_t k = ~okey(x);
+            keep = D < ds || (D == ds && (k < zstar || (k == zstar && i <= idstar)));
+        }
+        return keep ? massof(x) : 0ull;
     };
     if (!found) {
         if (rank == 0) {
