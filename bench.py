@@ -317,15 +317,16 @@ def run_gpu(args):
     status = pkv.new_status(dev)
     k_cache, v_cache = inp["k_cache"], inp["v_cache"]
 
-    def step(q, k_new, v_new, bt, sl, logits, temp, tk, tp, seeds, offs):
-        pkv.paged_decode_attention_append(q, k_new, v_new, k_cache, v_cache, bt, sl, out=out, workspace=ws,
-                                          status=status)
-        pkv.sample_tokens(logits, temp, tk, tp, seeds, offs, tokens=tokens, status=status)
+    def make_step(d):
+        """The public API's prepared step (buffers checked once) over the inputs d."""
+        return pkv.DecodeStep(d["q"], d["k_new"], d["v_new"], k_cache, v_cache, d["block_tables"], d["seq_lens"],
+                              d["logits"], d["temperature"], d["top_k"], d["top_p"], d["seeds"], d["offsets"],
+                              out=out, tokens=tokens, workspace=ws, status=status)
 
-    dev_args = (inp["q"], inp["k_new"], inp["v_new"], inp["block_tables"], inp["seq_lens"], inp["logits"],
-                inp["temperature"], inp["top_k"], inp["top_p"], inp["seeds"], inp["offsets"])
+    dstep = make_step(inp)
+    step = dstep.run
     for _ in range(max(3, args.warmup)):
-        step(*dev_args)
+        step()
     torch.cuda.synchronize()
     if pkv.check_status(status) != 0:
         raise SystemExit(f"device status {pkv.status_string(pkv.check_status(status))} during warm-up")
@@ -345,16 +346,13 @@ def run_gpu(args):
     torch.cuda.synchronize()
     t0.record(stream)
     for i in range(args.steps):
-        step(*dev_args)
+        step()
     t1.record(stream)
     for i in range(k2):
         a0[i].record(stream)
-        pkv.paged_decode_attention_append(inp["q"], inp["k_new"], inp["v_new"], k_cache, v_cache,
-                                          inp["block_tables"], inp["seq_lens"], out=out, workspace=ws,
-                                          status=status)
+        dstep.run_attention()
         a1[i].record(stream)
-        pkv.sample_tokens(inp["logits"], inp["temperature"], inp["top_k"], inp["top_p"], inp["seeds"],
-                          inp["offsets"], tokens=tokens, status=status)
+        dstep.run_sampler()
     torch.cuda.synchronize()
     _barrier(world)
     clk = clocks.stop()
@@ -372,10 +370,12 @@ def run_gpu(args):
         g = torch.cuda.CUDAGraph()
         gs = torch.cuda.Stream(dev)
         gs.wait_stream(stream)
+        dstep.set_stream(gs)
         with torch.cuda.stream(gs):
             with torch.cuda.graph(g, stream=gs):
                 for _ in range(kGraphSteps):
-                    step(*dev_args)
+                    step()
+        dstep.set_stream(stream)
         torch.cuda.synchronize()
         for _ in range(3):
             g.replay()
@@ -417,9 +417,10 @@ def run_gpu(args):
     free = [torch.cuda.Event() for _ in range(2)]
     e2e_steps = max(10, min(args.steps, 200))
 
-    def run_views(d):
-        step(d["q"], d["k_new"], d["v_new"], d["block_tables"], d["seq_lens"], d["logits"], d["temperature"],
-             d["top_k"], d["top_p"], d["seeds"], d["offsets"])
+    vsteps = [make_step(d) for d in dviews]
+
+    def run_views(j):
+        vsteps[j].run()
 
     def e2e_step_pipelined(i):
         j = i & 1
@@ -428,13 +429,13 @@ def run_gpu(args):
             dbufs[j].copy_(host_buf, non_blocking=True)
             ready[j].record(cstream)
         stream.wait_event(ready[j])
-        run_views(dviews[j])
+        run_views(j)
         free[j].record(stream)
         tok_host[j].copy_(tokens, non_blocking=True)
 
     def e2e_step_serial(i):
         dbufs[0].copy_(host_buf, non_blocking=True)
-        run_views(dviews[0])
+        run_views(0)
         tok_host[0].copy_(tokens, non_blocking=True)
 
     def time_e2e(fn):
@@ -459,6 +460,8 @@ def run_gpu(args):
         raise SystemExit(f"device status {pkv.status_string(pkv.check_status(status))} in the end-to-end steps")
     if not all(torch.equal(t, tokens.cpu()) for t in tok_host):
         raise SystemExit("end-to-end tokens differ from the device-resident step")
+
+    per_config = measure_per_config(pkv, dev) if world == 1 else None
 
     total_bytes = _sum_over_ranks(float(bytes_step["total"]), world, dev)
     value = total_bytes / (ms * 1e-3) / 1e9
@@ -494,6 +497,7 @@ def run_gpu(args):
                 "serial_value": total_bytes / (e2e_serial_ms * 1e-3) / 1e9},
         "gpu_launches": launches,
         "graph": graph,
+        "per_config": per_config,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -503,6 +507,72 @@ def run_gpu(args):
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+# ---------------------------------------------------------------- other configurations
+def measure_per_config(pkv, dev, calls: int = 30):
+    """The other workloads' hot calls, each timed with CUDA events on its stream
+    around every call (median and mean of `calls` calls after 3 warm-up calls):
+    the attention call with the append on the long-context (B 8, 64/8 heads,
+    L 32K..128K) and fragmented batch-512 workloads, whose 2.7 GB and 1.2 GB of
+    KV exceed L2, and the sampler alone on the batch-64, batch-512 and stress
+    workloads with L2 flushed (a 256 MB write) before every call.  Fractions are
+    of the measured copy peak and of 8 TB/s."""
+    peak, _ = _peaks()
+    scratch = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def flush():
+        scratch.fill_(1)
+
+    def stats(fn, flush_fn=None):
+        t = _time_calls(fn, calls, flush=flush_fn)
+        return t
+
+    res = {}
+    for num in (3, 4):
+        w = W.workload(num)
+        inp = W.make_decode_inputs(w, dev, with_logits=False)
+        out = torch.empty_like(inp["q"])
+        ws = torch.empty(pkv.decode_workspace_bytes(w.batch, w.n_q_heads, w.head_dim), dtype=torch.uint8,
+                         device=dev)
+        st = pkv.new_status(dev)
+        sb = W.step_bytes(w, inp["seq_lens"])
+        by = sb["attention"] + sb["append"]
+        t = stats(lambda: pkv.paged_decode_attention_append(inp["q"], inp["k_new"], inp["v_new"], inp["k_cache"],
+                                                            inp["v_cache"], inp["block_tables"], inp["seq_lens"],
+                                                            out=out, workspace=ws, status=st))
+        if pkv.check_status(st) != 0:
+            raise SystemExit(f"device status {pkv.status_string(pkv.check_status(st))} on workload {w.name}")
+        gbs = by / (t["median_us"] * 1e-6) / 1e9
+        res[f"config{num}_attention"] = {
+            "workload": w.name, "call": "paged_decode_attention_append", "algorithmic_bytes": by,
+            "median_us": t["median_us"], "mean_us": t["mean_us"], "p90_us": t["p90_us"], "calls": calls,
+            "GB/s": gbs, "frac_of_measured": gbs / peak, "frac_of_8TBps": gbs / 8000.0,
+            "l2": "no flush: the call reads more than the 126 MB L2"}
+        del inp, out, ws
+        torch.cuda.empty_cache()
+    for num in (2, 4, 5):
+        w = W.workload(num)
+        si = W.make_sampler_inputs(w, dev)
+        tok = torch.empty(w.batch, dtype=torch.int32, device=dev)
+        st = pkv.new_status(dev)
+        t = stats(lambda: pkv.sample_tokens(si["logits"], si["temperature"], si["top_k"], si["top_p"], si["seeds"],
+                                            si["offsets"], tokens=tok, status=st), flush)
+        if pkv.check_status(st) != 0:
+            raise SystemExit(f"device status {pkv.status_string(pkv.check_status(st))} on the sampler, {w.name}")
+        by = 4 * w.batch * w.vocab + w.batch * 32
+        gbs = by / (t["median_us"] * 1e-6) / 1e9
+        res[f"config{num}_sampler"] = {
+            "workload": f"{w.batch} x {w.vocab} logits ({w.name})", "call": "sample_tokens",
+            "algorithmic_bytes": by, "median_us": t["median_us"], "mean_us": t["mean_us"], "p90_us": t["p90_us"],
+            "calls": calls, "tokens_per_s": w.batch / (t["median_us"] * 1e-6), "GB/s": gbs,
+            "frac_of_measured": gbs / peak, "frac_of_8TBps": gbs / 8000.0,
+            "l2": "flushed before every call (256 MB write outside the events)"}
+        del si
+        torch.cuda.empty_cache()
+    del scratch
+    torch.cuda.empty_cache()
+    return res
 
 
 # ---------------------------------------------------------------- extra measurements
@@ -522,7 +592,8 @@ def _time_calls(fn, n: int, flush=None):
         e1.record(stream)
     torch.cuda.synchronize()
     t = sorted(e0.elapsed_time(e1) * 1e3 for e0, e1 in ev)
-    return {"median_us": t[len(t) // 2], "p90_us": t[min(len(t) - 1, (9 * len(t)) // 10)], "n": n}
+    return {"median_us": t[len(t) // 2], "mean_us": sum(t) / len(t), "p90_us": t[min(len(t) - 1, (9 * len(t)) // 10)],
+            "n": n}
 
 
 def run_extras(args):

@@ -163,9 +163,10 @@ pkv_status pkv_paged_decode_attention_append(void* out, const void* q, const voi
  * synchronisation of an allocation, or a C host program with no allocator).
  * Same arguments, semantics and results as pkv_paged_decode_attention; the
  * split-KV workspace is instead a fixed 16 MiB device array inside the library,
- * present on every GPU that loads it until the process exits.  The first call
- * on a device looks up that array's device address (cudaGetSymbolAddress), so
- * make the first call on each device before any stream capture.  Requests that
+ * present on every GPU that loads it until the process exits.  Every call looks
+ * up that array's device address on the current device (cudaGetSymbolAddress;
+ * the first lookup on a device loads the library's module there), so make the
+ * first call on each device before any stream capture.  Requests that
  * would need more than 16 MiB of workspace (pkv_decode_workspace_bytes(B, Hq, D,
  * 0) > 16 MiB; Hq = 32, D = 128 needs about 5 MiB on 152 SMs) return
  * PKV_ERR_UNSUPPORTED and launch nothing.  Nothing is allocated or freed.  All
@@ -180,6 +181,25 @@ pkv_status pkv_paged_decode_attention_noalloc(void* out, const void* q, const vo
                                               int Hq, int Hkv, int D, int block_size, int num_blocks,
                                               float scale, pkv_dtype dtype, int32_t* dev_status,
                                               void* stream);
+
+/*
+ * Test hook for the failure path of the attention kernels; off by default and
+ * not part of the decode step (the pages have no counterpart).  The fast
+ * attention kernel waits on its stage barriers with a bounded number of polls
+ * (about a second or more by default), after which it records PKV_ERR_TIMEOUT
+ * in dev_status and returns instead of hanging.  This call sets, for every
+ * later attention call of the process (all threads, all devices):
+ *   polls       the poll budget of those waits; 0 restores the default;
+ *   silent_cta  one CTA of the split-KV kernel whose loader issues no copy at
+ *               all (-1: none), so that its consumers wait on stages nothing
+ *               will fill and give up after `polls` polls, with no copy in
+ *               flight.
+ * With silent_cta >= 0 the output of the sequences that CTA covers is
+ * undefined and dev_status reads PKV_ERR_TIMEOUT; the next call after the
+ * hook is reset computes normally.  Returns PKV_ERR_INVALID_ARG for
+ * silent_cta < -1.  Not synchronised with attention calls on other threads.
+ */
+pkv_status pkv_test_set_wait_limit(uint32_t polls, int silent_cta);
 
 /*
  * Workspace bytes pkv_sample_tokens needs (B rows of V logits).  The current

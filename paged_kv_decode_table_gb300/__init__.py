@@ -17,6 +17,8 @@ Calls (names follow the C ABI):
   kv_append_chunk(k_new, v_new, k_cache, v_cache, block_tables, seq_lens, q_start)
   paged_prefill_attention(q, k_cache, v_cache, block_tables, seq_lens, q_start, out=None, scale=0.0)
   BlockPool(num_blocks, block_size, max_blocks_per_seq)   host-side refcounted block ids
+  DecodeStep(q, k_new, v_new, k_cache, v_cache, block_tables, seq_lens, logits, ...).run()
+      a whole decode step (append + attention + sampler) bound to fixed buffers
 """
 from __future__ import annotations
 
@@ -31,7 +33,7 @@ __all__ = ["PkvError", "load_library", "library_path", "kv_append", "paged_decod
            "decode_workspace_bytes", "sample_tokens", "sample_workspace_bytes", "status_string",
            "new_status", "check_status", "STATUS", "copy_blocks", "BlockPool", "spec_verify",
            "spec_verify_workspace_bytes", "apply_logits_processors", "kv_append_chunk",
-           "paged_prefill_attention"]
+           "paged_prefill_attention", "DecodeStep", "test_set_wait_limit"]
 
 STATUS = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED", 3: "PKV_ERR_CUDA",
           4: "PKV_ERR_DEVICE_BOUNDS", 5: "PKV_ERR_TIMEOUT", 6: "PKV_ERR_NONFINITE", 7: "PKV_ERR_CAPACITY"}
@@ -120,8 +122,17 @@ def load_library():
         lib.pkv_seq_length.restype = i32
         lib.pkv_block_tables.argtypes = [P, P, i32, P, P]
         lib.pkv_block_tables.restype = i32
+        lib.pkv_test_set_wait_limit.argtypes = [ctypes.c_uint32, i32]
+        lib.pkv_test_set_wait_limit.restype = i32
         _lib = lib
         return lib
+
+
+def test_set_wait_limit(polls: int = 0, silent_cta: int = -1) -> None:
+    """Failure-path test hook (pkv_test_set_wait_limit): the poll budget of the
+    attention kernel's waits (0: the default) and one CTA whose loader issues
+    no copy (-1: none).  Call with no arguments to restore the defaults."""
+    _raise("pkv_test_set_wait_limit", load_library().pkv_test_set_wait_limit(int(polls), int(silent_cta)))
 
 
 def status_string(code: int) -> str:
@@ -319,6 +330,108 @@ def sample_tokens(logits, temperature, top_k, top_p, seeds, offsets, tokens=None
                                             None, 0, _ptr(status), _stream(dev))
     _raise("pkv_sample_tokens", code)
     return tokens
+
+
+class DecodeStep:
+    """One decode step bound to fixed device buffers: the new token's K/V
+    appended through the block table, paged decode attention
+    (pkv_paged_decode_attention_append) and the sampler (pkv_sample_tokens, or
+    pkv_sample_tokens_ex with min_p).  The buffers are checked once, here;
+    run() passes the prepared pointers straight to the two C calls, so a
+    serving loop pays a few microseconds of host time per step instead of
+    re-validating every tensor.  The tensors must stay alive, in place and of
+    the same shapes while the object is used (refill them in place between
+    steps).  Returns the tokens tensor from run()."""
+
+    def __init__(self, q, k_new, v_new, k_cache, v_cache, block_tables, seq_lens, logits, temperature, top_k,
+                 top_p, seeds, offsets, out=None, tokens=None, workspace=None, status=None, min_p=None,
+                 scale: float = 0.0, stream=None):
+        B, Hq, D = q.shape
+        NB, Hkv, BS, D2 = k_cache.shape
+        dev = q.device
+        if D2 != D:
+            raise ValueError("head_dim of q and the cache differ")
+        _check_cuda("q", q)
+        _check_cuda("k_cache", k_cache, q.dtype, device=dev)
+        _check_cuda("v_cache", v_cache, q.dtype, k_cache.shape, dev)
+        _check_cuda("k_new", k_new, q.dtype, (B, Hkv, D), dev)
+        _check_cuda("v_new", v_new, q.dtype, (B, Hkv, D), dev)
+        _check_cuda("block_tables", block_tables, torch.int32, device=dev)
+        _check_cuda("seq_lens", seq_lens, torch.int32, (B,), dev)
+        if block_tables.dim() != 2 or block_tables.shape[0] != B:
+            raise ValueError("block_tables must be [B, max_blocks_per_seq]")
+        if logits.dim() != 2 or logits.shape[0] != B:
+            raise ValueError("logits must be [B, V]")
+        V = logits.shape[1]
+        _check_cuda("logits", logits, torch.float32, device=dev)
+        _check_cuda("temperature", temperature, torch.float32, (B,), dev)
+        _check_cuda("top_k", top_k, torch.int32, (B,), dev)
+        _check_cuda("top_p", top_p, torch.float32, (B,), dev)
+        if seeds.dtype not in (torch.int64, torch.uint64) or offsets.dtype not in (torch.int64, torch.uint64):
+            raise TypeError("seeds and offsets must be 64-bit integer tensors")
+        _check_cuda("seeds", seeds, shape=(B,), device=dev)
+        _check_cuda("offsets", offsets, shape=(B,), device=dev)
+        if min_p is not None:
+            _check_cuda("min_p", min_p, torch.float32, (B,), dev)
+        self.out = torch.empty_like(q) if out is None else out
+        _check_cuda("out", self.out, q.dtype, q.shape, dev)
+        self.tokens = torch.empty(B, dtype=torch.int32, device=dev) if tokens is None else tokens
+        _check_cuda("tokens", self.tokens, torch.int32, (B,), dev)
+        lib = load_library()
+        need = int(lib.pkv_decode_workspace_bytes(B, Hq, D, 0))
+        self.workspace = (torch.empty(max(need, 16), dtype=torch.uint8, device=dev) if workspace is None
+                          else workspace)
+        _check_cuda("workspace", self.workspace, device=dev)
+        ws_bytes = self.workspace.numel() * self.workspace.element_size()
+        if ws_bytes < need:
+            raise ValueError(f"workspace holds {ws_bytes} bytes, the call needs {need}")
+        if status is not None:
+            _check_cuda("status", status, torch.int32, (1,), dev)
+        self.status = status
+        # keep every bound tensor referenced for the object's lifetime
+        self._keep = (q, k_new, v_new, k_cache, v_cache, block_tables, seq_lens, logits, temperature, top_k,
+                      top_p, seeds, offsets, min_p)
+        self._dev = dev
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        sp = ctypes.c_void_p(s.cuda_stream)
+        self._attn_fn = lib.pkv_paged_decode_attention_append
+        self._attn = [_ptr(self.out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                      _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B, Hq, Hkv, D, BS, NB,
+                      ctypes.c_float(float(scale)), _dtype_code(q), _ptr(self.workspace), ws_bytes,
+                      _ptr(status), sp]
+        if min_p is None:
+            self._samp_fn, self._samp_name = lib.pkv_sample_tokens, "pkv_sample_tokens"
+            self._samp = [_ptr(self.tokens), _ptr(logits), B, V, _ptr(temperature), _ptr(top_k), _ptr(top_p),
+                          _ptr(seeds), _ptr(offsets), None, 0, _ptr(status), sp]
+        else:
+            self._samp_fn, self._samp_name = lib.pkv_sample_tokens_ex, "pkv_sample_tokens_ex"
+            self._samp = [_ptr(self.tokens), _ptr(logits), B, V, _ptr(temperature), _ptr(top_k), _ptr(top_p),
+                          _ptr(min_p), _ptr(seeds), _ptr(offsets), _ptr(status), sp]
+
+    def set_stream(self, stream) -> None:
+        """Enqueue later steps on `stream` (a torch.cuda.Stream)."""
+        sp = ctypes.c_void_p(stream.cuda_stream)
+        self._attn[-1] = sp
+        self._samp[-1] = sp
+
+    def run_attention(self) -> torch.Tensor:
+        """The append and the attention only; returns out."""
+        code = self._attn_fn(*self._attn)
+        if code != 0:
+            raise PkvError("pkv_paged_decode_attention_append", code)
+        return self.out
+
+    def run_sampler(self) -> torch.Tensor:
+        """The sampler only; returns the tokens."""
+        code = self._samp_fn(*self._samp)
+        if code != 0:
+            raise PkvError(self._samp_name, code)
+        return self.tokens
+
+    def run(self) -> torch.Tensor:
+        """The whole step; returns the tokens."""
+        self.run_attention()
+        return self.run_sampler()
 
 
 def sample_tokens_typical(logits, temperature, typical_p, seeds, offsets, tokens=None, status=None):

@@ -32,7 +32,7 @@
 #include <cuda.h>
 #include <math.h>
 
-#include <mutex>
+#include <atomic>
 
 #include "pkv_common.cuh"
 
@@ -135,7 +135,7 @@ __global__ void __launch_bounds__((kFastMaxKvHeads + 1) * 32, 1)
                             int BS, int NB, float scale_log2, int nst, const int32_t* __restrict__ seq_lens,
                             SeqInfo* __restrict__ info, float* __restrict__ part_ml, float* __restrict__ part_o,
                             int32_t* status, const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
-                            uint4* kpool, uint4* vpool) {
+                            uint4* kpool, uint4* vpool, uint32_t max_polls, int silent_cta) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int R = Hkv * BS;
@@ -170,7 +170,11 @@ __global__ void __launch_bounds__((kFastMaxKvHeads + 1) * 32, 1)
         prefetch_tmap(&tmV);
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the predecessor's writes (KV, lengths) are visible
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the combine kernel may launch
+    // The combine kernel may launch now.  It reads seq_lens before its own
+    // griddepcontrol.wait, which is safe only because every CTA reaches this
+    // trigger after the wait above (no return before it): keep the trigger
+    // after the wait.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // ---- schedule: the blocks of all sequences in order, cut into gridDim.x
     // ranges of W; this CTA takes range blockIdx.x and finds the sequence that
@@ -221,7 +225,41 @@ __global__ void __launch_bounds__((kFastMaxKvHeads + 1) * 32, 1)
         // invalid sequences have no blocks and are stepped over
         int b = sch[33], cs = sch[34];
         int cn = seq_blocks(seq_lens, b, max_blocks, BS), cL = seq_lens[b];
+        // The combine kernel's view of every sequence whose first block lies
+        // in this range, written before any wait, so that it is complete even
+        // when a wait below gives up.
+        if (lane == 0) {
+            int bb = b, bs = cs, bn = cn;
+            while (bs < end) {
+                if (bs >= start && bn > 0) {
+                    SeqInfo si;
+                    si.s = bs;
+                    si.n = bn;
+                    si.W = W;
+                    si.pad = 0;
+                    info[bb] = si;
+                }
+                bs += bn;
+                if (++bb >= B) break;
+                bn = seq_blocks(seq_lens, bb, max_blocks, BS);
+            }
+        }
+        // Test hook (off unless pkv_test_set_wait_limit named this CTA): issue
+        // no copy at all, so that this CTA's consumers wait on stages nothing
+        // will fill, give up after max_polls polls and report PKV_ERR_TIMEOUT
+        // with no copy in flight.
+        if (static_cast<int>(blockIdx.x) == silent_cta) return;
         int piece = 0;
+        // On a timeout, wait (bounded) for the copies this lane issued that
+        // no consumer has seen land, so that the CTA never exits with a bulk
+        // copy still writing into its shared memory: the latest round of each
+        // stage (iterations it - nst .. it - 1) and of each query slot.
+        auto drain = [&](int it) {
+            for (int k = max(0, it - nst); k < it; ++k)
+                mbar_wait(&full[k % nst], static_cast<uint32_t>(k / nst) & 1u, max_polls);
+            for (int pk = max(0, piece - 2); pk < piece; ++pk)
+                mbar_wait(&qfull[pk & 1], static_cast<uint32_t>(pk >> 1) & 1u, max_polls);
+        };
         for (int i = start, it = 0; i < end; ++i, ++it) {
             while (cs + cn <= i) {
                 cs += cn;
@@ -254,24 +292,16 @@ __global__ void __launch_bounds__((kFastMaxKvHeads + 1) * 32, 1)
                 const bool last = (j == cn - 1) || (i == end - 1);
                 const bool whole = (cs >= start) && (cs + cn <= end);
                 const bool head = cs < start;  // began in an earlier range (set on every stage of the piece)
-                if (j == 0) {
-                    SeqInfo si;  // the combine kernel's view of this sequence
-                    si.s = cs;
-                    si.n = cn;
-                    si.W = W;
-                    si.pad = 0;
-                    info[b] = si;
-                }
                 const int stage = it % nst;
                 const uint32_t round = static_cast<uint32_t>(it / nst);
-                if (!mbar_wait(&empty[stage], (round & 1u) ^ 1u)) {
+                if (!mbar_wait(&empty[stage], (round & 1u) ^ 1u, max_polls)) {
                     report(status, PKV_ERR_TIMEOUT);
                     ok = 0;
                 }
                 if (ok && first) {
                     const int qs = piece & 1;
                     const uint32_t qr = static_cast<uint32_t>(piece >> 1);
-                    if (!mbar_wait(&qempty[qs], (qr & 1u) ^ 1u)) {
+                    if (!mbar_wait(&qempty[qs], (qr & 1u) ^ 1u, max_polls)) {
                         report(status, PKV_ERR_TIMEOUT);
                         ok = 0;
                     } else {
@@ -303,6 +333,7 @@ __global__ void __launch_bounds__((kFastMaxKvHeads + 1) * 32, 1)
                         mbar_arrive(fb);
                     }
                 }
+                if (!ok) drain(it);
             }
             if (!__shfl_sync(0xffffffffu, ok, 0)) return;  // a wait ran out: the whole warp leaves
         }
@@ -323,7 +354,7 @@ __global__ void __launch_bounds__((kFastMaxKvHeads + 1) * 32, 1)
     for (int i = start, it = 0; i < end; ++i, ++it) {
         const int stage = it % nst;
         const uint32_t round = static_cast<uint32_t>(it / nst);
-        if (!mbar_wait(&full[stage], round & 1u)) {
+        if (!mbar_wait(&full[stage], round & 1u, max_polls)) {
             if (lane == 0) report(status, PKV_ERR_TIMEOUT);
             return;
         }
@@ -331,7 +362,7 @@ __global__ void __launch_bounds__((kFastMaxKvHeads + 1) * 32, 1)
         if (mt.flags & kFirst) {
             const int qs = piece & 1;
             const uint32_t qr = static_cast<uint32_t>(piece >> 1);
-            if (!mbar_wait(&qfull[qs], qr & 1u)) {
+            if (!mbar_wait(&qfull[qs], qr & 1u, max_polls)) {
                 if (lane == 0) report(status, PKV_ERR_TIMEOUT);
                 return;
             }
@@ -545,7 +576,7 @@ template <typename T>
 __global__ void __launch_bounds__(kCombThreads)
     combine_warp_kernel(const SeqInfo* __restrict__ info, const int32_t* __restrict__ seq_lens, int max_blocks,
                         int BS, const float* __restrict__ part_ml, const float* __restrict__ part_o,
-                        T* __restrict__ out, int B, int Hq, int32_t* status) {
+                        T* __restrict__ out, int B, int Hq, int P, int32_t* status) {
     const int lane = threadIdx.x & 31;
     const long long u = static_cast<long long>(blockIdx.x) * kCombWarps + (threadIdx.x >> 5);
     if (u >= static_cast<long long>(B) * Hq) return;
@@ -561,8 +592,13 @@ __global__ void __launch_bounds__(kCombThreads)
     int pieces = 0, f = 0;
     if (n > 0) {
         const SeqInfo si = info[b];
-        f = si.s / si.W;
-        pieces = (si.s + n - 1) / si.W - f + 1;
+        if (si.W > 0 && si.s >= 0) {
+            f = si.s / si.W;
+            pieces = (si.s + n - 1) / si.W - f + 1;
+        }
+        // a record that names slots outside the workspace's 2P (possible only
+        // when the main kernel gave up on a wait) merges nothing
+        if (f + pieces > P) pieces = 0;
     }
     if (pieces == 1) return;
     T* o = out + static_cast<size_t>(u) * kDim + 4 * lane;
@@ -632,7 +668,7 @@ template <typename T>
 __global__ void __launch_bounds__(kCombThreads)
     combine_kernel(const SeqInfo* __restrict__ info, const int32_t* __restrict__ seq_lens, int max_blocks, int BS,
                    const float* __restrict__ part_ml, const float* __restrict__ part_o, T* __restrict__ out,
-                   int Hq, int32_t* status) {
+                   int Hq, int P, int32_t* status) {
     __shared__ float wsh[kCombMaxPieces];
     __shared__ float4 accsh[kCombWarps][32];
     __shared__ float red[2][kCombWarps];
@@ -647,8 +683,13 @@ __global__ void __launch_bounds__(kCombThreads)
     int pieces = 0, f = 0;
     if (n > 0) {
         const SeqInfo si = info[b];
-        f = si.s / si.W;
-        pieces = (si.s + n - 1) / si.W - f + 1;
+        if (si.W > 0 && si.s >= 0) {
+            f = si.s / si.W;
+            pieces = (si.s + n - 1) / si.W - f + 1;
+        }
+        // a record that names slots outside the workspace's 2P (possible only
+        // when the main kernel gave up on a wait) merges nothing
+        if (f + pieces > P) pieces = 0;
     }
     if (pieces == 1) return;  // uniform over the CTA
     T* o = out + (static_cast<size_t>(b) * Hq + qh) * kDim;
@@ -937,6 +978,11 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_cache
                              const int32_t* block_tables, int max_blocks, const int32_t* seq_lens, int B, int Hkv,
                              int D, int BS, int NB, pkv_dtype dtype, int32_t* status, cudaStream_t stream);
 
+// State of the failure-path test hook (pkv_test_set_wait_limit): the poll
+// budget of the fast kernel's waits and the CTA whose loader stays silent.
+static std::atomic<uint32_t> g_wait_polls{kMaxWaitIters};
+static std::atomic<int> g_silent_cta{-1};
+
 // k_new / v_new non-null: append each sequence's new token first (same result
 // as launch_kv_append followed by attention).  The fast kernel does the append
 // itself; every other case launches the append kernel before attention.
@@ -1000,7 +1046,8 @@ cudaError_t launch_decode_attention(void* out, const void* q, const void* k_cach
                              static_cast<const uint4*>(fused ? k_new : nullptr),
                              static_cast<const uint4*>(fused ? v_new : nullptr),
                              static_cast<uint4*>(const_cast<void*>(k_cache)),
-                             static_cast<uint4*>(const_cast<void*>(v_cache)));
+                             static_cast<uint4*>(const_cast<void*>(v_cache)), g_wait_polls.load(),
+                             g_silent_cta.load());
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t ccfg = {};
     ccfg.blockDim = dim3(kCombThreads, 1, 1);
@@ -1013,12 +1060,13 @@ cudaError_t launch_decode_attention(void* out, const void* q, const void* k_cach
         ccfg.gridDim = dim3(static_cast<unsigned>((units + kCombWarps - 1) / kCombWarps), 1, 1);
         err = cudaLaunchKernelEx(&ccfg, combine_warp_kernel<__nv_bfloat16>, static_cast<const SeqInfo*>(info),
                                  seq_lens, max_blocks, BS, static_cast<const float*>(part_ml),
-                                 static_cast<const float*>(part_o), static_cast<__nv_bfloat16*>(out), B, Hq, status);
+                                 static_cast<const float*>(part_o), static_cast<__nv_bfloat16*>(out), B, Hq, P,
+                                 status);
     } else {
         ccfg.gridDim = dim3(static_cast<unsigned>(units), 1, 1);
         err = cudaLaunchKernelEx(&ccfg, combine_kernel<__nv_bfloat16>, static_cast<const SeqInfo*>(info), seq_lens,
                                  max_blocks, BS, static_cast<const float*>(part_ml),
-                                 static_cast<const float*>(part_o), static_cast<__nv_bfloat16*>(out), Hq, status);
+                                 static_cast<const float*>(part_o), static_cast<__nv_bfloat16*>(out), Hq, P, status);
     }
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
@@ -1039,29 +1087,14 @@ namespace pkv {
 constexpr size_t kStaticScratchBytes = static_cast<size_t>(16) << 20;  // 16 MiB
 static __device__ __align__(256) uint8_t g_decode_scratch[kStaticScratchBytes];
 
-constexpr int kMaxDevices = 64;
-
-// Device address of g_decode_scratch on the current device, looked up once per
-// device (the host-side symbol is only a stand-in, never a device address).
+// Device address of g_decode_scratch on the current device.  Looked up on
+// every call (cheap once the module is loaded on the device): a cached address
+// would go stale when the device's context is reset or another context is
+// current, and the host-side symbol is only a stand-in, never a device address.
 static void* decode_scratch_address(cudaError_t* err) {
-    static std::mutex mu;
-    static void* addr[kMaxDevices] = {};
-    int dev = 0;
-    *err = cudaGetDevice(&dev);
-    if (*err != cudaSuccess) return nullptr;
-    if (dev < 0 || dev >= kMaxDevices) {
-        *err = cudaErrorInvalidDevice;
-        return nullptr;
-    }
-    std::lock_guard<std::mutex> lock(mu);
-    if (addr[dev] == nullptr) {
-        void* p = nullptr;
-        *err = cudaGetSymbolAddress(&p, g_decode_scratch);
-        if (*err != cudaSuccess) return nullptr;
-        addr[dev] = p;
-    }
-    *err = cudaSuccess;
-    return addr[dev];
+    void* p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_decode_scratch);
+    return *err == cudaSuccess ? p : nullptr;
 }
 
 }  // namespace pkv
@@ -1087,4 +1120,11 @@ extern "C" pkv_status pkv_paged_decode_attention_noalloc(void* out, const void* 
                                        Hkv, D, block_size, num_blocks, scale, dtype, ws, P, dev_status,
                                        static_cast<cudaStream_t>(stream), nullptr, nullptr, nullptr);
     return err == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" pkv_status pkv_test_set_wait_limit(uint32_t polls, int silent_cta) {
+    if (silent_cta < -1) return PKV_ERR_INVALID_ARG;
+    pkv::g_wait_polls.store(polls == 0 ? pkv::kMaxWaitIters : polls);
+    pkv::g_silent_cta.store(silent_cta);
+    return PKV_OK;
 }

@@ -1,4 +1,7 @@
 """Shared helpers for the GPU parity tests: host copies and oracle comparisons."""
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -69,3 +72,15 @@ def compare_tokens(tokens_gpu, s):
     return dict(rows=int(got.shape[0]), mismatches=int(mism.sum()), exempt_draw=int(draw_ex.sum()),
                 exempt_cut=int(cut_ex.sum()), exempt_mismatch=int((mism & exempt).sum()),
                 status=res["status"])
+
+
+def record(name: str, counts: dict) -> None:
+    """Append one JSON line of parity counts to the file named by the
+    PKV_PARITY_RECORD environment variable (no-op when it is unset)."""
+    path = os.environ.get("PKV_PARITY_RECORD")
+    if not path:
+        return
+    row = {"case": name}
+    row.update({k: (v.tolist() if isinstance(v, np.ndarray) else v) for k, v in counts.items() if k != "status"})
+    with open(path, "a") as f:
+        f.write(json.dumps(row) + "\n")

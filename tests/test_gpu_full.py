@@ -2,8 +2,11 @@
 
 Attention: every query head of the longest and the shortest sequence plus a
 seeded sample of (sequence, head) rows is recomputed by the float64 oracle.
-Sampler: every row is recomputed by the oracle.  KV append: the whole pools are
-compared bit for bit.
+Sampler: every row is recomputed by the oracle; a token may differ only where
+the oracle's draw or top-p cut lies within 1e-6 of an edge, and at most
+max(1, rows // 50) rows may.  KV append: the whole pools are compared bit for
+bit.  With PKV_PARITY_RECORD set, the per-workload counts (rows, mismatches,
+exempt draws and cuts) are appended to that file as JSON lines.
 """
 import numpy as np
 import pytest
@@ -12,7 +15,7 @@ import torch
 import oracle
 import paged_kv_decode_table_gb300 as pkv
 from paged_kv_decode_table_gb300 import workloads as W
-from tests.gpu_helpers import compare_attention, compare_tokens, host, run_attention, sampler_args
+from tests.gpu_helpers import compare_attention, compare_tokens, host, record, run_attention, sampler_args
 
 pytestmark = pytest.mark.gpu
 
@@ -37,7 +40,7 @@ def _sample_rows(w, seq_lens, n_random, seed):
     return np.array(sorted(rows), dtype=np.int64)
 
 
-@pytest.mark.parametrize("num,n_random", [(2, 256), (3, 96), (4, 512)])
+@pytest.mark.parametrize("num,n_random", [(1, 8), (2, 256), (3, 96), (4, 512)])
 def test_full_size_decode_step(num, n_random):
     w = W.workload(num)
     inp = W.make_decode_inputs(w, "cuda")
@@ -58,11 +61,14 @@ def test_full_size_decode_step(num, n_random):
     del Kh, Vh
     # attention on sampled rows
     rows = _sample_rows(w, inp["seq_lens"], n_random, seed=num)
-    err, n = compare_attention(out, inp, "bf16", rows=rows)
+    err, n = compare_attention(out, inp, "f32" if inp["q"].dtype == torch.float32 else "bf16", rows=rows)
     print(f"workload {num}: attention max |err| {err:.3e} over {n} rows")
     # sampler, every row
     c = compare_tokens(tok, inp)
     print(f"workload {num}: sampler {c}")
+    assert c["exempt_mismatch"] <= max(1, c["rows"] // 50)
+    record(f"workload {num} ({w.name}): sampler", c)
+    record(f"workload {num} ({w.name}): attention", {"rows_checked": n, "max_abs_err": err})
     if num == 3:
         # T = 1e-3 is greedy-equivalent: the token is the argmax of each row
         am = torch.argmax(inp["logits"], dim=1).to(torch.int32)
@@ -80,5 +86,5 @@ def test_full_size_sampler_stress():
     assert torch.equal(tok, tok2)
     c = compare_tokens(tok, s)
     print(f"sampler stress: {c}")
-    # peaked rows at k=1000/p<=0.95 etc. still draw the spike most of the time
-    assert c["exempt_mismatch"] <= 0.05 * c["rows"]
+    assert c["exempt_mismatch"] <= max(1, c["rows"] // 50)
+    record(f"workload 5 ({w.name}): sampler", c)

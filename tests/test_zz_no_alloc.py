@@ -6,16 +6,21 @@ tolerance for an allocation's implicit synchronisation, or a plain C host with
 no device allocator): its split-KV scratch is a fixed array inside the library.
 This test drives it through the C ABI twice in a row, with different batches so
 that the second call finds the first call's leftovers in the shared scratch, and
-compares each result with pkv_paged_decode_attention on the same inputs, within
-the bf16 attention tolerance the other parity tests use.  It also checks that a
-request needing more scratch than the array holds is refused without a launch.
+compares each result with pkv_paged_decode_attention on the same inputs: both
+run the same kernels with the same split, so the outputs must be identical bit
+for bit.  One case is also checked against the float64 oracle on sampled rows,
+within the bf16 attention tolerance of the other parity tests.  It also checks
+that a request needing more scratch than the array holds is refused without a
+launch.
 """
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
 import paged_kv_decode_table_gb300 as pkv
+from gpu_helpers import compare_attention
 from paged_kv_decode_table_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -64,8 +69,13 @@ def test_noalloc_matches_workspace_entry_point_twice(lib):
         assert code == 0, pkv.status_string(code)
         assert pkv.check_status(status) == 0
         assert torch.isfinite(out.float()).all()
+        assert torch.equal(out, ref)
         err = (out.float() - ref.float()).abs()
         assert bool((err <= ATOL + RTOL * ref.float().abs()).all()), float(err.max())
+    # the second case against the float64 oracle, 64 sampled (sequence, head) rows
+    B, Hq, _ = out.shape
+    rows = np.random.default_rng(0).choice(B * Hq, size=min(64, B * Hq), replace=False)
+    compare_attention(out, inp, "bf16", rows=np.sort(rows))
 
 
 def test_noalloc_refuses_requests_beyond_its_scratch(lib):
