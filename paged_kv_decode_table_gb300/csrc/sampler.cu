@@ -1513,9 +1513,21 @@ static SamplerPlan plan_sampler(int B, int V) {
     return make_plan(V, 1, false);  // more rows than resident CTAs: one CTA per row, in waves
 }
 
+int device_sm_count();
+bool sampler_rows_fits(int B, int V, int sms);
+cudaError_t launch_sampler_rows(int32_t* tokens, const float* logits, int B, int V, const float* temperature,
+                                const int32_t* top_k, const float* top_p, const float* min_p,
+                                const uint64_t* seeds, const uint64_t* offsets, int32_t* status,
+                                cudaStream_t stream);
+
 cudaError_t launch_sampler(int32_t* tokens, const float* logits, int B, int V, const float* temperature,
                            const int32_t* top_k, const float* top_p, const float* min_p, const uint64_t* seeds,
                            const uint64_t* offsets, int32_t* status, cudaStream_t stream) {
+    // more rows of a moderate vocabulary than this kernel keeps resident: one
+    // 256-thread CTA per row (sampler_rows.cu), every row at once
+    if (sampler_rows_fits(B, V, device_sm_count()))
+        return launch_sampler_rows(tokens, logits, B, V, temperature, top_k, top_p, min_p, seeds, offsets, status,
+                                   stream);
     const SamplerPlan sp = plan_sampler(B, V);
     cudaError_t err = cudaFuncSetAttribute(sampler_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(sp.smem));

@@ -1,0 +1,149 @@
+"""GPU parity of the sampler on batches with more rows than the cluster kernel
+keeps resident (B > 2 x #SM, V <= 65536): those take the one-CTA-per-row
+kernel (sampler_rows.cu).  Every row is compared with the float64 oracle: the
+same token unless the oracle's draw or top-p cut lies within 1e-6 of an edge
+(counted, at most max(1, B // 50)).  Rows cover greedy, top-k from 1 to past the
+finite count, top-p from 0.3 to 1, min-p, banned tokens, rows that are not
+16-byte aligned (odd vocabularies), windows too large for the gather (blocks of
+equal logits, which take the exact radix selection), and the error codes.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_decode_table_gb300 as pkv
+from gpu_helpers import EXEMPT
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from paged_kv_decode_table_gb300 import build
+    build.build()
+    pkv.load_library()
+
+
+def _rows():
+    return 2 * torch.cuda.get_device_properties(0).multi_processor_count + 16
+
+
+def _run(z, T, k, p, seeds, offs, min_p=None):
+    cu = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    st = pkv.new_status()
+    args = (cu(z), cu(T), cu(k), cu(p), cu(seeds.view(np.int64)), cu(offs.view(np.int64)))
+    tok = pkv.sample_tokens(*args, status=st, min_p=None if min_p is None else cu(min_p))
+    tok2 = pkv.sample_tokens(*args, min_p=None if min_p is None else cu(min_p))
+    torch.cuda.synchronize()
+    assert torch.equal(tok, tok2), "not deterministic"
+    return tok.cpu().numpy(), pkv.check_status(st)
+
+
+def _compare(z, T, k, p, seeds, offs, min_p=None, max_exempt=None):
+    got, st = _run(z, T, k, p, seeds, offs, min_p)
+    assert st == 0, pkv.status_string(st)
+    B = z.shape[0]
+    exempt = 0
+    for b in range(B):
+        r = oracle.sample_row(z[b], float(T[b]), int(k[b]), float(p[b]), int(seeds[b]), int(offs[b]),
+                              min_p=0.0 if min_p is None else float(min_p[b]))
+        assert r["status"] == 0
+        if got[b] != r["token"]:
+            assert r["draw_margin"] < EXEMPT or r["cut_margin"] < EXEMPT, (b, int(got[b]), r)
+            exempt += 1
+    assert exempt <= (max_exempt if max_exempt is not None else max(1, B // 50))
+    return exempt
+
+
+def _params(rng, B, V):
+    T = rng.uniform(0.5, 1.5, B).astype(np.float32)
+    T[::9] = 0.0
+    k = rng.choice([0, 0, 1, 5, 50, 1000, V - 1, V + 7], B).astype(np.int32)
+    p = rng.choice([0.3, 0.8, 0.95, 1.0], B).astype(np.float32)
+    seeds = rng.integers(0, 2**63, B).astype(np.uint64)
+    offs = rng.integers(0, 1000, B).astype(np.uint64)
+    return T, k, p, seeds, offs
+
+
+@pytest.mark.parametrize("V,seed", [(32000, 1), (1001, 2), (65536, 3), (4099, 4)])
+def test_rows_match_oracle(V, seed):
+    rng = np.random.default_rng(seed)
+    B = _rows()
+    z = (rng.standard_normal((B, V)) * rng.choice([0.1, 1.0, 1.5, 3.0], (B, 1))).astype(np.float32)
+    z[1::5, : V // 3] = -np.inf                                        # banned tokens
+    z[2::7, rng.integers(V)] += 12.0                                   # peaked rows
+    T, k, p, seeds, offs = _params(rng, B, V)
+    e = _compare(z, T, k, p, seeds, offs)
+    print(f"rows B={B} V={V}: exempt mismatches {e}")
+
+
+def test_rows_min_p():
+    rng = np.random.default_rng(7)
+    B, V = _rows(), 20000
+    z = (rng.standard_normal((B, V)) * 1.5).astype(np.float32)
+    T, k, p, seeds, offs = _params(rng, B, V)
+    mp = rng.choice([0.0, 0.05, 0.3, 0.9, 1.0], B).astype(np.float32)
+    _compare(z, T, k, p, seeds, offs, min_p=mp)
+
+
+def test_rows_large_windows_and_ties():
+    """Blocks of equal logits larger than the gather window (the exact radix
+    path), top-k boundaries inside a tie, single-logit rows, uniform rows."""
+    rng = np.random.default_rng(11)
+    B, V = _rows(), 6000
+    z = np.empty((B, V), np.float32)
+    T = np.full(B, 1.0, np.float32)
+    k = np.zeros(B, np.int32)
+    p = np.ones(B, np.float32)
+    for b in range(B):
+        kind = b % 6
+        if kind == 0:                       # uniform row: every bin holds all logits
+            z[b] = 0.5
+            p[b] = rng.choice([0.20013, 0.50021, 0.90007])   # p * V not near an integer
+        elif kind == 1:                     # two values; the cut inside the lower block of 5000
+            z[b] = -1.0
+            z[b, rng.permutation(V)[:1000]] = 0.0
+            p[b] = 0.9
+        elif kind == 2:                     # top-k boundary inside a block of ties
+            z[b] = rng.standard_normal(V).astype(np.float32)
+            z[b, rng.permutation(V)[:300]] = 2.5
+            k[b] = 120
+            p[b] = rng.choice([0.5, 1.0])
+        elif kind == 3:                     # a single finite logit
+            z[b] = -np.inf
+            z[b, rng.integers(V)] = 3.0
+            p[b] = 0.5
+        elif kind == 4:                     # top-k larger than the window, top-p off
+            z[b] = (rng.standard_normal(V) * 0.01).astype(np.float32)
+            k[b] = 4000
+        else:                               # greedy over ties: the lowest id
+            z[b] = rng.integers(-3, 3, V).astype(np.float32)
+            T[b] = 0.0
+    seeds = rng.integers(0, 2**63, B).astype(np.uint64)
+    offs = rng.integers(0, 1000, B).astype(np.uint64)
+    _compare(z, T, k, p, seeds, offs)
+
+
+def test_rows_errors():
+    rng = np.random.default_rng(5)
+    B, V = _rows(), 3000
+    z = rng.standard_normal((B, V)).astype(np.float32)
+    T = np.ones(B, np.float32)
+    k = np.zeros(B, np.int32)
+    p = np.full(B, 0.9, np.float32)
+    z[3, 17] = np.nan
+    z[4] = -np.inf
+    T[5] = -1.0
+    p[6] = 0.0
+    seeds = np.arange(B, dtype=np.uint64)
+    offs = np.zeros(B, np.uint64)
+    got, st = _run(z, T, k, p, seeds, offs)
+    assert st in (1, 6)
+    assert got[3] == -1 and got[4] == -1 and got[5] == -1 and got[6] == -1
+    ok = [b for b in range(B) if b not in (3, 4, 5, 6)]
+    ref = oracle.sample_batch(z[ok], T[ok], k[ok], p[ok], seeds[ok], offs[ok])
+    mism = (got[ok] != ref["tokens"]) & (ref["draw_margin"] >= EXEMPT) & (ref["cut_margin"] >= EXEMPT)
+    assert not mism.any()
