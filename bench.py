@@ -862,6 +862,38 @@ def run_typical_case(args):
     return 0
 
 
+def run_sampler_case(args):
+    """The sampler case its profiles are captured on: sample_tokens alone on the
+    logits of workload `--sampler-case` (2: 64 x 128256, T 0.7, top-k 50,
+    top-p 0.9; 4: 512 x 32000, T 1, top-p 0.95; 5: the 256 x 152064 stress
+    rows); `--warmup` untimed calls, then `--steps` timed ones (CUDA events on
+    the stream; the logits stay in L2 between calls when they fit)."""
+    import paged_kv_decode_table_gb300 as pkv
+    from paged_kv_decode_table_gb300 import build as pkv_build
+    pkv_build.build()
+    pkv.load_library()
+    dev = torch.device("cuda", 0)
+    w = W.workload(args.sampler_case)
+    si = W.make_sampler_inputs(w, dev)
+    tok = torch.empty(w.batch, dtype=torch.int32, device=dev)
+    st = pkv.new_status()
+    call = lambda: pkv.sample_tokens(si["logits"], si["temperature"], si["top_k"], si["top_p"], si["seeds"],
+                                     si["offsets"], tokens=tok, status=st)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    assert pkv.check_status(st) == 0
+    print(json.dumps({"case": f"sample_tokens {w.batch} x {w.vocab} ({w.name})", "calls": args.steps,
+                      "us_per_call": e0.elapsed_time(e1) / max(1, args.steps) * 1000}))
+    return 0
+
+
 def run_prefill_case(args):
     """The chunked-prefill case the prefill profile is captured on:
     `--prefill-seqs` sequences (default 4) with a 512-token chunk each after a
@@ -925,7 +957,11 @@ def main():
                     help="time the speculative-verification case of its profile (--warmup, --steps calls)")
     ap.add_argument("--typical-case", action="store_true",
                     help="time the typical-sampling case of the typical sampler profile (--warmup, --steps calls)")
+    ap.add_argument("--sampler-case", type=int, default=0, choices=[0, 2, 4, 5],
+                    help="time sample_tokens alone on the logits of workload 2, 4 or 5 (--warmup, --steps calls)")
     args = ap.parse_args()
+    if args.sampler_case:
+        return run_sampler_case(args)
     if args.prefill_case:
         return run_prefill_case(args)
     if args.typical_case:
