@@ -8,28 +8,34 @@
 // order with the request's Philox uniform, as in the sampler.
 //
 // With u_i = (z_i - zmax) log2(e) / T and ubar = sum_i p_i u_i one has
-// -ln p_i - H = ln 2 (ubar - u_i): the order by d is the order by |u_i - ubar|,
-// so the kept set is an interval of logits around the p-weighted mean.  The
-// order is a decision taken in floating point and is fixed in float32: ubar is
-// rounded to a multiple of 2^-8, u_i = (z_i - zmax) * c2 and
-// dk_i = |u_i - ubar| are each rounded on their own (no fused multiply-add),
-// ties in dk go to the larger u_i, then to the smaller id.  Masses are the
-// sampler's 2^-40 fixed-point weights floor(2^u * 2^40), so the cut and the
-// draw are exact integer arithmetic.
+// -ln p_i - H = ln 2 (ubar - u_i): the order by d is the order by
+// D_i = |u_i - ubar|, so the kept set is an interval of logits around the
+// p-weighted mean.  The order is taken on D in double: ubar from Kahan float
+// sums per thread (u with the scale log2(e) / T carried in two floats),
+// combined in double across threads and CTAs (about 1e-7 in log2 units on
+// vocabulary rows); u_i = (z_i - zmax) * log2(e) / T in double.  A float
+// estimate of D with a stated error bound places each logit, so only the
+// logits within that bound of a threshold compute D in double.  Equal D go to
+// the larger logit, then to the smaller id.  Masses are 2^-40 fixed-point
+// weights floor(2^u * 2^40), so the cut and the draw are exact integer
+// arithmetic (with typical_p >= 1 they are the sampler's masses, so the draw
+// is the sampler's).
 //
 // A row is spread over a cluster of 1-8 CTAs (as many as fill the GPU with
 // one CTA per SM), each sweeping one slice; per-CTA partials are combined in
 // rank order through distributed shared memory, so every CTA holds the same
 // results.  Passes over the slices (the first from HBM, the rest from L2):
-// maximum and finiteness; the mass sum S and the weighted sum of u (for
-// ubar); 2048 float bins linear in dk, summed over the cluster, which locate
-// the cut approximately; the logits of a window of bins around it pushed into
-// rank 0 (with the exact mass above the window), where they are sorted and
-// the cut found exactly; the draw (chunk sums of the kept masses, a scan over
-// the cluster, one chunk walked by the CTA holding the draw).  When the
-// window misses or overflows, rank 0 alone takes an exact radix select over
-// the whole row (11/11/10 bits of dk, then of u, then the rank in id order)
-// and draws.
+// maximum and finiteness; the mass sum S and the weighted sums for ubar; 2048
+// float bins linear in the estimate of D, summed over the cluster, which
+// locate the cut approximately; the logits of a window of bins around it
+// (window membership decided on D in double near its edges) pushed into
+// rank 0 with the exact mass before and inside the window, where they are
+// sorted by (D, larger logit, id) and the cut found exactly; the draw (chunk
+// sums of the kept masses, a scan over the cluster, one chunk walked by the
+// CTA holding the draw).  When the window overflows 2048 logits or misses
+// the cut, rank 0 alone takes an exact radix select over the window (the
+// whole row when it missed): the 64 bits of D, then the logit, then the rank
+// in id order, and draws.
 #include <cooperative_groups.h>
 #include <math.h>
 
@@ -437,7 +443,7 @@ __global__ void __launch_bounds__(kTyT, 1)
     }
     const float c2 = fminf(1.4426950408889634f / T, 1.0e30f);  // log2(e) / T, kept finite
     auto uof = [&](float x) { return __fmul_rn(__fsub_rn(x, mx), c2); };
-    // the fixed-point mass of a logit, as the sampler's (cut and draw)
+    // the fixed-point mass of a logit, as the sampler's (the untruncated draw)
     auto massof = [&](float x) { return fx40(hw_exp2(uof(x))); };
     // u with the scale log2(e) / T carried in two floats (chi + clo), for the
     // centre and the order; exact_only when that scale is beyond 1e30 (then
@@ -451,6 +457,8 @@ __global__ void __launch_bounds__(kTyT, 1)
         const float dz = __fsub_rn(x, mx);
         return __fmaf_rn(dz, chi, __fmul_rn(dz, clo));
     };
+    // the fixed-point mass of the truncated path, from the same u as the order
+    auto massc = [&](float x) { return fx40(hw_exp2(ucof(x))); };
     auto draw_x = [&](uint64_t tot) {  // floor(u * tot) < tot
         return static_cast<uint64_t>((static_cast<unsigned __int128>(sm->u53) * tot) >> 53);
     };
@@ -472,9 +480,9 @@ __global__ void __launch_bounds__(kTyT, 1)
     float ws = 0.f, wc = 0.f, us = 0.f, uc = 0.f;
     ty_sweep(zs, n, [&](int, float x) {
         if (!(x > -INFINITY)) return;
-        s += massof(x);
         const float u = ucof(x);
         const float w = hw_exp2(u);
+        s += fx40(w);
         if (w > 0.f) {
             kahan_add(ws, wc, w);
             kahan_add(us, uc, __fmul_rn(w, u));
@@ -598,9 +606,9 @@ __global__ void __launch_bounds__(kTyT, 1)
         if (!(x > -INFINITY)) return;
         const int w = where(x, Ed, Fd);
         if (w == 0) {
-            at += massof(x);
+            at += massc(x);
         } else if (w == 1) {
-            in += massof(x);
+            in += massc(x);
             const unsigned int slot = atomicAdd(nwin0, 1u);
             if (slot < static_cast<unsigned int>(kTyBins)) {
                 key0[slot] = static_cast<unsigned long long>(__double_as_longlong(dex(x)));
@@ -660,7 +668,7 @@ __global__ void __launch_bounds__(kTyT, 1)
                 }
             // cumulative mass in sorted order: thread t takes entries [2t, 2t + 2)
             auto wmass = [&](int j) -> uint64_t {
-                return j < static_cast<int>(nw) ? massof(key_float(~zkw[j])) : 0ull;
+                return j < static_cast<int>(nw) ? massc(key_float(~zkw[j])) : 0ull;
             };
             const int j0 = 2 * tid;
             const uint64_t w0 = wmass(j0), w1 = wmass(j0 + 1);
@@ -705,7 +713,7 @@ __global__ void __launch_bounds__(kTyT, 1)
         auto kh = [&](float x, int, uint32_t& k, uint64_t& m) -> bool {
             if (!inw(x)) return false;
             k = static_cast<uint32_t>(static_cast<unsigned long long>(__double_as_longlong(dex(x))) >> 32);
-            m = massof(x);
+            m = massc(x);
             return true;
         };
         const uint32_t a0 = ty_radix(z, V, sm, kh, 0u, 0, 21, 11, target, above);
@@ -717,7 +725,7 @@ __global__ void __launch_bounds__(kTyT, 1)
             const unsigned long long db = static_cast<unsigned long long>(__double_as_longlong(dex(x)));
             if (static_cast<uint32_t>(db >> 32) != dhi) return false;
             k = static_cast<uint32_t>(db);
-            m = massof(x);
+            m = massc(x);
             return true;
         };
         const uint32_t b0 = ty_radix(z, V, sm, kl, 0u, 0, 21, 11, target, above);
@@ -739,7 +747,7 @@ __global__ void __launch_bounds__(kTyT, 1)
             auto kz = [&](float x, int, uint32_t& k, uint64_t& m) -> bool {
                 if (!inw(x) || dex(x) != ds) return false;
                 k = ~okey(x);
-                m = massof(x);
+                m = massc(x);
                 return true;
             };
             const uint32_t e0 = ty_radix(z, V, sm, kz, 0u, 0, 21, 11, target, above);
@@ -748,7 +756,7 @@ __global__ void __launch_bounds__(kTyT, 1)
             zstar = (e0 << 21) | (e1 << 10) | e2;
         }
         // the cut among equal (D, logit) (equal masses): the r-th in id order
-        const uint64_t mstar = massof(key_float(~zstar));
+        const uint64_t mstar = massc(key_float(~zstar));
         const uint64_t need = target - above;
         const uint64_t r = mstar ? (need + mstar - 1) / mstar : 1ull;
         const uint32_t zs_ = zstar;
@@ -765,6 +773,7 @@ __global__ void __launch_bounds__(kTyT, 1)
         if (!(x > -INFINITY)) return 0ull;
         const float u = ucof(x);
         const float dk = dkf(u), e = errf(u);
+        auto mass_u = [&] { return fx40(hw_exp2(u)); };
         bool keep;
         if (dk < dsf - e) {
             keep = true;
@@ -775,7 +784,7 @@ __global__ void __launch_bounds__(kTyT, 1)
             const uint32_t k = ~okey(x);
             keep = D < ds || (D == ds && (k < zstar || (k == zstar && i <= idstar)));
         }
-        return keep ? massof(x) : 0ull;
+        return keep ? mass_u() : 0ull;
     };
     if (!found) {
         if (rank == 0) {
