@@ -584,6 +584,9 @@ def _time_calls(fn, n: int, flush=None):
         fn()
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    # a spin kernel ahead of the loop keeps the GPU busy while the host enqueues
+    # every call, so no event pair spans host time
+    torch.cuda._sleep(int(n * 400_000))
     for e0, e1 in ev:
         if flush is not None:
             flush()

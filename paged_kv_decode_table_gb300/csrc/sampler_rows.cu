@@ -48,6 +48,7 @@ constexpr int kRwCap = 2048;         // gathered window capacity
 constexpr int kRChunk = 128;         // ids per draw chunk
 constexpr int kRowMaxV = 65536;      // largest vocabulary this kernel serves
 constexpr int kRChunks = kRowMaxV / kRChunk;
+constexpr int kRSmallK = 64;         // top_k served by the thread-maxima path
 
 struct RowSmem {
     unsigned int cnt[kRBins];            // count per bin
@@ -60,7 +61,7 @@ struct RowSmem {
     float fv[kRW];
     int iv[kRW];
     unsigned int nwin;
-    unsigned int pad;
+    unsigned int nq;                     // threads whose maximum is a candidate (small top-k)
     unsigned long long u53;
 };
 
@@ -299,7 +300,10 @@ __global__ void __launch_bounds__(kRT, 4)
         sm->mlo[i] = 0u;
     }
     for (int i = tid; i < kRChunks; i += kRT) sm->csum[i] = 0ull;
-    if (tid == 0) sm->nwin = 0u;
+    if (tid == 0) {
+        sm->nwin = 0u;
+        sm->nq = 0u;
+    }
     __syncthreads();
     float zmax = -INFINITY, zmin = INFINITY;
     unsigned int gbad = 0u, nfin = 0u;
@@ -348,6 +352,123 @@ __global__ void __launch_bounds__(kRT, 4)
         return t < static_cast<float>(kRBins - 1) ? __float_as_int(__fadd_rd(t, 8388608.0f)) - 0x4B000000
                                                   : kRBins - 1;
     };
+
+    // ---- small top-k (0 < kk <= kRSmallK): only the kk largest logits
+    // matter.  Bin b* is the first where the count of thread maxima (pass A)
+    // from the top reaches kk: at least kk logits lie in bins <= b*, and the
+    // binning is monotone, so the top kk all lie there.  Only threads whose
+    // maximum lies there can hold such a logit; their slots are read again
+    // (L2), spread over the CTA, and every logit in bins <= b* is kept as a
+    // sort key.  Each key's rank is the number of larger keys; the first kk in
+    // rank order get their masses, top-p keeps the prefix whose mass before
+    // the entry is below ceil(top_p * S_k), min-p drops masses below its
+    // threshold, and the token whose interval in id order holds
+    // X = floor(u * S_p) is drawn.  More than kRT candidates (a block of equal
+    // logits) take the general path below.
+    if (kk && kk <= kRSmallK) {
+        constexpr int kPerS = kRBins / kRT;
+        if (mx > -INFINITY) atomicAdd(&sm->cnt[bin(mx)], 1u);
+        if (tid == 0) sm->bc[0] = kRBins - 1;  // fewer than kk finite maxima: every finite logit
+        __syncthreads();
+        uint64_t tc = 0;
+        for (int q = 0; q < kPerS; ++q) tc += sm->cnt[kPerS * tid + q];
+        uint64_t ctot;
+        const uint64_t cex = rw_excl_scan(tc, sm, ctot);
+        const uint64_t kq = static_cast<uint64_t>(kk);
+        if (cex < kq && cex + tc >= kq) {
+            uint64_t cc = cex;
+            for (int q = 0; q < kPerS; ++q) {
+                const uint64_t c1 = sm->cnt[kPerS * tid + q];
+                if (cc < kq && cc + c1 >= kq) sm->bc[0] = static_cast<unsigned long long>(kPerS * tid + q);
+                cc += c1;
+            }
+        }
+        __syncthreads();
+        const int bstar = static_cast<int>(sm->bc[0]);
+        auto cand = [&](float x) { return x > -INFINITY && bin(x) <= bstar; };
+        unsigned int* qlist = sm->mhi;
+        if (cand(mx)) qlist[atomicAdd(&sm->nq, 1u)] = static_cast<unsigned int>(tid);
+        __syncthreads();
+        const int nq = static_cast<int>(sm->nq);
+        const int nvec = (V + 3) & ~3;
+        const int spt = (nvec + 4 * kRT - 1) / (4 * kRT);  // slots per thread
+        const int nwork = nq * spt;
+        for (int i0 = 0; i0 < nwork; i0 += 4 * kRT) {
+            float4 qv[4];
+            int ev[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {  // every load issued (slot 0 for idle lanes) before any is used
+                const int i = i0 + u * kRT + tid;
+                const int ic = i < nwork ? i : 0;
+                const int qi = ic / spt;
+                const int e = 4 * (static_cast<int>(qlist[qi]) + kRT * (ic - qi * spt));
+                ev[u] = (i < nwork && e < nvec) ? e : -1;
+                qv[u] = rw_load4(z, V, ev[u] >= 0 ? ev[u] : 0, a16);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float x = rw_at(qv[u], j);
+                    if (ev[u] >= 0 && cand(x)) {
+                        const unsigned int pos = atomicAdd(&sm->nwin, 1u);
+                        if (pos < static_cast<unsigned int>(kRwCap)) sm->win[pos] = sort_key(x, ev[u] + j);
+                    }
+                }
+        }
+        __syncthreads();
+        const int nl = static_cast<int>(sm->nwin);
+        if (nl <= kRT) {
+            unsigned long long* buf = sm->csum;        // the top kk keys in rank order
+            unsigned long long* kwm = sm->csum + kRSmallK;  // their kept masses
+            if (tid < nl) {
+                const unsigned long long key = sm->win[tid];
+                int rr = 0;
+                for (int jj = 0; jj < nl; ++jj) rr += sm->win[jj] > key ? 1 : 0;
+                if (rr < kk) buf[rr] = key;
+            }
+            __syncthreads();
+            // four threads per entry i = tid / 4 (strided sums, reduced over the four lanes)
+            const int i = tid >> 2, part = tid & 3;
+            auto wof = [&](int jj) { return mass(key_float(static_cast<uint32_t>(buf[jj] >> 32)), zmax, c2); };
+            uint64_t before = 0, sk = 0;
+            for (int jj = part; jj < kk; jj += 4) {
+                const uint64_t w = wof(jj);
+                sk += w;
+                before += jj < i ? w : 0ull;
+            }
+            sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+            sk += __shfl_xor_sync(0xffffffffu, sk, 2);
+            before += __shfl_xor_sync(0xffffffffu, before, 1);
+            before += __shfl_xor_sync(0xffffffffu, before, 2);
+            const uint64_t Wi = i < kk ? wof(i) : 0ull;
+            const bool kept = i < kk && (!(pp < 1.f) || before < ceil_mul_p(pp, sk)) && Wi >= mth;
+            const uint64_t kw = kept ? Wi : 0ull;
+            if (part == 0 && i < kk) kwm[i] = kw;
+            __syncthreads();
+            const uint32_t idi = i < kk ? static_cast<uint32_t>(sort_key_id(buf[i])) : 0xffffffffu;
+            uint64_t bl = 0, sp = 0;  // kept mass at smaller ids; the kept total
+            for (int jj = part; jj < kk; jj += 4) {
+                const uint64_t w = kwm[jj];
+                sp += w;
+                bl += static_cast<uint32_t>(sort_key_id(buf[jj])) < idi ? w : 0ull;
+            }
+            sp += __shfl_xor_sync(0xffffffffu, sp, 1);
+            sp += __shfl_xor_sync(0xffffffffu, sp, 2);
+            bl += __shfl_xor_sync(0xffffffffu, bl, 1);
+            bl += __shfl_xor_sync(0xffffffffu, bl, 2);
+            const uint64_t X = static_cast<uint64_t>((static_cast<unsigned __int128>(sm->u53) * sp) >> 53);
+            if (part == 0 && kw > 0 && bl <= X && X < bl + kw) *tok_out = static_cast<int32_t>(idi);
+            return;
+        }
+        // a block of equal logits: back to the general path with clean bins
+        for (int i = tid; i < kRBins; i += kRT) {
+            sm->cnt[i] = 0u;
+            sm->mhi[i] = 0u;
+        }
+        if (tid == 0) sm->nwin = 0u;
+        __syncthreads();
+    }
 
     // ---- B: count and exact mass per bin, as 32-bit sums of the mass's high
     // (>> 20) and low 20 bits: both stay below 2^32 while a bin holds fewer

@@ -147,3 +147,44 @@ def test_rows_errors():
     ref = oracle.sample_batch(z[ok], T[ok], k[ok], p[ok], seeds[ok], offs[ok])
     mism = (got[ok] != ref["tokens"]) & (ref["draw_margin"] >= EXEMPT) & (ref["cut_margin"] >= EXEMPT)
     assert not mism.any()
+
+
+@pytest.mark.parametrize("V,seed", [(32000, 31), (4099, 32)])
+def test_rows_small_top_k(V, seed):
+    """Rows with 0 < top_k <= 64 take the thread-maxima path (candidates from
+    the threads whose maximum can be in the top k): plain and peaked rows,
+    min-p, top-k 1 and 64, a top-k boundary inside a block of 60 equal logits,
+    blocks of 300 equal top logits (more candidates than threads: the general
+    path), few finite logits, and -0.0 / +0.0 ties."""
+    rng = np.random.default_rng(seed)
+    B = _rows()
+    z = (rng.standard_normal((B, V)) * rng.choice([0.1, 1.0, 2.0], (B, 1))).astype(np.float32)
+    T = rng.uniform(0.3, 2.0, B).astype(np.float32)
+    k = rng.choice([1, 2, 17, 50, 63, 64], B).astype(np.int32)
+    # top_p * (number of equal masses) never an integer: no cut exactly at p
+    p = rng.choice([0.50021, 0.90007, 1.0], B).astype(np.float32)
+    mp = np.where(rng.random(B) < 0.3, rng.choice([0.01, 0.2, 0.7], B), 0.0).astype(np.float32)
+    for b in range(B):
+        kind = b % 7
+        if kind == 1:
+            z[b, rng.integers(V)] += 12.0
+        elif kind == 2:                         # boundary inside a block of 60 equal logits
+            z[b, rng.permutation(V)[:60]] = 9.0
+            z[b, rng.permutation(V)[:20]] = 9.5
+            k[b] = 50
+        elif kind == 3:                         # 300 equal top logits
+            z[b, rng.permutation(V)[:300]] = 9.0
+            k[b] = rng.choice([1, 64])
+        elif kind == 4:                         # 40 finite logits
+            z[b] = -np.inf
+            z[b, rng.permutation(V)[:40]] = rng.standard_normal(40).astype(np.float32)
+            k[b] = rng.choice([5, 39])
+        elif kind == 5:                         # -0.0 and +0.0 on top
+            z[b] = np.minimum(z[b], -3.0)
+            z[b, rng.permutation(V)[:25]] = -0.0
+            z[b, rng.permutation(V)[:25]] = 0.0
+            k[b] = 30
+    seeds = rng.integers(0, 2**63, B).astype(np.uint64)
+    offs = rng.integers(0, 1000, B).astype(np.uint64)
+    _compare(z, T, k, p, seeds, offs)
+    _compare(z, T, k, p, seeds, offs, min_p=mp)
