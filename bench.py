@@ -638,9 +638,12 @@ def run_extras(args):
         del inp, out, ws
         torch.cuda.empty_cache()
 
-    for num, label in ((2, "T0.7 k50 p0.9"), (4, "T1.0 p0.95"), (5, "stress: mixed T / k / p")):
+    for num, label, topk in ((2, "T0.7 k50 p0.9", None), (4, "T1.0 p0.95", None), (4, "T1.0 k50 p0.95", 50),
+                             (5, "stress: mixed T / k / p", None)):
         w = W.workload(num)
         si = W.make_sampler_inputs(w, dev)
+        if topk is not None:
+            si["top_k"].fill_(topk)
         tok = torch.empty(w.batch, dtype=torch.int32, device=dev)
         t = _time_calls(lambda: pkv.sample_tokens(si["logits"], si["temperature"], si["top_k"], si["top_p"],
                                                   si["seeds"], si["offsets"], tokens=tok), 50, flush=flush)
@@ -869,8 +872,9 @@ def run_sampler_case(args):
     """The sampler case its profiles are captured on: sample_tokens alone on the
     logits of workload `--sampler-case` (2: 64 x 128256, T 0.7, top-k 50,
     top-p 0.9; 4: 512 x 32000, T 1, top-p 0.95; 5: the 256 x 152064 stress
-    rows); `--warmup` untimed calls, then `--steps` timed ones (CUDA events on
-    the stream; the logits stay in L2 between calls when they fit)."""
+    rows; `--sampler-top-k K` sets every row's top-k to K); `--warmup` untimed
+    calls, then `--steps` timed ones (CUDA events on the stream; the logits
+    stay in L2 between calls when they fit)."""
     import paged_kv_decode_table_gb300 as pkv
     from paged_kv_decode_table_gb300 import build as pkv_build
     pkv_build.build()
@@ -878,6 +882,8 @@ def run_sampler_case(args):
     dev = torch.device("cuda", 0)
     w = W.workload(args.sampler_case)
     si = W.make_sampler_inputs(w, dev)
+    if args.sampler_top_k is not None:
+        si["top_k"].fill_(args.sampler_top_k)
     tok = torch.empty(w.batch, dtype=torch.int32, device=dev)
     st = pkv.new_status()
     call = lambda: pkv.sample_tokens(si["logits"], si["temperature"], si["top_k"], si["top_p"], si["seeds"],
@@ -892,7 +898,8 @@ def run_sampler_case(args):
     e1.record()
     torch.cuda.synchronize()
     assert pkv.check_status(st) == 0
-    print(json.dumps({"case": f"sample_tokens {w.batch} x {w.vocab} ({w.name})", "calls": args.steps,
+    topk = "" if args.sampler_top_k is None else f", top-k {args.sampler_top_k}"
+    print(json.dumps({"case": f"sample_tokens {w.batch} x {w.vocab} ({w.name}){topk}", "calls": args.steps,
                       "us_per_call": e0.elapsed_time(e1) / max(1, args.steps) * 1000}))
     return 0
 
@@ -962,6 +969,7 @@ def main():
                     help="time the typical-sampling case of the typical sampler profile (--warmup, --steps calls)")
     ap.add_argument("--sampler-case", type=int, default=0, choices=[0, 2, 4, 5],
                     help="time sample_tokens alone on the logits of workload 2, 4 or 5 (--warmup, --steps calls)")
+    ap.add_argument("--sampler-top-k", type=int, default=None, help="with --sampler-case: every row's top-k")
     args = ap.parse_args()
     if args.sampler_case:
         return run_sampler_case(args)

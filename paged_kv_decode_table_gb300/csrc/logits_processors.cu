@@ -10,7 +10,9 @@
 //
 // One kernel, two kinds of CTA per row: mask CTAs each take 256 words of the
 // row's bitmask (8192 logits) and write -inf where a bit is clear (the logits
-// are not read); one penalty CTA walks the row's (token, count) list.  A
+// are not read; each warp reads 32 words, then per word its 32 lanes store the
+// word's 32 logits as one coalesced 128-byte masked store); one penalty CTA
+// walks the row's (token, count) list.  A
 // penalised token is skipped when its mask bit is clear or its logit is not
 // finite, so the two kinds write disjoint elements and need no ordering.  The
 // penalty arithmetic is double precision, each operation rounded on its own (no
@@ -38,14 +40,20 @@ __global__ void __launch_bounds__(kProcThreads)
     const int words = (V + 31) / 32;
     const uint32_t* mrow = mask ? mask + static_cast<size_t>(b) * words : nullptr;
     if (part < mask_ctas) {
-        const int w = part * kMaskWordsPerCta + threadIdx.x;
-        if (!mrow || w >= words) return;
-        const uint32_t bits = mrow[w];
-        if (bits == 0xffffffffu) return;
-        const int i0 = 32 * w;
-#pragma unroll 4
-        for (int j = 0; j < 32; ++j)
-            if (!((bits >> j) & 1u) && i0 + j < V) z[i0 + j] = -INFINITY;
+        if (!mrow) return;
+        const int lane = threadIdx.x & 31;
+        const int w0 = part * kMaskWordsPerCta + (threadIdx.x & ~31);  // the warp's first word
+        if (w0 >= words) return;                                        // warp-uniform
+        const int w = w0 + lane;
+        const uint32_t mine = w < words ? mrow[w] : 0xffffffffu;
+        uint32_t todo = __ballot_sync(0xffffffffu, mine != 0xffffffffu);  // words with a clear bit
+        while (todo) {
+            const int j = __ffs(todo) - 1;
+            todo &= todo - 1u;
+            const uint32_t bits = __shfl_sync(0xffffffffu, mine, j);
+            const int i = 32 * (w0 + j) + lane;
+            if (!((bits >> lane) & 1u) && i < V) z[i] = -INFINITY;
+        }
         return;
     }
     if (!row_ptr) return;
