@@ -516,13 +516,10 @@ def measure_per_config(pkv, dev, calls: int = 30):
     the attention call with the append on the long-context (B 8, 64/8 heads,
     L 32K..128K) and fragmented batch-512 workloads, whose 2.7 GB and 1.2 GB of
     KV exceed L2, and the sampler alone on the batch-64, batch-512 and stress
-    workloads with L2 flushed (a 256 MB write) before every call.  Fractions are
+    workloads with L2 flushed (a 256 MB write, then a 256 MB read) before every call.  Fractions are
     of the measured copy peak and of 8 TB/s."""
     peak, _ = _peaks()
-    scratch = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-
-    def flush():
-        scratch.fill_(1)
+    flush = _l2_flusher(dev)
 
     def stats(fn, flush_fn=None):
         t = _time_calls(fn, calls, flush=flush_fn)
@@ -567,7 +564,7 @@ def measure_per_config(pkv, dev, calls: int = 30):
             "algorithmic_bytes": by, "median_us": t["median_us"], "mean_us": t["mean_us"], "p90_us": t["p90_us"],
             "calls": calls, "tokens_per_s": w.batch / (t["median_us"] * 1e-6), "GB/s": gbs,
             "frac_of_measured": gbs / peak, "frac_of_8TBps": gbs / 8000.0,
-            "l2": "flushed before every call (256 MB write outside the events)"}
+            "l2": "flushed before every call (256 MB write, then 256 MB read of another buffer, outside the events)"}
         del si
         torch.cuda.empty_cache()
     del scratch
@@ -576,6 +573,20 @@ def measure_per_config(pkv, dev, calls: int = 30):
 
 
 # ---------------------------------------------------------------- extra measurements
+def _l2_flusher(dev):
+    """L2 flush run before every timed call, outside the events: a 256 MB
+    write (larger than the 126 MB L2), then a 256 MB read of another buffer, so
+    that the dirty lines the write leaves are written back here rather than
+    inside the next timed call."""
+    wbuf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    rbuf = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+
+    def flush():
+        wbuf.fill_(1)
+        rbuf.sum()
+    return flush
+
+
 def _time_calls(fn, n: int, flush=None):
     """Per-call device times (us) with CUDA events on the current stream; when
     `flush` is given it runs before every call, outside the events (L2 flush)."""
@@ -614,10 +625,7 @@ def run_extras(args):
     peak, _ = _peaks()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    scratch = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-
-    def flush():
-        scratch.fill_(1)
+    flush = _l2_flusher(dev)
 
     def emit(d):
         print(json.dumps(d), flush=True)
