@@ -344,6 +344,11 @@ def run_gpu(args):
     clocks.start()
     _barrier(world)
     torch.cuda.synchronize()
+    # a spin kernel (about 15 us of GPU time per step, outside the events) while
+    # the host enqueues the K steps, so that the timed region holds the steps'
+    # device time and no wait for the host's first launches (a serving loop
+    # keeps the host ahead of the GPU the same way)
+    torch.cuda._sleep(int(min(args.steps, 4000) * 30_000))
     t0.record(stream)
     for i in range(args.steps):
         step()
@@ -567,7 +572,7 @@ def measure_per_config(pkv, dev, calls: int = 30):
             "l2": "flushed before every call (256 MB write, then 256 MB read of another buffer, outside the events)"}
         del si
         torch.cuda.empty_cache()
-    del scratch
+    del flush
     torch.cuda.empty_cache()
     return res
 
