@@ -805,6 +805,58 @@ __device__ void fallback_select_and_draw(Ctx& c, const View& v, Keep& kp, bool v
     draw_pass(c, v, kp, vec, zmax, c2, tok_out);
 }
 
+// ------------------------------------------------------------------ row order
+// The row a CTA takes when the launch has one CTA per row and more rows than
+// SMs: the rows with the most work get the lowest CTA indices.  The hardware
+// places the first #SM CTAs one per SM and the later ones beside them, so two
+// heavy rows rarely share an SM (longest-processing-time-first order; the
+// tokens do not depend on it).  Classes: 2 = top-p alone (the cut and a draw
+// over a long kept prefix), 1 = top-k above kRegTopk or no truncation,
+// 0 = greedy, small top-k or invalid parameters; order: class descending, row
+// index ascending.  Counts per class travel packed in 21-bit fields of one
+// block-wide scan (B < 2^21).
+__device__ int lpt_row(int B, int V, const float* __restrict__ temperature, const int32_t* __restrict__ top_k,
+                       const float* __restrict__ top_p, SampSmem* sm) {
+    const int tid = threadIdx.x;
+    constexpr uint64_t kF = (1ull << 21) - 1ull;
+    auto cls = [&](int r) -> int {
+        const float t = temperature[r];
+        const int k = top_k[r];
+        if (!(t > 0.f)) return 0;
+        const bool k_on = k > 0 && k < V;
+        if (k_on && k <= kRegTopk) return 0;
+        if (!k_on && top_p[r] < 1.f) return 2;
+        return 1;
+    };
+    uint64_t tot = 0;
+    for (int r0 = 0; r0 < B; r0 += kST) {
+        const int r = r0 + tid;
+        uint64_t t;
+        block_excl_scan_u64(r < B ? (1ull << (21 * cls(r))) : 0ull, sm->wsum, t);
+        tot += t;
+    }
+    const uint64_t n2 = (tot >> 42) & kF, n1 = (tot >> 21) & kF;
+    if (tid == 0) sm->bc[7] = 0ull;
+    __syncthreads();
+    uint64_t run = 0;
+    for (int r0 = 0; r0 < B; r0 += kST) {
+        const int r = r0 + tid;
+        const int c = r < B ? cls(r) : 0;
+        uint64_t t;
+        const uint64_t ex = block_excl_scan_u64(r < B ? (1ull << (21 * c)) : 0ull, sm->wsum, t);
+        if (r < B) {
+            const uint64_t base = c == 2 ? 0ull : (c == 1 ? n2 : n2 + n1);
+            const uint64_t pos = base + (((run + ex) >> (21 * c)) & kF);
+            if (pos == blockIdx.x) sm->bc[7] = static_cast<unsigned long long>(r);
+        }
+        run += t;
+    }
+    __syncthreads();
+    const int row = static_cast<int>(sm->bc[7]);
+    __syncthreads();
+    return row;
+}
+
 // ------------------------------------------------------------------ kernel
 constexpr int kLoadChunks = 4;
 
@@ -812,7 +864,8 @@ __global__ void __launch_bounds__(kST, 2)
     sampler_kernel(int32_t* __restrict__ tokens, const float* __restrict__ logits, int V, int S, int smem_slice,
                    const float* __restrict__ temperature, const int32_t* __restrict__ top_k,
                    const float* __restrict__ top_p, const float* __restrict__ min_p,
-                   const uint64_t* __restrict__ seeds, const uint64_t* __restrict__ offsets, int32_t* status) {
+                   const uint64_t* __restrict__ seeds, const uint64_t* __restrict__ offsets, int32_t* status,
+                   int lpt_B) {
     extern __shared__ __align__(16) uint8_t samp_smem_raw[];
     SampSmem* sm = reinterpret_cast<SampSmem*>(samp_smem_raw);
     float* zslice = reinterpret_cast<float*>(samp_smem_raw + sizeof(SampSmem));
@@ -823,7 +876,11 @@ __global__ void __launch_bounds__(kST, 2)
     c.rank = static_cast<int>(cluster.block_rank());
     c.xb = 0;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int row = blockIdx.x / c.nc;
+    // launched as a programmatic dependent: the row parameters and the logits
+    // are read only after the predecessor grid has finished
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int row = lpt_B ? lpt_row(lpt_B, V, temperature, top_k, top_p, sm) : static_cast<int>(blockIdx.x) / c.nc;
     const int lo = c.rank * S;
     const int n = max(0, min(S, V - lo));
     const float* grow = logits + static_cast<size_t>(row) * V + lo;
@@ -837,10 +894,6 @@ __global__ void __launch_bounds__(kST, 2)
     v.g16 = (reinterpret_cast<uintptr_t>(grow) & 15u) == 0;
     const bool vec = smem_slice != 0;
 
-    // launched as a programmatic dependent: the logits are read only after the
-    // predecessor grid has finished
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // row parameters first: they decide what the passes must track
     const float T = temperature[row];
     const float pp = top_p[row];
@@ -1525,10 +1578,13 @@ cudaError_t launch_sampler(int32_t* tokens, const float* logits, int B, int V, c
                            const uint64_t* offsets, int32_t* status, cudaStream_t stream) {
     // more rows of a moderate vocabulary than this kernel keeps resident: one
     // 256-thread CTA per row (sampler_rows.cu), every row at once
-    if (sampler_rows_fits(B, V, device_sm_count()))
+    const int sms = device_sm_count();
+    if (sampler_rows_fits(B, V, sms))
         return launch_sampler_rows(tokens, logits, B, V, temperature, top_k, top_p, min_p, seeds, offsets, status,
                                    stream);
     const SamplerPlan sp = plan_sampler(B, V);
+    // one CTA per row with more rows than SMs: heaviest rows first
+    const int lpt_B = (sp.nc == 1 && B > sms && B < (1 << 21)) ? B : 0;
     cudaError_t err = cudaFuncSetAttribute(sampler_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(sp.smem));
     if (err != cudaSuccess) return err;
@@ -1547,7 +1603,7 @@ cudaError_t launch_sampler(int32_t* tokens, const float* logits, int B, int V, c
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, sampler_kernel, tokens, logits, V, sp.S, sp.smem_slice, temperature, top_k,
-                              top_p, min_p, seeds, offsets, status);
+                              top_p, min_p, seeds, offsets, status, lpt_B);
 }
 
 }  // namespace pkv
