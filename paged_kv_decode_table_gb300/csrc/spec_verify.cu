@@ -39,6 +39,8 @@ namespace pkv {
 constexpr int kVT = 512;             // threads per CTA
 constexpr int kVW = kVT / 32;
 constexpr int kDrawChunks = 2048;    // chunk sums kept in shared memory
+constexpr int kSS = 256;             // threads per CTA of the row statistics (four CTAs per SM)
+constexpr int kSSW = kSS / 32;
 
 struct RowStat {   // 32 bytes per logits row
     float zmax;
@@ -59,6 +61,7 @@ __device__ __forceinline__ float4 load4_row(const float* row, int e, int n, bool
     return q;
 }
 
+template <int W>
 __device__ __forceinline__ double block_sum_f64(double v, double* red) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -66,21 +69,23 @@ __device__ __forceinline__ double block_sum_f64(double v, double* red) {
     if (lane == 0) red[warp] = v;
     __syncthreads();
     double t = 0.0;
-    for (int w = 0; w < kVW; ++w) t += red[w];
+    for (int w = 0; w < W; ++w) t += red[w];
     __syncthreads();
     return t;
 }
 
 // ------------------------------------------------------------------ row statistics
 // Row r of request b: r < gamma + 1 is target row r, else draft row r - gamma - 1.
-__global__ void __launch_bounds__(kVT)
+// One 256-thread CTA per row, four per SM, so that a batch of up to 4 x #SM rows
+// (64 requests with 4 drafts: 576) streams in one wave.
+__global__ void __launch_bounds__(kSS, 4)
     spec_stats_kernel(const float* __restrict__ target, const float* __restrict__ draft, int gamma, int V,
                       const float* __restrict__ temperature, RowStat* __restrict__ stats) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    __shared__ float smax[kVW];
-    __shared__ int sid[kVW], sbad[kVW];
-    __shared__ double dred[kVW];
+    __shared__ float smax[kSSW];
+    __shared__ int sid[kSSW], sbad[kSSW];
+    __shared__ double dred[kSSW];
     const int rows = 2 * gamma + 1;
     const int b = blockIdx.x / rows, r = blockIdx.x - (blockIdx.x / rows) * rows;
     const float* row = r <= gamma ? target + (static_cast<size_t>(b) * (gamma + 1) + r) * V
@@ -100,10 +105,10 @@ __global__ void __launch_bounds__(kVT)
     int id = INT_MAX;
     int bad = 0;
     float ks = 0.f, kc = 0.f;  // the sum and its running compensation
-    for (int e0 = 4 * tid; e0 < V; e0 += 4 * kVT * kU) {
+    for (int e0 = 4 * tid; e0 < V; e0 += 4 * kSS * kU) {
         float4 q[kU];
 #pragma unroll
-        for (int u = 0; u < kU; ++u) q[u] = load4_row(row, e0 + 4 * kVT * u, V, al);
+        for (int u = 0; u < kU; ++u) q[u] = load4_row(row, e0 + 4 * kSS * u, V, al);
         float bm = -INFINITY;
         int bid = INT_MAX;
 #pragma unroll
@@ -114,7 +119,7 @@ __global__ void __launch_bounds__(kVT)
                 bad |= (zz[j] < INFINITY) ? 0 : 1;  // NaN or +inf (slots past V read -inf)
                 if (zz[j] > bm) {                   // ids grow within a batch: first max wins
                     bm = zz[j];
-                    bid = e0 + 4 * kVT * u + j;
+                    bid = e0 + 4 * kSS * u + j;
                 }
             }
         }
@@ -161,7 +166,7 @@ __global__ void __launch_bounds__(kVT)
     m = smax[0];
     id = sid[0];
     bad = sbad[0];
-    for (int w = 1; w < kVW; ++w) {
+    for (int w = 1; w < kSSW; ++w) {
         if (smax[w] > m || (smax[w] == m && sid[w] < id)) {
             m = smax[w];
             id = sid[w];
@@ -175,7 +180,7 @@ __global__ void __launch_bounds__(kVT)
         const double part = ks != 0.f ? (static_cast<double>(ks) - static_cast<double>(kc)) *
                                             static_cast<double>(hw_exp2((mt - m) * c2)) * 1099511627776.0
                                       : 0.0;
-        S = static_cast<uint64_t>(block_sum_f64(part, dred) + 0.5);
+        S = static_cast<uint64_t>(block_sum_f64<kSSW>(part, dred) + 0.5);
     }
     if (tid == 0) {
         RowStat st;
@@ -427,9 +432,13 @@ __global__ void __launch_bounds__(kVT)
                 const float4 a = load4_row(zt, e, V, alt);
                 const float4 d = load4_row(zd, e, V, ald);
                 const float pa[4] = {a.x, a.y, a.z, a.w}, pd[4] = {d.x, d.y, d.z, d.w};
+                // each operation rounded on its own: the chunk sums and the walk
+                // of the drawn chunk evaluate this in separate inlined copies,
+                // and a contraction into a fused multiply-add in one of them
+                // only would give the two different masses
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const float r = weight(pa[j], mt, c2) * at - weight(pd[j], mq, c2) * aq;
+                    const float r = __fsub_rn(__fmul_rn(weight(pa[j], mt, c2), at), __fmul_rn(weight(pd[j], mq, c2), aq));
                     m[j] = fx40(fminf(fmaxf(r, 0.f), 1.f));
                 }
             };
@@ -458,7 +467,7 @@ cudaError_t launch_spec_verify(int32_t* tokens_out, int32_t* n_accepted, int32_t
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(B) * (2 * gamma + 1), 1, 1);
-    cfg.blockDim = dim3(kVT, 1, 1);
+    cfg.blockDim = dim3(kSS, 1, 1);
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -480,6 +489,7 @@ cudaError_t launch_spec_verify(int32_t* tokens_out, int32_t* n_accepted, int32_t
     cfg.attrs = attr2;
     cfg.numAttrs = 2;
     cfg.gridDim = dim3(static_cast<unsigned>(B) * nc, 1, 1);
+    cfg.blockDim = dim3(kVT, 1, 1);  // the verification kernel's CTAs are 512 threads
     err = cudaLaunchKernelEx(&cfg, spec_verify_kernel, tokens_out, n_accepted, seq_lens_out, target, draft,
                              draft_tokens, seq_lens, gamma, V, slice, temperature, seeds, offsets,
                              static_cast<const RowStat*>(stats), status);
