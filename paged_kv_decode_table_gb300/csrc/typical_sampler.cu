@@ -57,6 +57,8 @@ struct TySmem {
     unsigned int nwin;
     unsigned long long wsum[kTyW];
     double dsum[kTyW];
+    double dres;    // a block sum in double, for every thread
+    double dsc[4];  // row scalars in double, computed by one thread: log2(e) / T, the centre, the window's edges
     float fv[kTyW];
     unsigned long long bc[4];
     unsigned long long u53;  // the row's uniform, top 53 bits of Philox word 0
@@ -97,6 +99,9 @@ __device__ uint64_t ty_sum_u64(uint64_t v, TySmem* sm) {
     __syncthreads();
     return ty_warp_sum(sm->wsum[lane]);
 }
+// The warps' partials are combined by warp 0 alone (this GPU's FP64 rate is a
+// small fraction of its FP32 rate, so double work repeated by every warp
+// costs microseconds) and handed out through shared memory.
 __device__ double ty_sum_f64(double v, TySmem* sm) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -104,10 +109,14 @@ __device__ double ty_sum_f64(double v, TySmem* sm) {
     __syncthreads();
     if (lane == 0) sm->dsum[warp] = v;
     __syncthreads();
-    double t = sm->dsum[lane];
+    if (warp == 0) {
+        double t = sm->dsum[lane];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-    return t;
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (lane == 0) sm->dres = t;
+    }
+    __syncthreads();
+    return sm->dres;
 }
 template <bool kMax>
 __device__ float ty_ext_f(float v, TySmem* sm) {
@@ -364,6 +373,8 @@ __global__ void __launch_bounds__(kTyT, 1)
     const float* zs = z + lo;  // this CTA's slice
     const float T = temperature[row], tp = typical_p[row];
     if (tid == kTyT - 1) sm->u53 = philox_word0(seeds[row], offsets[row]) >> 11;
+    // log2(e) / T in double, by one thread (read after the next barrier)
+    if (tid == 0) sm->dsc[0] = 1.4426950408889634 / static_cast<double>(T);
     if (rank == 0 && tid == 0) tokens[row] = -1;  // overwritten (after a cluster barrier) by the draw
 
     // cluster exchange: thread 0 publishes the CTA's partial, the barrier makes
@@ -449,7 +460,7 @@ __global__ void __launch_bounds__(kTyT, 1)
     // centre and the order; exact_only when that scale is beyond 1e30 (then
     // every order decision is taken on D in double)
     const double mxd = static_cast<double>(mx);
-    const double c2d = 1.4426950408889634 / static_cast<double>(T);
+    const double c2d = sm->dsc[0];
     const bool exact_only = !(c2d <= 1.0e30);
     const float chi = exact_only ? 1.0e30f : static_cast<float>(c2d);
     const float clo = exact_only ? 0.f : static_cast<float>(c2d - static_cast<double>(chi));
@@ -493,14 +504,18 @@ __global__ void __launch_bounds__(kTyT, 1)
     const double WUc = ty_sum_f64(static_cast<double>(us) - static_cast<double>(uc), sm);
     publish(Sc, 0ull, Wc, WUc, 0.f, 0.f);
     uint64_t S = 0;
-    double W = 0.0, WU = 0.0;
-    for (int r = 0; r < nc; ++r) {
-        S += rd(r)->u[0];
-        W += rd(r)->d[0];
-        WU += rd(r)->d[1];
+    for (int r = 0; r < nc; ++r) S += rd(r)->u[0];
+    if (tid == 0) {  // the centre, by one thread
+        double W = 0.0, WU = 0.0;
+        for (int r = 0; r < nc; ++r) {
+            W += rd(r)->d[0];
+            WU += rd(r)->d[1];
+        }
+        sm->dsc[1] = WU / W;  // W >= 1: the maximum weighs 1
     }
+    __syncthreads();
     ++xk;
-    const double ubar = WU / W;  // W >= 1: the maximum weighs 1
+    const double ubar = sm->dsc[1];
     const float ubf = static_cast<float>(ubar);
     // The order key: D = |u - ubar| in double (log2 units; d = D ln 2), with a
     // float estimate dk = |ucof(x) - ubf| within errf(u) of it (4x the error
@@ -572,14 +587,17 @@ __global__ void __launch_bounds__(kTyT, 1)
     }
     __syncthreads();
     const int blo = static_cast<int>(sm->bc[0]), bhi = max(blo, static_cast<int>(sm->bc[1]));
-    cl.sync();  // no CTA reads another's bins any more; rank 0's bins become the window list
-
-    // ---- the window: logits with Ed <= D < Fd (the bins' edges, in double);
-    // membership is decided on D itself wherever dk is within errf of an edge
+    // ---- the window: logits with Ed <= D < Fd (the bins' edges, in double,
+    // by one thread); membership is decided on D itself wherever dk is within
+    // errf of an edge
     const bool one_bin = !(scale > 0.f);
-    const double Ed = (one_bin || blo == 0) ? 0.0 : static_cast<double>(blo) / static_cast<double>(scale);
-    const double Fd = (one_bin || bhi >= kTyBins - 1) ? static_cast<double>(INFINITY)
-                                                      : static_cast<double>(bhi + 1) / static_cast<double>(scale);
+    if (tid == 0) {
+        sm->dsc[2] = (one_bin || blo == 0) ? 0.0 : static_cast<double>(blo) / static_cast<double>(scale);
+        sm->dsc[3] = (one_bin || bhi >= kTyBins - 1) ? static_cast<double>(INFINITY)
+                                                     : static_cast<double>(bhi + 1) / static_cast<double>(scale);
+    }
+    cl.sync();  // no CTA reads another's bins any more; rank 0's bins become the window list
+    const double Ed = sm->dsc[2], Fd = sm->dsc[3];
     // 0: before [lo, hi) in the order, 1: inside, 2: after
     auto where = [&](float x, double lod, double hid) -> int {
         const float u = ucof(x);
