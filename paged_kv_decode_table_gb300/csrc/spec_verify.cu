@@ -324,6 +324,7 @@ __global__ void __launch_bounds__(kVT)
     __shared__ unsigned long long red[kVW];
     __shared__ unsigned long long xslot[2];  // this slice's total, alternating per draw
     __shared__ int sel, nrej, err;
+    __shared__ float sat, saq;  // 2^40 / S of the target and draft rows at the first rejection
     cg::cluster_group cl = cg::this_cluster();
     const int nc = static_cast<int>(cl.num_blocks()), rank = static_cast<int>(cl.block_rank());
     const int b = blockIdx.x / nc, tid = threadIdx.x;
@@ -382,6 +383,13 @@ __global__ void __launch_bounds__(kVT)
     }
     __syncthreads();
     const int n = nrej;
+    // the residual's scales, in double by one thread (this GPU's FP64 rate makes
+    // a double division repeated by every thread cost microseconds)
+    if (tid == 0 && T != 0.f && n < gamma) {
+        sat = static_cast<float>(1099511627776.0 / static_cast<double>(st[n].S));
+        saq = static_cast<float>(1099511627776.0 / static_cast<double>(st[gamma + 1 + n].S));
+    }
+    __syncthreads();
     // rank 0 writes every output but the drawn token (before the draw's cluster
     // barrier, so that the CTA holding the draw writes that one after it)
     if (rank == 0) {
@@ -426,8 +434,7 @@ __global__ void __launch_bounds__(kVT)
             const float* zd = draft + (static_cast<size_t>(b) * gamma + n) * V;
             const bool ald = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(zd) & 15u) == 0);
             const float mq = st[gamma + 1 + n].zmax;
-            const float at = static_cast<float>(1099511627776.0 / static_cast<double>(st[n].S));
-            const float aq = static_cast<float>(1099511627776.0 / static_cast<double>(st[gamma + 1 + n].S));
+            const float at = sat, aq = saq;
             auto resid_mass = [&](int e, uint64_t* m) {
                 const float4 a = load4_row(zt, e, V, alt);
                 const float4 d = load4_row(zd, e, V, ald);
