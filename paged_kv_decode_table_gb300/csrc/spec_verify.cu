@@ -61,19 +61,6 @@ __device__ __forceinline__ float4 load4_row(const float* row, int e, int n, bool
     return q;
 }
 
-template <int W>
-__device__ __forceinline__ double block_sum_f64(double v, double* red) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    double t = 0.0;
-    for (int w = 0; w < W; ++w) t += red[w];
-    __syncthreads();
-    return t;
-}
-
 // ------------------------------------------------------------------ row statistics
 // Row r of request b: r < gamma + 1 is target row r, else draft row r - gamma - 1.
 // One 256-thread CTA per row, four per SM, so that a batch of up to 4 x #SM rows
@@ -85,7 +72,7 @@ __global__ void __launch_bounds__(kSS, 4)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ float smax[kSSW];
     __shared__ int sid[kSSW], sbad[kSSW];
-    __shared__ double dred[kSSW];
+    __shared__ unsigned long long ured[kSSW];
     const int rows = 2 * gamma + 1;
     const int b = blockIdx.x / rows, r = blockIdx.x - (blockIdx.x / rows) * rows;
     const float* row = r <= gamma ? target + (static_cast<size_t>(b) * (gamma + 1) + r) * V
@@ -175,12 +162,18 @@ __global__ void __launch_bounds__(kSS, 4)
     }
     uint64_t S = 0;
     if (!bad && m > -INFINITY && sum) {
-        // each thread's sum moved to the row maximum, in units of 2^-40 (relative
-        // error ~1e-7)
-        const double part = ks != 0.f ? (static_cast<double>(ks) - static_cast<double>(kc)) *
-                                            static_cast<double>(hw_exp2((mt - m) * c2)) * 1099511627776.0
-                                      : 0.0;
-        S = static_cast<uint64_t>(block_sum_f64<kSSW>(part, dred) + 0.5);
+        // each thread's sum moved to the row maximum, in units of 2^-40 (float
+        // products, one rounding each; below 2^50 units), rounded to an integer
+        // and summed exactly over the CTA (relative error ~1e-7; no double
+        // arithmetic, whose rate on this GPU is a small fraction of float's)
+        const float part =
+            ks != 0.f ? __fmul_rn(__fmul_rn(__fsub_rn(ks, kc), hw_exp2((mt - m) * c2)), 1099511627776.0f) : 0.f;
+        uint64_t v = __float2ull_rn(part);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) ured[warp] = v;
+        __syncthreads();
+        for (int w = 0; w < kSSW; ++w) S += ured[w];
     }
     if (tid == 0) {
         RowStat st;
