@@ -12,8 +12,9 @@
 // D_i = |u_i - ubar|, so the kept set is an interval of logits around the
 // p-weighted mean.  The order is taken on D in double: ubar from Kahan float
 // sums per thread (u with the scale log2(e) / T carried in two floats),
-// combined in double across threads and CTAs (about 1e-7 in log2 units on
-// vocabulary rows); u_i = (z_i - zmax) * log2(e) / T in double.  A float
+// combined exactly as 64-bit integers in 2^-40 units across threads and CTAs
+// (about 1e-7 in log2 units on vocabulary rows); u_i = (z_i - zmax) * log2(e) / T
+// in double.  A float
 // estimate of D with a stated error bound places each logit, so only the
 // logits within that bound of a threshold compute D in double.  Equal D go to
 // the larger logit, then to the smaller id.  Masses are 2^-40 fixed-point
@@ -56,8 +57,6 @@ struct TySmem {
     unsigned int zk[kTyBins];          // the window's logit keys ~okey(z) (ascending: larger logit first)
     unsigned int nwin;
     unsigned long long wsum[kTyW];
-    double dsum[kTyW];
-    double dres;    // a block sum in double, for every thread
     double dsc[4];  // row scalars in double, computed by one thread: log2(e) / T, the centre, the window's edges
     float fv[kTyW];
     unsigned long long bc[4];
@@ -98,25 +97,6 @@ __device__ uint64_t ty_sum_u64(uint64_t v, TySmem* sm) {
     if (lane == 0) sm->wsum[warp] = v;
     __syncthreads();
     return ty_warp_sum(sm->wsum[lane]);
-}
-// The warps' partials are combined by warp 0 alone (this GPU's FP64 rate is a
-// small fraction of its FP32 rate, so double work repeated by every warp
-// costs microseconds) and handed out through shared memory.
-__device__ double ty_sum_f64(double v, TySmem* sm) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    __syncthreads();
-    if (lane == 0) sm->dsum[warp] = v;
-    __syncthreads();
-    if (warp == 0) {
-        double t = sm->dsum[lane];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-        if (lane == 0) sm->dres = t;
-    }
-    __syncthreads();
-    return sm->dres;
 }
 template <bool kMax>
 __device__ float ty_ext_f(float v, TySmem* sm) {
@@ -484,9 +464,12 @@ __global__ void __launch_bounds__(kTyT, 1)
 
     // ---- S (exact fixed-point masses) and the p-weighted mean of u.  The
     // centre ubar = sum w u / sum w takes u from the compensated scale ucof and
-    // Kahan sums per thread, double across threads and CTAs (error ~1e-7 in
-    // log2 units on vocabulary rows; a plain float scale would bias it by the
-    // rounding of log2(e) / T times the spread of u).
+    // Kahan sums per thread (error ~1e-7 in log2 units on vocabulary rows; a
+    // plain float scale would bias it by the rounding of log2(e) / T times the
+    // spread of u); each thread's sum and compensation are turned into 2^-40
+    // units (exact at these magnitudes, the floats' ulps being multiples of
+    // 2^-40; |w u| <= 1 / (e ln 2) per logit keeps the totals below 2^57) and
+    // added exactly as 64-bit integers across threads and CTAs.
     uint64_t s = 0;
     float ws = 0.f, wc = 0.f, us = 0.f, uc = 0.f;
     ty_sweep(zs, n, [&](int, float x) {
@@ -500,18 +483,21 @@ __global__ void __launch_bounds__(kTyT, 1)
         }
     });
     const uint64_t Sc = ty_sum_u64(s, sm);
-    const double Wc = ty_sum_f64(static_cast<double>(ws) - static_cast<double>(wc), sm);
-    const double WUc = ty_sum_f64(static_cast<double>(us) - static_cast<double>(uc), sm);
-    publish(Sc, 0ull, Wc, WUc, 0.f, 0.f);
+    auto units = [](float v) { return static_cast<uint64_t>(__float2ll_rn(__fmul_rn(v, 0x1p40f))); };
+    const uint64_t Wc = ty_sum_u64(units(ws) - units(wc), sm);   // two's complement sums
+    const uint64_t WUc = ty_sum_u64(units(us) - units(uc), sm);
+    // (the signed total of w u travels as the bit pattern of a double slot)
+    publish(Sc, Wc, __longlong_as_double(static_cast<long long>(WUc)), 0.0, 0.f, 0.f);
     uint64_t S = 0;
     for (int r = 0; r < nc; ++r) S += rd(r)->u[0];
     if (tid == 0) {  // the centre, by one thread
-        double W = 0.0, WU = 0.0;
+        uint64_t W = 0, WU = 0;
         for (int r = 0; r < nc; ++r) {
-            W += rd(r)->d[0];
-            WU += rd(r)->d[1];
+            W += rd(r)->u[1];
+            WU += static_cast<uint64_t>(__double_as_longlong(rd(r)->d[0]));
         }
-        sm->dsc[1] = WU / W;  // W >= 1: the maximum weighs 1
+        // W >= 2^40: the maximum weighs 1
+        sm->dsc[1] = static_cast<double>(static_cast<long long>(WU)) / static_cast<double>(W);
     }
     __syncthreads();
     ++xk;
