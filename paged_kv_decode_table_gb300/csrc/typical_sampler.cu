@@ -72,6 +72,16 @@ struct TySmem {
     unsigned long long res[4];  // rank 0: the cut (found, D bits, logit key, id) for the cluster
 };
 
+// An opaque copy of a value: the compiler cannot trace it back to the double
+// arithmetic it came from, so under register pressure it keeps or spills the
+// value instead of recomputing it inside the per-logit loops (float <-> double
+// conversions run on this GPU's slow FP64 pipe).
+__device__ __forceinline__ float ty_pin(float v) {
+    float r;
+    asm volatile("mov.b32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+
 // Compensated (Kahan) float summation: the sum so far is s - c, c carrying the
 // rounding error of each addition (explicit round-to-nearest operations, so
 // that no contraction or reassociation undoes it).
@@ -441,9 +451,9 @@ __global__ void __launch_bounds__(kTyT, 1)
     // every order decision is taken on D in double)
     const double mxd = static_cast<double>(mx);
     const double c2d = sm->dsc[0];
-    const bool exact_only = !(c2d <= 1.0e30);
-    const float chi = exact_only ? 1.0e30f : static_cast<float>(c2d);
-    const float clo = exact_only ? 0.f : static_cast<float>(c2d - static_cast<double>(chi));
+    const bool exact_only = ty_pin(c2d <= 1.0e30 ? 0.f : 1.f) != 0.f;
+    const float chi = ty_pin(exact_only ? 1.0e30f : static_cast<float>(c2d));
+    const float clo = ty_pin(exact_only ? 0.f : static_cast<float>(c2d - static_cast<double>(static_cast<float>(c2d))));
     auto ucof = [&](float x) {
         const float dz = __fsub_rn(x, mx);
         return __fmaf_rn(dz, chi, __fmul_rn(dz, clo));
@@ -502,7 +512,7 @@ __global__ void __launch_bounds__(kTyT, 1)
     __syncthreads();
     ++xk;
     const double ubar = sm->dsc[1];
-    const float ubf = static_cast<float>(ubar);
+    const float ubf = ty_pin(static_cast<float>(ubar));
     // The order key: D = |u - ubar| in double (log2 units; d = D ln 2), with a
     // float estimate dk = |ucof(x) - ubf| within errf(u) of it (4x the error
     // bound of the float operations), so that only logits whose dk lies within
@@ -772,7 +782,7 @@ __global__ void __launch_bounds__(kTyT, 1)
 
     // ---- the draw over the kept set in id order: (D, logit key, id) up to the cut's
     const double ds = __longlong_as_double(static_cast<long long>(dstar));
-    const float dsf = static_cast<float>(ds);
+    const float dsf = ty_pin(static_cast<float>(ds));
     auto kept = [&](float x, int i) -> uint64_t {  // i: the id
         if (!(x > -INFINITY)) return 0ull;
         const float u = ucof(x);
