@@ -595,10 +595,10 @@ __global__ void __launch_bounds__(kTyT, 1)
     cl.sync();  // no CTA reads another's bins any more; rank 0's bins become the window list
     const double Ed = sm->dsc[2], Fd = sm->dsc[3];
     // 0: before [lo, hi) in the order, 1: inside, 2: after
-    auto where = [&](float x, double lod, double hid) -> int {
+    // (lof, hif: the bounds rounded to float once, outside the sweeps)
+    auto where = [&](float x, double lod, double hid, float lof, float hif) -> int {
         const float u = ucof(x);
         const float dk = dkf(u), e = errf(u);
-        const float lof = static_cast<float>(lod), hif = static_cast<float>(hid);
         if (dk < lof - e) return 0;
         if (dk > lof + e && dk < hif - e) return 1;
         if (dk > hif + e) return 2;
@@ -616,9 +616,10 @@ __global__ void __launch_bounds__(kTyT, 1)
     unsigned int* zk0 = cl.map_shared_rank(sm->zk, 0);
     unsigned int* nwin0 = cl.map_shared_rank(&sm->nwin, 0);
     uint64_t at = 0, in = 0;
+    const float Ef = ty_pin(static_cast<float>(Ed)), Ff = ty_pin(static_cast<float>(Fd));
     ty_sweep(zs, n, [&](int i, float x) {
         if (!(x > -INFINITY)) return;
-        const int w = where(x, Ed, Fd);
+        const int w = where(x, Ed, Fd, Ef, Ff);
         if (w == 0) {
             at += massc(x);
         } else if (w == 1) {
@@ -723,7 +724,8 @@ __global__ void __launch_bounds__(kTyT, 1)
         const bool whole = !cut_in_window;
         const double lod = whole ? 0.0 : Ed, hid = whole ? static_cast<double>(INFINITY) : Fd;
         above = whole ? 0ull : above;
-        auto inw = [&](float x) { return x > -INFINITY && (whole || where(x, lod, hid) == 1); };
+        const float lof = ty_pin(static_cast<float>(lod)), hif = ty_pin(static_cast<float>(hid));
+        auto inw = [&](float x) { return x > -INFINITY && (whole || where(x, lod, hid, lof, hif) == 1); };
         auto kh = [&](float x, int, uint32_t& k, uint64_t& m) -> bool {
             if (!inw(x)) return false;
             k = static_cast<uint32_t>(static_cast<unsigned long long>(__double_as_longlong(dex(x))) >> 32);
