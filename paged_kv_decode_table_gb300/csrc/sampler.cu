@@ -1562,11 +1562,16 @@ static SamplerPlan plan_sampler(int B, int V, int sms) {
         if (nc > 1 && (V + nc - 1) / nc < 4096) continue;  // keep slices long enough to be worth a CTA
         const SamplerPlan pg = make_plan(V, nc, false);
         if (B <= resident_clusters(pg)) {
-            // one CTA per row in one wave with more rows than SMs: two-CTA
-            // clusters in two waves instead, heaviest rows first.  On the
-            // 256 x 152064 stress batch (mixed row kinds) 131 us against 186;
+            // one CTA per row in one wave with more rows than SMs: clusters of
+            // the largest size (2, 3 or 4) whose CTAs fit two waves, heaviest
+            // rows first.  Mixed 152064-logit batches of 170 / 200 / 256 / 300
+            // rows: 106 / 111 / 132 / 152 us against 174 / 180 / 186 / 200;
             // batches of one kind move by -12% to +17%.
-            if (nc == 1 && B > sms && (V + 1) / 2 >= 4096) return make_plan(V, 2, false);
+            if (nc == 1 && B > sms) {
+                int nc2 = min(4, (2 * resident_clusters(pg)) / B);
+                while (nc2 > 1 && (V + nc2 - 1) / nc2 < 4096) --nc2;
+                if (nc2 >= 2) return make_plan(V, nc2, false);
+            }
             return pg;
         }
     }
