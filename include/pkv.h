@@ -63,7 +63,7 @@ extern "C" {
 typedef enum {
     PKV_OK = 0,
     PKV_ERR_INVALID_ARG = 1,   /* host: bad pointer/shape/size; device: T < 0 or top_p <= 0 */
-    PKV_ERR_UNSUPPORTED = 2,   /* host: a shape this build has no kernel for */
+    PKV_ERR_UNSUPPORTED = 2,   /* host: a shape the library has no kernel for */
     PKV_ERR_CUDA = 3,          /* host: a CUDA runtime call or launch failed */
     PKV_ERR_DEVICE_BOUNDS = 4, /* device: block id or sequence length out of range */
     PKV_ERR_TIMEOUT = 5,       /* device: a bounded wait ran out (kernel returned early) */
