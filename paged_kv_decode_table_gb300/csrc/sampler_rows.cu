@@ -241,21 +241,91 @@ __device__ int rw_tie(RowSmem* sm, const float* __restrict__ z, int n, In in, ui
     return id;
 }
 
-// ------------------------------------------------------------------ kernel
-__global__ void __launch_bounds__(kRT, 4)
-    sampler_rows_kernel(int32_t* __restrict__ tokens, const float* __restrict__ logits, int V,
-                        const float* __restrict__ temperature, const int32_t* __restrict__ top_k,
-                        const float* __restrict__ top_p, const float* __restrict__ min_p,
-                        const uint64_t* __restrict__ seeds, const uint64_t* __restrict__ offsets, int32_t* status) {
-    __shared__ RowSmem smem;
-    RowSmem* sm = &smem;
+// ------------------------------------------------------------------ row order
+// The row CTA blockIdx.x takes: the rows with the most work get the lowest CTA
+// indices, so that they start first and spread over the SMs
+// (longest-processing-time-first order; the tokens do not depend on it).
+// Classes: 2 = top-p alone, 1 = top-k above kRSmallK or no truncation,
+// 0 = greedy, small top-k or invalid parameters; order: class descending, row
+// index ascending: the CTA counts the rows per class, then (unless every row
+// is in one class, where it returns -1 for the natural order) finds the row of
+// its rank within its class with warp ballots.
+__device__ int rw_lpt_row(int B, int V, const float* __restrict__ temperature, const int32_t* __restrict__ top_k,
+                          const float* __restrict__ top_p, RowSmem* sm) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int row = blockIdx.x;
+    auto cls = [&](int r) -> int {  // loads all three parameters, so that no load waits on another
+        const float t = temperature[r];
+        const int k = top_k[r];
+        const float p = top_p[r];
+        const bool k_on = k > 0 && k < V;
+        if (!(t > 0.f) || (k_on && k <= kRSmallK)) return 0;
+        return !k_on && p < 1.f ? 2 : 1;
+    };
+    // scratch, cleared by pass A afterwards: the bin counts ([0..2] rows per
+    // class, [3] the answer, [8..8+kRW) rows of the sought class per warp) and
+    // the class of every row, one byte each, while they fit in the mass bins
+    unsigned int* cc = sm->cnt;
+    unsigned char* c8 = reinterpret_cast<unsigned char*>(sm->mhi);
+    const bool keep = B <= static_cast<int>(sizeof(sm->mhi));
+    if (tid < 4) cc[tid] = 0u;
+    unsigned long long own = 0ull;  // this thread's rows per class, 21 bits each
+#pragma unroll 4
+    for (int r = tid; r < B; r += kRT) {
+        const int c = cls(r);
+        own += 1ull << (21 * c);
+        if (keep) c8[r] = static_cast<unsigned char>(c);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) own += __shfl_xor_sync(0xffffffffu, own, o);
+    __syncthreads();  // cc[0..3] cleared
+    if (lane < 3) atomicAdd(&cc[lane], static_cast<unsigned int>((own >> (21 * lane)) & 0x1fffffull));
+    __syncthreads();
+    const int n2 = static_cast<int>(cc[2]), n1 = static_cast<int>(cc[1]);
+    const int u = static_cast<int>(blockIdx.x);
+    if (n2 == B || n1 == B || n2 + n1 == 0) {  // one class: the natural order
+        __syncthreads();
+        return -1;
+    }
+    const int cs = u < n2 ? 2 : (u < n2 + n1 ? 1 : 0);        // this CTA's class
+    const int jj = u - (cs == 2 ? 0 : (cs == 1 ? n2 : n2 + n1));  // its rank within the class
+    int before = 0;  // rows of class cs in earlier chunks (the same in every thread)
+    for (int r0 = 0; r0 < B && before <= jj; r0 += kRT) {
+        const int r = r0 + tid;
+        const bool f = r < B && (keep ? static_cast<int>(c8[r]) : cls(r)) == cs;
+        const unsigned int m = __ballot_sync(0xffffffffu, f);
+        if (lane == 0) cc[8 + warp] = static_cast<unsigned int>(__popc(m));
+        __syncthreads();
+        int wb = before, tot = 0;
+#pragma unroll
+        for (int w = 0; w < kRW; ++w) {
+            const int cw = static_cast<int>(cc[8 + w]);
+            wb += w < warp ? cw : 0;
+            tot += cw;
+        }
+        if (f && wb + __popc(m & ((1u << lane) - 1u)) == jj) cc[3] = static_cast<unsigned int>(r);
+        before += tot;
+        __syncthreads();
+    }
+    const int row = static_cast<int>(cc[3]);
+    __syncthreads();
+    return row;
+}
+
+// ------------------------------------------------------------------ kernel
+// One row: the passes below, in a function so that the kernel can compile it
+// twice, once for the natural order (row = blockIdx.x, which the compiler
+// re-reads rather than keeping it live in the passes at the 64-register cap)
+// and once for the row the ordering picked.
+__device__ __forceinline__ void rw_sample_row(int row, int32_t* __restrict__ tokens,
+                                              const float* __restrict__ logits, int V,
+                                              const float* __restrict__ temperature,
+                                              const int32_t* __restrict__ top_k, const float* __restrict__ top_p,
+                                              const float* __restrict__ min_p, const uint64_t* __restrict__ seeds,
+                                              const uint64_t* __restrict__ offsets, int32_t* status, RowSmem* sm) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float* z = logits + static_cast<size_t>(row) * V;
     const bool a16 = (reinterpret_cast<uintptr_t>(z) & 15u) == 0;
     int32_t* tok_out = tokens + row;
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const float T = temperature[row];
     const float pp = top_p[row];
     const float mp = min_p ? min_p[row] : 0.f;
@@ -818,7 +888,25 @@ __global__ void __launch_bounds__(kRT, 4)
     }
 }
 
-bool sampler_rows_fits(int B, int V, int sms) { return V >= 1 && V <= kRowMaxV && B > 2 * sms; }
+
+__global__ void __launch_bounds__(kRT, 4)
+    sampler_rows_kernel(int32_t* __restrict__ tokens, const float* __restrict__ logits, int V,
+                        const float* __restrict__ temperature, const int32_t* __restrict__ top_k,
+                        const float* __restrict__ top_p, const float* __restrict__ min_p,
+                        const uint64_t* __restrict__ seeds, const uint64_t* __restrict__ offsets, int32_t* status,
+                        int B) {
+    __shared__ RowSmem smem;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int row = rw_lpt_row(B, V, temperature, top_k, top_p, &smem);
+    if (row < 0)
+        rw_sample_row(static_cast<int>(blockIdx.x), tokens, logits, V, temperature, top_k, top_p, min_p, seeds,
+                      offsets, status, &smem);
+    else
+        rw_sample_row(row, tokens, logits, V, temperature, top_k, top_p, min_p, seeds, offsets, status, &smem);
+}
+
+bool sampler_rows_fits(int B, int V, int sms) { return V >= 1 && V <= kRowMaxV && B > 2 * sms && B < (1 << 21); }
 
 cudaError_t launch_sampler_rows(int32_t* tokens, const float* logits, int B, int V, const float* temperature,
                                 const int32_t* top_k, const float* top_p, const float* min_p,
@@ -834,7 +922,7 @@ cudaError_t launch_sampler_rows(int32_t* tokens, const float* logits, int B, int
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, sampler_rows_kernel, tokens, logits, V, temperature, top_k, top_p, min_p, seeds,
-                              offsets, status);
+                              offsets, status, B);
 }
 
 }  // namespace pkv

@@ -5,7 +5,8 @@ same token unless the oracle's draw or top-p cut lies within 1e-6 of an edge
 (counted, at most max(1, B // 50)).  Rows cover greedy, top-k from 1 to past the
 finite count, top-p from 0.3 to 1, min-p, banned tokens, rows that are not
 16-byte aligned (odd vocabularies), windows too large for the gather (blocks of
-equal logits, which take the exact radix selection), and the error codes.
+equal logits, which take the exact radix selection), the error codes, and
+batches in any row order (the kernel picks the order its CTAs take the rows in).
 """
 import numpy as np
 import pytest
@@ -188,3 +189,36 @@ def test_rows_small_top_k(V, seed):
     offs = rng.integers(0, 1000, B).astype(np.uint64)
     _compare(z, T, k, p, seeds, offs)
     _compare(z, T, k, p, seeds, offs, min_p=mp)
+
+
+@pytest.mark.parametrize("mix", ["mixed", "top_p_only", "heavy_tail"])
+def test_rows_order_independent(mix):
+    """The rows kernel hands its CTAs the rows heaviest first (top-p alone, then
+    large top-k or no truncation, then greedy, small top-k and invalid rows),
+    or in their natural order when every row is in one class: the token of a
+    row does not depend on where it sits in the batch, so permuting the rows
+    permutes the tokens.  A mixed batch, a batch of top-p rows only, and a
+    batch whose only heavy rows are its last ones."""
+    rng = np.random.default_rng({"mixed": 51, "top_p_only": 52, "heavy_tail": 53}[mix])
+    B, V = _rows(), 6000
+    z = (rng.standard_normal((B, V)) * rng.choice([0.5, 1.0, 2.0], (B, 1))).astype(np.float32)
+    T, k, p, seeds, offs = _params(rng, B, V)
+    if mix == "top_p_only":
+        T[:] = rng.uniform(0.5, 1.5, B).astype(np.float32)
+        k[:] = 0
+        p[:] = 0.90007
+    elif mix == "heavy_tail":
+        T[:] = 0.0
+        T[-20:] = 1.0
+        k[-20:] = 0
+        p[-20:] = 0.80007
+    got, st = _run(z, T, k, p, seeds, offs)
+    assert st == 0
+    perm = rng.permutation(B)
+    got_p, st_p = _run(z[perm], T[perm], k[perm], p[perm], seeds[perm], offs[perm])
+    assert st_p == 0
+    assert np.array_equal(got_p, got[perm])
+    for b in list(range(0, B, 37)) + list(range(B - 20, B)):
+        r = oracle.sample_row(z[b], float(T[b]), int(k[b]), float(p[b]), int(seeds[b]), int(offs[b]))
+        if got[b] != r["token"]:
+            assert r["draw_margin"] < EXEMPT or r["cut_margin"] < EXEMPT, (b, int(got[b]), r)
