@@ -631,6 +631,8 @@ def run_extras(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     flush = _l2_flusher(dev)
+    clocks = ClockSampler(0)
+    clocks.start()
 
     def emit(d):
         print(json.dumps(d), flush=True)
@@ -806,6 +808,7 @@ def run_extras(args):
           "logical_kv_bytes": logical, "unique_kv_bytes": unique, **t,
           "logical_GB/s": logical / (t["median_us"] * 1e-6) / 1e9,
           "unique_GB/s": unique / (t["median_us"] * 1e-6) / 1e9, "cow_pairs": len(pairs)})
+    emit({"extra": "clocks", "over": "every measurement above", **clocks.stop()})
     return 0
 
 
