@@ -16,24 +16,24 @@
 // 256 threads holds a row (four per SM), so a batch of up to 4 x #SM rows is
 // resident in one wave and the rows' chains overlap.
 //
-// Passes over the row (thread t takes the 16-byte slots 4 (t + 256 m); the
-// first pass reads HBM, the others hit L2):
-//  A: maximum, minimum, NaN/+inf flag, finite count, first index of the maximum;
-//  B: 4096 bins linear in (zmax - z): a count per bin (32-bit shared atomics,
-//     no exponential).  The exact cumulative counts give the top-k boundary
-//     bin bk; each bin's mass is bracketed by its count times the weights at
-//     its edges, which brackets S_k and the target ceil(top_p * S_k) and so
+// Passes over the row (the first reads HBM, the others hit L2):
+//  A: maximum, minimum, NaN/+inf flag, finite count, first index of the
+//     maximum (thread t takes the 16-byte slots 4 (t + 256 m));
+//  B: 2048 bins linear in (zmax - z): the count and the exact mass of every
+//     bin as 32-bit shared sums (count, mass >> 20, mass mod 2^20).  The
+//     cumulative counts give the top-k boundary bin bk, the cumulative masses
 //     the bins [wlo, whi] that can hold the top-p cut;
-//  C: exact fixed-point masses: every chunk of 128 consecutive ids gets the
-//     kept mass of its logits in bins < wlo, the masses of bins < wlo and of
-//     the bins between the window and the top-k boundary are summed, and the
-//     logits of bins wlo..whi (and of bin bk) are gathered as sort keys.
+//  C: in chunks of 512 consecutive ids (one warp, four float4 loads per lane):
+//     the kept mass of every chunk's logits in bins < wlo, the masses of bins
+//     < wlo and of the bins between the window and bk summed, and the logits of
+//     bins wlo..whi (and of bin bk) gathered as sort keys.
 // The gathered window is sorted (z desc, id asc); it gives the exact top-k
 // part of bin bk, S_k, the top-p cut (checked to lie in the window), and the
 // kept window entries, whose masses join their chunks.  An exclusive scan of
 // the chunk sums locates the draw, and one warp walks that chunk.  A window
-// larger than kRwCap logits, or a cut outside it, takes an exact radix
-// selection over the row instead.
+// larger than kRwCap logits, a bin of 4096 logits or more, or a cut outside
+// the window takes an exact radix selection over the row instead.  Rows with
+// 0 < top_k <= kRSmallK take the thread-maxima path after pass A.
 #include <math.h>
 
 #include "pkv_common.cuh"
@@ -45,17 +45,18 @@ constexpr int kRT = 256;             // threads per CTA
 constexpr int kRW = kRT / 32;        // warps
 constexpr int kRBins = 2048;         // linear bins
 constexpr int kRwCap = 2048;         // gathered window capacity
-constexpr int kRChunk = 128;         // ids per draw chunk
+constexpr int kRChunk = 512;         // ids per draw chunk (one warp's four loads of a chunk sweep)
 constexpr int kRowMaxV = 65536;      // largest vocabulary this kernel serves
 constexpr int kRChunks = kRowMaxV / kRChunk;
 constexpr int kRSmallK = 64;         // top_k served by the thread-maxima path
+static_assert(kRChunks >= 2 * kRSmallK, "the thread-maxima path keeps its keys and masses in csum");
 
 struct RowSmem {
     unsigned int cnt[kRBins];            // count per bin
     unsigned int mhi[kRBins];            // sum of mass >> 20 per bin
     unsigned int mlo[kRBins];            // sum of mass & (2^20 - 1) per bin
     unsigned long long win[kRwCap];      // the gathered window (sort keys); radix histograms
-    unsigned long long csum[kRChunks];   // kept mass per chunk of 128 ids
+    unsigned long long csum[kRChunks];   // kept mass per chunk of kRChunk ids
     unsigned long long wsum[kRW];
     unsigned long long bc[8];
     float fv[kRW];
@@ -109,8 +110,8 @@ __device__ __forceinline__ float4 rw_load4(const float* __restrict__ z, int n, i
 
 // Every slot of the thread (4 (t + kRT m)), four loads in flight; f(e, q).
 // The trip count is warp-uniform (lanes past the end see -inf), so f may use
-// warp-collective operations, and one iteration of a warp covers the chunk of
-// 128 ids starting at 4 (32 w + kRT m).
+// warp-collective operations, and one iteration of a warp covers the 128
+// consecutive ids starting at 4 (32 w + kRT m).
 template <typename F>
 __device__ __forceinline__ void rw_sweep(const float* __restrict__ z, int n, bool a16, F&& f) {
     const int lane = threadIdx.x & 31;
@@ -126,6 +127,25 @@ __device__ __forceinline__ void rw_sweep(const float* __restrict__ z, int n, boo
         for (int u = 0; u < 4; ++u) f(e0 + 4 * lane + 4 * kRT * u, q[u]);
     }
 }
+// The row in chunks of kRChunk ids: warp w takes the chunks w, w + kRW, ...,
+// lane l the float4s at 4 l + 128 u (u = 0..3) of each, four loads in flight;
+// f(c0, q) with c0 the chunk's first id, element (u, j) being id
+// c0 + 128 u + 4 l + j.  The trip count is warp-uniform.
+template <typename F>
+__device__ __forceinline__ void rw_sweep_chunks(const float* __restrict__ z, int n, bool a16, F&& f) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nvec = (n + 3) & ~3;
+    for (int c0 = kRChunk * warp; c0 < nvec; c0 += kRChunk * kRW) {
+        float4 q[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = c0 + 4 * lane + 128 * u;
+            q[u] = e < nvec ? rw_load4(z, n, e, a16) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        }
+        f(c0, q);
+    }
+}
+static_assert(kRChunk == 4 * 128, "a chunk is one warp's four float4 loads");
 __device__ __forceinline__ float rw_at(const float4& q, int j) {
     return j == 0 ? q.x : (j == 1 ? q.y : (j == 2 ? q.z : q.w));
 }
@@ -646,38 +666,52 @@ __device__ __forceinline__ void rw_sample_row(int row, int32_t* __restrict__ tok
     if (fits) {
         // ---- C: exact masses; chunk sums of bins < wlo; window gather
         uint64_t asum = 0, msum = 0;  // bins < wlo; top-k bins between the window and bk (top-k on)
-        rw_sweep(z, V, a16, [&](int e, const float4& q) {
+        rw_sweep_chunks(z, V, a16, [&](int c0, const float4 (&q)[4]) {
             uint64_t s = 0;
-            bool in[4];
+            unsigned int inm = 0u;  // bit 4 u + j: element (u, j) lies in the window
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float x = rw_at(q, j);
-                in[j] = false;
-                if (!(x > -INFINITY)) continue;
-                const int b = bin(x);
-                if (b < wlo) {
-                    const uint64_t m = mass(x, zmax, c2);
-                    asum += m;
-                    s += m >= mth ? m : 0ull;
-                } else if (b <= whi || (gather_bk && b == bk)) {
-                    in[j] = true;
-                } else if (kk && b < bk) {
-                    msum += mass(x, zmax, c2);
+            for (int u = 0; u < 4; ++u) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float x = rw_at(q[u], j);
+                    if (!(x > -INFINITY)) continue;
+                    const int b = bin(x);
+                    if (b < wlo) {
+                        const uint64_t m = mass(x, zmax, c2);
+                        asum += m;
+                        s += m >= mth ? m : 0ull;
+                    } else if (b <= whi || (gather_bk && b == bk)) {
+                        inm |= 1u << (4 * u + j);
+                    } else if (kk && b < bk) {
+                        msum += mass(x, zmax, c2);
+                    }
                 }
             }
-            // the window's logits, one shared atomic per warp and element slot
+            // the window's logits: a warp scan of the counts, one shared atomic per warp
+            if (__any_sync(0xffffffffu, inm != 0u)) {
+                const unsigned int cnt = __popc(inm);
+                unsigned int inc = cnt;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const unsigned int mask = __ballot_sync(0xffffffffu, in[j]);
-                if (mask) {
-                    unsigned int base = 0;
-                    if (lane == __ffs(mask) - 1) base = atomicAdd(&sm->nwin, static_cast<unsigned int>(__popc(mask)));
-                    base = __shfl_sync(0xffffffffu, base, __ffs(mask) - 1);
-                    if (in[j]) win[base + __popc(mask & ((1u << lane) - 1u))] = sort_key(rw_at(q, j), e + j);
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned int y = __shfl_up_sync(0xffffffffu, inc, o);
+                    if (lane >= o) inc += y;
+                }
+                unsigned int base = 0u;
+                if (lane == 31) base = atomicAdd(&sm->nwin, inc);
+                base = __shfl_sync(0xffffffffu, base, 31) + inc - cnt;
+                if (inm) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            if (inm & (1u << (4 * u + j)))
+                                win[base++] = sort_key(rw_at(q[u], j), c0 + 128 * u + 4 * lane + j);
+                        }
+                    }
                 }
             }
             s = rw_sum(s);
-            if (lane == 0 && e - 4 * lane < V) sm->csum[(e - 4 * lane) / kRChunk] = s;
+            if (lane == 0 && c0 < V) sm->csum[c0 / kRChunk] = s;
         });
         uint64_t A, M;
         rw_excl_scan(asum, sm, A);  // (begins with a barrier: the gather is complete after it)
@@ -802,44 +836,37 @@ __device__ __forceinline__ void rw_sample_row(int row, int32_t* __restrict__ tok
             kept_fn_cut = true;
         }
         // chunk sums of the kept masses
-        rw_sweep(z, V, a16, [&](int e, const float4& q) {
+        rw_sweep_chunks(z, V, a16, [&](int c0, const float4 (&q)[4]) {
             uint64_t s = 0;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float x = rw_at(q, j);
-                if (!(x > -INFINITY)) continue;
-                const uint32_t key = okey(x);
-                if (kept_fn_cut && !(key > cut_key || (key == cut_key && e + j <= cut_id))) continue;
-                const uint64_t m = mass(x, zmax, c2);
-                s += m >= mth ? m : 0ull;
+            for (int u = 0; u < 4; ++u) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float x = rw_at(q[u], j);
+                    if (!(x > -INFINITY)) continue;
+                    const uint32_t key = okey(x);
+                    const int id = c0 + 128 * u + 4 * lane + j;
+                    if (kept_fn_cut && !(key > cut_key || (key == cut_key && id <= cut_id))) continue;
+                    const uint64_t m = mass(x, zmax, c2);
+                    s += m >= mth ? m : 0ull;
+                }
             }
             s = rw_sum(s);
-            if (lane == 0 && e - 4 * lane < V) sm->csum[(e - 4 * lane) / kRChunk] = s;
+            if (lane == 0 && c0 < V) sm->csum[c0 / kRChunk] = s;
         });
     }
     __syncthreads();
 
     // ---- the draw: chunk holding X = floor(u * S_p), then one warp walks it
+    static_assert(kRChunks <= kRT, "one chunk per thread");
     const int nch = (V + kRChunk - 1) / kRChunk;
-    constexpr int kCpt = kRChunks / kRT;  // chunks per thread (2)
-    uint64_t cs[kCpt], ts = 0;
-#pragma unroll
-    for (int q = 0; q < kCpt; ++q) {
-        const int ch = kCpt * tid + q;
-        cs[q] = ch < nch ? sm->csum[ch] : 0ull;
-        ts += cs[q];
-    }
+    const uint64_t cs = tid < nch ? sm->csum[tid] : 0ull;
     uint64_t Sp;
-    uint64_t run = rw_excl_scan(ts, sm, Sp);
+    const uint64_t run = rw_excl_scan(cs, sm, Sp);
     const uint64_t X = static_cast<uint64_t>((static_cast<unsigned __int128>(sm->u53) * Sp) >> 53);
     if (tid == 0) sm->bc[7] = ~0ull;
     __syncthreads();
-#pragma unroll
-    for (int q = 0; q < kCpt; ++q) {
-        const int ch = kCpt * tid + q;
-        if (ch < nch && cs[q] && run <= X && X < run + cs[q]) sm->bc[7] = static_cast<unsigned long long>(ch);
-        run += cs[q];
-    }
+    if (cs && run <= X && X < run + cs) sm->bc[7] = static_cast<unsigned long long>(tid);
     __syncthreads();
     const unsigned long long cw = sm->bc[7];
     if (warp != 0 || cw == ~0ull) return;
@@ -850,24 +877,29 @@ __device__ __forceinline__ void rw_sample_row(int row, int32_t* __restrict__ tok
         for (int c = lane; c < ch; c += 32) p += sm->csum[c];
         base = rw_sum(p);
     }
-    const int e = ch * kRChunk + 4 * lane;
-    const float4 q = rw_load4(z, V, e, a16);
-    uint64_t m4[4];
+    // lane l: the 16 ids from ch * kRChunk + 16 l, in order
+    const int e = ch * kRChunk + 16 * lane;
+    uint64_t m16[16];
+    uint64_t mine = 0;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const float x = rw_at(q, j);
-        uint64_t m = 0;
-        if (x > -INFINITY) {
-            const uint32_t key = okey(x);
-            const bool keep = !kept_fn_cut || key > cut_key || (key == cut_key && e + j <= cut_id);
-            if (keep) {
-                m = mass(x, zmax, c2);
-                m = m >= mth ? m : 0ull;
+    for (int v = 0; v < 4; ++v) {
+        const float4 q = rw_load4(z, V, e + 4 * v, a16);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float x = rw_at(q, j);
+            uint64_t m = 0;
+            if (x > -INFINITY) {
+                const uint32_t key = okey(x);
+                const bool keep = !kept_fn_cut || key > cut_key || (key == cut_key && e + 4 * v + j <= cut_id);
+                if (keep) {
+                    m = mass(x, zmax, c2);
+                    m = m >= mth ? m : 0ull;
+                }
             }
+            m16[4 * v + j] = m;
+            mine += m;
         }
-        m4[j] = m;
     }
-    const uint64_t mine = m4[0] + m4[1] + m4[2] + m4[3];
     uint64_t inc = mine;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -878,8 +910,8 @@ __device__ __forceinline__ void rw_sample_row(int row, int32_t* __restrict__ tok
     if (before <= X && X < before + mine) {
         uint64_t cum = before;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            cum += m4[j];
+        for (int j = 0; j < 16; ++j) {
+            cum += m16[j];
             if (cum > X) {
                 *tok_out = e + j;
                 break;
