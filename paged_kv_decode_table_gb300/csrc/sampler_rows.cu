@@ -64,6 +64,13 @@ struct RowSmem {
     unsigned int nwin;
     unsigned int nq;                     // threads whose maximum is a candidate (small top-k)
     unsigned long long u53;
+    float edge[4];                       // pass C's bin bounds as logit thresholds
+    unsigned long long wsum2[kRW];
+    unsigned long long wtot;             // logits in the window's bins
+};
+template <bool B>
+struct RwFlag {
+    static constexpr bool value = B;
 };
 
 // ------------------------------------------------------------------ CTA helpers
@@ -95,6 +102,43 @@ __device__ uint64_t rw_excl_scan(uint64_t v, RowSmem* sm, uint64_t& total) {
     total = tot;
     __syncthreads();
     return before + inc - v;
+}
+
+// Two exclusive prefixes at once (one set of barriers); returns v0's, with
+// e1 = v1's and the two totals.
+__device__ uint64_t rw_excl_scan2(uint64_t v0, uint64_t v1, RowSmem* sm, uint64_t& t0, uint64_t& e1,
+                                  uint64_t& t1) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint64_t i0 = v0, i1 = v1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t y0 = __shfl_up_sync(0xffffffffu, i0, o);
+        const uint64_t y1 = __shfl_up_sync(0xffffffffu, i1, o);
+        if (lane >= o) {
+            i0 += y0;
+            i1 += y1;
+        }
+    }
+    __syncthreads();
+    if (lane == 31) {
+        sm->wsum[warp] = i0;
+        sm->wsum2[warp] = i1;
+    }
+    __syncthreads();
+    uint64_t b0 = 0, b1 = 0, s0 = 0, s1 = 0;
+#pragma unroll
+    for (int w = 0; w < kRW; ++w) {
+        const uint64_t a = sm->wsum[w], c = sm->wsum2[w];
+        b0 += w < warp ? a : 0ull;
+        b1 += w < warp ? c : 0ull;
+        s0 += a;
+        s1 += c;
+    }
+    t0 = s0;
+    t1 = s1;
+    e1 = b1 + i1 - v1;
+    __syncthreads();
+    return b0 + i0 - v0;
 }
 
 // Four consecutive logits from slot e (entries past n read as -inf).
@@ -592,9 +636,8 @@ __device__ __forceinline__ void rw_sample_row(int row, int32_t* __restrict__ tok
         wide |= cb(q) >= 4096u ? 1u : 0u;
     }
     const bool exact = __syncthreads_or(wide) == 0;
-    uint64_t ctot, S;
-    const uint64_t cex = rw_excl_scan(tc, sm, ctot);
-    const uint64_t mex = rw_excl_scan(tm, sm, S);
+    uint64_t ctot, S, mex;
+    const uint64_t cex = rw_excl_scan2(tc, tm, sm, ctot, mex, S);
     if (tid == 0) {
         sm->bc[0] = kRBins;  // bk (kRBins: top-k off)
         sm->bc[1] = 0ull;    // logits before bk
@@ -647,13 +690,40 @@ __device__ __forceinline__ void rw_sample_row(int row, int32_t* __restrict__ tok
     const int wlo = static_cast<int>(sm->bc[2]);
     const int whi = max(static_cast<int>(static_cast<long long>(sm->bc[3])), wlo - 1);
     const bool gather_bk = kk && bk > whi;  // bin bk is gathered on its own for the exact S_k
-    uint64_t wcount = 0;
-    for (int q = 0; q < kPer; ++q) {
-        const int b = kPer * tid + q;
-        wcount += ((b >= wlo && b <= whi) || (gather_bk && b == bk)) ? cb(q) : 0u;
+    if (warp == 1) {  // the window's size from its bins' counts
+        uint64_t wc = 0;
+        for (int b = wlo + lane; b <= whi; b += 32) wc += sm->cnt[b];
+        wc = rw_sum(wc);
+        if (lane == 0) sm->wtot = wc + (gather_bk ? sm->cnt[bk] : 0u);
     }
-    uint64_t wtot;
-    rw_excl_scan(wcount, sm, wtot);
+
+    // Pass C's bin tests as comparisons: bin(x) is monotone non-increasing in
+    // x, so bin(x) < c exactly when x >= edge(c), the smallest finite float
+    // whose bin is below c (+inf for c = 0), found by bisection on the
+    // order-preserving keys; -inf lies below every edge.
+    if (tid < 4) {
+        const int c = tid == 0 ? wlo : (tid == 1 ? whi + 1 : (tid == 2 ? bk : bk + 1));
+        float ed = INFINITY;
+        if (c > 0) {
+            uint32_t lo = okey(-3.40282347e38f), hi = okey(zmax);  // bin(hi) = 0 < c
+            if (bin(key_float(lo)) < c) {
+                hi = lo;
+            } else {
+                while (hi - lo > 1u) {  // bin(lo) >= c > bin(hi)
+                    const uint32_t mid = lo + (hi - lo) / 2u;
+                    if (bin(key_float(mid)) < c)
+                        hi = mid;
+                    else
+                        lo = mid;
+                }
+            }
+            ed = key_float(hi);
+        }
+        sm->edge[tid] = ed;
+    }
+    __syncthreads();
+    const float e_lo = sm->edge[0], e_win = sm->edge[1], e_bk = sm->edge[2], e_bk1 = sm->edge[3];
+    const uint64_t wtot = sm->wtot;
     const bool fits = exact && wtot <= static_cast<uint64_t>(kRwCap);
 
     unsigned long long* win = sm->win;
@@ -666,7 +736,11 @@ __device__ __forceinline__ void rw_sample_row(int row, int32_t* __restrict__ tok
     if (fits) {
         // ---- C: exact masses; chunk sums of bins < wlo; window gather
         uint64_t asum = 0, msum = 0;  // bins < wlo; top-k bins between the window and bk (top-k on)
-        rw_sweep_chunks(z, V, a16, [&](int c0, const float4 (&q)[4]) {
+        // compiled once with min-p and once without (then a chunk's sum is its
+        // whole mass above the window, and the chunk sums give asum)
+        auto pass_c = [&](auto minp_flag) {
+          constexpr bool kMinP = decltype(minp_flag)::value;
+          rw_sweep_chunks(z, V, a16, [&](int c0, const float4 (&q)[4]) {
             uint64_t s = 0;
             unsigned int inm = 0u;  // bit 4 u + j: element (u, j) lies in the window
 #pragma unroll
@@ -674,15 +748,17 @@ __device__ __forceinline__ void rw_sample_row(int row, int32_t* __restrict__ tok
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const float x = rw_at(q[u], j);
-                    if (!(x > -INFINITY)) continue;
-                    const int b = bin(x);
-                    if (b < wlo) {
+                    if (x >= e_lo) {  // bin < wlo
                         const uint64_t m = mass(x, zmax, c2);
-                        asum += m;
-                        s += m >= mth ? m : 0ull;
-                    } else if (b <= whi || (gather_bk && b == bk)) {
+                        if constexpr (kMinP) {
+                            asum += m;
+                            s += m >= mth ? m : 0ull;
+                        } else {
+                            s += m;
+                        }
+                    } else if (x >= e_win || (gather_bk && x >= e_bk1 && x < e_bk)) {  // wlo..whi, or bk
                         inm |= 1u << (4 * u + j);
-                    } else if (kk && b < bk) {
+                    } else if (kk && x >= e_bk) {  // between the window and bk
                         msum += mass(x, zmax, c2);
                     }
                 }
@@ -711,11 +787,23 @@ __device__ __forceinline__ void rw_sample_row(int row, int32_t* __restrict__ tok
                 }
             }
             s = rw_sum(s);
-            if (lane == 0 && c0 < V) sm->csum[c0 / kRChunk] = s;
-        });
-        uint64_t A, M;
-        rw_excl_scan(asum, sm, A);  // (begins with a barrier: the gather is complete after it)
-        rw_excl_scan(msum, sm, M);
+            if (lane == 0 && c0 < V) {
+                sm->csum[c0 / kRChunk] = s;
+                if constexpr (!kMinP) asum += s;
+            }
+          });
+        };
+        if (mth)
+            pass_c(RwFlag<true>{});
+        else
+            pass_c(RwFlag<false>{});
+        uint64_t A, M = 0;  // (the scans begin with a barrier: the gather is complete after it)
+        if (kk) {
+            uint64_t mex_unused;
+            rw_excl_scan2(asum, msum, sm, A, mex_unused, M);
+        } else {
+            rw_excl_scan(asum, sm, A);
+        }
         const int nw = static_cast<int>(wtot);
         int np2 = 1;
         while (np2 < nw) np2 <<= 1;
@@ -733,8 +821,8 @@ __device__ __forceinline__ void rw_sample_row(int row, int32_t* __restrict__ tok
         auto zof = [&](int i) { return key_float(static_cast<uint32_t>(win[i] >> 32)); };
         uint64_t nbk = 0;
         for (int i = e0; i < e1; ++i) nbk += bin(zof(i)) == bk ? 1u : 0u;
-        uint64_t nbk_tot;
-        const uint64_t nbk_ex = rw_excl_scan(nbk, sm, nbk_tot);
+        uint64_t nbk_tot = 0, nbk_ex = 0;  // (no entry lies in bin bk with top-k off)
+        if (kk) nbk_ex = rw_excl_scan(nbk, sm, nbk_tot);
         uint64_t wk = 0, ww = 0;  // top-k entries' mass; mass of the entries of the window proper
         {
             uint64_t bb = nbk_ex;  // bin-bk entries before i
@@ -748,9 +836,15 @@ __device__ __forceinline__ void rw_sample_row(int row, int32_t* __restrict__ tok
                 bb += is_bk ? 1u : 0u;
             }
         }
-        uint64_t wk_tot, ww_tot;
-        const uint64_t wk_ex = rw_excl_scan(wk, sm, wk_tot);
-        rw_excl_scan(ww, sm, ww_tot);
+        // with top-k off every entry is a top-k entry of the window proper: ww = wk
+        uint64_t wk_tot, ww_tot, wk_ex;
+        if (kk) {
+            uint64_t ww_ex_unused;
+            wk_ex = rw_excl_scan2(wk, ww, sm, wk_tot, ww_ex_unused, ww_tot);
+        } else {
+            wk_ex = rw_excl_scan(wk, sm, wk_tot);
+            ww_tot = wk_tot;
+        }
         const uint64_t Sk = kk ? A + M + wk_tot : S;
         const uint64_t target = p_on ? ceil_mul_p(pp, Sk) : 0ull;
         // the cut must lie in the window proper: A < target <= A + its mass

@@ -222,3 +222,24 @@ def test_rows_order_independent(mix):
         r = oracle.sample_row(z[b], float(T[b]), int(k[b]), float(p[b]), int(seeds[b]), int(offs[b]))
         if got[b] != r["token"]:
             assert r["draw_margin"] < EXEMPT or r["cut_margin"] < EXEMPT, (b, int(got[b]), r)
+
+
+def test_rows_logits_on_bin_edges():
+    """Logits on a grid of 1/256 over a range of 8: with 2048 bins over the
+    row's range every logit lies exactly on a bin edge, where the passes that
+    test a logit's bin by comparing it with the bin's lowest logit must agree
+    with the bin itself; top-p, top-k above 64, min-p and no truncation."""
+    rng = np.random.default_rng(61)
+    B, V = _rows(), 4099
+    grid = -np.arange(0, 2049, dtype=np.float64) / 256.0 + 3.0
+    z = grid[rng.integers(0, 2049, (B, V))].astype(np.float32)
+    z[:, 0] = 3.0       # the maximum and the minimum fix the range at 8
+    z[:, 1] = 3.0 - 8.0
+    T = rng.choice([0.25, 0.5, 1.0, 2.0], B).astype(np.float32)
+    k = rng.choice([0, 0, 100, 1000], B).astype(np.int32)
+    p = rng.choice([0.30011, 0.70013, 0.95003, 1.0], B).astype(np.float32)
+    seeds = rng.integers(0, 2**63, B).astype(np.uint64)
+    offs = rng.integers(0, 1000, B).astype(np.uint64)
+    mp = np.where(rng.random(B) < 0.3, 0.01, 0.0).astype(np.float32)
+    _compare(z, T, k, p, seeds, offs)
+    _compare(z, T, k, p, seeds, offs, min_p=mp)
