@@ -558,145 +558,67 @@ __device__ void draw_pass(Ctx& c, const View& v, const Keep& kp, bool vec, float
 
 // ------------------------------------------------------------------ rank-0 finish on a gathered list
 // The list holds n distinct candidate sort keys, a superset of the top-kk set.
-// Small lists (n <= 128): four candidates per lane of warp 0.  Ranks by
-// comparison with every candidate (the comparisons shared out over the CTA's
-// warps); masses are scattered to their rank (top-p prefix) and then to their
-// id order among the kept tokens (draw), each followed by a warp scan.
+// Small lists (n <= 128): G threads per candidate (G = 8 for n <= 64, else 4;
+// candidate i = tid / G), each taking every G-th candidate j.  One loop gives
+// the candidate's rank (larger keys) and the mass of the larger keys, its
+// prefix in the order (z desc, id asc); S_k is that prefix plus the own mass
+// of the candidate of rank kk - 1.  A second loop, over the kept masses, gives
+// the kept mass at smaller ids and the kept total S_p; the candidate whose
+// interval holds X = floor(u * S_p) is the token.  Two barriers, no atomics.
 constexpr int kSmallList = 128;
 
-// Exclusive scan of buf[0..128) (4 consecutive entries per lane) in place; returns the total.
-__device__ __forceinline__ uint64_t warp_scan128(unsigned long long* buf) {
-    const int lane = threadIdx.x & 31;
-    uint64_t v[4], t = 0;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        v[q] = buf[4 * lane + q];
-        t += v[q];
-    }
-    uint64_t inc = t;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint64_t y = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += y;
-    }
-    const uint64_t total = __shfl_sync(0xffffffffu, inc, 31);
-    uint64_t run = inc - t;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        buf[4 * lane + q] = run;
-        run += v[q];
-    }
-    __syncwarp();
-    return total;
-}
-
-__device__ void solo_finish_small(SampSmem* sm, int n, int kk, float pp, uint64_t mth, float zmax, float c2,
+__device__ __noinline__ void solo_finish_small(SampSmem* sm, int n, int kk, float pp, uint64_t mth, float zmax, float c2,
                                   int32_t* tok_out) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
     const unsigned long long* a = sm->list;
-    unsigned long long* buf = sm->hist;                                  // [128] scratch masses / prefixes
-    unsigned int* kf = reinterpret_cast<unsigned int*>(sm->hist + 128);  // [128] kept flags
-    unsigned int* ids = kf + 128;                                        // [128] token ids
-    unsigned int* rk = ids + 128;                                        // [128] ranks in (z desc, id asc)
-    unsigned int* idr = rk + 128;                                        // [128] ranks among kept ids
-    // the two all-pairs counts are split by j over the CTA's warps (warp w
-    // takes j in [w n / 16, (w + 1) n / 16)) and summed with shared atomics;
-    // the rest runs on warp 0.  Candidate i = lane + 32 q.
-    const int j0 = warp * n / kSW, j1 = (warp + 1) * n / kSW;
-    if (tid < 128) {
-        rk[tid] = 0u;
-        idr[tid] = 0u;
+    unsigned long long* wk = sm->hist;                                   // [128] kept masses (0: not kept)
+    unsigned int* ids = reinterpret_cast<unsigned int*>(sm->hist + 128);  // [128] token ids
+    unsigned long long* skp = sm->hist + 192;                             // S_k
+    const int lg = n <= 64 ? 3 : 2;
+    const int G = 1 << lg;
+    const int i = tid >> lg, p = tid & (G - 1);
+    const bool lead = i < n && p == 0;
+    const unsigned long long key = i < n ? a[i] : ~0ull;  // (an invalid slot counts no larger key)
+    const int ke = min(kk, n);
+    uint32_t cnt = 0u;
+    uint64_t P = 0;
+    for (int j = p; j < n; j += G) {
+        const unsigned long long kj = a[j];
+        if (kj > key) {
+            ++cnt;
+            P += mass(key_float(static_cast<uint32_t>(kj >> 32)), zmax, c2);
+        }
     }
-    unsigned long long key[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) key[q] = lane + 32 * q < n ? a[lane + 32 * q] : 0ull;
-    __syncthreads();
-    {
-        unsigned int r[4] = {0u, 0u, 0u, 0u};
-#pragma unroll 4
-        for (int j = j0; j < j1; ++j) {
-            const unsigned long long kj = a[j];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) r[q] += kj > key[q] ? 1u : 0u;
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            if (r[q]) atomicAdd(&rk[lane + 32 * q], r[q]);
+    for (int o = 1; o < G; o <<= 1) {
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+        P += __shfl_xor_sync(0xffffffffu, P, o);
     }
+    const uint64_t Wi = i < n ? mass(key_float(static_cast<uint32_t>(key >> 32)), zmax, c2) : 0ull;
+    if (lead && cnt == static_cast<uint32_t>(ke - 1)) *skp = P + Wi;
     __syncthreads();
-    uint64_t W[4];
-    bool kept[4];
-    if (warp == 0) {
-        unsigned int rank[4];
-        bool in_k[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const bool valid = lane + 32 * q < n;
-            rank[q] = rk[lane + 32 * q];
-            W[q] = valid ? mass(key_float(static_cast<uint32_t>(key[q] >> 32)), zmax, c2) : 0ull;
-            in_k[q] = valid && rank[q] < static_cast<unsigned int>(kk);
-            kept[q] = in_k[q];
-        }
-        // top-p on the top-k set in rank order
-#pragma unroll
-        for (int q = 0; q < 4; ++q) buf[4 * lane + q] = 0ull;
-        __syncwarp();
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            if (in_k[q]) buf[rank[q]] = W[q];
-        __syncwarp();
-        const uint64_t sk = warp_scan128(buf);
-        if (pp < 1.f) {
-            const uint64_t target = ceil_mul_p(pp, sk);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) kept[q] = in_k[q] && buf[rank[q]] < target;  // prefix before it < target
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) kept[q] = kept[q] && W[q] >= mth;  // min-p, after top-p
-        __syncwarp();
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int i = lane + 32 * q;
-            if (i < n) {
-                kf[i] = kept[q] ? 1u : 0u;
-                ids[i] = static_cast<unsigned int>(sort_key_id(key[q]));
-            }
-            buf[4 * lane + q] = 0ull;
-        }
+    // top-k, then top-p on the top-k set in rank order, then min-p
+    bool kept = i < n && cnt < static_cast<uint32_t>(ke);
+    if (pp < 1.f) kept = kept && P < ceil_mul_p(pp, *skp);
+    const uint64_t wi = (kept && Wi >= mth) ? Wi : 0ull;
+    const unsigned int idi = static_cast<unsigned int>(sort_key_id(key));
+    if (lead) {
+        wk[i] = wi;
+        ids[i] = idi;
     }
     __syncthreads();
-    // draw: kept tokens in id order
-    unsigned int myid[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) myid[q] = static_cast<unsigned int>(sort_key_id(key[q]));
-    {
-        unsigned int r[4] = {0u, 0u, 0u, 0u};
-#pragma unroll 4
-        for (int j = j0; j < j1; ++j) {
-            const unsigned int fj = kf[j], idj = ids[j];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) r[q] += (fj && idj < myid[q]) ? 1u : 0u;
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            if (r[q] && lane + 32 * q < n) atomicAdd(&idr[lane + 32 * q], r[q]);
+    // the draw: kept tokens in id order
+    uint64_t Q = 0, Sp = 0;
+    for (int j = p; j < n; j += G) {
+        const uint64_t wj = wk[j];
+        Sp += wj;
+        Q += ids[j] < idi ? wj : 0ull;
     }
-    __syncthreads();
-    if (warp != 0) return;
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-        if (kept[q]) buf[idr[lane + 32 * q]] = W[q];
-    __syncwarp();
-    const uint64_t Sp = warp_scan128(buf);
-    const uint64_t u53 = sm->u53;
-    const uint64_t X = static_cast<uint64_t>((static_cast<unsigned __int128>(u53) * Sp) >> 53);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        if (kept[q] && W[q] > 0) {
-            const uint64_t before = buf[idr[lane + 32 * q]];
-            if (before <= X && X < before + W[q]) *tok_out = static_cast<int>(myid[q]);
-        }
+    for (int o = 1; o < G; o <<= 1) {
+        Q += __shfl_xor_sync(0xffffffffu, Q, o);
+        Sp += __shfl_xor_sync(0xffffffffu, Sp, o);
     }
+    const uint64_t X = static_cast<uint64_t>((static_cast<unsigned __int128>(sm->u53) * Sp) >> 53);
+    if (lead && wi > 0 && Q <= X && X < Q + wi) *tok_out = static_cast<int>(idi);
 }
 
 // Larger lists: bitonic sort by (z desc, id asc), keep the first kk, apply

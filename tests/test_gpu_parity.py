@@ -288,3 +288,38 @@ def test_sampler_special_rows():
     assert tok[15] < V // 2 + 1                               # equal masses: the nucleus is the lowest ids
     c = compare_tokens(torch.from_numpy(tok), s)
     assert list(c["status"][7:12]) == [6, 6, 1, 1, 6]
+
+
+def test_sampler_small_top_k_lists():
+    """Top-k from 1 to 128 on the cluster kernel, with and without min-p: the
+    candidate lists (every logit in the bins up to the one holding the k-th
+    largest) take the rank-0 finish with eight threads per candidate up to 64
+    candidates, four up to 128, and the sort beyond; plain and peaked rows,
+    top-p on and off.  Every row matches the float64 oracle (exemptions as in
+    the other sampler tests)."""
+    from tests.gpu_helpers import EXEMPT
+    rng = np.random.default_rng(71)
+    B, V = 96, 50000
+    z = (rng.standard_normal((B, V)) * rng.choice([0.5, 1.0, 2.0], (B, 1))).astype(np.float32)
+    z[1::4, rng.integers(V)] += 10.0
+    T = rng.uniform(0.4, 1.5, B).astype(np.float32)
+    k = rng.choice([1, 2, 31, 32, 33, 63, 64, 65, 100, 127, 128], B).astype(np.int32)
+    p = rng.choice([0.30011, 0.90007, 1.0], B).astype(np.float32)
+    seeds = rng.integers(0, 2**63, B).astype(np.uint64)
+    offs = rng.integers(0, 1000, B).astype(np.uint64)
+    mp = np.where(rng.random(B) < 0.3, 0.02, 0.0).astype(np.float32)
+    cu = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    for with_min_p in (False, True):
+        st = pkv.new_status()
+        tok = pkv.sample_tokens(cu(z), cu(T), cu(k), cu(p), cu(seeds.view(np.int64)), cu(offs.view(np.int64)),
+                                status=st, min_p=cu(mp) if with_min_p else None)
+        got = tok.cpu().numpy()
+        assert pkv.check_status(st) == 0
+        exempt = 0
+        for b in range(B):
+            r = oracle.sample_row(z[b], float(T[b]), int(k[b]), float(p[b]), int(seeds[b]), int(offs[b]),
+                                  min_p=float(mp[b]) if with_min_p else 0.0)
+            if got[b] != r["token"]:
+                assert r["draw_margin"] < EXEMPT or r["cut_margin"] < EXEMPT, (b, int(got[b]), r)
+                exempt += 1
+        assert exempt <= 2
