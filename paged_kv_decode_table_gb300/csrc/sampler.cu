@@ -320,6 +320,23 @@ struct Bins {
     }
 };
 
+// The smallest finite logit whose bin is below c (+inf for c <= 0): the bins
+// are monotone non-increasing in z, so bins(z) < c exactly when z >= this
+// edge; found by bisection on the order-preserving keys (bins(zmax) = 0).
+__device__ float bin_edge(const Bins& bins, int c) {
+    if (c <= 0) return INFINITY;
+    uint32_t lo = okey(-3.40282347e38f), hi = okey(bins.zmax);
+    if (bins(key_float(lo)) < c) return key_float(lo);
+    while (hi - lo > 1u) {  // bins(lo) >= c > bins(hi)
+        const uint32_t mid = lo + (hi - lo) / 2u;
+        if (bins(key_float(mid)) < c)
+            hi = mid;
+        else
+            lo = mid;
+    }
+    return key_float(hi);
+}
+
 // Four consecutive logits of the slice starting at e (a multiple of 4); entries
 // at or past n read as -inf.  vec: the slice is the shared-memory copy, padded
 // with -inf up to a multiple of 4 slots.  Otherwise the slice is read from
@@ -1308,13 +1325,18 @@ __global__ void __launch_bounds__(kST, 2)
         if (total >= 1 && total <= static_cast<uint64_t>(kListCap)) {
             uint64_t at = 0, bt = 0;  // exact masses above and below the window
             if (exact) {
+                // blo <= bin <= bhi as comparisons with the bins' edges (-inf
+                // lies below both)
+                __shared__ float edge_sh[2];
+                if (tid < 2) edge_sh[tid] = bin_edge(bins, tid == 0 ? blo : bhi + 1);
+                __syncthreads();
+                const float e_in = edge_sh[0], e_out = edge_sh[1];
                 sweep4<4>(v, nvec, vec, [&](int el, const float4& q) {
                     bool in[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const float z = f4at(q, j);
-                        const int b = bins(z);
-                        in[j] = z > -INFINITY && b >= blo && b <= bhi;
+                        in[j] = z < e_in && z >= e_out;
                     }
                     if (!__any_sync(0xffffffffu, in[0] || in[1] || in[2] || in[3])) return;
 #pragma unroll
